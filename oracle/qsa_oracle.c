@@ -1,0 +1,290 @@
+/*
+ * qsa_oracle.c -- plain, slow CPU oracle for the QSA indexer and its top-k.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call this file:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg load
+ * it.  It shares no code, header, table or constant with the CUDA library.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [QSA]  "SGLang Day-0 support for Qwen3.8-Flash-Next: QSA sparse attention,
+ *         IndexShare MTP and HyperConnection kernel optimisations"
+ *         (theainews.cc), section "Qwen sparse attention (QSA): coarse
+ *         retrieval, fine attention" -- the compressed key, the score
+ *         equation, the 512-block budget and the 0-3 pending tokens, the
+ *         paged full_slot/4 compressed cache.
+ *  [TOPK] SGLang GLM-5.2 blog (aihot.virxact.com), section "Kernel
+ *         Optimization / TopK-V2", Figures 2-4 -- exact top-k (k <= 2048)
+ *         over FP32 score rows, fused with the page-table transform into
+ *         physical KV slots.
+ *  [SMLA] "vllm-sparse-mla-blackwell" (shadowgraph.io), section "Design notes
+ *         worth knowing" -- the consumer masks on index >= 0, so -1 is the
+ *         empty-entry sentinel.
+ *
+ * Every floating-point step that the pages leave open is done in FP64 and
+ * rounded once at the end, except the block mean, which [QSA] fixes as FP32.
+ * Readings of points the pages leave open (all listed in the design notes):
+ *  - "normalise" is the L2 norm; a zero mean vector stays zero;
+ *  - the block's first-token MRoPE position reduces, for text positions, to
+ *    plain RoPE with base `rope_base` over all 128 dims, rotate-half pairing
+ *    (i, i+64), angle p * base^(-2i/128);
+ *  - the query is already position-encoded and is used as given;
+ *  - 1/sqrt(128) multiplies the head sum;
+ *  - a query row sees L tokens, complete blocks b < floor(L/4) and
+ *    L mod 4 pending tokens;
+ *  - ties go to the lower index, -0 equals +0, NaN ranks below -inf;
+ *  - selected indices are returned ascending, -1 only as tail padding.
+ *
+ * Parity pins live in tests/ (hand-worked example, closed forms, brute
+ * force, invariants).  Functions here are kept obviously correct, not fast.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QSA_D 128      /* index head dim ([QSA]: 128-dim heads)           */
+#define QSA_H 4        /* index query heads ([QSA]: 4 query heads)         */
+#define QSA_C 4        /* compression ratio c4 ([QSA]: 4 raw keys / block) */
+
+/* ---------- BF16 helpers (bit patterns in uint16_t) ---------------------- */
+
+double oracle_bf16_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to the nearest BF16 value, ties to even, in one step (no
+ * intermediate FP32 rounding).  BF16 has 8 significant bits and FP32's
+ * exponent range; values below the smallest normal use the fixed subnormal
+ * quantum 2^-133.  Inputs here are finite and far from overflow. */
+uint16_t oracle_bf16_round(double x) {
+  if (x == 0.0) return signbit(x) ? 0x8000u : 0x0000u;
+  int e;
+  frexp(x, &e);                 /* |x| = m * 2^e, m in [0.5, 1) */
+  int qexp = e - 8;             /* quantum of an 8-significant-bit value */
+  if (qexp < -133) qexp = -133;
+  double q = ldexp(1.0, qexp);
+  double r = nearbyint(x / q) * q;   /* default rounding mode: to nearest even */
+  float f = (float)r;                /* exact: r is a BF16 value */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+void oracle_bf16_round_array(const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
+}
+
+/* ---------- paging ([QSA] paged cache; [TOPK] page-table transform) ------ */
+
+/* Physical KV slot of logical token position `pos` of a request whose page
+ * table row is `pt_row`: page pt_row[pos / P], offset pos mod P. */
+int64_t oracle_slot_of(const int32_t* pt_row, int64_t pos, int64_t page_size) {
+  return (int64_t)pt_row[pos / page_size] * page_size + pos % page_size;
+}
+
+/* Row of the compressed-key pool that holds block b: [QSA] addresses the
+ * compressed cache page-aligned as full_slot/4, where full_slot is the
+ * physical slot of the block's first token 4b. */
+int64_t oracle_pool_row(const int32_t* pt_row, int64_t b, int64_t page_size) {
+  return oracle_slot_of(pt_row, QSA_C * b, page_size) / QSA_C;
+}
+
+/* ---------- step 1: compressed index key ([QSA]) ------------------------- */
+
+/* One block: raw[4][128] BF16 keys -> out[128] BF16.
+ *   m   = FP32 mean of the four raw keys, summed in index order;
+ *   u   = m / ||m||_2  (FP64);
+ *   k   = RoPE at position first_pos, rotate-half pairs (i, i+64),
+ *         angle first_pos * rope_base^(-2i/128)  (FP64);
+ *   out = BF16(k), round to nearest even. */
+void oracle_compress_block(const uint16_t* raw, int64_t first_pos, double rope_base,
+                           uint16_t* out) {
+  float m[QSA_D];
+  for (int d = 0; d < QSA_D; ++d) {
+    float s = (float)oracle_bf16_to_double(raw[0 * QSA_D + d]);
+    s = s + (float)oracle_bf16_to_double(raw[1 * QSA_D + d]);
+    s = s + (float)oracle_bf16_to_double(raw[2 * QSA_D + d]);
+    s = s + (float)oracle_bf16_to_double(raw[3 * QSA_D + d]);
+    m[d] = s * 0.25f;
+  }
+  double norm2 = 0.0;
+  for (int d = 0; d < QSA_D; ++d) norm2 += (double)m[d] * (double)m[d];
+  double norm = sqrt(norm2);
+  double u[QSA_D];
+  for (int d = 0; d < QSA_D; ++d) u[d] = norm > 0.0 ? (double)m[d] / norm : 0.0;
+
+  const int half = QSA_D / 2;
+  double k[QSA_D];
+  for (int i = 0; i < half; ++i) {
+    double inv_freq = pow(rope_base, -2.0 * (double)i / (double)QSA_D);
+    double theta = (double)first_pos * inv_freq;
+    double c = cos(theta), s = sin(theta);
+    k[i] = u[i] * c - u[i + half] * s;
+    k[i + half] = u[i + half] * c + u[i] * s;
+  }
+  for (int d = 0; d < QSA_D; ++d) out[d] = oracle_bf16_round(k[d]);
+}
+
+/* All blocks: block i belongs to request block_req[i] and is that request's
+ * block block_id[i] (first token 4*block_id[i]).  With a page table the key
+ * goes to pool row full_slot/4; without one (page_table == NULL) to row i. */
+void oracle_compress(const uint16_t* raw, int64_t n_blocks, const int32_t* block_req,
+                     const int32_t* block_id, const int32_t* page_table, int64_t ld_pt,
+                     int64_t page_size, double rope_base, uint16_t* pool) {
+  for (int64_t i = 0; i < n_blocks; ++i) {
+    int64_t b = block_id[i];
+    int64_t row = i;
+    if (page_table) row = oracle_pool_row(page_table + (int64_t)block_req[i] * ld_pt, b, page_size);
+    oracle_compress_block(raw + i * QSA_C * QSA_D, QSA_C * b, rope_base, pool + row * QSA_D);
+  }
+}
+
+/* ---------- step 2: block scores ([QSA] score equation) ------------------ */
+
+/* s = (1/sqrt(128)) * sum_{h<4} ReLU(<q_h, kbar>), in FP64, rounded once to
+ * FP32.  q is [4][128] BF16, key is [128] BF16. */
+float oracle_score_one(const uint16_t* q, const uint16_t* key) {
+  double acc = 0.0;
+  for (int h = 0; h < QSA_H; ++h) {
+    double dot = 0.0;
+    for (int d = 0; d < QSA_D; ++d)
+      dot += oracle_bf16_to_double(q[h * QSA_D + d]) * oracle_bf16_to_double(key[d]);
+    acc += dot > 0.0 ? dot : 0.0;
+  }
+  return (float)(acc / sqrt((double)QSA_D));
+}
+
+/* Rows are grouped by request: rows req_row_start[r] .. req_row_start[r+1]-1
+ * belong to request r.  Row t sees row_len[t] tokens and so scores blocks
+ * b < row_len[t]/4, reading block b from pool row full_slot/4.  Writes
+ * scores[t][b] for those b only. */
+void oracle_index_scores(const uint16_t* q, const uint16_t* pool, int64_t n_req,
+                         const int32_t* req_row_start, const int32_t* row_len,
+                         const int32_t* page_table, int64_t ld_pt, int64_t page_size,
+                         float* scores, int64_t ld_scores) {
+  for (int64_t r = 0; r < n_req; ++r) {
+    const int32_t* pt_row = page_table + r * ld_pt;
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t) {
+      int64_t nb = row_len[t] / QSA_C;
+      for (int64_t b = 0; b < nb; ++b) {
+        const uint16_t* key = pool + oracle_pool_row(pt_row, b, page_size) * QSA_D;
+        scores[t * ld_scores + b] = oracle_score_one(q + t * QSA_H * QSA_D, key);
+      }
+    }
+  }
+}
+
+/* ---------- step 3: exact top-k ([TOPK]; ties to the lower index) -------- */
+
+/* Total order used for selection: larger score first; NaN below every
+ * number; -0 == +0 (IEEE compare); equal scores by ascending index. */
+static int ranks_before(float a, int64_t ia, float b, int64_t ib) {
+  int na = isnan(a), nb = isnan(b);
+  if (na || nb) {
+    if (na && nb) return ia < ib;
+    return nb;  /* the non-NaN one ranks first */
+  }
+  if (a > b) return 1;
+  if (a < b) return 0;
+  return ia < ib;
+}
+
+typedef struct { float s; int64_t i; } scored_t;
+
+static int cmp_rank(const void* pa, const void* pb) {
+  const scored_t* a = (const scored_t*)pa;
+  const scored_t* b = (const scored_t*)pb;
+  if (a->i == b->i) return 0;
+  return ranks_before(a->s, a->i, b->s, b->i) ? -1 : 1;
+}
+
+static int cmp_index(const void* pa, const void* pb) {
+  int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+  return (a > b) - (a < b);
+}
+
+/* One row: the k best of s[0..n) under the order above, returned as
+ * ascending indices; entries past min(k, n) are -1.  Returns min(k, n). */
+int64_t oracle_topk_row(const float* s, int64_t n, int64_t k, int32_t* out_idx) {
+  scored_t* tmp = (scored_t*)malloc(sizeof(scored_t) * (size_t)(n > 0 ? n : 1));
+  for (int64_t i = 0; i < n; ++i) { tmp[i].s = s[i]; tmp[i].i = i; }
+  qsort(tmp, (size_t)n, sizeof(scored_t), cmp_rank);
+  int64_t m = n < k ? n : k;
+  for (int64_t j = 0; j < m; ++j) out_idx[j] = (int32_t)tmp[j].i;
+  qsort(out_idx, (size_t)m, sizeof(int32_t), cmp_index);
+  for (int64_t j = m; j < k; ++j) out_idx[j] = -1;
+  free(tmp);
+  return m;
+}
+
+/* Many rows.  Row t has n_valid[t] candidates (all ld if n_valid == NULL).
+ * With a page table, out_slots[t][j] is the physical slot of index
+ * out_idx[t][j] in page-table row row_req[t] (row t if row_req == NULL);
+ * -1 stays -1. */
+void oracle_topk(const float* scores, int64_t ld, const int32_t* n_valid, int64_t n_rows,
+                 int64_t k, const int32_t* page_table, int64_t ld_pt, const int32_t* row_req,
+                 int64_t page_size, int32_t* out_idx, int32_t* out_slots) {
+  for (int64_t t = 0; t < n_rows; ++t) {
+    int64_t n = n_valid ? n_valid[t] : ld;
+    oracle_topk_row(scores + t * ld, n, k, out_idx + t * k);
+    if (out_slots && page_table) {
+      const int32_t* pt_row = page_table + (row_req ? row_req[t] : t) * ld_pt;
+      for (int64_t j = 0; j < k; ++j) {
+        int32_t i = out_idx[t * k + j];
+        out_slots[t * k + j] = i < 0 ? -1 : (int32_t)oracle_slot_of(pt_row, i, page_size);
+      }
+    }
+  }
+}
+
+/* ---------- steps 4-5: expansion + slot translation ([QSA], [TOPK]) ------ */
+
+/* One row.  sel[0..k_blk) are selected block ids (ascending, -1 tail).  Each
+ * block b expands to token positions 4b..4b+3; then the L mod 4 pending
+ * tokens of the incomplete block, positions 4*floor(L/4) .. L-1, follow.
+ * The row has 4*k_blk + 3 entries; unused ones are -1.  Slots are the
+ * page-table images of the positions; -1 stays -1. */
+void oracle_expand_row(const int32_t* sel, int64_t k_blk, int64_t L, const int32_t* pt_row,
+                       int64_t page_size, int32_t* out_pos, int32_t* out_slots) {
+  int64_t width = QSA_C * k_blk + (QSA_C - 1);
+  int64_t w = 0;
+  for (int64_t j = 0; j < k_blk; ++j) {
+    if (sel[j] < 0) continue;
+    for (int c = 0; c < QSA_C; ++c) out_pos[w++] = QSA_C * sel[j] + c;
+  }
+  for (int64_t p = (L / QSA_C) * QSA_C; p < L; ++p) out_pos[w++] = (int32_t)p;
+  for (; w < width; ++w) out_pos[w] = -1;
+  for (int64_t j = 0; j < width; ++j)
+    out_slots[j] = out_pos[j] < 0 ? -1 : (int32_t)oracle_slot_of(pt_row, out_pos[j], page_size);
+}
+
+void oracle_expand(const int32_t* sel, int64_t k_blk, int64_t n_req, const int32_t* req_row_start,
+                   const int32_t* row_len, const int32_t* page_table, int64_t ld_pt,
+                   int64_t page_size, int32_t* out_pos, int32_t* out_slots) {
+  int64_t width = QSA_C * k_blk + (QSA_C - 1);
+  for (int64_t r = 0; r < n_req; ++r)
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t)
+      oracle_expand_row(sel + t * k_blk, k_blk, row_len[t], page_table + r * ld_pt, page_size,
+                        out_pos + t * width, out_slots + t * width);
+}
+
+/* ---------- the whole decode path: score -> top-k blocks -> slots ------- */
+
+/* scores must hold n_rows * ld_scores floats (ld_scores >= max nb).  The
+ * selection runs on these FP32 scores, blocks b < row_len/4 only. */
+void oracle_indexer_select(const uint16_t* q, const uint16_t* pool, int64_t n_req,
+                           const int32_t* req_row_start, const int32_t* row_len,
+                           const int32_t* page_table, int64_t ld_pt, int64_t page_size,
+                           int64_t k_blk, float* scores, int64_t ld_scores, int32_t* out_blocks,
+                           int32_t* out_pos, int32_t* out_slots) {
+  oracle_index_scores(q, pool, n_req, req_row_start, row_len, page_table, ld_pt, page_size,
+                      scores, ld_scores);
+  for (int64_t r = 0; r < n_req; ++r)
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t)
+      oracle_topk_row(scores + t * ld_scores, row_len[t] / QSA_C, k_blk, out_blocks + t * k_blk);
+  oracle_expand(out_blocks, k_blk, n_req, req_row_start, row_len, page_table, ld_pt, page_size,
+                out_pos, out_slots);
+}

@@ -1,0 +1,378 @@
+"""Pins for the CPU oracle: each test checks the oracle against something other
+than itself -- the hand-worked example, closed forms, textbook identities,
+a library routine in a special case, brute force on tiny inputs, or
+invariants -- chosen so that a dropped term, a wrong sign or index, or a
+transposed operand fails at least one of them.
+
+Passages: Qwen3.8-Flash-Next day-0 write-up (theainews.cc), section "Qwen
+sparse attention (QSA)" (compressed key, score equation, 512-block budget,
+pending tokens, full_slot/4); SGLang GLM-5.2 blog, section "TopK-V2",
+Figures 2-4 (exact top-k, page-table transform); vllm-sparse-mla-blackwell,
+"Design notes worth knowing" (index >= 0 mask, -1 sentinel).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import bf16_bits, decode_workload, normal_bf16, topk_workload, TOPK_DISTS
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+D = 128
+
+
+def f2b(x):
+    """float -> BF16 bits via the generator's FP32 rounding (input prep only)."""
+    return bf16_bits(np.asarray(x, np.float32))
+
+
+def bf16_ulp(x):
+    x = abs(float(x))
+    if x == 0.0:
+        return 2.0 ** -133
+    e = math.frexp(x)[1]
+    return 2.0 ** max(e - 8, -133)
+
+
+# ----------------------------------------------------------------- BF16 rounding
+def test_bf16_round_matches_torch_on_fp32_values():
+    """Special case reducing to a library routine: for values that are exact in
+    FP32, one-step FP64->BF16 rounding equals torch's FP32->BF16 RNE."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(3.0)
+    # exact halfway cases: BF16 value plus half an ulp, both parities
+    base = bf16_bits(rng.standard_normal(2000).astype(np.float32)).astype(np.uint32) << 16
+    halfway = (base | 0x8000).view(np.float32)
+    tiny = (rng.standard_normal(500) * 1e-39).astype(np.float32)  # FP32 subnormals
+    allx = np.concatenate([x, halfway, tiny, np.array([0.0, -0.0, 1.0, -2.5], np.float32)])
+    want = torch.from_numpy(allx).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round_array(allx.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_bf16_round_double_rounding_case():
+    """One-step rounding from FP64: a value just above a BF16 halfway point
+    must round up even though FP32 rounding would land exactly on the tie."""
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40   # tie in FP32 (rounds to even = 1.0 via FP32), above tie in FP64
+    assert oracle.bf16_round(x) == 0x3F81
+    assert oracle.bf16_round(1.0 + 2.0 ** -8) == 0x3F80  # exact tie -> even
+
+
+# ----------------------------------------------------------------- hand example
+def _golden_raw(g):
+    raw = np.zeros((3 * 4, D), np.float32)
+    for b, dims in g["raw_keys"].items():
+        for d, vals in dims.items():
+            raw[int(b) * 4: int(b) * 4 + 4, int(d)] = vals
+    return f2b(raw)
+
+
+def _golden_q(g):
+    q = np.zeros((1, 4, D), np.float32)
+    for h, e in enumerate(g["q_heads_unit_dims"]):
+        if e is not None:
+            q[0, h, e[0]] = e[1]
+    return f2b(q)
+
+
+def test_hand_example_keys_and_pool_rows():
+    g = json.load(open(os.path.join(GOLDEN, "qsa_3block.json")))
+    pt = np.array([g["page_table"]], np.int32)
+    P = g["page_size"]
+    pool = np.zeros((pt.size * P // 4, D), np.uint16)
+    oracle.compress(_golden_raw(g), np.zeros(3, np.int32), np.arange(3, dtype=np.int32), pt, P,
+                    g["rope_base"], pool)
+    for b, (c, s) in enumerate(g["keys_dim0_dim64"]):
+        row = g["pool_rows"][b]
+        assert oracle.pool_row(pt[0], b, P) == row
+        key = oracle.bf16_to_float(pool[row])
+        expect = np.zeros(D)
+        expect[0], expect[64] = c, s
+        assert np.array_equal(key, expect), (b, key[[0, 1, 64]])
+    # the pool row not owned by any block stays untouched
+    assert not pool[1].any()
+
+
+def test_hand_example_scores_selection_slots():
+    g = json.load(open(os.path.join(GOLDEN, "qsa_3block.json")))
+    pt = np.array([g["page_table"]], np.int32)
+    P = g["page_size"]
+    pool = np.zeros((pt.size * P // 4, D), np.uint16)
+    oracle.compress(_golden_raw(g), np.zeros(3, np.int32), np.arange(3, dtype=np.int32), pt, P,
+                    g["rope_base"], pool)
+    q = _golden_q(g)
+    rrs = np.array([0, 1], np.int32)
+    rl = np.array([g["row_len"]], np.int32)
+    out = oracle.indexer_select(q, pool, rrs, rl, pt, P, k_blk=g["k_blk"])
+    want = np.array([eval(e, {"sqrt": math.sqrt}) for e in g["scores_expr"]], np.float32)
+    assert np.array_equal(out["scores"][0, :3], want)
+    assert out["blocks"][0].tolist() == g["selected_blocks"]
+    assert out["pos"][0].tolist() == g["positions"]
+    assert out["slots"][0].tolist() == g["slots"]
+
+
+# ----------------------------------------------------------------- compression
+def _theta(p, i, base=10000.0):
+    return p * base ** (-2.0 * i / 128.0)
+
+
+@pytest.mark.parametrize("p", [0, 1, 4, 100, 8188, 79996, 131068])
+@pytest.mark.parametrize("j", [0, 1, 5, 31, 63, 64, 65, 100, 127])
+def test_rope_closed_form_on_basis_vectors(p, j):
+    """All four raw keys = e_j: the normalised mean is e_j and RoPE rotates it
+    in the (i, i+64) plane by p * 10000^(-2i/128), i = j mod 64."""
+    raw = np.zeros((4, D), np.float32)
+    raw[:, j] = 1.0
+    key = oracle.bf16_to_float(oracle.compress_block(f2b(raw), p))
+    i = j % 64
+    c, s = math.cos(_theta(p, i)), math.sin(_theta(p, i))
+    expect = np.zeros(D)
+    if j < 64:
+        expect[i], expect[i + 64] = c, s
+    else:
+        expect[i], expect[i + 64] = -s, c
+    for d in range(D):
+        assert abs(key[d] - expect[d]) <= 0.5 * bf16_ulp(expect[d]) + 1e-300, (d, key[d], expect[d])
+
+
+def test_compress_position_zero_is_normalised_mean():
+    """p = 0: RoPE is the identity; each key is m/||m|| rounded once to BF16.
+    Raw keys are chosen so that the FP32 block sum is exact."""
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        raw = (rng.integers(-64, 65, size=(4, D)) / 16.0).astype(np.float32)
+        m = raw.astype(np.float64).sum(0) / 4
+        u = m / np.linalg.norm(m)
+        got = oracle.bf16_to_float(oracle.compress_block(f2b(raw), 0))
+        want = oracle.bf16_to_float(oracle.bf16_round_array(u))
+        assert np.array_equal(got, want)
+
+
+def test_compress_invariants():
+    """Symmetric in the four raw keys, invariant to a common power-of-two
+    scale, unit norm, and a rotation: two keys compressed at the same
+    position keep the inner product of their normalised means."""
+    rng = np.random.default_rng(2)
+    for trial in range(40):
+        raw = normal_bf16(rng, (4, D))
+        p = int(rng.integers(0, 131072))
+        k0 = oracle.compress_block(raw, p)
+        assert np.array_equal(oracle.compress_block(raw[[2, 0, 3, 1]], p), k0)
+        scaled = f2b(oracle.bf16_to_float(raw) * 4.0)
+        assert np.array_equal(oracle.compress_block(scaled, p), k0)
+        kf = oracle.bf16_to_float(k0)
+        assert abs(np.linalg.norm(kf) - 1.0) < 4e-3
+        raw2 = normal_bf16(rng, (4, D))
+        k1 = oracle.bf16_to_float(oracle.compress_block(raw2, p))
+        m0 = oracle.bf16_to_float(raw).sum(0)
+        m1 = oracle.bf16_to_float(raw2).sum(0)
+        ip = float(m0 @ m1) / (np.linalg.norm(m0) * np.linalg.norm(m1))
+        assert abs(float(kf @ k1) - ip) < 1e-2
+
+
+def test_compress_relative_position_property():
+    """<RoPE_p(u), RoPE_p'(v)> depends only on p - p': shifting both blocks by
+    the same multiple of 4 leaves the inner product of the keys unchanged
+    (up to BF16 rounding)."""
+    rng = np.random.default_rng(3)
+    a = normal_bf16(rng, (4, D))
+    b = normal_bf16(rng, (4, D))
+    base = []
+    for shift in [0, 4, 400, 40000]:
+        ka = oracle.bf16_to_float(oracle.compress_block(a, 100 + shift))
+        kb = oracle.bf16_to_float(oracle.compress_block(b, 36 + shift))
+        base.append(float(ka @ kb))
+    assert np.ptp(base) < 2e-2
+    # while a different offset changes it
+    ka = oracle.bf16_to_float(oracle.compress_block(a, 100))
+    kb = oracle.bf16_to_float(oracle.compress_block(b, 40))
+    assert abs(float(ka @ kb) - base[0]) > 1e-3
+
+
+def test_compress_zero_block_stays_zero():
+    raw = np.zeros((4, D), np.uint16)
+    assert (oracle.bf16_to_float(oracle.compress_block(raw, 12)) == 0.0).all()
+
+
+# ----------------------------------------------------------------- scores
+def test_score_closed_form_on_basis_keys():
+    """key = e_d: s = sum_h ReLU(q_h[d]) / sqrt(128)."""
+    rng = np.random.default_rng(4)
+    for d in [0, 7, 64, 127]:
+        key = np.zeros(D, np.float32)
+        key[d] = 1.0
+        for _ in range(20):
+            q = normal_bf16(rng, (4, D))
+            qd = oracle.bf16_to_float(q)[:, d]
+            want = np.float32(np.maximum(qd, 0).sum() / math.sqrt(128))
+            assert oracle.score_one(q, f2b(key)) == want
+
+
+def test_score_identities():
+    """ReLU(x) - ReLU(-x) = x gives s(q) - s(-q) = sum_h <q_h, k> / sqrt(128);
+    s is positively homogeneous (s(2q) = 2 s(q)) and symmetric in the heads;
+    s >= 0."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        q = normal_bf16(rng, (4, D))
+        k = normal_bf16(rng, (D,))
+        qf, kf = oracle.bf16_to_float(q), oracle.bf16_to_float(k)
+        s = oracle.score_one(q, k)
+        s_neg = oracle.score_one(q ^ np.uint16(0x8000), k)
+        lin = float((qf @ kf).sum()) / math.sqrt(128)
+        scale = float(np.abs(qf * kf).sum()) / math.sqrt(128)
+        assert abs((s - s_neg) - lin) <= 1e-6 * scale + 1e-7
+        assert s >= 0 and s_neg >= 0
+        assert oracle.score_one(f2b(qf * 2.0), k) == np.float32(2.0 * s)
+        assert oracle.score_one(q[[3, 1, 0, 2]], k) == s
+    # all heads anti-aligned with the key -> exactly zero
+    k = normal_bf16(rng, (D,))
+    q = np.stack([k ^ np.uint16(0x8000)] * 4)
+    assert oracle.score_one(q, k) == 0.0
+
+
+def test_index_scores_visibility_and_paging():
+    """Row t scores blocks b < L_t/4 only, reading block b from pool row
+    full_slot(4b)/4; compare with scoring each block's key directly."""
+    w = decode_workload(7, [[37, 40, 41], [9], [130, 131, 132, 133]], page_size=8, k_blk=4)
+    pool = np.zeros((w.pool_rows, D), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, w.page_table, w.page_size, w.rope_base, pool)
+    # unpaged copy: block i at row i
+    flat = np.zeros((w.n_blocks, D), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, None, 0, w.rope_base, flat)
+    s = oracle.index_scores(w.q, pool, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    first = {}
+    for i, (r, b) in enumerate(zip(w.block_req, w.block_id)):
+        first[(int(r), int(b))] = i
+    rr = w.row_req()
+    for t in range(w.n_rows):
+        nb = w.row_len[t] // 4
+        for b in range(s.shape[1]):
+            if b < nb:
+                assert s[t, b] == oracle.score_one(w.q[t], flat[first[(int(rr[t]), b)]])
+            else:
+                assert np.isnan(s[t, b])
+
+
+# ----------------------------------------------------------------- top-k
+def _brute_topk(row, k):
+    """Full sort by (NaN last, value desc, index asc), first k, ascending."""
+    keyed = sorted(range(len(row)), key=lambda i: (math.isnan(row[i]),
+                                                    -row[i] if not math.isnan(row[i]) else 0.0, i))
+    chosen = sorted(keyed[:k])
+    return chosen + [-1] * (k - len(chosen))
+
+
+def test_topk_bruteforce_exhaustive_small():
+    vals = [0.0, 1.0, -1.0, 2.0, -2.0]
+    for n in range(0, 6):
+        for row in itertools.product(vals, repeat=n):
+            r = np.array(row, np.float32)
+            for k in range(1, n + 2):
+                assert oracle.topk_row(r, k).tolist() == _brute_topk(list(row), k), (row, k)
+
+
+def test_topk_bruteforce_random_up_to_12():
+    rng = np.random.default_rng(6)
+    vals = np.array([0.0, -0.0, 1.0, -1.0, 2.0, -2.0, np.inf, -np.inf, np.nan], np.float32)
+    for _ in range(4000):
+        n = int(rng.integers(0, 13))
+        r = vals[rng.integers(0, vals.size, size=n)]
+        k = int(rng.integers(1, 14))
+        got = oracle.topk_row(r, k).tolist()
+        want = _brute_topk([float(x) if not (x == 0) else 0.0 for x in r], k)
+        assert got == want, (r, k)
+
+
+def _check_invariants(row, n, k, idx):
+    m = min(n, k)
+    sel = idx[:m]
+    assert (idx[m:] == -1).all()
+    assert (sel >= 0).all() and (sel < n).all()
+    assert (np.diff(sel) > 0).all()
+    if m == n:
+        return
+    mask = np.zeros(n, bool)
+    mask[sel] = True
+    v = row[:n].astype(np.float64)
+    lo = v[mask].min()
+    hi = v[~mask].max()
+    assert lo >= hi
+    if lo == hi:  # boundary ties: selected ones have the smallest indices
+        tie_sel = np.flatnonzero(mask & (v == lo))
+        tie_un = np.flatnonzero(~mask & (v == lo))
+        assert tie_sel.max() < tie_un.min()
+
+
+@pytest.mark.parametrize("dist", TOPK_DISTS)
+def test_topk_invariants(dist):
+    w = topk_workload(8, 6, 6000, k=2048, dist=dist, ragged=True)
+    idx, slots = oracle.topk(w.scores, w.k, n_valid=w.n_valid, page_table=w.page_table,
+                             page_size=w.page_size)
+    for t in range(6):
+        _check_invariants(w.scores[t], int(w.n_valid[t]), w.k, idx[t])
+        # slot translation inverts through the page table
+        inv = {int(p): j for j, p in enumerate(w.page_table[t])}
+        good = idx[t] >= 0
+        assert (slots[t][~good] == -1).all()
+        pages = np.array([inv[int(p)] for p in slots[t][good] // w.page_size], np.int64)
+        pos = pages * w.page_size + slots[t][good] % w.page_size
+        assert np.array_equal(pos, idx[t][good])
+
+
+def test_topk_special_cases():
+    k = 16
+    assert oracle.topk_row(np.full(100, 0.25, np.float32), k).tolist() == list(range(k))
+    assert oracle.topk_row(np.arange(5, dtype=np.float32), k).tolist() == list(range(5)) + [-1] * 11
+    assert oracle.topk_row(np.zeros(0, np.float32), 4).tolist() == [-1] * 4
+    r = np.array([0.0, -0.0, 0.0, -0.0], np.float32)
+    assert oracle.topk_row(r, 2).tolist() == [0, 1]
+    r = np.array([np.nan, -np.inf, 1.0, np.nan], np.float32)
+    assert oracle.topk_row(r, 3).tolist() == [0, 1, 2]
+    assert oracle.topk_row(r, 2).tolist() == [1, 2]
+
+
+# ----------------------------------------------------------------- expansion
+@pytest.mark.parametrize("L", [0, 1, 3, 4, 5, 6, 7, 8, 63, 64, 65, 66, 67, 2047, 2048, 2049, 2051])
+def test_expand_counts_and_order(L):
+    k_blk = 512
+    P = 64
+    pt = np.random.default_rng(L).permutation(64).astype(np.int32)
+    nb = L // 4
+    sel = np.full(k_blk, -1, np.int32)
+    chosen = np.sort(np.random.default_rng(L + 1).permutation(nb)[:k_blk]).astype(np.int32)
+    sel[:chosen.size] = chosen
+    pos, slots = oracle.expand_row(sel, L, pt, P)
+    assert pos.size == 4 * k_blk + 3
+    n_sel = min(nb, k_blk)
+    n_out = 4 * n_sel + L % 4
+    assert (pos[n_out:] == -1).all() and (pos[:n_out] >= 0).all()
+    assert (np.diff(pos[:n_out]) > 0).all()
+    assert set(pos[4 * n_sel:n_out].tolist()) == set(range(4 * nb, L))
+    for j, b in enumerate(chosen):
+        assert pos[4 * j: 4 * j + 4].tolist() == [4 * b, 4 * b + 1, 4 * b + 2, 4 * b + 3]
+    inv = np.argsort(pt)
+    good = pos >= 0
+    assert np.array_equal(inv[slots[good] // P] * P + slots[good] % P, pos[good])
+    assert (slots[~good] == -1).all()
+
+
+def test_indexer_select_composition_and_padding():
+    """Whole path on a small paged workload: selection equals top-k of the
+    scores; rows with fewer than k visible blocks are padded only at the tail."""
+    w = decode_workload(9, [[2048 * 4 + 3, 2000, 17], [1, 4, 5]], page_size=16, k_blk=512)
+    pool = np.zeros((w.pool_rows, D), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, w.page_table, w.page_size, w.rope_base, pool)
+    out = oracle.indexer_select(w.q, pool, w.req_row_start, w.row_len, w.page_table, w.page_size,
+                                k_blk=512)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        want = oracle.topk_row(out["scores"][t, :nb], 512)
+        assert np.array_equal(out["blocks"][t], want)
+        _check_invariants(out["scores"][t], nb, 512, out["blocks"][t])
+        assert ((out["blocks"][t] == -1).sum() > 0) == (nb < 512)
