@@ -1,0 +1,208 @@
+/*
+ * qsa.h -- C ABI of the GB300 QSA indexer library (libqsa.so).
+ *
+ * The library computes, on one GPU, the data-parallel hot path of the QSA
+ * sparse-attention indexer and a generic token-level top-k:
+ *
+ *   compress  block of 4 raw BF16 index keys -> one BF16 compressed key
+ *   score     s[t][b] = (1/sqrt(128)) * sum_{h<4} ReLU(<q[t][h], kbar[b]>)
+ *   select    best k visible blocks (ties: lower block id), ascending
+ *   expand    block b -> token positions 4b..4b+3, then the 0-3 pending
+ *             tokens of the incomplete block; -1 fills the rest
+ *   translate position -> physical KV slot through the request's page table
+ *
+ * Sources, cited by page title and section:
+ *  [QSA]  "SGLang Day-0 support for Qwen3.8-Flash-Next: QSA sparse attention,
+ *         IndexShare MTP and HyperConnection kernel optimisations"
+ *         (theainews.cc), section "Qwen sparse attention (QSA): coarse
+ *         retrieval, fine attention" -- 4 query heads x 128 dims and one
+ *         shared key head; every 4 raw index keys averaged in FP32,
+ *         normalised and rotated at the block's first-token position into
+ *         one compressed key; the score equation; the best 512 blocks
+ *         expanded to 2048 token positions plus the 0-3 pending tokens (at
+ *         most 2051); one BF16 compressed key per 4 tokens, stored
+ *         page-aligned at full_slot/4.
+ *  [TOPK] SGLang GLM-5.2 blog (aihot.virxact.com), section "Kernel
+ *         Optimization / TopK-V2", Figures 2-4 -- exact top-k (runtime k up
+ *         to 2048) over FP32 score rows, with the selected logical positions
+ *         translated into physical KV-cache slots in the same kernel.
+ *  [SMLA] "vllm-sparse-mla-blackwell" (shadowgraph.io), section "Design notes
+ *         worth knowing" -- the attention consumer's only mask is
+ *         index >= 0, so -1 marks an empty entry.
+ *
+ * Conventions shared by every call
+ *  - Every pointer is a DEVICE pointer unless its name starts with h_.  The
+ *    caller owns all memory; the library never allocates, frees, or keeps
+ *    per-call state, and never synchronises.  Scratch comes from a caller
+ *    workspace sized by the matching *_workspace_size() query.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call only enqueues work on it.
+ *  - BF16 tensors are passed as `const void*` / `void*` (IEEE bfloat16, 2 B).
+ *  - Fixed sizes: index head dim 128, 4 index query heads, 4 raw keys per
+ *    compressed block.  Indices and slots are int32; leading dimensions are
+ *    int64 element counts.  -1 is the sentinel for an empty entry.
+ *  - Rows are grouped by request: rows req_row_start[r] .. req_row_start[r+1]-1
+ *    (device int32 array of n_req+1 entries, non-decreasing, first entry 0)
+ *    belong to request r.  Row t sees row_len[t] tokens (its position + 1):
+ *    complete blocks b < row_len[t]/4 and row_len[t] mod 4 pending tokens.
+ *    `max_len` is a host-side upper bound of every row_len[t]; it sizes the
+ *    launch.
+ *  - Paging: page_table is [n_req][ld_pt] int32 physical page ids;
+ *    slot(pos) = page_table[r][pos / page_size] * page_size + pos % page_size.
+ *    The compressed key of block b of request r lives in pool row
+ *    slot(4b) / 4 (the page-aligned full_slot/4 address of [QSA]); the pool
+ *    holds pool_rows rows of 128 BF16 and page_size must be a multiple of 4.
+ *  - Errors: host-side argument checks return a negative qsa_status and
+ *    enqueue nothing.  Launch failures return QSA_ERR_CUDA.  Device-side
+ *    checks (a row longer than max_len, a page id or pool row out of range)
+ *    skip the offending access and latch a device fault word, read with
+ *    qsa_device_status().  No call traps or spins without a bound.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int qsa_status;
+#define QSA_OK 0
+#define QSA_ERR_INVALID_ARG (-1)        /* null pointer, negative size, misalignment */
+#define QSA_ERR_UNSUPPORTED (-2)        /* k > 2048, page_size % 4 != 0, row too long */
+#define QSA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define QSA_ERR_CUDA (-4)               /* a CUDA launch or query failed */
+#define QSA_ERR_DEVICE_FAULT (-5)       /* a device-side bounds check fired */
+
+#define QSA_HEAD_DIM 128
+#define QSA_HEADS 4
+#define QSA_BLOCK 4
+#define QSA_MAX_K 2048
+
+/* Human-readable name of a status code (static string). */
+const char* qsa_status_string(qsa_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int qsa_version(void);
+
+/* Synchronises `stream`, reads the device fault word latched by the
+ * device-side bounds checks of earlier calls, optionally clears it, and
+ * returns QSA_OK or QSA_ERR_DEVICE_FAULT.  *h_bits (may be NULL) receives the
+ * word: bit 0 row/page index out of range, bit 1 pool row out of range,
+ * bit 2 a bounded wait expired, bit 3 inconsistent row grouping. */
+qsa_status qsa_device_status(void* stream, int clear, uint32_t* h_bits);
+
+/* ---------------------------------------------------------------------
+ * Compressed index keys  ([QSA]: one compressed key per block of 4 raw index
+ * keys -- their FP32 average, normalised, rotated at the position of the
+ * block's first token -- kept in BF16 in a paged cache at full_slot/4).
+ *
+ *   raw        [n_blocks*4][128] BF16: the 4 raw index keys of each block,
+ *              in token order.
+ *   block_req  [n_blocks] request of each block (row of page_table).
+ *   block_id   [n_blocks] block index b within its request; the block's first
+ *              token is position 4b and its key goes to pool row slot(4b)/4.
+ *   page_table [n_req][ld_pt]; NULL stores block i in pool row i instead.
+ *   rope_base  RoPE base (10000 for the workloads here).
+ *   pool       [pool_rows][128] BF16, written in place.
+ *
+ * Per block: m = ((k0 + k1) + k2) + k3 in FP32, times 0.25; u = m / ||m||_2
+ * (u = 0 if m = 0); RoPE with rotate-half pairs (i, i+64), angle
+ * 4b * rope_base^(-2i/128); rounded to BF16 (nearest even).
+ * ------------------------------------------------------------------- */
+qsa_status qsa_compress_keys(const void* raw, const int32_t* block_req, const int32_t* block_id,
+                             int64_t n_blocks, int32_t n_req, const int32_t* page_table,
+                             int64_t ld_pt, int32_t page_size, double rope_base, void* pool,
+                             int64_t pool_rows, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Block scores  ([QSA] score equation:
+ *   s[t][b] = (1/sqrt(128)) * sum_{h=1..4} ReLU(<q[t][h], kbar[b]>)
+ * over the visible compressed blocks b < row_len[t]/4).
+ *
+ *   q          [n_rows][4][128] BF16 index queries (already position-encoded).
+ *   pool       compressed-key pool, addressed through page_table.
+ *   scores     [n_rows][ld_scores] FP32 out.  Entries b < row_len[t]/4 are
+ *              written; entries row_len[t]/4 <= b < n_fill are set to -inf;
+ *              nothing else is touched.  ld_scores >= max_len/4.
+ *   max_rows_per_req  host upper bound of the rows of any one request.
+ * Products of BF16 are exact; accumulation is FP32.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                            const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                            int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                            int64_t ld_pt, int32_t page_size, float* scores, int64_t ld_scores,
+                            int64_t n_fill, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Exact top-k over FP32 rows  ([TOPK]: a selection rather than a sort,
+ * returning exactly k entries for a runtime k of at most 2048, with the
+ * page-table transform to physical KV-cache slots done in the same kernel).
+ *
+ *   scores     [n_rows][ld] FP32.
+ *   n_valid    [n_rows] candidates per row (entries 0..n_valid-1), or NULL:
+ *              every row has n_max candidates.
+ *   n_max      host upper bound of n_valid (<= ld).
+ *   k          1..2048.
+ *   page_table [.][ld_pt] or NULL (then out_slots must be NULL).
+ *   row_req    [n_rows] page-table row of each row, or NULL: row t uses
+ *              page-table row t.
+ *   out_idx    [n_rows][k]: the k best indices in ascending order; -1 after
+ *              the first min(k, n_valid) entries.
+ *   out_slots  [n_rows][k] or NULL: slot(out_idx), -1 stays -1.
+ * Order: larger value first; equal values by ascending index; -0 == +0; NaN
+ * below every number.  The result is unique, so it is bit-exact.
+ * ------------------------------------------------------------------- */
+size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k);
+qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int32_t n_rows,
+                       int32_t n_max, int32_t k, const int32_t* page_table, int64_t ld_pt,
+                       const int32_t* row_req, int32_t page_size, int32_t* out_idx,
+                       int32_t* out_slots, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Expansion of selected blocks to token positions and KV slots  ([QSA]:
+ * each kept block stands for its 4 token positions, and the 0-3 tokens of
+ * the still-incomplete block are added after them; [TOPK] page-table
+ * transform; [SMLA] -1 sentinel).
+ *
+ *   sel_blocks [n_rows][k_blk] ascending block ids, -1 only as tail padding.
+ *   out_pos    [n_rows][4*k_blk+3] or NULL: 4b..4b+3 for each selected b in
+ *              order, then positions 4*(row_len/4) .. row_len-1, then -1.
+ *   out_slots  [n_rows][4*k_blk+3]: slot(out_pos), -1 stays -1.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_req,
+                            const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                            const int32_t* page_table, int64_t ld_pt, int32_t page_size,
+                            int32_t* out_pos, int32_t* out_slots, void* stream);
+
+/* ---------------------------------------------------------------------
+ * The fused decode path: score -> top-k_blk blocks -> expand -> slots, one
+ * call  ([QSA] score equation and 512-block selection; [TOPK] selection
+ * fused with the page-table transform).
+ *
+ *   out_blocks [n_rows][k_blk] or NULL: the selected block ids.
+ *   out_pos    [n_rows][4*k_blk+3] or NULL: token positions.
+ *   out_slots  [n_rows][4*k_blk+3]: physical KV slots, -1 padded.
+ *   scores_out [n_rows][ld_scores] or NULL: the FP32 scores the selection
+ *              ran on (entries b < row_len/4); when NULL they live in the
+ *              workspace.
+ * Workspace: when scores_out is NULL the scores live in the workspace, which
+ * must hold qsa_indexer_select_workspace_size(n_rows, max_len, k_blk) bytes;
+ * when scores_out is given the workspace may be NULL with 0 bytes.
+ * ------------------------------------------------------------------- */
+size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_t k_blk);
+qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                              const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                              int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                              int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                              int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                              int64_t ld_scores, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

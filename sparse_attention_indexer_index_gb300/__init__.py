@@ -1,0 +1,256 @@
+"""GB300-native QSA sparse-attention indexer and top-k selection.
+
+A thin Python binding over the C ABI of ``libqsa.so`` (declared in
+``include/qsa.h``).  Every step of the path runs in the library's CUDA
+kernels; this module only checks tensor placement and dtypes, passes raw
+device pointers and the current CUDA stream, and turns a non-zero status into
+an exception.  PyTorch provides device memory and streams.
+
+There is no CPU fallback: if the library is missing the import of the
+functions below fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+__all__ = [
+    "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
+    "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
+    "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
+]
+
+HEAD_DIM, HEADS, BLOCK, MAX_K = 128, 4, 4, 2048
+_lib = None
+
+
+class QSAError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} failed: {lib().qsa_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+def lib():
+    """The loaded ``libqsa.so`` (ctypes), with argument types declared."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libqsa.so not built at {LIB_PATH}: run build() first "
+                              "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i32, i64, sz, d = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
+                              ctypes.c_double)
+        sig = {
+            "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "qsa_version": (ctypes.c_int, []),
+            "qsa_device_status": (ctypes.c_int, [p, ctypes.c_int, p]),
+            "qsa_compress_keys": (ctypes.c_int, [p, p, p, i64, i32, p, i64, i32, d, p, i64, p]),
+            "qsa_index_scores": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
+                                                i64, i64, p]),
+            "topk_select_workspace_size": (sz, [i32, i32, i32]),
+            "topk_select": (ctypes.c_int, [p, i64, p, i32, i32, i32, p, i64, p, i32, p, p, p, sz, p]),
+            "qsa_expand_slots": (ctypes.c_int, [p, i32, i32, p, i32, p, p, i64, i32, p, p, p]),
+            "qsa_indexer_select_workspace_size": (sz, [i32, i32, i32]),
+            "qsa_indexer_select": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
+                                                  i32, p, p, p, p, i64, p, sz, p]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return t
+
+
+def _check(fn, status):
+    if status != 0:
+        raise QSAError(fn, status)
+
+
+def out_width(k_blk: int) -> int:
+    """Entries per expanded row: 4 positions per block plus 3 pending slots."""
+    return BLOCK * k_blk + (BLOCK - 1)
+
+
+# ----------------------------------------------------------------- entry points
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device fault bits (0 = none)."""
+    bits = ctypes.c_uint32(0)
+    lib().qsa_device_status(_stream(stream), int(clear), ctypes.byref(bits))
+    return int(bits.value)
+
+
+def compress_keys(raw, block_id, pool, block_req=None, page_table=None, page_size=0,
+                  rope_base=10000.0, stream=None):
+    """raw [n_blocks*4][128] bf16 -> pool rows (in place).  With a page table,
+    block i of request block_req[i] goes to pool row slot(4*block_id[i])/4."""
+    torch = _torch()
+    _dev(raw, torch.bfloat16, "raw", 2)
+    _dev(block_id, torch.int32, "block_id", 1)
+    _dev(pool, torch.bfloat16, "pool", 2)
+    n_blocks = block_id.numel()
+    if raw.shape[0] != 4 * n_blocks or raw.shape[1] != HEAD_DIM:
+        raise ValueError("raw must be [4*n_blocks][128]")
+    n_req, ld_pt = 0, 0
+    if page_table is not None:
+        _dev(page_table, torch.int32, "page_table", 2)
+        _dev(block_req, torch.int32, "block_req", 1)
+        n_req, ld_pt = page_table.shape
+    _check("qsa_compress_keys", lib().qsa_compress_keys(
+        _ptr(raw), _ptr(block_req), _ptr(block_id), n_blocks, n_req, _ptr(page_table), ld_pt,
+        int(page_size), float(rope_base), _ptr(pool), pool.shape[0], _stream(stream)))
+    return pool
+
+
+def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len,
+                 max_rows_per_req=None, scores=None, n_fill=0, stream=None):
+    """Block scores [n_rows][ld] float32 (entries b < row_len/4 written,
+    [row_len/4, n_fill) set to -inf)."""
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
+    _dev(pool, torch.bfloat16, "pool", 2)
+    _dev(req_row_start, torch.int32, "req_row_start", 1)
+    _dev(row_len, torch.int32, "row_len", 1)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_rows = row_len.numel()
+    if max_rows_per_req is None:
+        max_rows_per_req = n_rows
+    if scores is None:
+        ld = max(1, (max(int(max_len) // BLOCK, int(n_fill)) + 3) // 4 * 4)
+        scores = torch.empty((n_rows, ld), dtype=torch.float32, device=q.device)
+    _dev(scores, torch.float32, "scores", 2)
+    _check("qsa_index_scores", lib().qsa_index_scores(
+        _ptr(q), _ptr(pool), pool.shape[0], req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+        _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
+        int(page_size), _ptr(scores), scores.shape[1], int(n_fill), _stream(stream)))
+    return scores
+
+
+def topk_select(scores, k, n_valid=None, n_max=None, page_table=None, row_req=None, page_size=0,
+                out_idx=None, out_slots=None, want_slots=None, stream=None):
+    """Exact top-k per row, ascending indices, -1 padded; optionally slots.
+    Returns (idx, slots or None)."""
+    torch = _torch()
+    _dev(scores, torch.float32, "scores", 2)
+    n_rows, ld = scores.shape
+    if n_valid is not None:
+        _dev(n_valid, torch.int32, "n_valid", 1)
+    if n_max is None:
+        n_max = ld
+    if page_table is not None:
+        _dev(page_table, torch.int32, "page_table", 2)
+    if row_req is not None:
+        _dev(row_req, torch.int32, "row_req", 1)
+    if want_slots is None:
+        want_slots = page_table is not None
+    if out_idx is None:
+        out_idx = torch.empty((n_rows, k), dtype=torch.int32, device=scores.device)
+    if want_slots and out_slots is None:
+        out_slots = torch.empty((n_rows, k), dtype=torch.int32, device=scores.device)
+    ws_bytes = lib().topk_select_workspace_size(n_rows, int(n_max), int(k))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    _check("topk_select", lib().topk_select(
+        _ptr(scores), ld, _ptr(n_valid), n_rows, int(n_max), int(k), _ptr(page_table),
+        0 if page_table is None else page_table.shape[1], _ptr(row_req), int(page_size),
+        _ptr(out_idx), _ptr(out_slots), _ptr(ws), ws_bytes, _stream(stream)))
+    return out_idx, out_slots
+
+
+def expand_slots(sel_blocks, req_row_start, row_len, page_table, page_size, want_pos=True,
+                 stream=None):
+    """Selected blocks [n_rows][k] -> (positions or None, slots) [n_rows][4k+3]."""
+    torch = _torch()
+    _dev(sel_blocks, torch.int32, "sel_blocks", 2)
+    _dev(req_row_start, torch.int32, "req_row_start", 1)
+    _dev(row_len, torch.int32, "row_len", 1)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_rows, k = sel_blocks.shape
+    w = out_width(k)
+    slots = torch.empty((n_rows, w), dtype=torch.int32, device=sel_blocks.device)
+    pos = torch.empty((n_rows, w), dtype=torch.int32, device=sel_blocks.device) if want_pos else None
+    _check("qsa_expand_slots", lib().qsa_expand_slots(
+        _ptr(sel_blocks), k, req_row_start.numel() - 1, _ptr(req_row_start), n_rows, _ptr(row_len),
+        _ptr(page_table), page_table.shape[1], int(page_size), _ptr(pos), _ptr(slots),
+        _stream(stream)))
+    return pos, slots
+
+
+def indexer_select_workspace_size(n_rows, max_len, k_blk=512) -> int:
+    return int(lib().qsa_indexer_select_workspace_size(int(n_rows), int(max_len), int(k_blk)))
+
+
+def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, max_len,
+                   max_rows_per_req=None, k_blk=512, want_blocks=False, want_pos=False,
+                   scores_out=None, workspace=None, out_slots=None, stream=None):
+    """Fused decode path: score -> top-k_blk blocks -> expand -> slots.
+    Returns dict(slots, blocks?, pos?, scores?)."""
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
+    _dev(pool, torch.bfloat16, "pool", 2)
+    _dev(req_row_start, torch.int32, "req_row_start", 1)
+    _dev(row_len, torch.int32, "row_len", 1)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_rows = row_len.numel()
+    dev = q.device
+    if max_rows_per_req is None:
+        max_rows_per_req = n_rows
+    w = out_width(k_blk)
+    if out_slots is None:
+        out_slots = torch.empty((n_rows, w), dtype=torch.int32, device=dev)
+    blocks = torch.empty((n_rows, k_blk), dtype=torch.int32, device=dev) if want_blocks else None
+    pos = torch.empty((n_rows, w), dtype=torch.int32, device=dev) if want_pos else None
+    ld = 0
+    ws_bytes = 0
+    if scores_out is not None:
+        _dev(scores_out, torch.float32, "scores_out", 2)
+        ld = scores_out.shape[1]
+    else:
+        ws_bytes = indexer_select_workspace_size(n_rows, max_len, k_blk)
+        if workspace is None and ws_bytes:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        elif workspace is not None:
+            ws_bytes = workspace.numel() * workspace.element_size()
+    _check("qsa_indexer_select", lib().qsa_indexer_select(
+        _ptr(q), _ptr(pool), pool.shape[0], req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+        _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
+        int(page_size), int(k_blk), _ptr(blocks), _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld,
+        _ptr(workspace), ws_bytes, _stream(stream)))
+    out = {"slots": out_slots}
+    if blocks is not None:
+        out["blocks"] = blocks
+    if pos is not None:
+        out["pos"] = pos
+    if scores_out is not None:
+        out["scores"] = scores_out
+    return out

@@ -1,0 +1,160 @@
+// compress.cuh -- compressed index keys of the QSA indexer.
+//
+// Qwen3.8-Flash-Next day-0 write-up (theainews.cc), section "Qwen sparse
+// attention (QSA)": each block of 4 raw index keys becomes one key -- the FP32
+// average of the four, normalised, then rotated by the position encoding of
+// the block's first token -- kept as BF16 in a paged cache addressed
+// page-aligned at full_slot/4.
+//
+// Readings: "normalised" is the L2 norm (a zero mean stays zero); for text
+// positions the multi-section RoPE reduces to plain RoPE over all 128 dims
+// with rotate-half pairs (i, i+64) and angle p * base^(-2i/128).
+//
+// Work split: 8 lanes per block; lane j owns dims [8j, 8j+8) and
+// [64+8j, 64+8j+8), i.e. exactly the rotation pairs it needs, so every load
+// and store is one 16-byte vector and only the norm needs shuffles.
+//
+// Angle: p * base^(-2i/128) grows to ~1.3e5 rad at 131k tokens, so it is
+// reduced exactly: t_i = base^(-2i/128) / (2 pi) is held as a 64-bit binary
+// fraction of a turn (computed once per thread in FP64), p * t_i mod 1 is a
+// wrapping 64-bit integer product, and the top 32 bits give the angle in
+// units of pi for sincospif.  Error < 3e-7 rad for p < 2^31.
+#pragma once
+#include "common.cuh"
+
+namespace qsa {
+
+struct CompressArgs {
+  const __nv_bfloat16* raw;   // [n_blocks*4][128]
+  const int32_t* block_req;   // [n_blocks]
+  const int32_t* block_id;    // [n_blocks]
+  int64_t n_blocks;
+  int32_t n_req;
+  const int32_t* page_table;  // [n_req][ld_pt] or nullptr
+  int64_t ld_pt;
+  int32_t page_size;
+  double rope_base;
+  __nv_bfloat16* pool;        // [pool_rows][128]
+  int64_t pool_rows;
+};
+
+constexpr int kCompressThreads = 256;
+constexpr int kCompressLanes = 8;  // lanes per block
+
+__device__ __forceinline__ void accumulate_bf16x8(float (&acc)[8], uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float2 f = bf16x2_to_float2(w[e]);
+    acc[2 * e] = acc[2 * e] + f.x;
+    acc[2 * e + 1] = acc[2 * e + 1] + f.y;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(kCompressThreads)
+compress_keys_kernel(CompressArgs a) {
+  const int lane8 = threadIdx.x & (kCompressLanes - 1);
+  // Rotation frequencies of this lane's 8 pairs, as 64-bit turn fractions.
+  uint64_t turn_frac[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = kCompressLanes * lane8 + e;
+    const double inv_freq = pow(a.rope_base, -2.0 * (double)i / (double)kDim);
+    const double turns = inv_freq * 0.15915494309189533577;  // 1 / (2 pi)
+    turn_frac[e] = __double2ull_rn(turns * 18446744073709551616.0);  // * 2^64
+  }
+
+  const int64_t groups_per_cta = kCompressThreads / kCompressLanes;
+  const int64_t stride = (int64_t)gridDim.x * groups_per_cta;
+  for (int64_t blk = (int64_t)blockIdx.x * groups_per_cta + threadIdx.x / kCompressLanes;
+       blk < a.n_blocks; blk += stride) {
+    // Destination pool row: slot of the block's first token, divided by 4.
+    const int64_t b = a.block_id[blk];
+    const uint64_t pos = (uint64_t)(kBlock * b);
+    int64_t row = blk;
+    bool ok = b >= 0;
+    if (a.page_table != nullptr && ok) {
+      const int r = a.block_req[blk];
+      const int64_t page_idx = (int64_t)(pos / (uint64_t)a.page_size);
+      ok = r >= 0 && r < a.n_req && page_idx < a.ld_pt;
+      if (ok) {
+        const int64_t page = a.page_table[(int64_t)r * a.ld_pt + page_idx];
+        row = page * (a.page_size / kBlock) + (int64_t)(pos % (uint64_t)a.page_size) / kBlock;
+        ok = page >= 0;
+      }
+    }
+    if (!ok) {
+      if (lane8 == 0) raise_fault(kFaultIndex);
+      continue;
+    }
+    if (row < 0 || row >= a.pool_rows) {
+      if (lane8 == 0) raise_fault(kFaultPool);
+      continue;
+    }
+
+    // FP32 block mean, summed in token order: ((k0 + k1) + k2) + k3, * 0.25.
+    const __nv_bfloat16* src = a.raw + blk * (kBlock * kDim);
+    float lo[8], hi[8];
+    {
+      uint4 v0 = ld_stream_16(src + 8 * lane8);
+      uint4 w0 = ld_stream_16(src + 64 + 8 * lane8);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t x = (&v0.x)[e], y = (&w0.x)[e];
+        float2 fx = bf16x2_to_float2(x), fy = bf16x2_to_float2(y);
+        lo[2 * e] = fx.x; lo[2 * e + 1] = fx.y;
+        hi[2 * e] = fy.x; hi[2 * e + 1] = fy.y;
+      }
+    }
+#pragma unroll
+    for (int k = 1; k < kBlock; ++k) {
+      accumulate_bf16x8(lo, ld_stream_16(src + k * kDim + 8 * lane8));
+      accumulate_bf16x8(hi, ld_stream_16(src + k * kDim + 64 + 8 * lane8));
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      lo[e] *= 0.25f;
+      hi[e] *= 0.25f;
+      ss = fmaf(lo[e], lo[e], ss);
+      ss = fmaf(hi[e], hi[e], ss);
+    }
+    // The 8 lanes of a block always take the same path, so the shuffles name
+    // only their own group.
+    const unsigned group = 0xffu << (threadIdx.x & 24);
+    ss += __shfl_xor_sync(group, ss, 1);
+    ss += __shfl_xor_sync(group, ss, 2);
+    ss += __shfl_xor_sync(group, ss, 4);
+    const float inv_norm = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+
+    uint32_t out_lo[4], out_hi[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float r_lo[2], r_hi[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t ph = pos * turn_frac[e + h];            // turns mod 1, wraps
+        const int32_t top = (int32_t)(ph >> 32);               // signed: [-1/2, 1/2) turn
+        const float y = (float)top * 4.656612873077392578125e-10f;  // * 2^-31: units of pi
+        float s, c;
+        sincospif(y, &s, &c);
+        const float u = lo[e + h] * inv_norm, v = hi[e + h] * inv_norm;
+        r_lo[h] = u * c - v * s;
+        r_hi[h] = v * c + u * s;
+      }
+      out_lo[e / 2] = pack_bf16x2(r_lo[0], r_lo[1]);
+      out_hi[e / 2] = pack_bf16x2(r_hi[0], r_hi[1]);
+    }
+    __nv_bfloat16* dst = a.pool + row * kDim;
+    *reinterpret_cast<uint4*>(dst + 8 * lane8) = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+    *reinterpret_cast<uint4*>(dst + 64 + 8 * lane8) =
+        make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+  }
+}
+
+}  // namespace qsa

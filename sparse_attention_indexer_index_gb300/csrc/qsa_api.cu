@@ -1,0 +1,334 @@
+// qsa_api.cu -- the extern "C" entry points of libqsa.so: host-side argument
+// checks, launch shapes, and launches on the caller's stream.  Declarations
+// and the contract of every call are in include/qsa.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/qsa.h"
+#include "common.cuh"
+#include "compress.cuh"
+#include "expand.cuh"
+#include "score_decode.cuh"
+#include "select.cuh"
+
+using namespace qsa;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Largest row slice one CTA keeps in shared memory (keys), and the largest
+// cluster used for one row.
+constexpr int kSegCap = 48 * 1024;
+constexpr int kMaxCluster = 8;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device one-time set-up: SM count and the shared-memory opt-in of the
+// selection kernels.
+qsa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QSA_ERR_CUDA;
+    const int smem = (int)(sizeof(SelShared) + (size_t)kSegCap * sizeof(uint32_t));
+    if (cudaFuncSetAttribute(select_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return QSA_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return QSA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+qsa_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+// Cluster size and slice length for rows of up to n_max candidates: the
+// smallest power of two whose slices fit in shared memory, then doubled
+// while the grid stays under half the SMs and each CTA keeps >= 2048
+// candidates (small batches of long rows spread over more SMs).
+bool plan_select(int n_rows, int n_max, int sm_count, int* cs_out, int* seg_out) {
+  int cs = 1;
+  while (cs < kMaxCluster && (n_max + cs - 1) / cs > kSegCap) cs *= 2;
+  if ((n_max + cs - 1) / cs > kSegCap) return false;
+  while (cs < kMaxCluster && (int64_t)n_rows * cs * 2 <= sm_count && n_max / (cs * 2) >= 2048) cs *= 2;
+  int seg = (n_max + cs - 1) / cs;
+  seg = std::max(4, (seg + 3) & ~3);
+  *cs_out = cs;
+  *seg_out = seg;
+  return true;
+}
+
+template <int kMode>
+qsa_status launch_select(const SelectArgs& a, int cs, bool pdl, cudaStream_t stream) {
+  if (a.n_rows == 0) return QSA_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_rows * (unsigned)cs, 1, 1);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(SelShared) + (size_t)a.seg * sizeof(uint32_t);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)cs;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, select_kernel<kMode>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
+qsa_status check_rows(int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                      const int32_t* row_len, int32_t max_len) {
+  if (n_req < 0 || n_rows < 0 || max_len < 0) return QSA_ERR_INVALID_ARG;
+  if (n_rows > 0 && (n_req < 1 || !req_row_start || !row_len)) return QSA_ERR_INVALID_ARG;
+  if (n_req > 65535) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+qsa_status check_paging(const int32_t* page_table, int64_t ld_pt, int32_t page_size,
+                        int32_t max_len) {
+  if (!page_table || page_size <= 0 || ld_pt < 0) return QSA_ERR_INVALID_ARG;
+  if (page_size % kBlock != 0) return QSA_ERR_UNSUPPORTED;
+  if (max_len > 0 && (int64_t)(max_len - 1) / page_size >= ld_pt) return QSA_ERR_INVALID_ARG;
+  return QSA_OK;
+}
+
+qsa_status launch_scores(const ScoreArgs& s, cudaStream_t stream) {
+  const int64_t nb_max = s.max_len / kBlock;
+  const int64_t cols = std::max<int64_t>(nb_max, s.n_fill);
+  if (s.n_req == 0 || cols == 0) return QSA_OK;
+  dim3 grid((unsigned)((cols + kScoreTile - 1) / kScoreTile), (unsigned)s.n_req, 1);
+  score_decode_kernel<<<grid, kScoreThreads, 0, stream>>>(s);
+  return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qsa_status_string(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported size or layout";
+    case QSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case QSA_ERR_CUDA: return "CUDA error";
+    case QSA_ERR_DEVICE_FAULT: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int qsa_version(void) { return 100; }
+
+qsa_status qsa_device_status(void* stream, int clear, uint32_t* h_bits) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned bits = 0;
+  if (cudaMemcpyFromSymbolAsync(&bits, g_fault_word, sizeof(bits), 0, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QSA_ERR_CUDA;
+  if (clear && bits) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_fault_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return QSA_ERR_CUDA;
+  }
+  if (h_bits) *h_bits = bits;
+  return bits ? QSA_ERR_DEVICE_FAULT : QSA_OK;
+}
+
+qsa_status qsa_compress_keys(const void* raw, const int32_t* block_req, const int32_t* block_id,
+                             int64_t n_blocks, int32_t n_req, const int32_t* page_table,
+                             int64_t ld_pt, int32_t page_size, double rope_base, void* pool,
+                             int64_t pool_rows, void* stream) {
+  if (n_blocks < 0 || pool_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (n_blocks == 0) return QSA_OK;
+  if (!raw || !block_id || !pool || !aligned16(raw) || !aligned16(pool)) return QSA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0)) return QSA_ERR_INVALID_ARG;
+  if (page_table) {
+    if (!block_req || n_req < 1 || ld_pt < 1 || page_size <= 0) return QSA_ERR_INVALID_ARG;
+    if (page_size % kBlock != 0) return QSA_ERR_UNSUPPORTED;
+  }
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  CompressArgs a{static_cast<const __nv_bfloat16*>(raw), block_req, block_id, n_blocks, n_req,
+                 page_table, ld_pt, page_size, rope_base, static_cast<__nv_bfloat16*>(pool),
+                 pool_rows};
+  const int64_t per_cta = kCompressThreads / kCompressLanes;
+  const int64_t grid = std::min<int64_t>((n_blocks + per_cta - 1) / per_cta, (int64_t)d->sm_count * 8);
+  compress_keys_kernel<<<(unsigned)grid, kCompressThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
+qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                            const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                            int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                            int64_t ld_pt, int32_t page_size, float* scores, int64_t ld_scores,
+                            int64_t n_fill, void* stream) {
+  (void)max_rows_per_req;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+  if (!q || !pool || !scores || pool_rows < 0 || n_fill < 0) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool) || !aligned4(scores)) return QSA_ERR_INVALID_ARG;
+  if (ld_scores < std::max<int64_t>(max_len / kBlock, n_fill)) return QSA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
+              pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
+              page_size, scores, ld_scores, n_fill, 0};
+  return launch_scores(s, static_cast<cudaStream_t>(stream));
+}
+
+size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k) {
+  (void)n_rows; (void)n_max; (void)k;
+  return 0;  // the selection keeps everything on chip
+}
+
+qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int32_t n_rows,
+                       int32_t n_max, int32_t k, const int32_t* page_table, int64_t ld_pt,
+                       const int32_t* row_req, int32_t page_size, int32_t* out_idx,
+                       int32_t* out_slots, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (n_rows < 0 || n_max < 0 || ld < 0) return QSA_ERR_INVALID_ARG;
+  if (k < 1 || k > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return QSA_OK;
+  if (!out_idx || (n_max > 0 && !scores) || n_max > ld) return QSA_ERR_INVALID_ARG;
+  if (out_slots && (!page_table || page_size <= 0 || ld_pt < 1)) return QSA_ERR_INVALID_ARG;
+  if (scores && !aligned4(scores)) return QSA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  int cs = 1, seg = 4;
+  if (!plan_select(n_rows, n_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
+  SelectArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.n_rows = n_rows;
+  a.k = k;
+  a.n_max = n_max;
+  a.seg = seg;
+  a.vec_ok = aligned16(scores) && (ld % 4 == 0);
+  a.wait_primary = 0;
+  a.n_valid = n_valid;
+  a.row_req = row_req;
+  a.out_idx = out_idx;
+  a.out_slots = out_slots;
+  a.page_table = page_table;
+  a.ld_pt = ld_pt;
+  a.page_size = page_size > 0 ? page_size : 1;
+  if (qsa_status st = launch_select<kModeTopk>(a, cs, false, static_cast<cudaStream_t>(stream)))
+    return st;
+  return QSA_OK;
+}
+
+qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_req,
+                            const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                            const int32_t* page_table, int64_t ld_pt, int32_t page_size,
+                            int32_t* out_pos, int32_t* out_slots, void* stream) {
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, 0)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (!sel_blocks || !out_slots || !page_table || ld_pt < 1 || page_size <= 0)
+    return QSA_ERR_INVALID_ARG;
+  if (page_size % kBlock != 0) return QSA_ERR_UNSUPPORTED;
+  ExpandArgs a{sel_blocks, k_blk, n_req, req_row_start, n_rows, row_len, page_table, ld_pt,
+               page_size, out_pos, out_slots};
+  expand_kernel<<<(unsigned)n_rows, kExpThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
+size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_t k_blk) {
+  (void)k_blk;
+  if (n_rows <= 0 || max_len <= 0) return 0;
+  const int64_t ld = ((int64_t)(max_len / kBlock) + 3) & ~int64_t(3);
+  return (size_t)(n_rows * ld * (int64_t)sizeof(float)) + 256;
+}
+
+qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                              const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                              int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                              int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                              int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                              int64_t ld_scores, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  (void)max_rows_per_req;
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+  if (!q || !pool || !out_slots || pool_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool)) return QSA_ERR_INVALID_ARG;
+  const int32_t nb_max = max_len / kBlock;
+  float* scores = scores_out;
+  int64_t ld = ld_scores;
+  if (scores_out) {
+    if (ld_scores < nb_max || !aligned4(scores_out)) return QSA_ERR_INVALID_ARG;
+  } else {
+    const size_t need = qsa_indexer_select_workspace_size(n_rows, max_len, k_blk);
+    if (need > 0) {
+      if (!workspace || workspace_bytes < need) return QSA_ERR_WORKSPACE_TOO_SMALL;
+      scores = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
+    }
+    ld = (nb_max + 3) & ~3;
+  }
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  int cs = 1, seg = 4;
+  if (!plan_select(n_rows, nb_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
+              pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
+              page_size, scores, ld, 0, 1};
+  if (qsa_status e = launch_scores(s, st)) return e;
+
+  SelectArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.n_rows = n_rows;
+  a.k = k_blk;
+  a.n_max = nb_max;
+  a.seg = seg;
+  a.vec_ok = scores && aligned16(scores) && (ld % 4 == 0);
+  a.wait_primary = 1;
+  a.n_req = n_req;
+  a.req_row_start = req_row_start;
+  a.row_len = row_len;
+  a.out_idx = out_blocks;
+  a.out_pos = out_pos;
+  a.out_xslots = out_slots;
+  a.page_table = page_table;
+  a.ld_pt = ld_pt;
+  a.page_size = page_size;
+  return launch_select<kModeQsa>(a, cs, nb_max > 0, st);
+}
+
+}  // extern "C"

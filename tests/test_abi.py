@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point declared in include/qsa.h, and rejects bad arguments on the host
+(returning an error status and launching nothing).  No call here reaches a
+CUDA launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import sparse_attention_indexer_index_gb300 as qsa
+    qsa.build()
+    return qsa.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ["qsa_compress_keys", "qsa_index_scores", "topk_select", "qsa_expand_slots",
+              "qsa_indexer_select"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    assert L.qsa_status_string(0) == b"ok"
+    assert L.qsa_status_string(-2) == b"unsupported size or layout"
+    assert L.qsa_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: the checks fail first
+
+
+def test_topk_rejects_bad_k(L):
+    for k in (0, -1, 2049):
+        assert L.topk_select(FAKE, 100, None, 1, 100, k, None, 0, None, 0, FAKE, None, None, 0,
+                             None) == -2
+
+
+def test_topk_rejects_null_output_and_slots_without_table(L):
+    assert L.topk_select(FAKE, 100, None, 1, 100, 8, None, 0, None, 0, None, None, None, 0, None) == -1
+    assert L.topk_select(FAKE, 100, None, 1, 100, 8, None, 0, None, 64, FAKE, FAKE, None, 0, None) == -1
+    # n_max beyond the leading dimension
+    assert L.topk_select(FAKE, 100, None, 1, 101, 8, None, 0, None, 0, FAKE, None, None, 0, None) == -1
+
+
+def test_expand_rejects_page_size_not_multiple_of_4(L):
+    assert L.qsa_expand_slots(FAKE, 512, 1, FAKE, 1, FAKE, FAKE, 10, 62, None, FAKE, None) == -2
+    assert L.qsa_expand_slots(FAKE, 4096, 1, FAKE, 1, FAKE, FAKE, 10, 64, None, FAKE, None) == -2
+
+
+def test_scores_reject_short_page_table_and_leading_dim(L):
+    # max_len 8192 needs 128 pages of 64, table has 100
+    assert L.qsa_index_scores(FAKE, FAKE, 1 << 20, 1, FAKE, 1, FAKE, 8192, 1, FAKE, 100, 64, FAKE,
+                              2048, 0, None) == -1
+    # ld_scores below max_len/4
+    assert L.qsa_index_scores(FAKE, FAKE, 1 << 20, 1, FAKE, 1, FAKE, 8192, 1, FAKE, 128, 64, FAKE,
+                              2047, 0, None) == -1
+    # misaligned q
+    assert L.qsa_index_scores(ctypes.c_void_p(0x1002), FAKE, 1 << 20, 1, FAKE, 1, FAKE, 8192, 1, FAKE,
+                              128, 64, FAKE, 2048, 0, None) == -1
+
+
+def test_indexer_select_rejects_small_workspace(L):
+    need = L.qsa_indexer_select_workspace_size(6, 80000, 512)
+    assert need >= 6 * 20000 * 4
+    assert L.qsa_indexer_select(FAKE, FAKE, 1 << 20, 1, FAKE, 6, FAKE, 80000, 6, FAKE, 1250, 64, 512,
+                                None, None, FAKE, None, 0, FAKE, need - 1, None) == -3
+    assert L.qsa_indexer_select(FAKE, FAKE, 1 << 20, 1, FAKE, 6, FAKE, 80000, 6, FAKE, 1250, 64, 4096,
+                                None, None, FAKE, None, 0, FAKE, need, None) == -2
+
+
+def test_compress_rejects_bad_arguments(L):
+    assert L.qsa_compress_keys(None, FAKE, FAKE, 4, 1, FAKE, 4, 64, 10000.0, FAKE, 16, None) == -1
+    assert L.qsa_compress_keys(FAKE, FAKE, FAKE, 4, 1, FAKE, 4, 6, 10000.0, FAKE, 16, None) == -2
+    assert L.qsa_compress_keys(FAKE, FAKE, FAKE, 4, 1, FAKE, 4, 64, 0.0, FAKE, 16, None) == -1
+    # nothing to do is fine and touches nothing
+    assert L.qsa_compress_keys(None, None, None, 0, 0, None, 0, 0, 10000.0, None, 0, None) == 0
+
+
+def test_zero_rows_are_a_no_op(L):
+    assert L.topk_select(None, 0, None, 0, 0, 8, None, 0, None, 0, None, None, None, 0, None) == 0
+    assert L.qsa_indexer_select(None, None, 0, 0, None, 0, None, 0, 0, None, 0, 64, 512, None, None,
+                                None, None, 0, None, 0, None) == 0

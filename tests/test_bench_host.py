@@ -1,0 +1,63 @@
+"""Host-side logic of the benchmark without a GPU: the max-over-ranks timing
+used when every rank runs an independent replica (world size 2, gloo), the
+algorithmic byte counts, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    t = bench.aggregate_time(1.0 + rank, world)  # rank 1 is the slow one
+    bench.barrier(world)
+    q.put((rank, t))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 2000)
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 2.0, 1: 2.0}
+    assert all(p.exitcode == 0 for p in ps)
+
+
+def test_decode_bytes_c2():
+    import bench
+    from workloads import c2_verify
+    w = c2_verify(0)
+    by = bench.decode_bytes(w)
+    assert by["keys"] == 20000 * 256          # keys read once for all 6 rows
+    assert by["q"] == 6 * 1024
+    assert by["slots"] == 6 * 2051 * 4
+    assert by["page_table"] == 1250 * 4
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "rows/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0

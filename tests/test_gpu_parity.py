@@ -1,0 +1,254 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: compressed keys within 1 BF16 ulp (FP32 vs FP64 normalisation and
+rotation), scores within 2e-5 * (1/sqrt(128)) * sum|q k| + 1e-6 of the FP64
+oracle (FP32 accumulation of exact BF16 products), and selection, expansion
+and slot translation bit-exact when both sides see the same FP32 scores.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import bf16_dev, bf16_host, score_tolerance, to_dev
+from workloads import (c1_decode, c2_verify, c3_batched, c4_dsa_topk, decode_workload,
+                       topk_workload, TOPK_DISTS)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import sparse_attention_indexer_index_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _no_device_faults(qsa):
+    yield
+    assert qsa.device_status(clear=True) == 0, "a device-side bounds check fired"
+
+
+def oracle_pool(w):
+    pool = np.zeros((w.pool_rows, 128), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, w.page_table, w.page_size, w.rope_base, pool)
+    return pool
+
+
+def gpu_pool(qsa, w):
+    import torch
+    pool = torch.zeros((w.pool_rows, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(bf16_dev(w.raw_keys), to_dev(w.block_id), pool, block_req=to_dev(w.block_req),
+                      page_table=to_dev(w.page_table), page_size=w.page_size, rope_base=w.rope_base)
+    return pool
+
+
+# ----------------------------------------------------------------- compress
+SMALL_DECODE = [
+    ("one_row_ragged_tiles", [[4 * 300 + 2]], 64),
+    ("verify_rows", [[5001, 5002, 5003, 5004, 5005, 5006]], 64),
+    ("multi_request", [[37, 40, 41], [9], [1030, 1031], [4096 * 4 + 3]], 16),
+    ("tiny_pages", [[77, 78], [130]], 4),
+    ("ten_rows", [[2000 + i for i in range(10)], [513]], 32),
+]
+
+
+@pytest.mark.parametrize("name,rows,P", SMALL_DECODE)
+def test_compress_parity(qsa, name, rows, P):
+    w = decode_workload(21, rows, page_size=P, k_blk=64)
+    want = oracle_pool(w)
+    got = bf16_host(gpu_pool(qsa, w))
+    a, b = oracle.bf16_to_float(got), oracle.bf16_to_float(want)
+    ulp = np.maximum(np.abs(b), 2.0 ** -126)
+    ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
+    assert (np.abs(a - b) <= ulp).all()
+    assert (got == want).mean() > 0.99
+
+
+def test_compress_parity_long_positions_sampled(qsa):
+    """The c3 workload (32 requests up to 131,072 tokens): every block on the
+    GPU, a random sample of 4,000 blocks on the oracle."""
+    w = c3_batched(0)
+    got = bf16_host(gpu_pool(qsa, w))
+    rng = np.random.default_rng(5)
+    for i in rng.choice(w.n_blocks, 4000, replace=False):
+        r, b = int(w.block_req[i]), int(w.block_id[i])
+        row = oracle.pool_row(w.page_table[r], b, w.page_size)
+        want = oracle.compress_block(w.raw_keys[4 * i: 4 * i + 4], 4 * b, w.rope_base)
+        a, e = oracle.bf16_to_float(got[row]), oracle.bf16_to_float(want)
+        assert (np.abs(a - e) <= 2.0 ** (np.floor(np.log2(np.maximum(np.abs(e), 2.0 ** -126))) - 7)).all()
+
+
+# ----------------------------------------------------------------- scores
+@pytest.mark.parametrize("name,rows,P", SMALL_DECODE)
+def test_scores_parity(qsa, name, rows, P):
+    import torch
+    w = decode_workload(22, rows, page_size=P, k_blk=64)
+    pool_h = oracle_pool(w)
+    ld = w.max_len // 4 + 40
+    n_fill = ld - 8
+    want = oracle.index_scores(w.q, pool_h, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    scores = torch.full((w.n_rows, ld), 7.0, device="cuda")
+    qsa.index_scores(bf16_dev(w.q), bf16_dev(pool_h), to_dev(w.req_row_start), to_dev(w.row_len),
+                     to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, scores=scores,
+                     n_fill=n_fill)
+    got = scores.cpu().numpy()
+    tol = score_tolerance(w.q, pool_h, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        err = np.abs(got[t, :nb].astype(np.float64) - want[t, :nb])
+        assert (err <= tol[t, :nb]).all(), (t, err.max())
+        assert np.isneginf(got[t, nb:n_fill]).all()
+        assert (got[t, n_fill:] == 7.0).all()
+
+
+# ----------------------------------------------------------------- top-k
+def run_topk(qsa, w, k=None, with_slots=True):
+    k = k or w.k
+    idx, slots = qsa.topk_select(to_dev(w.scores), k, n_valid=to_dev(w.n_valid),
+                                 n_max=int(w.n_valid.max()) if w.n_valid.size else 0,
+                                 page_table=to_dev(w.page_table) if with_slots else None,
+                                 page_size=w.page_size)
+    ref_idx, ref_slots = oracle.topk(w.scores, k, n_valid=w.n_valid,
+                                     page_table=w.page_table if with_slots else None,
+                                     page_size=w.page_size)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    if with_slots:
+        assert np.array_equal(slots.cpu().numpy(), ref_slots)
+
+
+@pytest.mark.parametrize("dist", TOPK_DISTS)
+@pytest.mark.parametrize("k", [1, 7, 512, 2048])
+def test_topk_parity_ragged(qsa, dist, k):
+    run_topk(qsa, topk_workload(31, 9, 6000, k=k, dist=dist, ragged=True), k)
+
+
+@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (200, 3000)])
+def test_topk_parity_cluster_shapes(qsa, n_rows, n):
+    """Shapes that select clusters of 8, 4-8, 1-2 and 1 CTAs per row."""
+    run_topk(qsa, topk_workload(32, n_rows, n, k=2048, dist="fp16dup"))
+
+
+@pytest.mark.parametrize("dist", TOPK_DISTS)
+def test_topk_parity_dsa_full_size(qsa, dist):
+    """64 rows x 80,000 FP32 scores, k = 2048, with slot translation."""
+    run_topk(qsa, c4_dsa_topk(0, dist))
+
+
+def test_topk_special_rows(qsa):
+    import torch
+    n = 5000
+    s = np.zeros((6, n), np.float32)
+    s[0] = 0.25                                    # all equal -> 0..k-1
+    s[1] = -0.0                                    # signed zeros tie with +0
+    s[1, ::3] = 0.0
+    s[2] = np.nan                                  # NaN below everything
+    s[2, 4000:] = -np.inf
+    s[3] = np.arange(n, dtype=np.float32)          # strictly increasing
+    s[4] = -np.arange(n, dtype=np.float32)
+    s[5, 100] = np.inf
+    nv = np.array([n, n, n, n, n, 0], np.int32)
+    for k in [1, 100, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
+# ----------------------------------------------------------------- expand
+@pytest.mark.parametrize("P", [4, 16, 64])
+def test_expand_parity(qsa, P):
+    rng = np.random.default_rng(P)
+    lens = [[int(x) for x in rng.integers(0, 9000, size=4)] + [1, 2, 3, 4, 5]]
+    w = decode_workload(41, lens, page_size=P, k_blk=512)
+    k = 512
+    sel = np.full((w.n_rows, k), -1, np.int32)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        c = np.sort(rng.permutation(nb)[:k])
+        sel[t, :c.size] = c
+    pos, slots = qsa.expand_slots(to_dev(sel), to_dev(w.req_row_start), to_dev(w.row_len),
+                                  to_dev(w.page_table), w.page_size)
+    rpos, rslots = oracle.expand(sel, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(pos.cpu().numpy(), rpos)
+    assert np.array_equal(slots.cpu().numpy(), rslots)
+
+
+# ----------------------------------------------------------------- fused path
+def check_fused(qsa, w, sample_rows=None):
+    import torch
+    pool_h = oracle_pool(w) if w.n_blocks < 200_000 else None
+    if pool_h is None:
+        pool = gpu_pool(qsa, w)
+        pool_h = bf16_host(pool)
+    else:
+        pool = bf16_dev(pool_h)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.indexer_select(bf16_dev(w.q), pool, to_dev(w.req_row_start), to_dev(w.row_len),
+                             to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req,
+                             k_blk=w.k_blk, want_blocks=True, want_pos=True, scores_out=scores)
+    s = scores.cpu().numpy()
+    rows = np.arange(w.n_rows) if sample_rows is None else sample_rows
+    # scores against the oracle (on the same keys)
+    rr = w.row_req()
+    for t in rows:
+        r = int(rr[t])
+        nb = int(w.row_len[t]) // 4
+        sub_rrs = np.array([0, 1], np.int32)
+        want = oracle.index_scores(w.q[t:t + 1], pool_h, sub_rrs, w.row_len[t:t + 1],
+                                   w.page_table[r:r + 1], w.page_size, max(1, nb))
+        tol = score_tolerance(w.q[t:t + 1], pool_h, sub_rrs, w.row_len[t:t + 1],
+                              w.page_table[r:r + 1], w.page_size, max(1, nb))
+        err = np.abs(s[t, :nb].astype(np.float64) - want[0, :nb])
+        assert (err <= tol[0, :nb]).all(), (t, float(err.max()))
+    # selection / expansion / slots bit-exact on the GPU's own scores
+    sel_ref, _ = oracle.topk(s, w.k_blk, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+    return out
+
+
+@pytest.mark.parametrize("name,rows,P", SMALL_DECODE)
+def test_fused_parity_small(qsa, name, rows, P):
+    check_fused(qsa, decode_workload(51, rows, page_size=P, k_blk=64))
+
+
+def test_fused_parity_padding_and_pending(qsa):
+    """Rows with fewer visible blocks than k (padding), L mod 4 = 0..3, L < 4."""
+    w = decode_workload(52, [[1, 2, 3, 4, 5, 6, 7], [2047, 2048, 2049, 2050, 2051]], page_size=64,
+                        k_blk=512)
+    out = check_fused(qsa, w)
+    slots = out["slots"].cpu().numpy()
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        n_out = 4 * min(nb, 512) + int(w.row_len[t]) % 4
+        assert (slots[t, n_out:] == -1).all() and (slots[t, :n_out] >= 0).all()
+
+
+def test_fused_parity_c1_decode(qsa):
+    check_fused(qsa, c1_decode(0))
+
+
+def test_fused_parity_c2_verify(qsa):
+    check_fused(qsa, c2_verify(0))
+
+
+def test_fused_parity_c3_batched_sampled(qsa):
+    w = c3_batched(0)
+    check_fused(qsa, w, sample_rows=np.arange(0, w.n_rows, 4))
+
+
+def test_fused_workspace_path_matches_scores_out_path(qsa):
+    """Scores kept in the caller's workspace give the same slots."""
+    w = c2_verify(1)
+    pool = gpu_pool(qsa, w)
+    args = (bf16_dev(w.q), pool, to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table),
+            w.page_size, w.max_len, w.max_rows_per_req)
+    import torch
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    a = qsa.indexer_select(*args, k_blk=512, scores_out=torch.empty((w.n_rows, ld), device="cuda"))
+    b = qsa.indexer_select(*args, k_blk=512)
+    assert torch.equal(a["slots"], b["slots"])
