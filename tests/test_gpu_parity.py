@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
-Bars: compressed keys within 1 BF16 ulp (FP32 vs FP64 normalisation and
-rotation), scores within 2e-5 * (1/sqrt(128)) * sum|q k| + 1e-6 of the FP64
+Bars: compressed keys within 1 BF16 ulp plus 2^-20 absolute, with more than
+99% of elements bit-identical (FP32 vs FP64 normalisation and rotation), scores within 2e-5 * (1/sqrt(128)) * sum|q k| + 1e-6 of the FP64
 oracle (FP32 accumulation of exact BF16 products), and selection, expansion
 and slot translation bit-exact when both sides see the same FP32 scores.
 """
@@ -54,15 +54,23 @@ SMALL_DECODE = [
 ]
 
 
+def key_tolerance(a, b):
+    """Compressed-key bound: one BF16 ulp of the larger magnitude plus 2^-20
+    absolute.  The GPU normalises and rotates in FP32 (absolute error a few
+    2^-24 for unit vectors); where u*cos - v*sin nearly cancels, that error is
+    larger than an ulp of the tiny result, so a pure ulp bound cannot hold."""
+    m = np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(m)) - 7) + 2.0 ** -20
+
+
 @pytest.mark.parametrize("name,rows,P", SMALL_DECODE)
 def test_compress_parity(qsa, name, rows, P):
     w = decode_workload(21, rows, page_size=P, k_blk=64)
     want = oracle_pool(w)
     got = bf16_host(gpu_pool(qsa, w))
     a, b = oracle.bf16_to_float(got), oracle.bf16_to_float(want)
-    ulp = np.maximum(np.abs(b), 2.0 ** -126)
-    ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
-    assert (np.abs(a - b) <= ulp).all()
+    bad = np.abs(a - b) > key_tolerance(a, b)
+    assert not bad.any(), (np.argwhere(bad)[:5], a[bad][:5], b[bad][:5])
     assert (got == want).mean() > 0.99
 
 
@@ -77,7 +85,7 @@ def test_compress_parity_long_positions_sampled(qsa):
         row = oracle.pool_row(w.page_table[r], b, w.page_size)
         want = oracle.compress_block(w.raw_keys[4 * i: 4 * i + 4], 4 * b, w.rope_base)
         a, e = oracle.bf16_to_float(got[row]), oracle.bf16_to_float(want)
-        assert (np.abs(a - e) <= 2.0 ** (np.floor(np.log2(np.maximum(np.abs(e), 2.0 ** -126))) - 7)).all()
+        assert (np.abs(a - e) <= key_tolerance(a, e)).all(), (i, a, e)
 
 
 # ----------------------------------------------------------------- scores
