@@ -201,6 +201,45 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
                               int64_t ld_scores, void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/* ---------------------------------------------------------------------
+ * The fused decode path for callers that cannot allocate device memory.
+ * (Library addition with no counterpart in the source pages.)
+ *
+ * Who needs it: code that must not call cudaMalloc at the point where the
+ * indexer runs -- for example a serving step being recorded into a CUDA
+ * graph, an engine whose memory planner hands out every byte up front, or a
+ * plugin living inside another framework that gives it no allocator.  Such
+ * callers cannot size and pass the workspace of qsa_indexer_select, so this
+ * call keeps the FP32 scores in a fixed scratch array that is part of the
+ * library itself: QSA_NOALLOC_SCRATCH_BYTES bytes of device memory, held on
+ * every GPU that loads the library until the process exits.
+ *
+ * Arguments and results are those of qsa_indexer_select without scores_out
+ * and the workspace; the caller still passes (and owns) all inputs and
+ * outputs.  The call allocates and frees nothing.
+ *
+ *  - Limit: n_rows * round_up(max_len/4, 4) * 4 bytes of scores must fit in
+ *    QSA_NOALLOC_SCRATCH_BYTES; larger calls return QSA_ERR_UNSUPPORTED and
+ *    enqueue nothing.
+ *  - Set-up: the first call on each device looks up the scratch array's
+ *    device address (cudaGetSymbolAddress) with that device current; make
+ *    that first call outside any stream capture.
+ *  - Sharing: all calls in the process share the one array per device, and
+ *    it keeps whatever the previous call left in it.  Nothing needs to start
+ *    at zero (every score the selection reads is written first by the same
+ *    call), but two calls whose work overlaps on the GPU -- on different
+ *    streams, or from different threads -- race on the array.  Serialise
+ *    them (one stream, or events).
+ * ------------------------------------------------------------------- */
+#define QSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+qsa_status qsa_indexer_select_noalloc(const void* q, const void* pool, int64_t pool_rows,
+                                      int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                      const int32_t* row_len, int32_t max_len,
+                                      int32_t max_rows_per_req, const int32_t* page_table,
+                                      int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                      int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

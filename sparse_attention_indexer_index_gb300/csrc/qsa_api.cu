@@ -332,3 +332,89 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// qsa_indexer_select_noalloc: the fused path with its score scratch in a
+// library-owned device array instead of a caller workspace, for callers that
+// may not allocate device memory (graph capture, pre-planned memory, plugins
+// without an allocator).  See include/qsa.h for the contract.
+// ---------------------------------------------------------------------------
+namespace {
+
+// The scratch array itself.  Host code must not take its address directly
+// (on the host the name is only a stand-in for the device symbol); the
+// device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QSA_NOALLOC_SCRATCH_BYTES];
+
+float* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device, with that device current).
+qsa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return QSA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" qsa_status qsa_indexer_select_noalloc(
+    const void* q, const void* pool, int64_t pool_rows, int32_t n_req, const int32_t* req_row_start,
+    int32_t n_rows, const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+    const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+    int32_t* out_pos, int32_t* out_slots, void* stream) {
+  (void)max_rows_per_req;
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+  if (!q || !pool || !out_slots || pool_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool)) return QSA_ERR_INVALID_ARG;
+  const int32_t nb_max = max_len / kBlock;
+  const int64_t ld = (nb_max + 3) & ~3;
+  if ((uint64_t)n_rows * (uint64_t)ld * sizeof(float) > (uint64_t)QSA_NOALLOC_SCRATCH_BYTES)
+    return QSA_ERR_UNSUPPORTED;  // the scores do not fit in the fixed scratch array
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  float* scores = nullptr;
+  if (qsa_status st = noalloc_scratch(&scores)) return st;
+  int cs = 1, seg = 4;
+  if (!plan_select(n_rows, nb_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
+              pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
+              page_size, scores, ld, 0, 1};
+  if (qsa_status e = launch_scores(s, st)) return e;
+
+  SelectArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.n_rows = n_rows;
+  a.k = k_blk;
+  a.n_max = nb_max;
+  a.seg = seg;
+  a.vec_ok = 1;  // the array is 256-byte aligned and ld is a multiple of 4
+  a.wait_primary = 1;
+  a.n_req = n_req;
+  a.req_row_start = req_row_start;
+  a.row_len = row_len;
+  a.out_idx = out_blocks;
+  a.out_pos = out_pos;
+  a.out_xslots = out_slots;
+  a.page_table = page_table;
+  a.ld_pt = ld_pt;
+  a.page_size = page_size;
+  return launch_select<kModeQsa>(a, cs, nb_max > 0, st);
+}
