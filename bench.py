@@ -12,6 +12,9 @@ events on the launching stream.  W untimed warm-up steps come first.  Under
 torchrun every rank runs an independent replica (the path shards by request
 with no exchange), and the time is the maximum over ranks.
 
+--workload picks another decode workload for the primary line (profiling
+runs use it); the default is the 6-row verify step above.
+
 --impl reference times the CPU oracle (plain C, FP64) on the host cores, on a
 bounded sample of the same workload.
 """
@@ -154,13 +157,29 @@ class Gpu:
     def bf16(self, a):
         return self.h2d(np.ascontiguousarray(a, np.uint16).view(np.int16), self.torch.bfloat16)
 
-    def timed(self, fn, iters, warmup, flush=True):
-        """Per-iteration CUDA-event times (ms) with an L2 flush before each."""
+    def capture(self, fn):
+        """Record fn's launches into a CUDA graph (after fn has run eagerly, so
+        every one-time set-up is done outside the capture)."""
+        torch = self.torch
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        torch.cuda.synchronize()
+        return graph.replay
+
+    def timed(self, fn, iters, warmup, flush=True, graph=True):
+        """Per-iteration CUDA-event times (ms) with an L2 flush before each.
+        With graph=True the step is replayed from a CUDA graph, so the events
+        see device time rather than Python launch overhead."""
         torch = self.torch
         for _ in range(warmup):
             if flush:
                 self.flush()
             fn()
+        torch.cuda.synchronize()
+        run = self.capture(fn) if graph else fn
+        for _ in range(2):
+            run()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(iters)]
@@ -168,7 +187,7 @@ class Gpu:
             if flush:
                 self.flush()
             s.record(self.stream)
-            fn()
+            run()
             e.record(self.stream)
         torch.cuda.synchronize()
         return [s.elapsed_time(e) for s, e in ev]
@@ -268,7 +287,7 @@ def e2e_decode(g: Gpu, st, iters, warmup):
                              workspace=st["ws"], out_slots=st["slots"])
         out_h.copy_(st["slots"], non_blocking=True)
 
-    times = g.timed(step, iters, warmup)
+    times = g.timed(step, iters, warmup, graph=False)
     return times, h2d, d2h
 
 
@@ -341,8 +360,8 @@ def cpu_oracle_rate(w, budget_s=10.0):
         if el >= budget_s:
             break
     return {"value": rows / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full verify steps ({w.n_rows} rows each, L=80,000) of the same workload "
-                      f"in {el:.1f} s on one host core; key compression excluded"}
+            "sample": f"{n} full steps of {w.name} ({w.n_rows} rows each) in {el:.1f} s on one "
+                      f"host core; key compression excluded"}
 
 
 def run_reference(args):
@@ -378,14 +397,26 @@ def run_reference(args):
     return 0
 
 
+WORKLOADS = {
+    "c2": lambda seed: (c2_verify(seed), 2),
+    "c1": lambda seed: (c1_decode(seed), 1),
+    "c2x32": lambda seed: (c2_batched(seed), 2),
+    "c3": lambda seed: (c3_batched(seed), 1),
+}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS),
+                    help="decode workload of the primary line (default: the 6-row verify step)")
     ap.add_argument("--no-variants", action="store_true", help="primary workload only")
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time (0: skip)")
+    ap.add_argument("--clock-window", type=float, default=1.5,
+                    help="seconds of untimed steps run under the clock sampler before timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -405,26 +436,34 @@ def main():
     peaks = load_peaks()
     g = Gpu(device)
 
-    # ---- primary: decode verify step, batch 1, 6 rows, L = 80,000 ----------
-    w = c2_verify(seed=rank)
-    st = setup_decode(g, w, new_blocks=2)
+    # ---- primary: one decode step of the chosen workload ------------------
+    w, new_blocks = WORKLOADS[args.workload](rank)
+    st = setup_decode(g, w, new_blocks=new_blocks)
     for _ in range(args.warmup):
         g.flush()
         decode_step(g, st)
-    barrier(ws)
     torch.cuda.synchronize()
+    replay = g.capture(lambda: decode_step(g, st))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
+        t_end = time.perf_counter() + args.clock_window
+        while time.perf_counter() < t_end:  # untimed: clocks settle, sampler starts
+            for _ in range(20):
+                g.flush()
+                replay()
+            torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for s, e in ev:
             g.flush()
             s.record(g.stream)
-            decode_step(g, st)
+            replay()
             e.record(g.stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
-    barrier(ws)
+        barrier(ws)
     step_ms = [s.elapsed_time(e) for s, e in ev]
     local_ms = statistics.mean(step_ms)
     ms = aggregate_time(local_ms, ws, device)
@@ -439,27 +478,32 @@ def main():
     step_bytes = by["keys"] + by["q"] + by["page_table"] + by["slots"]
 
     # ---- end to end through the API with host buffers ---------------------
-    t_e2e, h2d, d2h = e2e_decode(g, st, args.steps, args.warmup)
+    t_e2e, h2d, d2h = e2e_decode(g, st, min(args.steps, 100), args.warmup)
     e2e_ms = aggregate_time(statistics.mean(t_e2e), ws, device)
 
     out = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.n_rows, "L": 80000, "k_blk": 512, "page_size": 64,
-                   "step": "compress 2 new blocks + fused score/top-512/expand/slots",
+        "config": {"workload": w.name, "rows": w.n_rows, "requests": w.n_req,
+                   "L": int(w.max_len), "k_blk": w.k_blk, "page_size": w.page_size,
+                   "step": f"compress {new_blocks} new block(s) per request + fused "
+                           "score/top-512/expand/slots, replayed from a CUDA graph",
                    "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": 1e3 * ms,
+        "us_per_step_median": 1e3 * statistics.median(step_ms),
         "step_alg_bytes": step_bytes,
         "step_alg_GBps": step_bytes / (ms * 1e-3) / 1e9,
+        "step_frac_hbm": step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "kernel": "score_decode_kernel", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": None, "alg_bytes_per_launch": score_bytes,
                      "us_per_launch": 1e3 * score_ms,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst)"},
         "e2e": {"value": ws * w.n_rows / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": "eager Python API calls per step, pinned host buffers, no graph"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
@@ -477,7 +521,8 @@ def main():
             "c5_prefill_4096rows": bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
         }
     if rank == 0:
-        out["cpu_baseline"] = cpu_oracle_rate(w, args.cpu_budget)
+        if args.cpu_budget > 0:
+            out["cpu_baseline"] = cpu_oracle_rate(w, args.cpu_budget)
         print(json.dumps(out))
     if ws > 1:
         import torch.distributed as dist

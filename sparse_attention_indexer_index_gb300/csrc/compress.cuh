@@ -16,9 +16,12 @@
 //
 // Angle: p * base^(-2i/128) grows to ~1.3e5 rad at 131k tokens, so it is
 // reduced exactly: t_i = base^(-2i/128) / (2 pi) is held as a 64-bit binary
-// fraction of a turn (computed once per thread in FP64), p * t_i mod 1 is a
-// wrapping 64-bit integer product, and the top 32 bits give the angle in
-// units of pi for sincospif.  Error < 3e-7 rad for p < 2^31.
+// fraction of a turn, p * t_i mod 1 is a wrapping 64-bit integer product, and
+// the top 32 bits give the angle in units of pi for sincospif.  Error
+// < 3e-7 rad for p < 2^31.  The 64 fractions depend only on the RoPE base;
+// the launching host code derives them once per base in FP64 and passes them
+// as a kernel parameter (FP64 arithmetic is slow on this GPU: one pow per
+// thread cost ~8 us of latency).
 #pragma once
 #include "common.cuh"
 
@@ -36,6 +39,11 @@ struct CompressArgs {
   double rope_base;
   __nv_bfloat16* pool;        // [pool_rows][128]
   int64_t pool_rows;
+};
+
+// Rotation frequency i as a 64-bit fraction of a turn: base^(-2i/128)/(2 pi).
+struct RopeTurns {
+  uint64_t frac[kDim / 2];
 };
 
 constexpr int kCompressThreads = 256;
@@ -57,17 +65,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(kCompressThreads)
-compress_keys_kernel(CompressArgs a) {
+compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
   const int lane8 = threadIdx.x & (kCompressLanes - 1);
-  // Rotation frequencies of this lane's 8 pairs, as 64-bit turn fractions.
   uint64_t turn_frac[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int i = kCompressLanes * lane8 + e;
-    const double inv_freq = pow(a.rope_base, -2.0 * (double)i / (double)kDim);
-    const double turns = inv_freq * 0.15915494309189533577;  // 1 / (2 pi)
-    turn_frac[e] = __double2ull_rn(turns * 18446744073709551616.0);  // * 2^64
-  }
+  for (int e = 0; e < 8; ++e) turn_frac[e] = turns.frac[kCompressLanes * lane8 + e];
 
   const int64_t groups_per_cta = kCompressThreads / kCompressLanes;
   const int64_t stride = (int64_t)gridDim.x * groups_per_cta;

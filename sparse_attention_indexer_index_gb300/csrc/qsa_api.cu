@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/qsa.h"
@@ -20,7 +21,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 // Largest row slice one CTA keeps in shared memory (keys), and the largest
 // cluster used for one row.
-constexpr int kSegCap = 48 * 1024;
+constexpr int kSegCap = 44 * 1024;
 constexpr int kMaxCluster = 8;
 
 struct DeviceInfo {
@@ -40,11 +41,13 @@ qsa_status device_info(DeviceInfo** out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QSA_ERR_CUDA;
-    const int smem = (int)(sizeof(SelShared) + (size_t)kSegCap * sizeof(uint32_t));
+    const int smem = (int)(kSelKeysOffset + (size_t)kSegCap * sizeof(uint32_t));
     if (cudaFuncSetAttribute(select_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(select_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScoreSmem) != cudaSuccess)
       return QSA_ERR_CUDA;
     d.ready = true;
   }
@@ -54,6 +57,30 @@ qsa_status device_info(DeviceInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// RoPE turn fractions for one base, cached (the last few bases used).
+// frac[i] = round(2^64 * base^(-2i/128) / (2 pi)).
+std::mutex g_rope_mu;
+struct RopeCacheEntry {
+  double base = 0.0;
+  RopeTurns turns;
+};
+RopeCacheEntry g_rope_cache[4];
+int g_rope_next = 0;
+
+RopeTurns rope_turns(double base) {
+  std::lock_guard<std::mutex> lk(g_rope_mu);
+  for (const RopeCacheEntry& e : g_rope_cache)
+    if (e.base == base) return e.turns;
+  RopeCacheEntry& e = g_rope_cache[g_rope_next];
+  g_rope_next = (g_rope_next + 1) % 4;
+  e.base = base;
+  for (int i = 0; i < kDim / 2; ++i) {
+    const double turns = std::pow(base, -2.0 * (double)i / (double)kDim) * 0.15915494309189533577;
+    e.turns.frac[i] = (uint64_t)std::llround(std::ldexp(turns, 62)) << 2;  // turns < 1/4
+  }
+  return e.turns;
+}
 
 qsa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
@@ -81,7 +108,7 @@ qsa_status launch_select(const SelectArgs& a, int cs, bool pdl, cudaStream_t str
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_rows * (unsigned)cs, 1, 1);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(SelShared) + (size_t)a.seg * sizeof(uint32_t);
+  cfg.dynamicSmemBytes = kSelKeysOffset + (size_t)a.seg * sizeof(uint32_t);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -120,12 +147,18 @@ qsa_status check_paging(const int32_t* page_table, int64_t ld_pt, int32_t page_s
   return QSA_OK;
 }
 
-qsa_status launch_scores(const ScoreArgs& s, cudaStream_t stream) {
+// Persistent scorer: tile slots (request, 64-block tile) strided over at most
+// two CTAs per SM.
+qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream) {
   const int64_t nb_max = s.max_len / kBlock;
   const int64_t cols = std::max<int64_t>(nb_max, s.n_fill);
   if (s.n_req == 0 || cols == 0) return QSA_OK;
-  dim3 grid((unsigned)((cols + kScoreTile - 1) / kScoreTile), (unsigned)s.n_req, 1);
-  score_decode_kernel<<<grid, kScoreThreads, 0, stream>>>(s);
+  const int64_t tpr = (cols + kScoreTile - 1) / kScoreTile;
+  const int64_t slots = tpr * s.n_req;
+  if (slots > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  s.tiles_per_req = (int32_t)tpr;
+  const int64_t grid = std::min<int64_t>(slots, 2 * (int64_t)sm_count);
+  score_decode_kernel<<<(unsigned)grid, kScoreThreads, kScoreSmem, stream>>>(s);
   return launch_status();
 }
 
@@ -184,7 +217,8 @@ qsa_status qsa_compress_keys(const void* raw, const int32_t* block_req, const in
                  pool_rows};
   const int64_t per_cta = kCompressThreads / kCompressLanes;
   const int64_t grid = std::min<int64_t>((n_blocks + per_cta - 1) / per_cta, (int64_t)d->sm_count * 8);
-  compress_keys_kernel<<<(unsigned)grid, kCompressThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  compress_keys_kernel<<<(unsigned)grid, kCompressThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      a, rope_turns(rope_base));
   return launch_status();
 }
 
@@ -204,8 +238,8 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
   if (qsa_status st = device_info(&d)) return st;
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld_scores, n_fill, 0};
-  return launch_scores(s, static_cast<cudaStream_t>(stream));
+              page_size, scores, ld_scores, n_fill, 0, 0};
+  return launch_scores(s, d->sm_count, static_cast<cudaStream_t>(stream));
 }
 
 size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k) {
@@ -307,8 +341,8 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1};
-  if (qsa_status e = launch_scores(s, st)) return e;
+              page_size, scores, ld, 0, 1, 0};
+  if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
 
   SelectArgs a{};
   a.scores = scores;
@@ -395,8 +429,8 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1};
-  if (qsa_status e = launch_scores(s, st)) return e;
+              page_size, scores, ld, 0, 1, 0};
+  if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
 
   SelectArgs a{};
   a.scores = scores;

@@ -15,17 +15,22 @@
 // result is returned in ascending index order with -1 only as tail padding.
 //
 // Design (GB300): one row is owned by a thread-block cluster of CS CTAs
-// (CS = 1, 2, 4, 8, 16).  Each CTA reads its contiguous slice of the row from
-// global memory ONCE, converts it to order-preserving u32 keys in shared
-// memory and builds a histogram of the top 11 key bits.  The CTAs add their
-// histograms over distributed shared memory, every CTA finds the same
-// threshold bin, and two more passes (11 and 10 bits) over the on-chip keys
-// refine it to the exact k-th key, stopping early when the bin holds exactly
-// the remaining count.  Emission walks the slice in index order: counts of
-// keys above / equal to the threshold are prefix-summed over warps, CTAs
-// and the cluster, so every selected index lands directly at its ascending
-// output position and equal keys at the boundary are taken lowest-index
-// first.  No sort, no global scratch, no spin-waits (cluster barriers only).
+// (CS = 1, 2, 4, 8).  Each CTA pulls its contiguous slice of the row into
+// shared memory ONCE with a bulk asynchronous copy (TMA engine), converts it
+// in place to order-preserving u32 keys and builds a histogram of the top 11
+// key bits.  Cluster histograms are summed in two levels over distributed
+// shared memory: CTA c adds everyone's counts for its 1/CS share of the bins
+// with 16-byte remote loads, then every CTA reads the CS share totals and the
+// one share that holds the k-th key -- a few hundred remote transactions per
+// CTA and pass.  Two more passes (11 and 10 bits) over the on-chip keys refine
+// the bin to the exact k-th key, stopping early when a bin holds exactly the
+// remaining count.  Emission walks the slice in index order; warp ballots and
+// warp/CTA/cluster prefix counts of keys above and equal to the threshold put
+// every selected index straight at its ascending output position, equal keys
+// at the boundary lowest-index first.  The page-table entries of the slice
+// are staged in shared memory before the kernel waits for its input.  No
+// sort, no global scratch; every wait is a hardware cluster barrier or a
+// time-bounded mbarrier wait.
 #pragma once
 #include "common.cuh"
 
@@ -34,6 +39,8 @@ namespace qsa {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kHistBins = 2048;
+constexpr int kMaxClusterSel = 8;    // largest cluster used for one row
+constexpr int kSelPtCap = 2048;      // page-table entries staged per CTA
 
 enum SelectMode { kModeTopk = 0, kModeQsa = 1 };
 
@@ -94,54 +101,44 @@ __device__ __forceinline__ int2 block_scan2(int a, int b, int2* s_warp, int2& to
   return make_int2(base.x + x - a, base.y + y - b);
 }
 
-// Warp exclusive scan of one counter; also returns the warp total.
-__device__ __forceinline__ int warp_excl_scan(int v, int& total) {
-  const int lane = threadIdx.x & 31;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  total = __shfl_sync(0xffffffffu, x, 31);
-  return x - v;
+struct SelShared {
+  uint32_t hist[2][kHistBins];           // local histograms, double-buffered
+  uint32_t stage[kHistBins];             // remote share rows being summed
+  uint32_t red[2][kHistBins / 2];        // this CTA's reduced share (CS >= 2)
+  uint32_t share_tot[2];                 // total of this CTA's share
+  int32_t pt[kSelPtCap];                 // page-table entries of the slice
+  int2 warp_scan[kSelWarps + 1];
+  int2 cta_counts;                       // (above, equal) counts, read by peers
+  int bin_info[4];                       // found bin, count above it, its count, owner
+  uint64_t load_bar;                     // completion of the slice's bulk copy
+};
+// The row slice (u32 keys) follows the fixed part, 128-byte aligned.
+constexpr size_t kSelKeysOffset = (sizeof(SelShared) + 127) & ~size_t(127);
+
+__device__ __forceinline__ int32_t slot_lookup(const SelectArgs& a, const SelShared& sh,
+                                               const int32_t* pt_row, int pt0, int pt_n,
+                                               int64_t pos) {
+  const int64_t page_idx = pos / a.page_size;
+  const int32_t off = (int32_t)(pos - page_idx * a.page_size);
+  if (page_idx >= pt0 && page_idx < pt0 + pt_n) return sh.pt[page_idx - pt0] * a.page_size + off;
+  if (page_idx < a.ld_pt) return __ldg(pt_row + page_idx) * a.page_size + off;
+  raise_fault(kFaultIndex);
+  return -1;
 }
 
-struct SelShared {
-  uint32_t hist[2][kHistBins];  // double-buffered (peers read the other one)
-  int2 warp_scan[kSelWarps + 1];
-  int2 cta_counts;              // this CTA's (above, equal) counts, read by peers
-  int bin_info[4];              // found bin, count above it, its count
-};
-
 template <int kMode>
-__device__ __forceinline__ void emit_one(const SelectArgs& a, int t, int req, int64_t idx, int pos) {
+__device__ __forceinline__ void emit_one(const SelectArgs& a, const SelShared& sh, int t,
+                                         const int32_t* pt_row, int pt0, int pt_n, int64_t idx,
+                                         int pos) {
   if (kMode == kModeTopk) {
     a.out_idx[(int64_t)t * a.k + pos] = (int32_t)idx;
-    if (a.out_slots != nullptr) {
-      const int tr = a.row_req ? __ldg(a.row_req + t) : t;
-      const int64_t page_idx = idx / a.page_size;
-      int32_t slot = -1;
-      if (page_idx < a.ld_pt && tr >= 0) {
-        slot = __ldg(a.page_table + (int64_t)tr * a.ld_pt + page_idx) * a.page_size +
-               (int32_t)(idx - page_idx * a.page_size);
-      } else {
-        raise_fault(kFaultIndex);
-      }
-      a.out_slots[(int64_t)t * a.k + pos] = slot;
-    }
+    if (a.out_slots != nullptr)
+      a.out_slots[(int64_t)t * a.k + pos] = slot_lookup(a, sh, pt_row, pt0, pt_n, idx);
   } else {
     if (a.out_idx != nullptr) a.out_idx[(int64_t)t * a.k + pos] = (int32_t)idx;
     const int64_t width = (int64_t)kBlock * a.k + (kBlock - 1);
-    const int64_t p0 = kBlock * idx;  // first token of block idx
-    const int64_t page_idx = p0 / a.page_size;
-    int32_t base = -1;
-    if (page_idx < a.ld_pt) {
-      base = __ldg(a.page_table + (int64_t)req * a.ld_pt + page_idx) * a.page_size +
-             (int32_t)(p0 - page_idx * a.page_size);
-    } else {
-      raise_fault(kFaultIndex);
-    }
+    const int64_t p0 = kBlock * idx;  // first token of block idx (same page as p0+3)
+    const int32_t base = slot_lookup(a, sh, pt_row, pt0, pt_n, p0);
     // Rows are 4k+3 entries wide, so these stores are not 16-byte aligned.
     int32_t* xs = a.out_xslots + (int64_t)t * width + kBlock * pos;
 #pragma unroll
@@ -157,7 +154,8 @@ __device__ __forceinline__ void emit_one(const SelectArgs& a, int t, int req, in
 // Tail of a row once m = min(k, n) entries are emitted: -1 padding (token
 // mode) or pending tokens then -1 (QSA mode).  Run by one CTA of the cluster.
 template <int kMode>
-__device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, int req, int m, int L) {
+__device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, const int32_t* pt_row, int m,
+                                          int L) {
   if (kMode == kModeTopk) {
     for (int j = m + threadIdx.x; j < a.k; j += kSelThreads) {
       a.out_idx[(int64_t)t * a.k + j] = -1;
@@ -176,8 +174,7 @@ __device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, int req, i
         pos = kBlock * nb + i;
         const int page_idx = pos / a.page_size;
         if (page_idx < a.ld_pt) {
-          slot = __ldg(a.page_table + (int64_t)req * a.ld_pt + page_idx) * a.page_size +
-                 (pos - page_idx * a.page_size);
+          slot = __ldg(pt_row + page_idx) * a.page_size + (pos - page_idx * a.page_size);
         } else {
           raise_fault(kFaultIndex);
         }
@@ -188,28 +185,68 @@ __device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, int req, i
   }
 }
 
+// Among `nb` counts listed in DESCENDING bin order (read through get(d)),
+// with `above_base` keys above the first, find the one holding the k_rem-th
+// key: sh.bin_info = (its descending index, keys above it, its count).
+template <typename Get>
+__device__ __forceinline__ void find_bin(SelShared& sh, int nb, int above_base, int k_rem,
+                                         Get get) {
+  const int per = (nb + kSelThreads - 1) / kSelThreads;  // <= 4
+  uint32_t c[4];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int d = threadIdx.x * per + j;
+    c[j] = (j < per && d < nb) ? get(d) : 0u;
+    sum += (int)c[j];
+  }
+  int2 tot;
+  int above = above_base + block_scan2(sum, 0, sh.warp_scan, tot).x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < per && above < k_rem && k_rem <= above + (int)c[j]) {
+      sh.bin_info[0] = threadIdx.x * per + j;
+      sh.bin_info[1] = above;
+      sh.bin_info[2] = (int)c[j];
+    }
+    above += (int)c[j];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t cluster_addr) {
+  uint4 x;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+               : "r"(cluster_addr));
+  return x;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(SelectArgs a) {
-  extern __shared__ __align__(16) unsigned char sel_smem_raw[];
+  extern __shared__ __align__(128) unsigned char sel_smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(sel_smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem_raw + sizeof(SelShared));
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem_raw + kSelKeysOffset);
 
   const uint32_t cs = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int t = blockIdx.x / cs;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  if (a.wait_primary) pdl_wait_primary();
-
-  // Candidates of this row.
-  int n, req = 0, L = 0;
+  // ---- row metadata and the slice's page-table entries: inputs that do
+  // not come from the producing grid, so they are read before waiting ------
+  int n, L = 0;
+  const int32_t* pt_row = nullptr;
   if (kMode == kModeTopk) {
     n = a.n_valid ? __ldg(a.n_valid + t) : a.n_max;
+    if (a.out_slots != nullptr)
+      pt_row = a.page_table + (int64_t)(a.row_req ? __ldg(a.row_req + t) : t) * a.ld_pt;
   } else {
-    req = row_request(a.req_row_start, a.n_req, t);
+    const int req = row_request(a.req_row_start, a.n_req, t);
     L = __ldg(a.row_len + t);
     n = L / kBlock;
+    pt_row = a.page_table + (int64_t)req * a.ld_pt;
   }
   if (n < 0 || n > a.n_max) {  // bad length: emit an empty row
     if (threadIdx.x == 0 && rank == 0) raise_fault(kFaultGrouping);
@@ -219,43 +256,58 @@ select_kernel(SelectArgs a) {
   const int lo = (int)rank * a.seg;
   const int hi = min(n, lo + a.seg);
   const int len = max(0, hi - lo);
+  // pages covering the positions of candidates [lo, hi) (QSA: 4 tokens each)
+  const int64_t scale = kMode == kModeQsa ? kBlock : 1;
+  int pt0 = 0, pt_n = 0;
+  if (pt_row != nullptr && len > 0) {
+    pt0 = (int)((scale * lo) / a.page_size);
+    const int pt1 = (int)((scale * hi - 1) / a.page_size) + 1;
+    int64_t np = min(pt1 - pt0, kSelPtCap);
+    if (np > a.ld_pt - pt0) np = a.ld_pt - pt0;
+    pt_n = np > 0 ? (int)np : 0;
+    for (int i = threadIdx.x; i < pt_n; i += kSelThreads) sh.pt[i] = __ldg(pt_row + pt0 + i);
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.load_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (a.wait_primary) pdl_wait_primary();
   const float* row = a.scores + (int64_t)t * a.ld;
 
   if (n <= a.k) {
     // Everything is selected: index i goes to output position i.
-    for (int i = lo + threadIdx.x; i < hi; i += kSelThreads) emit_one<kMode>(a, t, req, i, i);
-    if (rank == 0) emit_tail<kMode>(a, t, req, n, L);
+    for (int i = lo + threadIdx.x; i < hi; i += kSelThreads)
+      emit_one<kMode>(a, sh, t, pt_row, pt0, pt_n, i, i);
+    if (rank == 0) emit_tail<kMode>(a, t, pt_row, n, L);
     return;  // no shared memory was shared, so CTAs may leave independently
   }
 
-  // ---- load the slice once, build the first histogram (top 11 bits) -----
+  // ---- load the slice once, convert in place, first histogram ----------
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh.hist[0][i] = 0;
+  const int len_vec = a.vec_ok ? (len & ~3) : 0;  // bulk-copied part
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&sh.load_bar, (uint32_t)len_vec * 4u);
+    for (int off = 0; off < len_vec; off += 8192)  // 32 KB pieces
+      bulk_copy_g2s(keys + off, row + lo + off, (uint32_t)min(8192, len_vec - off) * 4u, &sh.load_bar);
+  }
+  for (int i = len_vec + threadIdx.x; i < len; i += kSelThreads) keys[i] = __float_as_uint(row[lo + i]);
+  // A copy that never lands latches the fault and the row is garbage, but the
+  // CTA keeps to the cluster's barrier sequence (leaving early could strand
+  // its peers at a cluster barrier).
+  if (!mbar_wait_bounded(&sh.load_bar, 0) && threadIdx.x == 0) raise_fault(kFaultWait);
   __syncthreads();
-  if (a.vec_ok) {
-    const int len4 = (len + 3) & ~3;
-    for (int i = 4 * threadIdx.x; i < len4; i += 4 * kSelThreads) {
-      float4 v;
-      if (i + 3 < len) {
-        v = __ldg(reinterpret_cast<const float4*>(row + lo + i));
-      } else {
-        v.x = row[lo + i];
-        v.y = i + 1 < len ? row[lo + i + 1] : 0.f;
-        v.z = i + 2 < len ? row[lo + i + 2] : 0.f;
-        v.w = i + 3 < len ? row[lo + i + 3] : 0.f;
-      }
-      uint4 kq = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
-      *reinterpret_cast<uint4*>(keys + i) = kq;
-      atomicAdd(&sh.hist[0][kq.x >> 21], 1u);
-      if (i + 1 < len) atomicAdd(&sh.hist[0][kq.y >> 21], 1u);
-      if (i + 2 < len) atomicAdd(&sh.hist[0][kq.z >> 21], 1u);
-      if (i + 3 < len) atomicAdd(&sh.hist[0][kq.w >> 21], 1u);
-    }
-  } else {
-    for (int i = threadIdx.x; i < len; i += kSelThreads) {
-      const uint32_t kq = order_key(row[lo + i]);
-      keys[i] = kq;
-      atomicAdd(&sh.hist[0][kq >> 21], 1u);
-    }
+  const int len4 = (len + 3) & ~3;
+  for (int i = 4 * threadIdx.x; i < len4; i += 4 * kSelThreads) {
+    const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+    const uint4 kq = make_uint4(order_key(__uint_as_float(v.x)), order_key(__uint_as_float(v.y)),
+                                order_key(__uint_as_float(v.z)), order_key(__uint_as_float(v.w)));
+    *reinterpret_cast<uint4*>(keys + i) = kq;
+    atomicAdd(&sh.hist[0][kq.x >> 21], 1u);
+    if (i + 1 < len) atomicAdd(&sh.hist[0][kq.y >> 21], 1u);
+    if (i + 2 < len) atomicAdd(&sh.hist[0][kq.z >> 21], 1u);
+    if (i + 3 < len) atomicAdd(&sh.hist[0][kq.w >> 21], 1u);
   }
 
   // ---- radix refinement: 11 + 11 + 10 bits -------------------------------
@@ -271,40 +323,75 @@ select_kernel(SelectArgs a) {
       for (int i = threadIdx.x; i < nbins; i += kSelThreads) hist[i] = 0;
       __syncthreads();
       const uint32_t mask = (uint32_t)nbins - 1u;
-      for (int i = threadIdx.x; i < len; i += kSelThreads) {
-        const uint32_t kq = keys[i];
-        if ((kq >> shift) == prefix) atomicAdd(&hist[(kq >> nshift) & mask], 1u);
+      for (int i = 4 * threadIdx.x; i < len4; i += 4 * kSelThreads) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < len && (kk[e] >> shift) == prefix) atomicAdd(&hist[(kk[e] >> nshift) & mask], 1u);
       }
     }
-    // Sum the cluster's histograms; thread tid owns descending bins
-    // [tid*per, tid*per + per) counted from the top.
-    if (cs > 1) cluster_sync(); else __syncthreads();
-    const int per = nbins / kSelThreads;  // 4 or 2
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
-    int sum = 0;
-    for (int j = 0; j < per; ++j) {
-      const int bin = nbins - 1 - (threadIdx.x * per + j);
-      uint32_t v = hist[bin];
-      for (uint32_t p = 1; p < cs; ++p) v += ld_dsmem_u32(map_shared_rank(&hist[bin], (rank + p) % cs));
-      c[j] = v;
-      sum += (int)v;
-    }
-    int2 tot;
-    const int above0 = block_scan2(sum, 0, sh.warp_scan, tot).x;
-    int above = above0;
-    for (int j = 0; j < per; ++j) {
-      if (above < k_rem && k_rem <= above + (int)c[j]) {
-        sh.bin_info[0] = nbins - 1 - (threadIdx.x * per + j);
-        sh.bin_info[1] = above;
-        sh.bin_info[2] = (int)c[j];
+    int bin;
+    if (cs == 1) {
+      __syncthreads();
+      find_bin(sh, nbins, 0, k_rem, [&](int d) { return hist[nbins - 1 - d]; });
+      bin = nbins - 1 - sh.bin_info[0];
+    } else {
+      // Level 1: CTA `rank` sums every CTA's counts for its share of the
+      // bins -- descending positions [rank*S, rank*S + S), i.e. bins
+      // [nbins - (rank+1)*S, nbins - rank*S) -- with 16-byte remote loads.
+      const int S = nbins / (int)cs;
+      const int q4 = S / 4;
+      const int share_lo = nbins - ((int)rank + 1) * S;
+      uint32_t* red = sh.red[pass & 1];
+      cluster_sync();  // every local histogram of this pass is final
+      for (int i = threadIdx.x; i < q4 * (int)cs; i += kSelThreads) {
+        const int p = i / q4, v = i - p * q4;
+        const uint4 x = ld_dsmem_v4(map_shared_rank(&hist[share_lo + 4 * v], (uint32_t)p));
+        *reinterpret_cast<uint4*>(&sh.stage[p * S + 4 * v]) = x;
       }
-      above += (int)c[j];
+      __syncthreads();
+      int part = 0;
+      for (int b = threadIdx.x; b < S; b += kSelThreads) {
+        uint32_t v = 0;
+        for (int p = 0; p < (int)cs; ++p) v += sh.stage[p * S + b];
+        red[b] = v;
+        part += (int)v;
+      }
+      int2 tot;
+      block_scan2(part, 0, sh.warp_scan, tot);
+      if (threadIdx.x == 0) sh.share_tot[pass & 1] = (uint32_t)tot.x;
+      cluster_sync();  // every share is reduced
+      // Level 2: the share holding the k_rem-th key (shares in descending
+      // order belong to ranks 0, 1, ...), then the bin inside it.
+      if (warp == 0) {
+        uint32_t st = 0;
+        if (lane < (int)cs) st = ld_dsmem_u32(map_shared_rank(&sh.share_tot[pass & 1], (uint32_t)lane));
+        int incl = (int)st;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int excl = incl - (int)st;
+        if (lane < (int)cs && excl < k_rem && k_rem <= incl) {
+          sh.bin_info[3] = lane;
+          sh.bin_info[1] = excl;
+        }
+      }
+      __syncthreads();
+      const int owner = sh.bin_info[3];
+      const int above_share = sh.bin_info[1];
+      for (int v = threadIdx.x; v < q4; v += kSelThreads)
+        *reinterpret_cast<uint4*>(&sh.stage[4 * v]) = ld_dsmem_v4(map_shared_rank(&red[4 * v], (uint32_t)owner));
+      __syncthreads();
+      const int owner_lo = nbins - (owner + 1) * S;
+      find_bin(sh, S, above_share, k_rem, [&](int d) { return sh.stage[S - 1 - d]; });
+      bin = owner_lo + (S - 1 - sh.bin_info[0]);
     }
-    __syncthreads();
-    const uint32_t bin = (uint32_t)sh.bin_info[0];
     k_rem -= sh.bin_info[1];
     const int bin_count = sh.bin_info[2];
-    prefix = pass == 0 ? bin : ((prefix << bits) | bin);
+    prefix = pass == 0 ? (uint32_t)bin : ((prefix << bits) | (uint32_t)bin);
     shift = nshift;
     __syncthreads();
     if (bin_count == k_rem) break;  // the whole bin is selected
@@ -318,16 +405,20 @@ select_kernel(SelectArgs a) {
   const int w_lo = min(len, warp * piece);
   const int w_hi = min(len, w_lo + piece);
   int gt = 0, eq = 0;
-  for (int i = w_lo + lane; i < w_hi; i += 32) {
-    const uint32_t hb = keys[i] >> shift;
-    gt += hb > prefix;
-    eq += hb == prefix;
-  }
+  for (int i = w_lo + 4 * lane; i < w_hi; i += 128) {
+    const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    for (int e = 0; e < 4; ++e) {
+      if (i + e < w_hi) {
+        const uint32_t hb = kk[e] >> shift;
+        gt += hb > prefix;
+        eq += hb == prefix;
+      }
+    }
   }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
   // Warp bases inside the CTA (only lane 0's counts enter the scan).
   int2 cta_tot;
   int2 wbase = block_scan2(lane == 0 ? gt : 0, lane == 0 ? eq : 0, sh.warp_scan, cta_tot);
@@ -338,52 +429,71 @@ select_kernel(SelectArgs a) {
   if (cs > 1) {
     if (threadIdx.x == 0) sh.cta_counts = cta_tot;
     cluster_sync();
-    for (uint32_t p = 0; p < rank; ++p) {
-      const uint32_t addr = map_shared_rank(&sh.cta_counts, p);
-      cta_gt += (int)ld_dsmem_u32(addr);
-      cta_eq += (int)ld_dsmem_u32(addr + 4);
+    if (warp == 0) {
+      int cx = 0, cy = 0;
+      if (lane < (int)rank) {
+        const uint32_t addr = map_shared_rank(&sh.cta_counts, (uint32_t)lane);
+        cx = (int)ld_dsmem_u32(addr);
+        cy = (int)ld_dsmem_u32(addr + 4);
+      }
+      cx = __reduce_add_sync(0xffffffffu, cx);
+      cy = __reduce_add_sync(0xffffffffu, cy);
+      if (lane == 0) {
+        sh.bin_info[0] = cx;
+        sh.bin_info[1] = cy;
+      }
     }
+    __syncthreads();
+    cta_gt = sh.bin_info[0];
+    cta_eq = sh.bin_info[1];
   }
-  int run_gt = cta_gt + wbase.x;  // keys above the threshold before this point
-  int run_eq = cta_eq + wbase.y;  // keys equal to it before this point
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int run_gt = cta_gt + wbase.x;  // keys above the threshold before this chunk
+  int run_eq = cta_eq + wbase.y;  // keys equal to it before this chunk
   for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
     const int i0 = c0 + 4 * lane;
     uint4 kq = make_uint4(0u, 0u, 0u, 0u);
     if (i0 < w_hi) kq = *reinterpret_cast<const uint4*>(keys + i0);
     const uint32_t kk[4] = {kq.x, kq.y, kq.z, kq.w};
-    int f_gt = 0, f_eq = 0;  // bit masks over this lane's 4 keys
+    bool f_gt[4], f_eq[4];
+    unsigned b_gt[4], b_eq[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (i0 + e < w_hi) {
-        const uint32_t hb = kk[e] >> shift;
-        f_gt |= (hb > prefix) << e;
-        f_eq |= (hb == prefix) << e;
-      }
+      const uint32_t hb = kk[e] >> shift;
+      const bool in = i0 + e < w_hi;
+      f_gt[e] = in && hb > prefix;
+      f_eq[e] = in && hb == prefix;
+      b_gt[e] = __ballot_sync(0xffffffffu, f_gt[e]);
+      b_eq[e] = __ballot_sync(0xffffffffu, f_eq[e]);
     }
-    int eq_tot;
-    const int eq_before = run_eq + warp_excl_scan(__popc(f_eq), eq_tot);
-    // Equal keys of this lane with rank < need are taken.
-    int take = 0, r = eq_before;
+    if ((b_gt[0] | b_gt[1] | b_gt[2] | b_gt[3] | b_eq[0] | b_eq[1] | b_eq[2] | b_eq[3]) == 0u)
+      continue;  // nothing selected in this chunk (warp-uniform)
+    int eq_rank = run_eq;  // keys equal to the threshold before this lane's first key
+    int n_gt = 0, n_eq = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if ((f_eq >> e) & 1) {
-        if (r < need) take |= 1 << e;
-        ++r;
-      }
+      eq_rank += __popc(b_eq[e] & lt_mask);
+      n_gt += __popc(b_gt[e]);
+      n_eq += __popc(b_eq[e]);
     }
-    const int sel = f_gt | take;
-    int sel_tot;
-    int out = run_gt + min(run_eq, need) + warp_excl_scan(__popc(sel), sel_tot);
+    bool sel[4];
+    unsigned b_sel[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if ((sel >> e) & 1) emit_one<kMode>(a, t, req, (int64_t)lo + i0 + e, out++);
+      sel[e] = f_gt[e] || (f_eq[e] && eq_rank < need);
+      eq_rank += f_eq[e];
+      b_sel[e] = __ballot_sync(0xffffffffu, sel[e]);
     }
-    int gt_tot;
-    warp_excl_scan(__popc(f_gt), gt_tot);
-    run_gt += gt_tot;
-    run_eq += eq_tot;
+    int out = run_gt + min(run_eq, need);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) out += __popc(b_sel[e] & lt_mask);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (sel[e]) emit_one<kMode>(a, sh, t, pt_row, pt0, pt_n, (int64_t)lo + i0 + e, out++);
+    run_gt += n_gt;
+    run_eq += n_eq;
   }
-  if (rank == 0) emit_tail<kMode>(a, t, req, a.k, L);
+  if (rank == 0) emit_tail<kMode>(a, t, pt_row, a.k, L);
   if (cs > 1) cluster_sync();  // peers may still read this CTA's shared memory
 }
 
