@@ -19,10 +19,12 @@ using namespace qsa;
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Largest row slice one CTA keeps in shared memory (keys), and the largest
-// cluster used for one row.
-constexpr int kSegCap = 44 * 1024;
-constexpr int kMaxCluster = 8;
+// Shared-memory plan of the selection kernel: candidate list and staged
+// page-table entries per CTA, and the largest dynamic size it may use.
+constexpr int kSelListCap = 6144;
+constexpr int kSelPtStage = 2048;
+constexpr int kSelMaxSmem = kSelFixedBytes + kSelPtStage * 4 + kSelListCap * 8 +
+                            kSelResidentCap * 4;
 
 struct DeviceInfo {
   bool ready = false;
@@ -41,7 +43,7 @@ qsa_status device_info(DeviceInfo** out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QSA_ERR_CUDA;
-    const int smem = (int)(kSelKeysOffset + (size_t)kSegCap * sizeof(uint32_t));
+    const int smem = kSelMaxSmem;
     if (cudaFuncSetAttribute(select_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(select_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -86,37 +88,38 @@ qsa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 
-// Cluster size and slice length for rows of up to n_max candidates: the
-// smallest power of two whose slices fit in shared memory, then doubled
-// while the grid stays under half the SMs and each CTA keeps >= 2048
-// candidates (small batches of long rows spread over more SMs).
-bool plan_select(int n_rows, int n_max, int sm_count, int* cs_out, int* seg_out) {
-  int cs = 1;
-  while (cs < kMaxCluster && (n_max + cs - 1) / cs > kSegCap) cs *= 2;
-  if ((n_max + cs - 1) / cs > kSegCap) return false;
-  while (cs < kMaxCluster && (int64_t)n_rows * cs * 2 <= sm_count && n_max / (cs * 2) >= 2048) cs *= 2;
-  int seg = (n_max + cs - 1) / cs;
-  seg = std::max(4, (seg + 3) & ~3);
-  *cs_out = cs;
-  *seg_out = seg;
-  return true;
+// Shared-memory layout of one selection CTA for rows of up to n_max
+// candidates: resident rows (<= kSelResidentCap) live in shared memory, longer
+// rows stream through the bulk-copy ring.
+void plan_select(SelectArgs& a) {
+  a.resident = a.n_max <= kSelResidentCap;
+  a.list_cap = kSelListCap;
+  a.pt_cap = kSelPtStage;
+  int off = kSelFixedBytes;
+  a.off_pt = off;
+  off += a.pt_cap * 4;
+  a.off_list = off;
+  off += a.list_cap * 4;
+  a.off_lkey = off;
+  off += a.list_cap * 4;
+  a.off_row = off;
+}
+
+size_t select_smem_bytes(const SelectArgs& a) {
+  const size_t row = a.resident ? (size_t)((a.n_max + 3) & ~3) * 4 : (size_t)kSelRing * kSelPiece * 4;
+  return (size_t)a.off_row + row;
 }
 
 template <int kMode>
-qsa_status launch_select(const SelectArgs& a, int cs, bool pdl, cudaStream_t stream) {
+qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream) {
   if (a.n_rows == 0) return QSA_OK;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.n_rows * (unsigned)cs, 1, 1);
+  cfg.gridDim = dim3((unsigned)a.n_rows, 1, 1);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSelKeysOffset + (size_t)a.seg * sizeof(uint32_t);
+  cfg.dynamicSmemBytes = select_smem_bytes(a);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   int na = 0;
-  attr[na].id = cudaLaunchAttributeClusterDimension;
-  attr[na].val.clusterDim.x = (unsigned)cs;
-  attr[na].val.clusterDim.y = 1;
-  attr[na].val.clusterDim.z = 1;
-  ++na;
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -147,19 +150,29 @@ qsa_status check_paging(const int32_t* page_table, int64_t ld_pt, int32_t page_s
   return QSA_OK;
 }
 
-// Persistent scorer: tile slots (request, 64-block tile) strided over at most
-// two CTAs per SM.
+// Persistent scorer: two CTAs per SM walk balanced ranges of 128-block
+// tiles.  Requests are handled in windows of at most kScoreMaxReq per launch.
 qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream) {
   const int64_t nb_max = s.max_len / kBlock;
   const int64_t cols = std::max<int64_t>(nb_max, s.n_fill);
   if (s.n_req == 0 || cols == 0) return QSA_OK;
-  const int64_t tpr = (cols + kScoreTile - 1) / kScoreTile;
-  const int64_t slots = tpr * s.n_req;
-  if (slots > INT32_MAX) return QSA_ERR_UNSUPPORTED;
-  s.tiles_per_req = (int32_t)tpr;
-  const int64_t grid = std::min<int64_t>(slots, 2 * (int64_t)sm_count);
-  score_decode_kernel<<<(unsigned)grid, kScoreThreads, kScoreSmem, stream>>>(s);
-  return launch_status();
+  const int32_t n_req = s.n_req;
+  const int32_t* rrs = s.req_row_start;
+  const int32_t* pt = s.page_table;
+  const int32_t trigger = s.trigger_dependents;
+  for (int32_t r0 = 0; r0 < n_req; r0 += kScoreMaxReq) {
+    s.n_req = std::min<int32_t>(kScoreMaxReq, n_req - r0);
+    // only the last launch may let the dependent selection start early
+    s.trigger_dependents = trigger && (r0 + kScoreMaxReq >= n_req);
+    s.req_row_start = rrs + r0;
+    s.page_table = pt + (int64_t)r0 * s.ld_pt;
+    const int64_t tiles = (int64_t)s.n_req * ((cols + kScoreTile - 1) / kScoreTile);
+    if (tiles > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)sm_count);
+    score_decode_kernel<<<(unsigned)grid, kScoreThreads, kScoreSmem, stream>>>(s);
+    if (qsa_status e = launch_status()) return e;
+  }
+  return QSA_OK;
 }
 
 }  // namespace
@@ -238,7 +251,7 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
   if (qsa_status st = device_info(&d)) return st;
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld_scores, n_fill, 0, 0};
+              page_size, scores, ld_scores, n_fill, 0};
   return launch_scores(s, d->sm_count, static_cast<cudaStream_t>(stream));
 }
 
@@ -260,15 +273,13 @@ qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, 
   if (scores && !aligned4(scores)) return QSA_ERR_INVALID_ARG;
   DeviceInfo* d = nullptr;
   if (qsa_status st = device_info(&d)) return st;
-  int cs = 1, seg = 4;
-  if (!plan_select(n_rows, n_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
   SelectArgs a{};
   a.scores = scores;
   a.ld = ld;
   a.n_rows = n_rows;
   a.k = k;
   a.n_max = n_max;
-  a.seg = seg;
+  plan_select(a);
   a.vec_ok = aligned16(scores) && (ld % 4 == 0);
   a.wait_primary = 0;
   a.n_valid = n_valid;
@@ -278,7 +289,7 @@ qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, 
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size > 0 ? page_size : 1;
-  if (qsa_status st = launch_select<kModeTopk>(a, cs, false, static_cast<cudaStream_t>(stream)))
+  if (qsa_status st = launch_select<kModeTopk>(a, false, static_cast<cudaStream_t>(stream)))
     return st;
   return QSA_OK;
 }
@@ -335,13 +346,11 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   }
   DeviceInfo* d = nullptr;
   if (qsa_status st = device_info(&d)) return st;
-  int cs = 1, seg = 4;
-  if (!plan_select(n_rows, nb_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1, 0};
+              page_size, scores, ld, 0, 1};
   if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
 
   SelectArgs a{};
@@ -350,7 +359,7 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   a.n_rows = n_rows;
   a.k = k_blk;
   a.n_max = nb_max;
-  a.seg = seg;
+  plan_select(a);
   a.vec_ok = scores && aligned16(scores) && (ld % 4 == 0);
   a.wait_primary = 1;
   a.n_req = n_req;
@@ -362,7 +371,7 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
-  return launch_select<kModeQsa>(a, cs, nb_max > 0, st);
+  return launch_select<kModeQsa>(a, nb_max > 0, st);
 }
 
 }  // extern "C"
@@ -423,13 +432,11 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   if (qsa_status st = device_info(&d)) return st;
   float* scores = nullptr;
   if (qsa_status st = noalloc_scratch(&scores)) return st;
-  int cs = 1, seg = 4;
-  if (!plan_select(n_rows, nb_max, d->sm_count, &cs, &seg)) return QSA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1, 0};
+              page_size, scores, ld, 0, 1};
   if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
 
   SelectArgs a{};
@@ -438,7 +445,7 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   a.n_rows = n_rows;
   a.k = k_blk;
   a.n_max = nb_max;
-  a.seg = seg;
+  plan_select(a);
   a.vec_ok = 1;  // the array is 256-byte aligned and ld is a multiple of 4
   a.wait_primary = 1;
   a.n_req = n_req;
@@ -450,5 +457,5 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
-  return launch_select<kModeQsa>(a, cs, nb_max > 0, st);
+  return launch_select<kModeQsa>(a, nb_max > 0, st);
 }

@@ -6,20 +6,27 @@
 // for the visible compressed blocks b < row_len[t]/4; decode uses the paged
 // form of the scorer (keys found through the page table at full_slot/4).
 //
-// Design: for a few query rows per request the work is a stream of 256-byte
+// Design: with a few query rows per request the work is a stream of 256-byte
 // keys (4 FLOP per byte per row), so the kernel is built for HBM bandwidth.
-// Persistent CTAs walk tiles of 64 consecutive blocks of one request.  One
-// thread feeds a 6-stage shared-memory ring with bulk asynchronous copies
-// (the TMA engine, one copy per page run -- 4 KB for 64-token pages), so up
-// to five tiles per CTA are in flight without holding registers.  Each
-// half-warp takes one key per step from shared memory (16 lanes x 16 B,
-// conflict-free); every lane keeps its 8 dims of the 4 query heads in
-// registers, the 4 partial dot products are reduced across the 16 lanes with
-// a reduce-scatter (5 shuffles), ReLU and the head sum follow (2 shuffles),
-// and the tile's scores are staged in shared memory and written as coalesced
-// rows.  Keys cross HBM once per request; all rows of the request reuse the
-// staged tile.
+// Measured on this GPU, plain 16-byte vector loads with many keys in flight
+// stream scattered 4 KB pages faster than bulk-copy rings (each bulk copy
+// carries a fixed cost of ~90 ns), so:
+//  - Work items are tiles of 64 consecutive blocks of one request.  Every
+//    CTA computes the per-request tile counts, prefix-sums them, and takes a
+//    balanced contiguous range of tiles (consecutive tiles mostly share a
+//    request).  CTAs are persistent: two per SM.
+//  - A half-warp (16 lanes x 16 B) owns one key per step and 4 keys per
+//    tile; the next tile's 4 keys are loaded into registers while the
+//    current tile is computed, so loads stay in flight continuously.
+//  - The query rows of the current request are staged in shared memory
+//    (re-staged only when the request changes); each lane keeps its 8 dims
+//    of the 4 heads of one row in registers while it walks its keys.
+//  - The 4 partial dot products are reduced over the 16 lanes with a
+//    reduce-scatter (5 shuffles); ReLU, the head sum (2 shuffles) and the
+//    1/sqrt(128) scale follow in registers; one lane stores the FP32 score.
 #pragma once
+#include <cstddef>
+
 #include "common.cuh"
 
 namespace qsa {
@@ -28,40 +35,34 @@ struct ScoreArgs {
   const __nv_bfloat16* q;       // [n_rows][4][128]
   const __nv_bfloat16* pool;    // [pool_rows][128]
   int64_t pool_rows;
-  int32_t n_req;
-  const int32_t* req_row_start; // [n_req+1]
+  int32_t n_req;                // requests in this launch (<= kScoreMaxReq)
+  const int32_t* req_row_start; // [n_req+1] (absolute row indices)
   int32_t n_rows;
   const int32_t* row_len;       // [n_rows]
   int32_t max_len;
-  const int32_t* page_table;    // [n_req][ld_pt]
+  const int32_t* page_table;    // [n_req][ld_pt] (row 0 = first request of the launch)
   int64_t ld_pt;
   int32_t page_size;
   float* scores;                // [n_rows][ld_scores]
   int64_t ld_scores;
   int64_t n_fill;
   int32_t trigger_dependents;   // let a dependent grid launch early (PDL)
-  int32_t tiles_per_req;        // ceil(max(max_len/4, n_fill) / kScoreTile)
 };
 
 constexpr int kScoreThreads = 256;
-constexpr int kScoreTile = 64;                              // blocks per tile
-constexpr int kScoreStages = 6;                             // ring depth
-constexpr int kScoreHalfWarps = kScoreThreads / 16;         // 16
-constexpr int kScoreKeysPerHW = kScoreTile / kScoreHalfWarps;  // 4
-constexpr int kScoreRowGroup = 8;                           // rows staged per pass
-
-struct ScoreTileInfo {
-  int r, b0, nb_req, row0, row1;
-};
+constexpr int kScoreHalfWarps = kScoreThreads / 16;            // 16
+constexpr int kScoreKeysPerHW = 4;
+constexpr int kScoreTile = kScoreHalfWarps * kScoreKeysPerHW;  // 64 blocks per tile
+constexpr int kScoreRowGroup = 8;                              // q rows staged at once
+constexpr int kScoreMaxReq = 4096;                             // requests per launch
 
 struct ScoreShared {
-  __nv_bfloat16 keys[kScoreStages][kScoreTile][kDim];   // 96 KB ring
-  uint64_t full[kScoreStages];
-  ScoreTileInfo info[kScoreStages];
-  float s_tile[kScoreRowGroup][kScoreTile];
-  int s_nb[kScoreRowGroup];
-  int abort_flag;
+  // read and written as 16-byte vectors: first member, 16-byte aligned
+  alignas(16) __nv_bfloat16 q[kScoreRowGroup][kHeads][kDim];
+  int tile_start[kScoreMaxReq + 1];
+  int warp_sum[kScoreThreads / 32];
 };
+static_assert(offsetof(ScoreShared, q) % 16 == 0, "q stage must be 16-byte aligned");
 constexpr size_t kScoreSmem = sizeof(ScoreShared);
 
 // Sum 4 values over the 16 lanes of a half-warp; lane l ends with the total
@@ -78,53 +79,44 @@ __device__ __forceinline__ float reduce_scatter4_x16(float a0, float a1, float a
   return c;
 }
 
-// Producer side (one thread): fill stage `stage` with tile slot `slot`.
-__device__ __forceinline__ void score_issue_tile(const ScoreArgs& a, ScoreShared& sh, int stage,
-                                                 int slot) {
-  ScoreTileInfo inf;
-  inf.r = slot / a.tiles_per_req;
-  inf.b0 = (slot - inf.r * a.tiles_per_req) * kScoreTile;
-  inf.row0 = __ldg(a.req_row_start + inf.r);
-  inf.row1 = __ldg(a.req_row_start + inf.r + 1);
-  if (inf.row0 < 0 || inf.row1 < inf.row0 || inf.row1 > a.n_rows) {
+// Visible blocks of request r: the longest of its rows, / 4.
+__device__ __forceinline__ int request_blocks(const ScoreArgs& a, int r) {
+  const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
+  if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
     raise_fault(kFaultGrouping);
-    inf.row0 = inf.row1 = 0;
+    return 0;
   }
   int nb = 0;
-  for (int t = inf.row0; t < inf.row1; ++t) {
+  for (int t = row0; t < row1; ++t) {
     int L = __ldg(a.row_len + t);
     if (L < 0 || L > a.max_len) { raise_fault(kFaultGrouping); L = 0; }
     nb = max(nb, L / kBlock);
   }
-  inf.nb_req = nb;
-  sh.info[stage] = inf;
-  // Copy the tile's keys page run by page run.
+  return nb;
+}
+
+// This half-warp's 8 keys of tile (r, tile j): lane16 loads bytes
+// [16*lane16, 16*lane16 + 16) of each key row; keys outside the request's
+// visible blocks are zero (and never stored).
+__device__ __forceinline__ void load_tile_keys(const ScoreArgs& a, int r, int j, int nb_req, int hw,
+                                               int lane16, uint4 (&kv)[kScoreKeysPerHW]) {
   const int kpp = a.page_size / kBlock;  // keys per page
-  const int end = min(nb, inf.b0 + kScoreTile);
-  uint32_t bytes = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    // pass 0 counts the bytes (announced first), pass 1 issues the copies
-    for (int b = inf.b0; b < end;) {
+  const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
+#pragma unroll
+  for (int u = 0; u < kScoreKeysPerHW; ++u) {
+    const int b = j * kScoreTile + hw + kScoreHalfWarps * u;
+    kv[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (b < nb_req) {
       const int page_idx = b / kpp;
-      const int in_page = b - page_idx * kpp;
-      const int n = min(kpp - in_page, end - b);
-      bool ok = page_idx < a.ld_pt;
-      int64_t row = 0;
-      if (ok) {
-        const int64_t page = __ldg(a.page_table + (int64_t)inf.r * a.ld_pt + page_idx);
-        row = page * kpp + in_page;
-        ok = page >= 0 && row + n <= a.pool_rows;
+      if (page_idx < a.ld_pt) {
+        const int64_t page = __ldg(pt_row + page_idx);
+        const int64_t row = page * kpp + (b - page_idx * kpp);
+        if (page >= 0 && row < a.pool_rows) kv[u] = ld_stream_16(a.pool + row * kDim + 8 * lane16);
+        else if (lane16 == 0) raise_fault(kFaultPool);
+      } else if (lane16 == 0) {
+        raise_fault(kFaultIndex);
       }
-      if (ok) {
-        if (pass == 0) bytes += (uint32_t)n * (kDim * 2);
-        else bulk_copy_g2s(&sh.keys[stage][b - inf.b0][0], a.pool + row * kDim,
-                           (uint32_t)n * (kDim * 2), &sh.full[stage]);
-      } else if (pass == 0) {
-        raise_fault(page_idx < a.ld_pt ? kFaultPool : kFaultIndex);
-      }
-      b += n;
     }
-    if (pass == 0) mbar_arrive_expect_tx(&sh.full[stage], bytes);
   }
 }
 
@@ -132,56 +124,117 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 score_decode_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char score_smem_raw[];
   ScoreShared& sh = *reinterpret_cast<ScoreShared*>(score_smem_raw);
-
   if (a.trigger_dependents) pdl_launch_dependents();
 
-  const int n_slots = a.n_req * a.tiles_per_req;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lane16 = threadIdx.x & 15;
   const int hw = threadIdx.x >> 4;
-  // this CTA's slots: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int n_mine = blockIdx.x < n_slots ? (n_slots - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t cols_fill = a.n_fill;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScoreStages; ++s) mbar_init(&sh.full[s], 1);
-    sh.abort_flag = 0;
-    fence_mbar_init();
+  // ---- per-request tile counts and their prefix sum ---------------------
+  // Tiles of request r cover max(visible blocks, n_fill) columns.  Counts are
+  // computed one request per thread, then scanned in place in contiguous
+  // chunks of kPer entries per thread.
+  for (int r = threadIdx.x; r < a.n_req; r += kScoreThreads) {
+    const int64_t nbr = request_blocks(a, r);
+    const int64_t cols = nbr > cols_fill ? nbr : cols_fill;
+    sh.tile_start[r] = (int)((cols + kScoreTile - 1) / kScoreTile);
   }
   __syncthreads();
-  if (threadIdx.x == 0)
-    for (int n = 0; n < kScoreStages - 1 && n < n_mine; ++n)
-      score_issue_tile(a, sh, n, blockIdx.x + n * gridDim.x);
-
-  for (int n = 0; n < n_mine; ++n) {
-    const int stage = n % kScoreStages;
-    if (threadIdx.x == 0 && n + kScoreStages - 1 < n_mine)
-      score_issue_tile(a, sh, (n + kScoreStages - 1) % kScoreStages,
-                       blockIdx.x + (n + kScoreStages - 1) * gridDim.x);
-    if (!mbar_wait_bounded(&sh.full[stage], (uint32_t)(n / kScoreStages) & 1u)) {
-      sh.abort_flag = 1;
-      raise_fault(kFaultWait);
+  constexpr int kPer = (kScoreMaxReq + kScoreThreads - 1) / kScoreThreads;  // 16
+  int local = 0;
+  for (int i = 0; i < kPer; ++i) {
+    const int r = threadIdx.x * kPer + i;
+    if (r < a.n_req) local += sh.tile_start[r];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.warp_sum[warp] = incl;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kScoreThreads / 32; ++w) {
+    const int v = sh.warp_sum[w];
+    if (w < warp) wbase += v;
+    total += v;
+  }
+  int run = wbase + incl - local;
+  for (int i = 0; i < kPer; ++i) {
+    const int r = threadIdx.x * kPer + i;
+    if (r < a.n_req) {
+      const int c = sh.tile_start[r];
+      sh.tile_start[r] = run;
+      run += c;
     }
-    // B0: the tile's info (written by thread 0 before it issued the copies)
-    // and the abort flag are now visible to every thread; it also orders the
-    // previous tile's write-out before this tile's use of s_tile / s_nb.
-    __syncthreads();
-    if (sh.abort_flag) return;  // a copy never arrived: leave together
-    const ScoreTileInfo inf = sh.info[stage];
-    const bool any_key = inf.b0 < inf.nb_req;
+  }
+  if (threadIdx.x == 0) sh.tile_start[a.n_req] = total;
+  __syncthreads();
 
-    for (int g0 = inf.row0; g0 < inf.row1; g0 += kScoreRowGroup) {
-      if (g0 != inf.row0) __syncthreads();  // previous group's write-out done
-      const int g1 = min(inf.row1, g0 + kScoreRowGroup);
-      if (threadIdx.x < g1 - g0) {
-        const int L = __ldg(a.row_len + g0 + threadIdx.x);
-        sh.s_nb[threadIdx.x] = (L < 0 || L > a.max_len) ? 0 : L / kBlock;
+  // ---- this CTA's contiguous range of tiles -----------------------------
+  const int t_lo = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int t_hi = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  if (t_lo >= t_hi) return;
+
+  // request of a tile index: advance a cursor (ranges are ascending)
+  int cur_r = 0;
+  {
+    int lo = 0, hi = a.n_req - 1;  // last r with tile_start[r] <= t_lo
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sh.tile_start[mid] <= t_lo) lo = mid; else hi = mid - 1;
+    }
+    cur_r = lo;
+  }
+  int next_r = cur_r;
+  auto advance = [&](int tile, int& rr) {
+    while (rr + 1 < a.n_req && sh.tile_start[rr + 1] <= tile) ++rr;
+  };
+
+  uint4 kcur[kScoreKeysPerHW], knext[kScoreKeysPerHW];
+  int nb_next = request_blocks(a, next_r);
+  load_tile_keys(a, next_r, t_lo - sh.tile_start[next_r], nb_next, hw, lane16, knext);
+  int staged_r = -1, staged_g0 = -1;
+
+  for (int tile = t_lo; tile < t_hi; ++tile) {
+    // rotate the prefetched keys in, start loading the next tile's keys
+    const int r = next_r;
+    const int j = tile - sh.tile_start[r];
+#pragma unroll
+    for (int u = 0; u < kScoreKeysPerHW; ++u) kcur[u] = knext[u];
+    if (tile + 1 < t_hi) {
+      advance(tile + 1, next_r);
+      if (next_r != r) nb_next = request_blocks(a, next_r);
+      load_tile_keys(a, next_r, tile + 1 - sh.tile_start[next_r], nb_next, hw, lane16, knext);
+    }
+    cur_r = r;
+
+    const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
+    const int b_base = j * kScoreTile;
+    for (int g0 = row0; g0 < row1; g0 += kScoreRowGroup) {
+      const int g1 = min(row1, g0 + kScoreRowGroup);
+      if (staged_r != r || staged_g0 != g0) {
+        // stage the group's query rows (16-byte pieces)
+        __syncthreads();
+        const int pieces = (g1 - g0) * (kHeads * kDim / 8);
+        const uint4* src = reinterpret_cast<const uint4*>(a.q + (int64_t)g0 * kHeads * kDim);
+        uint4* dst = reinterpret_cast<uint4*>(&sh.q[0][0][0]);
+        for (int i = threadIdx.x; i < pieces; i += kScoreThreads) dst[i] = __ldg(src + i);
+        __syncthreads();
+        staged_r = r;
+        staged_g0 = g0;
       }
-      if (any_key) {
-        for (int t = g0; t < g1; ++t) {
+      for (int t = g0; t < g1; ++t) {
+        const int L = __ldg(a.row_len + t);
+        const int nb_t = (L < 0 || L > a.max_len) ? 0 : L / kBlock;
+        float* srow = a.scores + (int64_t)t * a.ld_scores;
+        if (b_base < nb_t) {
           float qv[kHeads][8];
-          const __nv_bfloat16* qrow = a.q + (int64_t)t * (kHeads * kDim);
 #pragma unroll
           for (int h = 0; h < kHeads; ++h) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + h * kDim + 8 * lane16));
+            const uint4 v = *reinterpret_cast<const uint4*>(&sh.q[t - g0][h][8 * lane16]);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -191,10 +244,9 @@ score_decode_kernel(ScoreArgs a) {
             }
           }
 #pragma unroll
-          for (int j = 0; j < kScoreKeysPerHW; ++j) {
-            const int kk = hw + kScoreHalfWarps * j;
-            const uint4 kv = *reinterpret_cast<const uint4*>(&sh.keys[stage][kk][8 * lane16]);
-            const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+          for (int u = 0; u < kScoreKeysPerHW; ++u) {
+            const int b = b_base + hw + kScoreHalfWarps * u;
+            const uint32_t w[4] = {kcur[u].x, kcur[u].y, kcur[u].z, kcur[u].w};
             float kf[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -215,22 +267,17 @@ score_decode_kernel(ScoreArgs a) {
             sc = fmaxf(sc, 0.f);
             sc += __shfl_xor_sync(0xffffffffu, sc, 4);
             sc += __shfl_xor_sync(0xffffffffu, sc, 8);
-            if (lane16 == 0) sh.s_tile[t - g0][kk] = sc * kScoreScale;
+            if (lane16 == 0 && b < nb_t) srow[b] = sc * kScoreScale;
           }
         }
-      }
-      __syncthreads();  // B1: the group's scores are staged
-      // Coalesced write-out: visible blocks get their score, [nb_t, n_fill) -inf.
-      for (int idx = threadIdx.x; idx < (g1 - g0) * kScoreTile; idx += kScoreThreads) {
-        const int tr = idx / kScoreTile;
-        const int kk = idx % kScoreTile;
-        const int64_t b = inf.b0 + kk;
-        float* dst = a.scores + (int64_t)(g0 + tr) * a.ld_scores + b;
-        if (b < sh.s_nb[tr]) *dst = sh.s_tile[tr][kk];
-        else if (b < a.n_fill) *dst = -__int_as_float(0x7f800000);
+        // columns [nb_t, n_fill) of this tile get -inf
+        const int64_t f_lo = nb_t > b_base ? nb_t : b_base;
+        const int64_t f_hi = cols_fill < b_base + kScoreTile ? cols_fill : (int64_t)(b_base + kScoreTile);
+        for (int64_t b = f_lo + threadIdx.x; b < f_hi; b += kScoreThreads) srow[b] = -__int_as_float(0x7f800000);
       }
     }
   }
+  (void)cur_r;
 }
 
 }  // namespace qsa

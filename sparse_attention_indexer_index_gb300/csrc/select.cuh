@@ -14,33 +14,47 @@
 // Readings: ties go to the lower index; -0 == +0; NaN ranks below -inf; the
 // result is returned in ascending index order with -1 only as tail padding.
 //
-// Design (GB300): one row is owned by a thread-block cluster of CS CTAs
-// (CS = 1, 2, 4, 8).  Each CTA pulls its contiguous slice of the row into
-// shared memory ONCE with a bulk asynchronous copy (TMA engine), converts it
-// in place to order-preserving u32 keys and builds a histogram of the top 11
-// key bits.  Cluster histograms are summed in two levels over distributed
-// shared memory: CTA c adds everyone's counts for its 1/CS share of the bins
-// with 16-byte remote loads, then every CTA reads the CS share totals and the
-// one share that holds the k-th key -- a few hundred remote transactions per
-// CTA and pass.  Two more passes (11 and 10 bits) over the on-chip keys refine
-// the bin to the exact k-th key, stopping early when a bin holds exactly the
-// remaining count.  Emission walks the slice in index order; warp ballots and
-// warp/CTA/cluster prefix counts of keys above and equal to the threshold put
-// every selected index straight at its ascending output position, equal keys
-// at the boundary lowest-index first.  The page-table entries of the slice
-// are staged in shared memory before the kernel waits for its input.  No
-// sort, no global scratch; every wait is a hardware cluster barrier or a
-// time-bounded mbarrier wait.
+// Design (GB300): one 1024-thread CTA per row; every step synchronises with
+// CTA barriers only, and as few as possible (a 1024-thread barrier plus its
+// scan costs about half a microsecond).  Scores become order-preserving u32
+// keys (larger float -> larger key).
+//  1. Histogram of the top 11 key bits over the whole row (four copies to
+//     spread atomic contention); a two-barrier scan finds the bin B0 holding
+//     the k-th largest key.
+//  2. Order-preserving compaction of every entry whose top bits are >= B0 --
+//     the sure winners plus the boundary bin, typically k plus a few percent
+//     of the row -- into a shared-memory list: each warp owns a contiguous
+//     segment, counts, and after one barrier writes its matches with ballot
+//     prefix counts.
+//  3. Two radix passes (11 and 10 bits) over the boundary entries of the list
+//     give the exact k-th key T (early exit when a bin holds exactly the
+//     remaining count).
+//  4. Emission over the list, segmented the same way: above T, or equal to T
+//     among the first `need` equal ones, goes straight to its ascending
+//     output position, with the slot translation (or the QSA expansion to 4
+//     positions and slots) in the same step.
+// A row of up to 32K scores is pulled once into shared memory by bulk
+// asynchronous copies (TMA engine; one barrier per 16 KB piece, so the
+// conversion overlaps the transfer).  A longer row streams through a 4-stage
+// ring for step 1 and again for step 2.  If the list would overflow (heavy
+// ties), steps 3-4 run over the whole row instead.  No sort, no global
+// scratch, no cluster; every wait is a CTA barrier or a time-bounded mbarrier
+// wait.
 #pragma once
+#include <cstddef>
+
 #include "common.cuh"
 
 namespace qsa {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kHistBins = 2048;
-constexpr int kMaxClusterSel = 8;    // largest cluster used for one row
-constexpr int kSelPtCap = 2048;      // page-table entries staged per CTA
+constexpr int kHistCopies = 4;
+constexpr int kSelPiece = 4096;          // elements per bulk piece (16 KB)
+constexpr int kSelRing = 4;              // ring stages for streamed rows
+constexpr int kSelResidentCap = 32768;   // longest row kept in shared memory
+constexpr int kSelMaxBars = 8;           // >= kSelResidentCap / kSelPiece and kSelRing
 
 enum SelectMode { kModeTopk = 0, kModeQsa = 1 };
 
@@ -50,9 +64,12 @@ struct SelectArgs {
   int32_t n_rows;
   int32_t k;
   int32_t n_max;                // host bound of a row's candidates
-  int32_t seg;                  // candidates per CTA slice (multiple of 4)
   int32_t vec_ok;               // rows are 16-byte aligned
   int32_t wait_primary;         // wait for the producing grid (PDL)
+  int32_t resident;             // rows fit in shared memory (n_max <= kSelResidentCap)
+  int32_t list_cap;             // entries of the candidate list
+  int32_t pt_cap;               // page-table entries staged in shared memory
+  int32_t off_pt, off_list, off_lkey, off_row;  // dynamic shared memory layout (bytes)
   // token top-k mode
   const int32_t* n_valid;       // [n_rows] or nullptr (all rows n_max)
   const int32_t* row_req;       // [n_rows] or nullptr (row t -> table row t)
@@ -70,75 +87,44 @@ struct SelectArgs {
   int32_t page_size;
 };
 
-// Exclusive block-wide scan of two counters at once (kSelThreads threads).
-__device__ __forceinline__ int2 block_scan2(int a, int b, int2* s_warp, int2& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x = a, y = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int xa = __shfl_up_sync(0xffffffffu, x, o);
-    const int ya = __shfl_up_sync(0xffffffffu, y, o);
-    if (lane >= o) { x += xa; y += ya; }
-  }
-  if (lane == 31) s_warp[w] = make_int2(x, y);
-  __syncthreads();
-  if (w == 0) {
-    int2 v = lane < kSelWarps ? s_warp[lane] : make_int2(0, 0);
-    int ix = v.x, iy = v.y;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int xa = __shfl_up_sync(0xffffffffu, ix, o);
-      const int ya = __shfl_up_sync(0xffffffffu, iy, o);
-      if (lane >= o) { ix += xa; iy += ya; }
-    }
-    if (lane < kSelWarps) s_warp[lane] = make_int2(ix - v.x, iy - v.y);
-    if (lane == kSelWarps - 1) s_warp[kSelWarps] = make_int2(ix, iy);
-  }
-  __syncthreads();
-  const int2 base = s_warp[w];
-  total = s_warp[kSelWarps];
-  __syncthreads();
-  return make_int2(base.x + x - a, base.y + y - b);
-}
-
-struct SelShared {
-  uint32_t hist[2][kHistBins];           // local histograms, double-buffered
-  uint32_t stage[kHistBins];             // remote share rows being summed
-  uint32_t red[2][kHistBins / 2];        // this CTA's reduced share (CS >= 2)
-  uint32_t share_tot[2];                 // total of this CTA's share
-  int32_t pt[kSelPtCap];                 // page-table entries of the slice
-  int2 warp_scan[kSelWarps + 1];
-  int2 cta_counts;                       // (above, equal) counts, read by peers
-  int bin_info[4];                       // found bin, count above it, its count, owner
-  uint64_t load_bar;                     // completion of the slice's bulk copy
+struct SelFixed {
+  uint32_t hist[kHistCopies][kHistBins];
+  int warp_tot[2][kSelWarps];   // per-warp counts (two counters)
+  int info[8];
+  uint64_t bar[kSelMaxBars];
 };
-// The row slice (u32 keys) follows the fixed part, 128-byte aligned.
-constexpr size_t kSelKeysOffset = (sizeof(SelShared) + 127) & ~size_t(127);
+constexpr int kSelFixedBytes = (int)((sizeof(SelFixed) + 127) & ~size_t(127));
+static_assert(offsetof(SelFixed, bar) % 8 == 0, "mbarriers must be 8-byte aligned");
 
-__device__ __forceinline__ int32_t slot_lookup(const SelectArgs& a, const SelShared& sh,
-                                               const int32_t* pt_row, int pt0, int pt_n,
-                                               int64_t pos) {
+// Per-row context.
+struct SelRow {
+  int t, n, L;
+  const float* row;
+  const int32_t* pt_row;
+  int pt_n;
+  const int32_t* pt_s;  // staged page-table entries [0, pt_n)
+};
+
+__device__ __forceinline__ int32_t slot_lookup(const SelectArgs& a, const SelRow& r, int64_t pos) {
   const int64_t page_idx = pos / a.page_size;
   const int32_t off = (int32_t)(pos - page_idx * a.page_size);
-  if (page_idx >= pt0 && page_idx < pt0 + pt_n) return sh.pt[page_idx - pt0] * a.page_size + off;
-  if (page_idx < a.ld_pt) return __ldg(pt_row + page_idx) * a.page_size + off;
+  if (page_idx < r.pt_n) return r.pt_s[page_idx] * a.page_size + off;
+  if (page_idx < a.ld_pt) return __ldg(r.pt_row + page_idx) * a.page_size + off;
   raise_fault(kFaultIndex);
   return -1;
 }
 
 template <int kMode>
-__device__ __forceinline__ void emit_one(const SelectArgs& a, const SelShared& sh, int t,
-                                         const int32_t* pt_row, int pt0, int pt_n, int64_t idx,
-                                         int pos) {
+__device__ __forceinline__ void emit_one(const SelectArgs& a, const SelRow& r, int64_t idx, int pos) {
+  const int t = r.t;
   if (kMode == kModeTopk) {
     a.out_idx[(int64_t)t * a.k + pos] = (int32_t)idx;
-    if (a.out_slots != nullptr)
-      a.out_slots[(int64_t)t * a.k + pos] = slot_lookup(a, sh, pt_row, pt0, pt_n, idx);
+    if (a.out_slots != nullptr) a.out_slots[(int64_t)t * a.k + pos] = slot_lookup(a, r, idx);
   } else {
     if (a.out_idx != nullptr) a.out_idx[(int64_t)t * a.k + pos] = (int32_t)idx;
     const int64_t width = (int64_t)kBlock * a.k + (kBlock - 1);
     const int64_t p0 = kBlock * idx;  // first token of block idx (same page as p0+3)
-    const int32_t base = slot_lookup(a, sh, pt_row, pt0, pt_n, p0);
+    const int32_t base = slot_lookup(a, r, p0);
     // Rows are 4k+3 entries wide, so these stores are not 16-byte aligned.
     int32_t* xs = a.out_xslots + (int64_t)t * width + kBlock * pos;
 #pragma unroll
@@ -152,10 +138,10 @@ __device__ __forceinline__ void emit_one(const SelectArgs& a, const SelShared& s
 }
 
 // Tail of a row once m = min(k, n) entries are emitted: -1 padding (token
-// mode) or pending tokens then -1 (QSA mode).  Run by one CTA of the cluster.
+// mode) or pending tokens then -1 (QSA mode).
 template <int kMode>
-__device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, const int32_t* pt_row, int m,
-                                          int L) {
+__device__ __forceinline__ void emit_tail(const SelectArgs& a, const SelRow& r, int m) {
+  const int t = r.t;
   if (kMode == kModeTopk) {
     for (int j = m + threadIdx.x; j < a.k; j += kSelThreads) {
       a.out_idx[(int64_t)t * a.k + j] = -1;
@@ -165,19 +151,14 @@ __device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, const int3
     if (a.out_idx != nullptr)
       for (int j = m + threadIdx.x; j < a.k; j += kSelThreads) a.out_idx[(int64_t)t * a.k + j] = -1;
     const int width = kBlock * a.k + (kBlock - 1);
-    const int nb = L / kBlock;
-    const int pend = L - kBlock * nb;
+    const int nb = r.L / kBlock;
+    const int pend = r.L - kBlock * nb;
     for (int j = kBlock * m + threadIdx.x; j < width; j += kSelThreads) {
       const int i = j - kBlock * m;
       int32_t pos = -1, slot = -1;
       if (i < pend) {
         pos = kBlock * nb + i;
-        const int page_idx = pos / a.page_size;
-        if (page_idx < a.ld_pt) {
-          slot = __ldg(pt_row + page_idx) * a.page_size + (pos - page_idx * a.page_size);
-        } else {
-          raise_fault(kFaultIndex);
-        }
+        slot = slot_lookup(a, r, pos);
       }
       a.out_xslots[(int64_t)t * width + j] = slot;
       if (a.out_pos != nullptr) a.out_pos[(int64_t)t * width + j] = pos;
@@ -185,316 +166,441 @@ __device__ __forceinline__ void emit_tail(const SelectArgs& a, int t, const int3
   }
 }
 
-// Among `nb` counts listed in DESCENDING bin order (read through get(d)),
-// with `above_base` keys above the first, find the one holding the k_rem-th
-// key: sh.bin_info = (its descending index, keys above it, its count).
-template <typename Get>
-__device__ __forceinline__ void find_bin(SelShared& sh, int nb, int above_base, int k_rem,
-                                         Get get) {
-  const int per = (nb + kSelThreads - 1) / kSelThreads;  // <= 4
-  uint32_t c[4];
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Publish per-warp totals (two counters) and return this warp's exclusive
+// prefixes over the CTA; one barrier.  `tot` receives the CTA totals.
+__device__ __forceinline__ int2 warp_bases(SelFixed& fx, int buf, int g, int q, int2& tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    fx.warp_tot[0][warp] = g;
+    fx.warp_tot[1][warp] = q;
+  }
+  (void)buf;
+  __syncthreads();
+  const int vg = fx.warp_tot[0][lane], vq = fx.warp_tot[1][lane];
+  const int ig = warp_incl_scan(vg), iq = warp_incl_scan(vq);
+  tot.x = __shfl_sync(0xffffffffu, ig, 31);
+  tot.y = __shfl_sync(0xffffffffu, iq, 31);
+  const int2 base = make_int2(__shfl_sync(0xffffffffu, ig - vg, warp), __shfl_sync(0xffffffffu, iq - vq, warp));
+  __syncthreads();  // warp_tot may be rewritten by the next caller
+  return base;
+}
+
+// Among `nb` bins (nb = 2048 or 1024) of the histogram copies 0..ncopies-1,
+// listed from the top bin down, with `above_base` keys above the first, find
+// the bin holding the k_rem-th key: info[0..2] = (bin, keys above it, count).
+__device__ __forceinline__ void find_bin(SelFixed& fx, int nb, int ncopies, int above_base, int k_rem) {
+  const int per = nb / kSelThreads;  // 2 or 1
+  uint32_t c[2] = {0u, 0u};
   int sum = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int d = threadIdx.x * per + j;
-    c[j] = (j < per && d < nb) ? get(d) : 0u;
-    sum += (int)c[j];
+  for (int j = 0; j < 2; ++j) {
+    if (j < per) {
+      const int bin = nb - 1 - (threadIdx.x * per + j);
+      uint32_t v = 0;
+      for (int cp = 0; cp < ncopies; ++cp) v += fx.hist[cp][bin];
+      c[j] = v;
+      sum += (int)v;
+    }
   }
+  const int lane = threadIdx.x & 31;
+  const int incl = warp_incl_scan(sum);
   int2 tot;
-  int above = above_base + block_scan2(sum, 0, sh.warp_scan, tot).x;
+  const int2 wb = warp_bases(fx, 0, __shfl_sync(0xffffffffu, incl, 31), 0, tot);
+  int above = above_base + wb.x + incl - sum;
+  (void)lane;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 2; ++j) {
     if (j < per && above < k_rem && k_rem <= above + (int)c[j]) {
-      sh.bin_info[0] = threadIdx.x * per + j;
-      sh.bin_info[1] = above;
-      sh.bin_info[2] = (int)c[j];
+      fx.info[0] = nb - 1 - (threadIdx.x * per + j);
+      fx.info[1] = above;
+      fx.info[2] = (int)c[j];
     }
     above += (int)c[j];
   }
   __syncthreads();
 }
 
-__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t cluster_addr) {
-  uint4 x;
-  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
-               : "r"(cluster_addr));
-  return x;
+// Ordered compaction / emission over a segment-per-warp layout.  The items
+// are [0, cnt); warp w owns [w*seg, (w+1)*seg) (seg a multiple of 128) and
+// walks it 128 at a time, 4 consecutive items per lane.
+__device__ __forceinline__ int warp_segment(int cnt) {
+  return (((cnt + kSelWarps - 1) / kSelWarps) + 127) & ~127;
+}
+
+// Streams a long row through the ring: f(keys accessor for the piece, base,
+// count) on every piece in order.  The piece's bulk part is read from shared
+// memory as uint4; the (< 4) tail and rows that are not 16-byte aligned are
+// read from global memory.
+struct RowStream {
+  int n;
+  const float* row;
+  int vec_ok;
+  uint64_t* bar;
+  float* ring;   // kSelRing * kSelPiece floats
+  int seq;
+
+  __device__ __forceinline__ void issue(int piece) {
+    const int s = (seq + piece) % kSelRing;
+    const int base = piece * kSelPiece;
+    const int cnt = min(kSelPiece, n - base);
+    const int bulk = vec_ok ? (cnt & ~3) : 0;
+    mbar_arrive_expect_tx(&bar[s], (uint32_t)bulk * 4u);
+    if (bulk > 0) bulk_copy_g2s(ring + (size_t)s * kSelPiece, row + base, (uint32_t)bulk * 4u, &bar[s]);
+  }
+
+  // f(const float* piece_smem, int bulk, const float* piece_global, int base, int cnt)
+  template <typename F>
+  __device__ __forceinline__ void walk(F f) {
+    const int np = (n + kSelPiece - 1) / kSelPiece;
+    if (threadIdx.x == 0)
+      for (int p = 0; p < min(np, kSelRing); ++p) issue(p);
+    for (int p = 0; p < np; ++p) {
+      const int s = (seq + p) % kSelRing;
+      const uint32_t parity = (uint32_t)((seq + p) / kSelRing) & 1u;
+      if (!mbar_wait_bounded(&bar[s], parity) && threadIdx.x == 0) raise_fault(kFaultWait);
+      const int base = p * kSelPiece;
+      const int cnt = min(kSelPiece, n - base);
+      f(ring + (size_t)s * kSelPiece, vec_ok ? (cnt & ~3) : 0, row + base, base, cnt);
+      __syncthreads();  // the stage is free again
+      if (threadIdx.x == 0 && p + kSelRing < np) issue(p + kSelRing);
+    }
+    seq += np;
+  }
+};
+
+// Four keys of items [i, i+4) of a piece: from shared memory (bulk part, as
+// floats to convert or as keys) or from global memory.
+__device__ __forceinline__ void load4_keys(const float* sm, int bulk, const float* gl, int i, int cnt,
+                                           bool already_keys, uint32_t (&kk)[4]) {
+  if (i + 3 < bulk) {
+    const uint4 v = *reinterpret_cast<const uint4*>(sm + i);
+    if (already_keys) {
+      kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
+    } else {
+      kk[0] = order_key(__uint_as_float(v.x));
+      kk[1] = order_key(__uint_as_float(v.y));
+      kk[2] = order_key(__uint_as_float(v.z));
+      kk[3] = order_key(__uint_as_float(v.w));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t x = 0u;
+      if (i + e < cnt) {
+        if (i + e < bulk) x = already_keys ? __float_as_uint(sm[i + e]) : order_key(sm[i + e]);
+        else x = order_key(__ldg(gl + i + e));
+      }
+      kk[e] = x;
+    }
+  }
 }
 
 template <int kMode>
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, 1)
 select_kernel(SelectArgs a) {
   extern __shared__ __align__(128) unsigned char sel_smem_raw[];
-  SelShared& sh = *reinterpret_cast<SelShared*>(sel_smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem_raw + kSelKeysOffset);
-
-  const uint32_t cs = cluster_nctarank();
-  const uint32_t rank = cluster_ctarank();
-  const int t = blockIdx.x / cs;
+  SelFixed& fx = *reinterpret_cast<SelFixed*>(sel_smem_raw);
+  int32_t* pt_s = reinterpret_cast<int32_t*>(sel_smem_raw + a.off_pt);
+  int32_t* list_idx = reinterpret_cast<int32_t*>(sel_smem_raw + a.off_list);
+  uint32_t* list_key = reinterpret_cast<uint32_t*>(sel_smem_raw + a.off_lkey);
+  float* row_area = reinterpret_cast<float*>(sel_smem_raw + a.off_row);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
 
-  // ---- row metadata and the slice's page-table entries: inputs that do
-  // not come from the producing grid, so they are read before waiting ------
-  int n, L = 0;
-  const int32_t* pt_row = nullptr;
+  SelRow r;
+  r.t = blockIdx.x;
+  r.L = 0;
+  r.pt_row = nullptr;
+  r.pt_s = pt_s;
+  r.pt_n = 0;
+  // ---- row metadata and the row's page-table entries: inputs that do not
+  // come from the producing grid, so they are read before waiting ---------
   if (kMode == kModeTopk) {
-    n = a.n_valid ? __ldg(a.n_valid + t) : a.n_max;
+    r.n = a.n_valid ? __ldg(a.n_valid + r.t) : a.n_max;
     if (a.out_slots != nullptr)
-      pt_row = a.page_table + (int64_t)(a.row_req ? __ldg(a.row_req + t) : t) * a.ld_pt;
+      r.pt_row = a.page_table + (int64_t)(a.row_req ? __ldg(a.row_req + r.t) : r.t) * a.ld_pt;
   } else {
-    const int req = row_request(a.req_row_start, a.n_req, t);
-    L = __ldg(a.row_len + t);
-    n = L / kBlock;
-    pt_row = a.page_table + (int64_t)req * a.ld_pt;
+    const int req = row_request(a.req_row_start, a.n_req, r.t);
+    r.L = __ldg(a.row_len + r.t);
+    r.n = r.L / kBlock;
+    r.pt_row = a.page_table + (int64_t)req * a.ld_pt;
   }
-  if (n < 0 || n > a.n_max) {  // bad length: emit an empty row
-    if (threadIdx.x == 0 && rank == 0) raise_fault(kFaultGrouping);
-    n = 0;
-    L = 0;
+  if (r.n < 0 || r.n > a.n_max) {  // bad length: emit an empty row
+    if (threadIdx.x == 0) raise_fault(kFaultGrouping);
+    r.n = 0;
+    r.L = 0;
   }
-  const int lo = (int)rank * a.seg;
-  const int hi = min(n, lo + a.seg);
-  const int len = max(0, hi - lo);
-  // pages covering the positions of candidates [lo, hi) (QSA: 4 tokens each)
-  const int64_t scale = kMode == kModeQsa ? kBlock : 1;
-  int pt0 = 0, pt_n = 0;
-  if (pt_row != nullptr && len > 0) {
-    pt0 = (int)((scale * lo) / a.page_size);
-    const int pt1 = (int)((scale * hi - 1) / a.page_size) + 1;
-    int64_t np = min(pt1 - pt0, kSelPtCap);
-    if (np > a.ld_pt - pt0) np = a.ld_pt - pt0;
-    pt_n = np > 0 ? (int)np : 0;
-    for (int i = threadIdx.x; i < pt_n; i += kSelThreads) sh.pt[i] = __ldg(pt_row + pt0 + i);
+  if (r.pt_row != nullptr) {
+    const int64_t last = kMode == kModeQsa ? (int64_t)r.L : (int64_t)r.n;  // positions < last
+    int64_t np = last > 0 ? (last - 1) / a.page_size + 1 : 0;
+    if (np > a.pt_cap) np = a.pt_cap;
+    if (np > a.ld_pt) np = a.ld_pt;
+    r.pt_n = (int)np;
+    for (int i = threadIdx.x; i < r.pt_n; i += kSelThreads) pt_s[i] = __ldg(r.pt_row + i);
   }
   if (threadIdx.x == 0) {
-    mbar_init(&sh.load_bar, 1);
+    for (int i = 0; i < kSelMaxBars; ++i) mbar_init(&fx.bar[i], 1);
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < kHistCopies * kHistBins; i += kSelThreads) (&fx.hist[0][0])[i] = 0;
   __syncthreads();
 
   if (a.wait_primary) pdl_wait_primary();
-  const float* row = a.scores + (int64_t)t * a.ld;
+  r.row = a.scores + (int64_t)r.t * a.ld;
+  const int n = r.n;
 
   if (n <= a.k) {
     // Everything is selected: index i goes to output position i.
-    for (int i = lo + threadIdx.x; i < hi; i += kSelThreads)
-      emit_one<kMode>(a, sh, t, pt_row, pt0, pt_n, i, i);
-    if (rank == 0) emit_tail<kMode>(a, t, pt_row, n, L);
-    return;  // no shared memory was shared, so CTAs may leave independently
+    for (int i = threadIdx.x; i < n; i += kSelThreads) emit_one<kMode>(a, r, i, i);
+    emit_tail<kMode>(a, r, n);
+    return;
   }
 
-  // ---- load the slice once, convert in place, first histogram ----------
-  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh.hist[0][i] = 0;
-  const int len_vec = a.vec_ok ? (len & ~3) : 0;  // bulk-copied part
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&sh.load_bar, (uint32_t)len_vec * 4u);
-    for (int off = 0; off < len_vec; off += 8192)  // 32 KB pieces
-      bulk_copy_g2s(keys + off, row + lo + off, (uint32_t)min(8192, len_vec - off) * 4u, &sh.load_bar);
-  }
-  for (int i = len_vec + threadIdx.x; i < len; i += kSelThreads) keys[i] = __float_as_uint(row[lo + i]);
-  // A copy that never lands latches the fault and the row is garbage, but the
-  // CTA keeps to the cluster's barrier sequence (leaving early could strand
-  // its peers at a cluster barrier).
-  if (!mbar_wait_bounded(&sh.load_bar, 0) && threadIdx.x == 0) raise_fault(kFaultWait);
-  __syncthreads();
-  const int len4 = (len + 3) & ~3;
-  for (int i = 4 * threadIdx.x; i < len4; i += 4 * kSelThreads) {
-    const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-    const uint4 kq = make_uint4(order_key(__uint_as_float(v.x)), order_key(__uint_as_float(v.y)),
-                                order_key(__uint_as_float(v.z)), order_key(__uint_as_float(v.w)));
-    *reinterpret_cast<uint4*>(keys + i) = kq;
-    atomicAdd(&sh.hist[0][kq.x >> 21], 1u);
-    if (i + 1 < len) atomicAdd(&sh.hist[0][kq.y >> 21], 1u);
-    if (i + 2 < len) atomicAdd(&sh.hist[0][kq.z >> 21], 1u);
-    if (i + 3 < len) atomicAdd(&sh.hist[0][kq.w >> 21], 1u);
-  }
-
-  // ---- radix refinement: 11 + 11 + 10 bits -------------------------------
-  uint32_t prefix = 0;
-  int shift = 32;
-  int k_rem = a.k;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int bits = pass < 2 ? 11 : 10;
-    const int nbins = 1 << bits;
-    const int nshift = shift - bits;
-    uint32_t* hist = sh.hist[pass & 1];
-    if (pass > 0) {
-      for (int i = threadIdx.x; i < nbins; i += kSelThreads) hist[i] = 0;
-      __syncthreads();
-      const uint32_t mask = (uint32_t)nbins - 1u;
-      for (int i = 4 * threadIdx.x; i < len4; i += 4 * kSelThreads) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-        const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+  // ---- 1. histogram of the top 11 bits ---------------------------------
+  uint32_t* hcopy = fx.hist[warp & (kHistCopies - 1)];
+  RowStream rs{n, r.row, a.vec_ok, fx.bar, row_area, 0};
+  if (a.resident) {
+    // Bulk-load the whole row (one barrier per 16 KB piece), convert in place.
+    const int np = (n + kSelPiece - 1) / kSelPiece;
+    if (threadIdx.x == 0) {
+      for (int p = 0; p < np; ++p) {
+        const int base = p * kSelPiece;
+        const int bulk = a.vec_ok ? (min(kSelPiece, n - base) & ~3) : 0;
+        mbar_arrive_expect_tx(&fx.bar[p], (uint32_t)bulk * 4u);
+        if (bulk > 0) bulk_copy_g2s(row_area + base, r.row + base, (uint32_t)bulk * 4u, &fx.bar[p]);
+      }
+    }
+    for (int p = 0; p < np; ++p) {
+      const int base = p * kSelPiece;
+      const int cnt = min(kSelPiece, n - base);
+      const int bulk = a.vec_ok ? (cnt & ~3) : 0;
+      if (!mbar_wait_bounded(&fx.bar[p], 0) && threadIdx.x == 0) raise_fault(kFaultWait);
+      const int i = 4 * threadIdx.x;  // kSelPiece == 4 * kSelThreads
+      if (i < cnt) {
+        uint32_t kk[4];
+        load4_keys(row_area + base, bulk, r.row + base, i, cnt, false, kk);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(row_area + base);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (i + e < cnt) {
+            dst[i + e] = kk[e];
+            atomicAdd(&hcopy[kk[e] >> 21], 1u);
+          }
+        }
+      }
+    }
+  } else {
+    rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+      const int i = 4 * threadIdx.x;
+      if (i < cnt) {
+        uint32_t kk[4];
+        load4_keys(sm, bulk, gl, i, cnt, false, kk);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (i + e < len && (kk[e] >> shift) == prefix) atomicAdd(&hist[(kk[e] >> nshift) & mask], 1u);
+          if (i + e < cnt) atomicAdd(&hcopy[kk[e] >> 21], 1u);
       }
-    }
-    int bin;
-    if (cs == 1) {
-      __syncthreads();
-      find_bin(sh, nbins, 0, k_rem, [&](int d) { return hist[nbins - 1 - d]; });
-      bin = nbins - 1 - sh.bin_info[0];
-    } else {
-      // Level 1: CTA `rank` sums every CTA's counts for its share of the
-      // bins -- descending positions [rank*S, rank*S + S), i.e. bins
-      // [nbins - (rank+1)*S, nbins - rank*S) -- with 16-byte remote loads.
-      const int S = nbins / (int)cs;
-      const int q4 = S / 4;
-      const int share_lo = nbins - ((int)rank + 1) * S;
-      uint32_t* red = sh.red[pass & 1];
-      cluster_sync();  // every local histogram of this pass is final
-      for (int i = threadIdx.x; i < q4 * (int)cs; i += kSelThreads) {
-        const int p = i / q4, v = i - p * q4;
-        const uint4 x = ld_dsmem_v4(map_shared_rank(&hist[share_lo + 4 * v], (uint32_t)p));
-        *reinterpret_cast<uint4*>(&sh.stage[p * S + 4 * v]) = x;
-      }
-      __syncthreads();
-      int part = 0;
-      for (int b = threadIdx.x; b < S; b += kSelThreads) {
-        uint32_t v = 0;
-        for (int p = 0; p < (int)cs; ++p) v += sh.stage[p * S + b];
-        red[b] = v;
-        part += (int)v;
-      }
-      int2 tot;
-      block_scan2(part, 0, sh.warp_scan, tot);
-      if (threadIdx.x == 0) sh.share_tot[pass & 1] = (uint32_t)tot.x;
-      cluster_sync();  // every share is reduced
-      // Level 2: the share holding the k_rem-th key (shares in descending
-      // order belong to ranks 0, 1, ...), then the bin inside it.
-      if (warp == 0) {
-        uint32_t st = 0;
-        if (lane < (int)cs) st = ld_dsmem_u32(map_shared_rank(&sh.share_tot[pass & 1], (uint32_t)lane));
-        int incl = (int)st;
+    });
+  }
+  __syncthreads();
+  find_bin(fx, kHistBins, kHistCopies, 0, a.k);
+  const uint32_t b0 = (uint32_t)fx.info[0];
+  const int above0 = fx.info[1];
+  const int cnt0 = fx.info[2];
+
+  uint32_t prefix = b0;
+  int shift = 21;
+  int k_rem = a.k - above0;
+  const int m_list = above0 + cnt0;  // entries with top bits >= b0
+  const bool use_list = m_list <= a.list_cap;
+
+  // ---- 2. ordered compaction of the entries with top bits >= b0 --------
+  // (resident rows: segment per warp over the whole row; streamed rows:
+  // segment per warp within each piece)
+  auto compact = [&](const float* sm, int bulk, const float* gl, int base, int cnt, bool keys_in_sm,
+                     int& run) {
+    const int seg = warp_segment(cnt);
+    const int w_lo = min(cnt, warp * seg), w_hi = min(cnt, w_lo + seg);
+    int c = 0;
+    for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
+      uint32_t kk[4];
+      load4_keys(sm, bulk, gl, c0 + 4 * lane, w_hi, keys_in_sm, kk);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int excl = incl - (int)st;
-        if (lane < (int)cs && excl < k_rem && k_rem <= incl) {
-          sh.bin_info[3] = lane;
-          sh.bin_info[1] = excl;
+      for (int e = 0; e < 4; ++e) c += (c0 + 4 * lane + e < w_hi) && (kk[e] >> 21) >= b0;
+    }
+    c = __reduce_add_sync(0xffffffffu, c);
+    int2 tot;
+    int pos = run + warp_bases(fx, 0, c, 0, tot).x;
+    for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
+      const int i = c0 + 4 * lane;
+      uint32_t kk[4];
+      load4_keys(sm, bulk, gl, i, w_hi, keys_in_sm, kk);
+      bool f[4];
+      unsigned bf[4];
+      int before = 0, all = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[e] = (i + e < w_hi) && (kk[e] >> 21) >= b0;
+        bf[e] = __ballot_sync(0xffffffffu, f[e]);
+        before += __popc(bf[e] & lt_mask);
+        all += __popc(bf[e]);
+      }
+      int o = pos + before;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (f[e]) {
+          list_idx[o] = base + i + e;
+          list_key[o] = kk[e];
+          ++o;
         }
       }
-      __syncthreads();
-      const int owner = sh.bin_info[3];
-      const int above_share = sh.bin_info[1];
-      for (int v = threadIdx.x; v < q4; v += kSelThreads)
-        *reinterpret_cast<uint4*>(&sh.stage[4 * v]) = ld_dsmem_v4(map_shared_rank(&red[4 * v], (uint32_t)owner));
-      __syncthreads();
-      const int owner_lo = nbins - (owner + 1) * S;
-      find_bin(sh, S, above_share, k_rem, [&](int d) { return sh.stage[S - 1 - d]; });
-      bin = owner_lo + (S - 1 - sh.bin_info[0]);
+      pos += all;
     }
-    k_rem -= sh.bin_info[1];
-    const int bin_count = sh.bin_info[2];
-    prefix = pass == 0 ? (uint32_t)bin : ((prefix << bits) | (uint32_t)bin);
-    shift = nshift;
+    run += tot.x;
+  };
+  if (use_list) {
+    int run = 0;
+    if (a.resident) compact(row_area, n, r.row, 0, n, true, run);
+    else rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+      compact(sm, bulk, gl, base, cnt, false, run);
+    });
     __syncthreads();
-    if (bin_count == k_rem) break;  // the whole bin is selected
+  }
+
+  // ---- 3. exact threshold: two more radix passes ------------------------
+  if (cnt0 != k_rem) {
+    for (int pass = 1; pass < 3; ++pass) {
+      const int bits = pass == 1 ? 11 : 10;
+      const int nbins = 1 << bits;
+      const int nshift = shift - bits;
+      const uint32_t mask = (uint32_t)nbins - 1u;
+      for (int i = threadIdx.x; i < nbins; i += kSelThreads) fx.hist[0][i] = 0;
+      __syncthreads();
+      auto add = [&](uint32_t kq) {
+        if ((kq >> shift) == prefix) atomicAdd(&fx.hist[0][(kq >> nshift) & mask], 1u);
+      };
+      if (use_list) {
+        for (int i = threadIdx.x; i < m_list; i += kSelThreads) add(list_key[i]);
+      } else if (a.resident) {
+        const uint32_t* keys = reinterpret_cast<const uint32_t*>(row_area);
+        for (int i = threadIdx.x; i < n; i += kSelThreads) add(keys[i]);
+      } else {
+        rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+          const int i = 4 * threadIdx.x;
+          if (i < cnt) {
+            uint32_t kk[4];
+            load4_keys(sm, bulk, gl, i, cnt, false, kk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (i + e < cnt) add(kk[e]);
+          }
+        });
+      }
+      __syncthreads();
+      find_bin(fx, nbins, 1, 0, k_rem);
+      const uint32_t bin = (uint32_t)fx.info[0];
+      k_rem -= fx.info[1];
+      const int bin_count = fx.info[2];
+      prefix = (prefix << bits) | bin;
+      shift = nshift;
+      if (bin_count == k_rem) break;  // the whole bin is selected
+    }
   }
   const int need = k_rem;  // keys equal to the threshold prefix to take
 
-  // ---- emission in ascending index order --------------------------------
-  // Each warp owns a contiguous piece of the slice, walked in chunks of 128
-  // (4 consecutive keys per lane).
-  const int piece = (((len + kSelWarps - 1) / kSelWarps) + 127) & ~127;
-  const int w_lo = min(len, warp * piece);
-  const int w_hi = min(len, w_lo + piece);
-  int gt = 0, eq = 0;
-  for (int i = w_lo + 4 * lane; i < w_hi; i += 128) {
-    const uint4 v = *reinterpret_cast<const uint4*>(keys + i);
-    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+  // ---- 4. emission in ascending index order -----------------------------
+  int run_gt = 0, run_eq = 0;  // above / equal keys before the current piece
+  // items [0, cnt) of a piece whose keys come from key4(i, kk) and whose
+  // indices are index(i)
+  auto emit_piece = [&](auto key4, auto index, int cnt) {
+    const int seg = warp_segment(cnt);
+    const int w_lo = min(cnt, warp * seg), w_hi = min(cnt, w_lo + seg);
+    int g = 0, q = 0;
+    for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
+      uint32_t kk[4];
+      key4(c0 + 4 * lane, w_hi, kk);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i + e < w_hi) {
+      for (int e = 0; e < 4; ++e) {
+        const bool in = c0 + 4 * lane + e < w_hi;
         const uint32_t hb = kk[e] >> shift;
-        gt += hb > prefix;
-        eq += hb == prefix;
+        g += in && hb > prefix;
+        q += in && hb == prefix;
       }
     }
-  }
-  gt = __reduce_add_sync(0xffffffffu, gt);
-  eq = __reduce_add_sync(0xffffffffu, eq);
-  // Warp bases inside the CTA (only lane 0's counts enter the scan).
-  int2 cta_tot;
-  int2 wbase = block_scan2(lane == 0 ? gt : 0, lane == 0 ? eq : 0, sh.warp_scan, cta_tot);
-  wbase.x = __shfl_sync(0xffffffffu, wbase.x, 0);
-  wbase.y = __shfl_sync(0xffffffffu, wbase.y, 0);
-  // CTA bases inside the cluster.
-  int cta_gt = 0, cta_eq = 0;
-  if (cs > 1) {
-    if (threadIdx.x == 0) sh.cta_counts = cta_tot;
-    cluster_sync();
-    if (warp == 0) {
-      int cx = 0, cy = 0;
-      if (lane < (int)rank) {
-        const uint32_t addr = map_shared_rank(&sh.cta_counts, (uint32_t)lane);
-        cx = (int)ld_dsmem_u32(addr);
-        cy = (int)ld_dsmem_u32(addr + 4);
+    g = __reduce_add_sync(0xffffffffu, g);
+    q = __reduce_add_sync(0xffffffffu, q);
+    int2 tot;
+    const int2 wb = warp_bases(fx, 0, g, q, tot);
+    int gt_b = run_gt + wb.x, eq_b = run_eq + wb.y;
+    for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
+      const int i = c0 + 4 * lane;
+      uint32_t kk[4];
+      key4(i, w_hi, kk);
+      bool fg[4], fq[4];
+      unsigned bg[4], bq[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool in = i + e < w_hi;
+        const uint32_t hb = kk[e] >> shift;
+        fg[e] = in && hb > prefix;
+        fq[e] = in && hb == prefix;
+        bg[e] = __ballot_sync(0xffffffffu, fg[e]);
+        bq[e] = __ballot_sync(0xffffffffu, fq[e]);
       }
-      cx = __reduce_add_sync(0xffffffffu, cx);
-      cy = __reduce_add_sync(0xffffffffu, cy);
-      if (lane == 0) {
-        sh.bin_info[0] = cx;
-        sh.bin_info[1] = cy;
+      int gb = gt_b, qb = eq_b, ng = 0, nq = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        gb += __popc(bg[e] & lt_mask);
+        qb += __popc(bq[e] & lt_mask);
+        ng += __popc(bg[e]);
+        nq += __popc(bq[e]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (fg[e] || (fq[e] && qb < need)) emit_one<kMode>(a, r, index(i + e), gb + min(qb, need));
+        gb += fg[e];
+        qb += fq[e];
+      }
+      gt_b += ng;
+      eq_b += nq;
     }
-    __syncthreads();
-    cta_gt = sh.bin_info[0];
-    cta_eq = sh.bin_info[1];
+    run_gt += tot.x;
+    run_eq += tot.y;
+  };
+  if (use_list) {
+    emit_piece([&](int i, int hi, uint32_t(&kk)[4]) {
+                 if (i + 3 < hi) {
+                   const uint4 v = *reinterpret_cast<const uint4*>(list_key + i);
+                   kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
+                 } else {
+#pragma unroll
+                   for (int e = 0; e < 4; ++e) kk[e] = i + e < hi ? list_key[i + e] : 0u;
+                 }
+               },
+               [&](int i) { return (int64_t)list_idx[i]; }, m_list);
+  } else if (a.resident) {
+    const uint32_t* keys = reinterpret_cast<const uint32_t*>(row_area);
+    emit_piece([&](int i, int hi, uint32_t(&kk)[4]) {
+                 load4_keys(row_area, n, r.row, i, hi, true, kk);
+               },
+               [&](int i) { return (int64_t)i; }, n);
+    (void)keys;
+  } else {
+    rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+      emit_piece([&](int i, int hi, uint32_t(&kk)[4]) { load4_keys(sm, bulk, gl, i, hi, false, kk); },
+                 [&](int i) { return (int64_t)base + i; }, cnt);
+    });
   }
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int run_gt = cta_gt + wbase.x;  // keys above the threshold before this chunk
-  int run_eq = cta_eq + wbase.y;  // keys equal to it before this chunk
-  for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
-    const int i0 = c0 + 4 * lane;
-    uint4 kq = make_uint4(0u, 0u, 0u, 0u);
-    if (i0 < w_hi) kq = *reinterpret_cast<const uint4*>(keys + i0);
-    const uint32_t kk[4] = {kq.x, kq.y, kq.z, kq.w};
-    bool f_gt[4], f_eq[4];
-    unsigned b_gt[4], b_eq[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t hb = kk[e] >> shift;
-      const bool in = i0 + e < w_hi;
-      f_gt[e] = in && hb > prefix;
-      f_eq[e] = in && hb == prefix;
-      b_gt[e] = __ballot_sync(0xffffffffu, f_gt[e]);
-      b_eq[e] = __ballot_sync(0xffffffffu, f_eq[e]);
-    }
-    if ((b_gt[0] | b_gt[1] | b_gt[2] | b_gt[3] | b_eq[0] | b_eq[1] | b_eq[2] | b_eq[3]) == 0u)
-      continue;  // nothing selected in this chunk (warp-uniform)
-    int eq_rank = run_eq;  // keys equal to the threshold before this lane's first key
-    int n_gt = 0, n_eq = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      eq_rank += __popc(b_eq[e] & lt_mask);
-      n_gt += __popc(b_gt[e]);
-      n_eq += __popc(b_eq[e]);
-    }
-    bool sel[4];
-    unsigned b_sel[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sel[e] = f_gt[e] || (f_eq[e] && eq_rank < need);
-      eq_rank += f_eq[e];
-      b_sel[e] = __ballot_sync(0xffffffffu, sel[e]);
-    }
-    int out = run_gt + min(run_eq, need);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) out += __popc(b_sel[e] & lt_mask);
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (sel[e]) emit_one<kMode>(a, sh, t, pt_row, pt0, pt_n, (int64_t)lo + i0 + e, out++);
-    run_gt += n_gt;
-    run_eq += n_eq;
-  }
-  if (rank == 0) emit_tail<kMode>(a, t, pt_row, a.k, L);
-  if (cs > 1) cluster_sync();  // peers may still read this CTA's shared memory
+  emit_tail<kMode>(a, r, a.k);
 }
 
 }  // namespace qsa

@@ -132,10 +132,29 @@ def test_topk_parity_ragged(qsa, dist, k):
     run_topk(qsa, topk_workload(31, 9, 6000, k=k, dist=dist, ragged=True), k)
 
 
-@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (200, 3000)])
-def test_topk_parity_cluster_shapes(qsa, n_rows, n):
-    """Shapes that select clusters of 8, 4-8, 1-2 and 1 CTAs per row."""
+@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (200, 3000),
+                                      (5, 32_768), (2, 32_772)])
+def test_topk_parity_row_lengths(qsa, n_rows, n):
+    """Rows kept in shared memory (<= 32,768 scores) and rows streamed through
+    the bulk-copy ring, around the boundary between the two."""
     run_topk(qsa, topk_workload(32, n_rows, n, k=2048, dist="fp16dup"))
+
+
+@pytest.mark.parametrize("n", [20_000, 45_000])
+def test_topk_heavy_ties_take_the_full_row_path(qsa, n):
+    """So many scores share the boundary bin that the candidate list would
+    overflow: the exact passes and the emission run over the whole row."""
+    rng = np.random.default_rng(n)
+    s = np.zeros((4, n), np.float32)
+    s[0] = 1.5                                              # all equal
+    s[1] = rng.integers(0, 3, size=n).astype(np.float32)    # three values
+    s[2] = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)  # one top-bits bin
+    s[3] = rng.standard_normal(n).astype(np.float32)        # ordinary row beside them
+    nv = np.full(4, n, np.int32)
+    for k in [512, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
 
 
 @pytest.mark.parametrize("dist", TOPK_DISTS)
