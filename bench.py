@@ -43,6 +43,29 @@ METRIC = "indexer+top-k query rows/sec at L=80k decode; achieved HBM GB/s vs roo
 L2_FLUSH_BYTES = 256 << 20
 
 
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    capture (profiles/traffic.json), or None once the kernel's source no
+    longer matches the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec or workload not in rec:
+        return None
+    m = hashlib.sha256()
+    for f in rec["sources"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        m.update(open(fp, "rb").read())
+    if m.hexdigest() != rec["csrc_sha256"]:
+        return None
+    w = rec[workload]
+    return int(w["dram_read_bytes"]) + int(w["dram_write_bytes"])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -498,7 +521,8 @@ def main():
         "step_frac_hbm": step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "kernel": "score_decode_kernel", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None, "alg_bytes_per_launch": score_bytes,
+                     "traffic": captured_traffic("score_decode_kernel", w.name),
+                     "alg_bytes_per_launch": score_bytes,
                      "us_per_launch": 1e3 * score_ms,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst)"},
         "e2e": {"value": ws * w.n_rows / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,

@@ -55,6 +55,7 @@ constexpr int kSelPiece = 4096;          // elements per bulk piece (16 KB)
 constexpr int kSelRing = 4;              // ring stages for streamed rows
 constexpr int kSelResidentCap = 32768;   // longest row kept in shared memory
 constexpr int kSelMaxBars = 8;           // >= kSelResidentCap / kSelPiece and kSelRing
+constexpr int kSelSampleMin = 4096;      // shorter rows take the exact histogram directly
 
 enum SelectMode { kModeTopk = 0, kModeQsa = 1 };
 
@@ -366,7 +367,7 @@ select_kernel(SelectArgs a) {
     return;
   }
 
-  // ---- 1. histogram of the top 11 bits ---------------------------------
+  // ---- 0. load: resident rows are pulled into shared memory as keys -----
   uint32_t* hcopy = fx.hist[warp & (kHistCopies - 1)];
   RowStream rs{n, r.row, a.vec_ok, fx.bar, row_area, 0};
   if (a.resident) {
@@ -391,43 +392,20 @@ select_kernel(SelectArgs a) {
         load4_keys(row_area + base, bulk, r.row + base, i, cnt, false, kk);
         uint32_t* dst = reinterpret_cast<uint32_t*>(row_area + base);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (i + e < cnt) {
-            dst[i + e] = kk[e];
-            atomicAdd(&hcopy[kk[e] >> 21], 1u);
-          }
-        }
+        for (int e = 0; e < 4; ++e)
+          if (i + e < cnt) dst[i + e] = kk[e];
       }
     }
-  } else {
-    rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
-      const int i = 4 * threadIdx.x;
-      if (i < cnt) {
-        uint32_t kk[4];
-        load4_keys(sm, bulk, gl, i, cnt, false, kk);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (i + e < cnt) atomicAdd(&hcopy[kk[e] >> 21], 1u);
-      }
-    });
+    __syncthreads();
   }
-  __syncthreads();
-  find_bin(fx, kHistBins, kHistCopies, 0, a.k);
-  const uint32_t b0 = (uint32_t)fx.info[0];
-  const int above0 = fx.info[1];
-  const int cnt0 = fx.info[2];
 
-  uint32_t prefix = b0;
-  int shift = 21;
-  int k_rem = a.k - above0;
-  const int m_list = above0 + cnt0;  // entries with top bits >= b0
-  const bool use_list = m_list <= a.list_cap;
-
-  // ---- 2. ordered compaction of the entries with top bits >= b0 --------
-  // (resident rows: segment per warp over the whole row; streamed rows:
-  // segment per warp within each piece)
+  // ---- 2. ordered compaction of the entries whose top 11 bits are >= b0
+  // into the list: each warp owns a segment of the piece, counts, and after
+  // one barrier writes its matches at ballot-prefix positions.  Writing
+  // stops (overflow) once the list would exceed its capacity.
+  bool overflow = false;
   auto compact = [&](const float* sm, int bulk, const float* gl, int base, int cnt, bool keys_in_sm,
-                     int& run) {
+                     uint32_t b0, int& run) {
     const int seg = warp_segment(cnt);
     const int w_lo = min(cnt, warp * seg), w_hi = min(cnt, w_lo + seg);
     int c = 0;
@@ -440,6 +418,11 @@ select_kernel(SelectArgs a) {
     c = __reduce_add_sync(0xffffffffu, c);
     int2 tot;
     int pos = run + warp_bases(fx, 0, c, 0, tot).x;
+    if (run + tot.x > a.list_cap) {  // uniform: totals are the CTA's
+      overflow = true;
+      run += tot.x;
+      return;
+    }
     for (int c0 = w_lo; c0 < w_hi; c0 += 128) {
       const int i = c0 + 4 * lane;
       uint32_t kk[4];
@@ -467,26 +450,99 @@ select_kernel(SelectArgs a) {
     }
     run += tot.x;
   };
-  if (use_list) {
+  auto compact_row = [&](uint32_t b0) {
     int run = 0;
-    if (a.resident) compact(row_area, n, r.row, 0, n, true, run);
-    else rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
-      compact(sm, bulk, gl, base, cnt, false, run);
-    });
+    overflow = false;
+    if (a.resident) {
+      compact(row_area, n, r.row, 0, n, true, b0, run);
+    } else {
+      rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+        if (!overflow) compact(sm, bulk, gl, base, cnt, false, b0, run);
+      });
+    }
     __syncthreads();
+    return run;
+  };
+
+  // ---- 1. a lower bound b0 for the top bits of the k-th key -------------
+  // Sample 1024 keys at even strides; take the bin of the sample's r-th
+  // largest key, r set so that about 1.5k + 8n/1024 keys of the row are
+  // expected at or above it.  The estimate only steers the work: if the
+  // list ends up with fewer than k entries (b0 too high) or overflows, the
+  // exact histogram of the whole row decides b0 instead.
+  uint32_t prefix = 0;
+  int shift = 32;
+  int k_rem = a.k;
+  int m_list = 0;
+  bool use_list = false;
+  int first_pass = 0;
+  if (n >= kSelSampleMin) {
+    {
+      const int64_t i = (int64_t)threadIdx.x * n / kSelThreads;
+      const uint32_t kq = a.resident ? reinterpret_cast<const uint32_t*>(row_area)[i]
+                                     : order_key(__ldg(r.row + i));
+      atomicAdd(&fx.hist[0][kq >> 21], 1u);
+    }
+    __syncthreads();
+    const int target = min(kSelThreads, (int)((3LL * a.k * kSelThreads + 2LL * n - 1) / (2LL * n)) + 8);
+    find_bin(fx, kHistBins, 1, 0, target);
+    const uint32_t b_s = (uint32_t)fx.info[0];
+    m_list = compact_row(b_s);
+    use_list = !overflow && m_list >= a.k;
+  }
+  if (!use_list) {
+    // exact: histogram of the top 11 bits over the whole row
+    for (int i = threadIdx.x; i < kHistCopies * kHistBins; i += kSelThreads) (&fx.hist[0][0])[i] = 0;
+    __syncthreads();
+    if (a.resident) {
+      const uint32_t* keys = reinterpret_cast<const uint32_t*>(row_area);
+      for (int i = 4 * threadIdx.x; i < n; i += 4 * kSelThreads) {
+        uint32_t kk[4];
+        load4_keys(row_area, n, r.row, i, n, true, kk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < n) atomicAdd(&hcopy[kk[e] >> 21], 1u);
+      }
+      (void)keys;
+    } else {
+      rs.walk([&](const float* sm, int bulk, const float* gl, int base, int cnt) {
+        const int i = 4 * threadIdx.x;
+        if (i < cnt) {
+          uint32_t kk[4];
+          load4_keys(sm, bulk, gl, i, cnt, false, kk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (i + e < cnt) atomicAdd(&hcopy[kk[e] >> 21], 1u);
+        }
+      });
+    }
+    __syncthreads();
+    find_bin(fx, kHistBins, kHistCopies, 0, a.k);
+    const uint32_t b0 = (uint32_t)fx.info[0];
+    const int above0 = fx.info[1];
+    const int cnt0 = fx.info[2];
+    prefix = b0;
+    shift = 21;
+    k_rem = a.k - above0;
+    first_pass = 1;
+    if (above0 + cnt0 <= a.list_cap) {
+      m_list = compact_row(b0);
+      use_list = true;
+    }
+    if (cnt0 == k_rem) first_pass = 3;  // the whole bin is selected
   }
 
-  // ---- 3. exact threshold: two more radix passes ------------------------
-  if (cnt0 != k_rem) {
-    for (int pass = 1; pass < 3; ++pass) {
-      const int bits = pass == 1 ? 11 : 10;
+  // ---- 3. exact threshold: radix passes (11, 11, 10 bits) ---------------
+  {
+    for (int pass = first_pass; pass < 3; ++pass) {
+      const int bits = pass < 2 ? 11 : 10;
       const int nbins = 1 << bits;
       const int nshift = shift - bits;
       const uint32_t mask = (uint32_t)nbins - 1u;
       for (int i = threadIdx.x; i < nbins; i += kSelThreads) fx.hist[0][i] = 0;
       __syncthreads();
       auto add = [&](uint32_t kq) {
-        if ((kq >> shift) == prefix) atomicAdd(&fx.hist[0][(kq >> nshift) & mask], 1u);
+        if (shift == 32 || (kq >> shift) == prefix) atomicAdd(&fx.hist[0][(kq >> nshift) & mask], 1u);
       };
       if (use_list) {
         for (int i = threadIdx.x; i < m_list; i += kSelThreads) add(list_key[i]);
@@ -510,7 +566,7 @@ select_kernel(SelectArgs a) {
       const uint32_t bin = (uint32_t)fx.info[0];
       k_rem -= fx.info[1];
       const int bin_count = fx.info[2];
-      prefix = (prefix << bits) | bin;
+      prefix = shift == 32 ? bin : ((prefix << bits) | bin);
       shift = nshift;
       if (bin_count == k_rem) break;  // the whole bin is selected
     }

@@ -141,6 +141,24 @@ def test_topk_parity_row_lengths(qsa, n_rows, n):
 
 
 @pytest.mark.parametrize("n", [20_000, 45_000])
+def test_topk_misleading_sample_falls_back_to_exact_histogram(qsa, n):
+    """The selection first estimates a lower bound for the k-th key from
+    1024 evenly strided scores (positions floor(j*n/1024)).  Planting the
+    largest values exactly there makes the estimate too high (fewer than k
+    candidates); the exact whole-row histogram must take over."""
+    rng = np.random.default_rng(n + 1)
+    s = (rng.standard_normal((2, n)) * 0.01).astype(np.float32)
+    pos = (np.arange(1024, dtype=np.int64) * n) // 1024
+    s[0, pos] = 100.0 + rng.standard_normal(1024).astype(np.float32)
+    s[1, pos] = 5.0
+    nv = np.full(2, n, np.int32)
+    for k in [1500, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
+@pytest.mark.parametrize("n", [20_000, 45_000])
 def test_topk_heavy_ties_take_the_full_row_path(qsa, n):
     """So many scores share the boundary bin that the candidate list would
     overflow: the exact passes and the emission run over the whole row."""
