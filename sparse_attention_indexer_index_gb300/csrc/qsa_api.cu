@@ -12,6 +12,7 @@
 #include "compress.cuh"
 #include "expand.cuh"
 #include "score_decode.cuh"
+#include "score_tc.cuh"
 #include "select.cuh"
 
 using namespace qsa;
@@ -19,6 +20,11 @@ using namespace qsa;
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Tensor-core scorer limits: rows per tile (N = 4 rows <= 256 columns) and
+// the largest shared-memory request (occupancy may be limited with it).
+constexpr int kTcMaxRowsPerTile = 64;
+constexpr int kTcMinRows = 2;  // requests with this many rows or more use the tensor cores
+constexpr int kTcMaxSmem = 227 * 1024;
 // Shared-memory plan of the selection kernel: candidate list and staged
 // page-table entries per CTA, and the largest dynamic size it may use.
 constexpr int kSelListCap = 6144;
@@ -49,7 +55,11 @@ qsa_status device_info(DeviceInfo** out) {
         cudaFuncSetAttribute(select_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kScoreSmem) != cudaSuccess)
+                             (int)kScoreSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return QSA_ERR_CUDA;
     d.ready = true;
   }
@@ -130,6 +140,64 @@ qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream) {
   if (cudaLaunchKernelEx(&cfg, select_kernel<kMode>, a) != cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
+// Tensor-core scorer for requests with several rows: tiles of 128 keys x up
+// to 64 rows (N = 4 * rows, multiple of 16), a group of key tiles per CTA
+// when rows are plentiful (prefill), one otherwise (decode verify).  The
+// dynamic shared memory is raised if needed so that the CTAs resident on an
+// SM never ask for more than the 512 TMEM columns.
+qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_count,
+                            cudaStream_t stream) {
+  const int64_t nb_max = s.max_len / kBlock;
+  if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
+  TcArgs t{};
+  t.q = s.q;
+  t.pool = s.pool;
+  t.pool_rows = s.pool_rows;
+  t.n_req = s.n_req;
+  t.req_row_start = s.req_row_start;
+  t.n_rows = s.n_rows;
+  t.row_len = s.row_len;
+  t.max_len = s.max_len;
+  t.page_table = s.page_table;
+  t.ld_pt = s.ld_pt;
+  t.page_size = s.page_size;
+  t.scores = s.scores;
+  t.ld_scores = s.ld_scores;
+  t.rows_per_tile = std::min(kTcMaxRowsPerTile, max_rows_per_req);
+  t.n_cols = ((4 * t.rows_per_tile) + 15) & ~15;
+  int cols = 32;
+  while (cols < t.n_cols) cols *= 2;
+  t.tmem_cols = cols;
+  t.trigger_dependents = s.trigger_dependents;
+  const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
+  const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
+  if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
+  const size_t smem = 1024 + (size_t)kTcStages * 2 * kTcHalf + 2 * (size_t)t.n_cols * 128 + 16 +
+                      4 * (size_t)t.rows_per_tile + 4 * (size_t)kTcPtStage;
+  if (smem > (size_t)kTcMaxSmem) return QSA_ERR_UNSUPPORTED;
+  // resident CTAs per SM (shared memory bound; with the 4-stage ring this is
+  // one) must never ask for more than the 512 TMEM columns
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tc_kernel, kTcThreads, smem) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
+  // Key tiles per CTA: about one wave of CTAs in total, consecutive tiles of
+  // a CTA double-buffered (a lone CTA per tile pays its set-up every time).
+  const int64_t wave = (int64_t)std::max(occ, 1) * sm_count;
+  const int64_t x_ctas = std::max<int64_t>(1, std::min<int64_t>(n_kt, wave / (row_tiles * s.n_req)));
+  t.tiles_per_cta = (int32_t)((n_kt + x_ctas - 1) / x_ctas);
+  dim3 grid((unsigned)((n_kt + t.tiles_per_cta - 1) / t.tiles_per_cta), (unsigned)row_tiles,
+            (unsigned)s.n_req);
+  score_tc_kernel<<<grid, kTcThreads, smem, stream>>>(t);
+  if (qsa_status e = launch_status()) return e;
+  if (s.n_fill > 0) {
+    fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
+                                                              s.n_fill);
+    return launch_status();
   }
   return QSA_OK;
 }
@@ -240,7 +308,6 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
                             int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
                             int64_t ld_pt, int32_t page_size, float* scores, int64_t ld_scores,
                             int64_t n_fill, void* stream) {
-  (void)max_rows_per_req;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
   if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
@@ -252,6 +319,8 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld_scores, n_fill, 0};
+  if (max_rows_per_req >= kTcMinRows)
+    return launch_scores_tc(s, max_rows_per_req, d->sm_count, static_cast<cudaStream_t>(stream));
   return launch_scores(s, d->sm_count, static_cast<cudaStream_t>(stream));
 }
 
@@ -324,7 +393,6 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
                               int32_t* out_pos, int32_t* out_slots, float* scores_out,
                               int64_t ld_scores, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  (void)max_rows_per_req;
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
@@ -351,7 +419,9 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld, 0, 1};
-  if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
+  if (qsa_status e = max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, d->sm_count, st)
+                                                     : launch_scores(s, d->sm_count, st))
+    return e;
 
   SelectArgs a{};
   a.scores = scores;
@@ -417,7 +487,6 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
     int32_t n_rows, const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
     const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
     int32_t* out_pos, int32_t* out_slots, void* stream) {
-  (void)max_rows_per_req;
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
@@ -437,7 +506,9 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld, 0, 1};
-  if (qsa_status e = launch_scores(s, d->sm_count, st)) return e;
+  if (qsa_status e = max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, d->sm_count, st)
+                                                     : launch_scores(s, d->sm_count, st))
+    return e;
 
   SelectArgs a{};
   a.scores = scores;

@@ -1,0 +1,335 @@
+// score_tc.cuh -- block scorer on the 5th-generation tensor cores (tcgen05).
+//
+// Qwen3.8-Flash-Next day-0 write-up (theainews.cc), section "Qwen sparse
+// attention (QSA)": prefill scores many query rows against the compressed
+// keys with a custom kernel; the score equation is
+//   s[t][b] = (1/sqrt(128)) * sum_{h<4} ReLU(<q[t][h], kbar[b]>).
+// With several query rows per request the 4 head dot products of every row
+// against every key form a dense contraction, so they run on the tensor
+// cores:
+//   D[key][c] = sum_k K[key][k] * Q[c][k],   c = 4*row + head,
+// with M = 128 keys per tile (TMEM lanes), N = 4 * rows per tile (rounded up
+// to a multiple of 16, zero-padded), K = 128 in 8 steps of 16 (BF16 inputs,
+// FP32 accumulation in TMEM).  Both operands are K-major in shared memory
+// with the 128-byte swizzle, filled by 16-byte cp.async pieces (keys come
+// from scattered pages, so every 256-byte key row is fetched on its own).
+// One thread issues the MMAs and commits them to an mbarrier; the epilogue
+// reads TMEM (each warp its 32 lanes = 32 keys), applies ReLU, sums the 4
+// head columns of each row, scales, and stores the FP32 scores (coalesced:
+// consecutive keys of one row).  A CTA keeps its query rows resident and
+// walks a group of key tiles through a 4-stage ring of key buffers, so the
+// loads of the next three tiles overlap this tile's MMA and epilogue (one
+// CTA per SM keeps ~96 KB of keys in flight).
+//
+// Every wait is bounded (a timeout latches kFaultWait and the CTA frees its
+// tensor memory before leaving).
+#pragma once
+#include "common.cuh"
+
+namespace qsa {
+
+constexpr int kTcThreads = 512;           // 16 warps: all issue key copies; TMEM lane quarter = warp % 4
+constexpr int kTcM = 128;                 // keys per tile
+constexpr int kTcHalf = kTcM * 128;       // bytes of one K-half of the key tile (128 rows x 128 B)
+constexpr int kTcStages = 4;              // key tiles in flight per CTA (ring of 32 KB stages)
+constexpr int kTcPtStage = 4096;          // page-table entries staged in shared memory per CTA
+
+struct TcArgs {
+  const __nv_bfloat16* q;       // [n_rows][4][128]
+  const __nv_bfloat16* pool;    // [pool_rows][128]
+  int64_t pool_rows;
+  int32_t n_req;
+  const int32_t* req_row_start; // [n_req+1]
+  int32_t n_rows;
+  const int32_t* row_len;       // [n_rows]
+  int32_t max_len;
+  const int32_t* page_table;    // [n_req][ld_pt]
+  int64_t ld_pt;
+  int32_t page_size;
+  float* scores;                // [n_rows][ld_scores]
+  int64_t ld_scores;
+  int32_t rows_per_tile;        // RT <= 64
+  int32_t n_cols;               // N = round16(4 * RT)
+  int32_t tmem_cols;            // power of two >= max(32, N)
+  int32_t tiles_per_cta;        // key tiles walked by one CTA
+  int32_t trigger_dependents;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (tcgen05, cp.async).
+// ---------------------------------------------------------------------------
+// No memory clobber: the copies are ordered by cp.async.wait_group, the proxy
+// fence and the CTA barrier that follow them, and without it the compiler may
+// hoist the address loads of later copies above earlier ones.
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// K-major, 128-byte swizzle shared-memory matrix descriptor: start address,
+// stride between 8-row groups = 1024 B, descriptor version 1, layout 2.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                               // leading byte offset (unused, 16 B)
+  d |= (uint64_t)(1024 >> 4) << 32;                     // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                               // descriptor version
+  d |= (uint64_t)2 << 61;                               // 128-byte swizzle
+  return d;
+}
+// kind::f16 instruction descriptor: D = F32, A = B = BF16, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+        "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+        "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+        "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk c (0..15 along the 256-byte key row) of row r
+// in a [2 K-halves][rows][128 B] region with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
+  const int kh = c >> 3, cc = c & 7;
+  return (uint32_t)(kh * rows * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
+}
+
+// Load key tile `kt` of request r (blocks [kt*128, kt*128 + 128) clipped to
+// nb) into the swizzled A buffer; rows past nb or on bad pages are zero.
+// Thread t copies 16-byte chunk t % 16 of rows t/16 + 32j (j < 4): its
+// page-table entries are looked up first, then its copies are issued.
+// (cp.async throughput grows with the number of issuing warps, hence 16.)
+// Page-table entries [pt0, pt0 + pt_n) of the CTA's key range are staged in
+// shared memory (pt_s); others are read from global memory.
+__device__ __forceinline__ void tc_load_keys(const TcArgs& a, int r, int kt, int nb, unsigned char* buf,
+                                             const int32_t* pt_s, int pt0, int pt_n) {
+  constexpr int kRowStep = kTcThreads / 16;  // 32
+  constexpr int kRowsPerThread = kTcM / kRowStep;  // 4
+  const int kpp = a.page_size / kBlock;
+  const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
+  const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
+  int64_t prow[kRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kRowsPerThread; ++j) {
+    const int b = kt * kTcM + r0 + kRowStep * j;
+    prow[j] = -1;
+    if (b < nb) {
+      const int page_idx = b / kpp;
+      if (page_idx < a.ld_pt) {
+        const int64_t page = (page_idx >= pt0 && page_idx < pt0 + pt_n) ? pt_s[page_idx - pt0]
+                                                                          : __ldg(pt_row + page_idx);
+        const int64_t pr = page * kpp + (b - page_idx * kpp);
+        if (page >= 0 && pr < a.pool_rows) prow[j] = pr;
+        else if (c == 0) raise_fault(kFaultPool);
+      } else if (c == 0) {
+        raise_fault(kFaultIndex);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRowsPerThread; ++j) {
+    const bool ok = prow[j] >= 0;
+    cp_async_16(buf + sw128_offset(r0 + kRowStep * j, c, kTcM), ok ? a.pool + prow[j] * kDim + c * 8 : a.pool,
+                ok ? 16u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads)
+score_tc_kernel(TcArgs a) {
+  extern __shared__ __align__(16) unsigned char tc_smem_raw[];
+  // layout from the first 1024-byte boundary (the swizzle atoms need it):
+  // [A stages: 4 x 32 KB][B: 2 x N x 128 B][mbarrier][TMEM address][fail flag][row lengths]
+  unsigned char* base = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
+  auto abuf = [&](int stage) { return base + (size_t)stage * 2 * kTcHalf; };
+  unsigned char* bbuf = base + (size_t)kTcStages * 2 * kTcHalf;
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(bbuf + 2 * a.n_cols * 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_nb = s_fail + 1;               // [rows_per_tile]
+  int32_t* pt_s = s_nb + a.rows_per_tile;  // [kTcPtStage]
+
+  if (a.trigger_dependents) pdl_launch_dependents();
+
+  const int r = blockIdx.z;
+  const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
+  if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
+    return;
+  }
+  if (row1 - row0 > (int)gridDim.y * a.rows_per_tile) {  // more rows than max_rows_per_req promised
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
+  }
+  const int t0 = row0 + blockIdx.y * a.rows_per_tile;
+  const int t1 = min(row1, t0 + a.rows_per_tile);
+  if (t0 >= t1) return;
+  // visible blocks of each row of the tile; the tile's key range ends at their max
+  if (threadIdx.x < t1 - t0) {
+    int L = __ldg(a.row_len + t0 + threadIdx.x);
+    if (L < 0 || L > a.max_len) { raise_fault(kFaultGrouping); L = 0; }
+    s_nb[threadIdx.x] = L / kBlock;
+  }
+  __syncthreads();
+  int nb_tile = 0;
+  for (int i = 0; i < t1 - t0; ++i) nb_tile = max(nb_tile, s_nb[i]);
+  const int n_kt = (nb_tile + kTcM - 1) / kTcM;
+  const int kt0 = blockIdx.x * a.tiles_per_cta;
+  const int kt1 = min(n_kt, kt0 + a.tiles_per_cta);
+  if (kt0 >= kt1) return;
+
+  // ---- page-table entries of this CTA's key range, staged once ------------
+  const int kpp = a.page_size / kBlock;
+  const int pt0 = (kt0 * kTcM) / kpp;
+  int pt_n = min((kt1 * kTcM - 1) / kpp + 1 - pt0, kTcPtStage);
+  if (pt_n > a.ld_pt - pt0) pt_n = (int)(a.ld_pt - pt0);
+  if (pt_n < 0) pt_n = 0;
+  {
+    const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
+    for (int i = threadIdx.x; i < pt_n; i += kTcThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
+  }
+  __syncthreads();
+
+  // ---- query rows -> B (zero rows beyond 4 * (t1 - t0)) and the first key tile
+  const int valid_cols = 4 * (t1 - t0);
+  for (int i = threadIdx.x; i < a.n_cols * 16; i += kTcThreads) {
+    const int col = i >> 4, c = i & 15;
+    const bool ok = col < valid_cols;
+    const __nv_bfloat16* src = ok ? a.q + ((int64_t)t0 * kHeads + col) * kDim + c * 8 : a.q;
+    cp_async_16(bbuf + sw128_offset(col, c, a.n_cols), src, ok ? 16u : 0u);
+  }
+  tc_load_keys(a, r, kt0, nb_tile, abuf(0), pt_s, pt0, pt_n);
+  cp_async_commit();  // group 0: B and the first key tile
+  for (int i = 1; i < kTcStages - 1; ++i) {  // groups 1..S-2: the next key tiles (or empty)
+    if (kt0 + i < kt1) tc_load_keys(a, r, kt0 + i, nb_tile, abuf(i), pt_s, pt0, pt_n);
+    cp_async_commit();
+  }
+
+  // ---- tensor memory for the accumulator ----------------------------------
+  if (threadIdx.x < 32) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(mma_bar, 1);
+    *s_fail = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t idesc = umma_idesc_bf16(kTcM, a.n_cols);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int kt = kt0; kt < kt1; ++kt) {
+    const int cur = (kt - kt0) % kTcStages;
+    // refill the stage of tile kt-1 (its MMA has completed: we waited on it)
+    // with tile kt+S-1
+    if (kt + kTcStages - 1 < kt1)
+      tc_load_keys(a, r, kt + kTcStages - 1, nb_tile, abuf((kt + kTcStages - 1 - kt0) % kTcStages), pt_s,
+                   pt0, pt_n);
+    cp_async_commit();
+    cp_async_wait<kTcStages - 1>();  // tile kt (and everything older) has landed
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(abuf(cur));
+      const uint32_t b_base = smem_u32(bbuf);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t koff = (uint32_t)(s >> 2);          // K-half index
+        const uint32_t within = (uint32_t)((s & 3) * 32);  // bytes along the 128-byte row
+        const uint64_t ad = umma_desc_sw128(a_base + koff * kTcHalf + within);
+        const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(a.n_cols * 128) + within);
+        umma_bf16(tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
+      }
+      umma_commit(mma_bar);
+    }
+    const uint32_t parity = (uint32_t)(kt - kt0) & 1u;
+    // warp-uniform outcome: the TMEM loads below are warp-collective
+    const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, parity));
+    if (!done && lane == 0) {
+      *s_fail = 1;
+      raise_fault(kFaultWait);
+    }
+    tc_fence_after();
+    if (done) {
+      // ---- epilogue: warp w reads TMEM lane quarter w % 4 (keys 32(w%4) ..
+      // +31) and the column chunks 32 * (w / 4 + 4m) ----------------------
+      const int quarter = warp & 3;
+      const int b = kt * kTcM + quarter * 32 + lane;
+      for (int c0 = 32 * (warp >> 2); c0 < a.n_cols; c0 += 32 * (kTcThreads / 128)) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int tr = c0 / 4 + j;  // row within the tile
+          if (tr < t1 - t0 && b < s_nb[tr]) {
+            float s = fmaxf(__uint_as_float(v[4 * j]), 0.f);
+            s += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
+            s += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
+            s += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
+            a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = s * kScoreScale;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // TMEM and the key buffer are free for the next tile
+    if (*s_fail) break;  // uniform: read after the barrier
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+// -inf into scores[t][b] for row_len[t]/4 <= b < n_fill (one CTA per row).
+__global__ void fill_neginf_kernel(const int32_t* row_len, int32_t max_len, float* scores, int64_t ld,
+                                   int64_t n_fill) {
+  const int t = blockIdx.x;
+  int L = __ldg(row_len + t);
+  if (L < 0 || L > max_len) L = 0;
+  for (int64_t b = L / kBlock + threadIdx.x; b < n_fill; b += blockDim.x)
+    scores[(int64_t)t * ld + b] = -__int_as_float(0x7f800000);
+}
+
+}  // namespace qsa

@@ -10,8 +10,8 @@ import pytest
 
 import oracle
 from gpu_util import bf16_dev, bf16_host, score_tolerance, to_dev
-from workloads import (c1_decode, c2_verify, c3_batched, c4_dsa_topk, decode_workload,
-                       topk_workload, TOPK_DISTS)
+from workloads import (c1_decode, c2_verify, c2_batched, c3_batched, c4_dsa_topk, c5_prefill,
+                       decode_workload, topk_workload, TOPK_DISTS)
 
 pytestmark = pytest.mark.gpu
 
@@ -220,7 +220,7 @@ def test_expand_parity(qsa, P):
 
 
 # ----------------------------------------------------------------- fused path
-def check_fused(qsa, w, sample_rows=None):
+def check_fused(qsa, w, sample_rows=None, select_rows=None):
     import torch
     pool_h = oracle_pool(w) if w.n_blocks < 200_000 else None
     if pool_h is None:
@@ -248,11 +248,22 @@ def check_fused(qsa, w, sample_rows=None):
         err = np.abs(s[t, :nb].astype(np.float64) - want[0, :nb])
         assert (err <= tol[0, :nb]).all(), (t, float(err.max()))
     # selection / expansion / slots bit-exact on the GPU's own scores
-    sel_ref, _ = oracle.topk(s, w.k_blk, n_valid=w.row_len // 4)
-    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
-    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
-    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
-    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+    if select_rows is None:
+        sel_ref, _ = oracle.topk(s, w.k_blk, n_valid=w.row_len // 4)
+        pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+        assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+        assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+        assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+    else:
+        blocks, pos, slots = (out[k].cpu().numpy() for k in ("blocks", "pos", "slots"))
+        for t in select_rows:
+            r = int(rr[t])
+            nb = int(w.row_len[t]) // 4
+            sel = oracle.topk_row(s[t, :nb], w.k_blk)
+            p_ref, s_ref = oracle.expand_row(sel, int(w.row_len[t]), w.page_table[r], w.page_size)
+            assert np.array_equal(blocks[t], sel), t
+            assert np.array_equal(pos[t], p_ref), t
+            assert np.array_equal(slots[t], s_ref), t
     return out
 
 
@@ -284,6 +295,28 @@ def test_fused_parity_c2_verify(qsa):
 def test_fused_parity_c3_batched_sampled(qsa):
     w = c3_batched(0)
     check_fused(qsa, w, sample_rows=np.arange(0, w.n_rows, 4))
+
+
+def test_fused_parity_prefill_chunk(qsa):
+    """300 consecutive query rows of one request: the tensor-core scorer with
+    several row tiles (the last one partial) and causal visibility per row."""
+    check_fused(qsa, decode_workload(53, [[4000 + i for i in range(300)]], page_size=64, k_blk=512))
+
+
+def test_fused_parity_prefill_c5_sampled(qsa):
+    """The full prefill chunk (4096 rows, L = 131,072): scores checked on 24
+    sampled rows, selection and slots on 64."""
+    w = c5_prefill(0)
+    rng = np.random.default_rng(7)
+    check_fused(qsa, w, sample_rows=np.sort(rng.choice(w.n_rows, 24, replace=False)),
+                select_rows=np.sort(rng.choice(w.n_rows, 64, replace=False)))
+
+
+def test_fused_parity_verify_batched_sampled(qsa):
+    """32 verify requests of 6 rows at L = 80,000 (tensor-core scorer, one key
+    tile per CTA): scores on every 8th row, selection on all rows."""
+    w = c2_batched(0)
+    check_fused(qsa, w, sample_rows=np.arange(0, w.n_rows, 8))
 
 
 def test_fused_workspace_path_matches_scores_out_path(qsa):
