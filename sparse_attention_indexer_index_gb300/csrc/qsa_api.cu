@@ -170,15 +170,18 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   t.rows_per_tile = std::min(kTcMaxRowsPerTile, max_rows_per_req);
   t.n_cols = ((4 * t.rows_per_tile) + 15) & ~15;
   int cols = 32;
-  while (cols < t.n_cols) cols *= 2;
+  while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
   t.tmem_cols = cols;
   t.trigger_dependents = s.trigger_dependents;
   const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
   const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
   if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
-  const size_t smem = 1024 + (size_t)kTcStages * 2 * kTcHalf + 2 * (size_t)t.n_cols * 128 + 16 +
-                      4 * (size_t)t.rows_per_tile + 4 * (size_t)kTcPtStage;
-  if (smem > (size_t)kTcMaxSmem) return QSA_ERR_UNSUPPORTED;
+  // key-ring stages: as many 32 KB stages as fit beside B and the rest
+  const size_t fixed = 1024 + 2 * (size_t)t.n_cols * 128 + 32 + 4 * (size_t)t.rows_per_tile +
+                       4 * (size_t)kTcPtStage;
+  t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / (2 * kTcHalf));
+  if (t.stages < 3) return QSA_ERR_UNSUPPORTED;
+  const size_t smem = fixed + (size_t)t.stages * 2 * kTcHalf;
   // resident CTAs per SM (shared memory bound; with the 4-stage ring this is
   // one) must never ask for more than the 512 TMEM columns
   int occ = 0;

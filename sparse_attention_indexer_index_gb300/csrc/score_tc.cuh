@@ -17,9 +17,9 @@
 // reads TMEM (each warp its 32 lanes = 32 keys), applies ReLU, sums the 4
 // head columns of each row, scales, and stores the FP32 scores (coalesced:
 // consecutive keys of one row).  A CTA keeps its query rows resident and
-// walks a group of key tiles through a 4-stage ring of key buffers, so the
-// loads of the next three tiles overlap this tile's MMA and epilogue (one
-// CTA per SM keeps ~96 KB of keys in flight).
+// walks a group of key tiles through a ring of up to 8 key buffers (loads run
+// stages-2 tiles ahead), and the accumulator is double-buffered in TMEM, so
+// tile k's MMA overlaps tile k-1's epilogue.
 //
 // Every wait is bounded (a timeout latches kFaultWait and the CTA frees its
 // tensor memory before leaving).
@@ -28,10 +28,10 @@
 
 namespace qsa {
 
-constexpr int kTcThreads = 512;           // 16 warps: all issue key copies; TMEM lane quarter = warp % 4
+constexpr int kTcThreads = 1024;          // 32 warps: all issue key copies; TMEM lane quarter = warp % 4
 constexpr int kTcM = 128;                 // keys per tile
 constexpr int kTcHalf = kTcM * 128;       // bytes of one K-half of the key tile (128 rows x 128 B)
-constexpr int kTcStages = 4;              // key tiles in flight per CTA (ring of 32 KB stages)
+constexpr int kTcMaxStages = 8;           // key-ring stages (32 KB each), sized to the shared memory left
 constexpr int kTcPtStage = 4096;          // page-table entries staged in shared memory per CTA
 
 struct TcArgs {
@@ -52,6 +52,7 @@ struct TcArgs {
   int32_t n_cols;               // N = round16(4 * RT)
   int32_t tmem_cols;            // power of two >= max(32, N)
   int32_t tiles_per_cta;        // key tiles walked by one CTA
+  int32_t stages;               // key-ring stages (3..kTcMaxStages)
   int32_t trigger_dependents;
 };
 
@@ -69,6 +70,18 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// wait_group takes an immediate: dispatch a runtime count (0..6).
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    default: cp_async_wait<6>(); break;
+  }
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -136,8 +149,8 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
 // shared memory (pt_s); others are read from global memory.
 __device__ __forceinline__ void tc_load_keys(const TcArgs& a, int r, int kt, int nb, unsigned char* buf,
                                              const int32_t* pt_s, int pt0, int pt_n) {
-  constexpr int kRowStep = kTcThreads / 16;  // 32
-  constexpr int kRowsPerThread = kTcM / kRowStep;  // 4
+  constexpr int kRowStep = kTcThreads / 16;
+  constexpr int kRowsPerThread = kTcM / kRowStep;
   const int kpp = a.page_size / kBlock;
   const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
   const int c = threadIdx.x & 15, r0 = threadIdx.x >> 4;
@@ -171,12 +184,13 @@ __global__ void __launch_bounds__(kTcThreads)
 score_tc_kernel(TcArgs a) {
   extern __shared__ __align__(16) unsigned char tc_smem_raw[];
   // layout from the first 1024-byte boundary (the swizzle atoms need it):
-  // [A stages: 4 x 32 KB][B: 2 x N x 128 B][mbarrier][TMEM address][fail flag][row lengths]
+  // [A stages x 32 KB][B: 2 x N x 128 B][2 mbarriers][TMEM address][fail flag][row lengths][page table]
   unsigned char* base = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
+  const int S = a.stages;
   auto abuf = [&](int stage) { return base + (size_t)stage * 2 * kTcHalf; };
-  unsigned char* bbuf = base + (size_t)kTcStages * 2 * kTcHalf;
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(bbuf + 2 * a.n_cols * 128);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  unsigned char* bbuf = base + (size_t)S * 2 * kTcHalf;
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(bbuf + 2 * a.n_cols * 128);  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 2);
   int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
   int* s_nb = s_fail + 1;               // [rows_per_tile]
   int32_t* pt_s = s_nb + a.rows_per_tile;  // [kTcPtStage]
@@ -231,7 +245,7 @@ score_tc_kernel(TcArgs a) {
   }
   tc_load_keys(a, r, kt0, nb_tile, abuf(0), pt_s, pt0, pt_n);
   cp_async_commit();  // group 0: B and the first key tile
-  for (int i = 1; i < kTcStages - 1; ++i) {  // groups 1..S-2: the next key tiles (or empty)
+  for (int i = 1; i < S - 2; ++i) {  // groups 1..S-3: the next key tiles (or empty)
     if (kt0 + i < kt1) tc_load_keys(a, r, kt0 + i, nb_tile, abuf(i), pt_s, pt0, pt_n);
     cp_async_commit();
   }
@@ -245,7 +259,8 @@ score_tc_kernel(TcArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 0) {
-    mbar_init(mma_bar, 1);
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
     *s_fail = 0;
     fence_mbar_init();
   }
@@ -256,64 +271,77 @@ score_tc_kernel(TcArgs a) {
   const uint32_t idesc = umma_idesc_bf16(kTcM, a.n_cols);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  for (int kt = kt0; kt < kt1; ++kt) {
-    const int cur = (kt - kt0) % kTcStages;
-    // refill the stage of tile kt-1 (its MMA has completed: we waited on it)
-    // with tile kt+S-1
-    if (kt + kTcStages - 1 < kt1)
-      tc_load_keys(a, r, kt + kTcStages - 1, nb_tile, abuf((kt + kTcStages - 1 - kt0) % kTcStages), pt_s,
-                   pt0, pt_n);
-    cp_async_commit();
-    cp_async_wait<kTcStages - 1>();  // tile kt (and everything older) has landed
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-      const uint32_t a_base = smem_u32(abuf(cur));
-      const uint32_t b_base = smem_u32(bbuf);
+  // Epilogue of tile kt (accumulator `acc`): warp w reads TMEM lane quarter
+  // w % 4 (keys 32(w%4) .. +31) and the column chunks 32 * (w / 4 + 8m).
+  auto epilogue = [&](int kt, int acc) {
+    const int quarter = warp & 3;
+    const int b = kt * kTcM + quarter * 32 + lane;
+    const uint32_t acc_col = (uint32_t)(acc * a.n_cols);
+    for (int c0 = 32 * (warp >> 2); c0 < a.n_cols; c0 += 32 * (kTcThreads / 128)) {
+      uint32_t v[32];
+      tmem_ld_32cols(tmem + ((uint32_t)(quarter * 32) << 16) + acc_col + (uint32_t)c0, v);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t koff = (uint32_t)(s >> 2);          // K-half index
-        const uint32_t within = (uint32_t)((s & 3) * 32);  // bytes along the 128-byte row
-        const uint64_t ad = umma_desc_sw128(a_base + koff * kTcHalf + within);
-        const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(a.n_cols * 128) + within);
-        umma_bf16(tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
+      for (int j = 0; j < 8; ++j) {
+        const int tr = c0 / 4 + j;  // row within the tile
+        if (tr < t1 - t0 && b < s_nb[tr]) {
+          float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
+          sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
+          sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
+          sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
+          a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = sc * kScoreScale;
+        }
       }
-      umma_commit(mma_bar);
     }
-    const uint32_t parity = (uint32_t)(kt - kt0) & 1u;
-    // warp-uniform outcome: the TMEM loads below are warp-collective
-    const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, parity));
-    if (!done && lane == 0) {
+  };
+  // Warps that read TMEM in the epilogue; only they wait on the MMA barrier
+  // (the CTA barrier that follows orders everyone else after them, and a
+  // thousand spinning threads would steal issue slots from the copies).
+  const bool epi_warp = 32 * (warp >> 2) < a.n_cols;
+  // Wait for the MMA of local tile i (accumulator i & 1, its (i >> 1)-th use).
+  auto wait_mma = [&](int i) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&mma_bar[i & 1], (uint32_t)(i >> 1) & 1u));
+    if (!ok && lane == 0) {
       *s_fail = 1;
       raise_fault(kFaultWait);
     }
     tc_fence_after();
-    if (done) {
-      // ---- epilogue: warp w reads TMEM lane quarter w % 4 (keys 32(w%4) ..
-      // +31) and the column chunks 32 * (w / 4 + 4m) ----------------------
-      const int quarter = warp & 3;
-      const int b = kt * kTcM + quarter * 32 + lane;
-      for (int c0 = 32 * (warp >> 2); c0 < a.n_cols; c0 += 32 * (kTcThreads / 128)) {
-        uint32_t v[32];
-        tmem_ld_32cols(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+    return ok;
+  };
+
+  const int n_local = kt1 - kt0;
+  for (int i = 0; i < n_local; ++i) {
+    const int kt = kt0 + i;
+    // Refill the stage of tile i-2 (its MMA completed: waited in iteration
+    // i-1) with tile i+S-2.
+    if (i + S - 2 < n_local) tc_load_keys(a, r, kt + S - 2, nb_tile, abuf((i + S - 2) % S), pt_s, pt0, pt_n);
+    cp_async_commit();
+    cp_async_wait_dyn(S - 2);  // tile i (and everything older) has landed
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(abuf(i % S));
+      const uint32_t b_base = smem_u32(bbuf);
+      const uint32_t d = tmem + (uint32_t)((i & 1) * a.n_cols);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int tr = c0 / 4 + j;  // row within the tile
-          if (tr < t1 - t0 && b < s_nb[tr]) {
-            float s = fmaxf(__uint_as_float(v[4 * j]), 0.f);
-            s += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
-            s += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
-            s += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-            a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = s * kScoreScale;
-          }
-        }
+      for (int st = 0; st < 8; ++st) {
+        const uint32_t koff = (uint32_t)(st >> 2);          // K-half index
+        const uint32_t within = (uint32_t)((st & 3) * 32);  // bytes along the 128-byte row
+        const uint64_t ad = umma_desc_sw128(a_base + koff * kTcHalf + within);
+        const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(a.n_cols * 128) + within);
+        umma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
       }
+      umma_commit(&mma_bar[i & 1]);
     }
+    // meanwhile: the epilogue of the previous tile
+    if (i > 0 && epi_warp && wait_mma(i - 1)) epilogue(kt - 1, (i - 1) & 1);
     tc_fence_before();
-    __syncthreads();  // TMEM and the key buffer are free for the next tile
+    __syncthreads();  // the previous accumulator and stage are free again
     if (*s_fail) break;  // uniform: read after the barrier
   }
+  if (!*s_fail && n_local > 0 && epi_warp && wait_mma(n_local - 1)) epilogue(kt1 - 1, (n_local - 1) & 1);
+  tc_fence_before();
+  __syncthreads();
   cp_async_wait<0>();
   __syncthreads();
   if (threadIdx.x < 32) {
