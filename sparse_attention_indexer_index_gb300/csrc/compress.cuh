@@ -66,6 +66,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kCompressThreads)
 compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
+  // A dependent grid (launched with programmatic serialisation) may start
+  // its own set-up now; it waits for this grid before reading the pool.
+  pdl_launch_dependents();
   const int lane8 = threadIdx.x & (kCompressLanes - 1);
   uint64_t turn_frac[8];
 #pragma unroll
@@ -75,18 +78,29 @@ compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
   const int64_t stride = (int64_t)gridDim.x * groups_per_cta;
   for (int64_t blk = (int64_t)blockIdx.x * groups_per_cta + threadIdx.x / kCompressLanes;
        blk < a.n_blocks; blk += stride) {
-    // Destination pool row: slot of the block's first token, divided by 4.
+    // Everything indexed by blk is loaded up front, so only the page-table
+    // entry waits on another load.
     const int64_t b = a.block_id[blk];
-    const uint64_t pos = (uint64_t)(kBlock * b);
+    const int r = a.page_table != nullptr ? a.block_req[blk] : 0;
+    const __nv_bfloat16* src = a.raw + blk * (kBlock * kDim);
+    uint4 vlo[kBlock], vhi[kBlock];
+#pragma unroll
+    for (int k = 0; k < kBlock; ++k) {
+      vlo[k] = ld_stream_16(src + k * kDim + 8 * lane8);
+      vhi[k] = ld_stream_16(src + k * kDim + 64 + 8 * lane8);
+    }
+    // Destination pool row: slot of the block's first token, divided by 4
+    // (positions are int32, so the page arithmetic is 32-bit).
+    const uint32_t pos = (uint32_t)(kBlock * b);
     int64_t row = blk;
-    bool ok = b >= 0;
+    bool ok = b >= 0 && b <= INT32_MAX / kBlock;
     if (a.page_table != nullptr && ok) {
-      const int r = a.block_req[blk];
-      const int64_t page_idx = (int64_t)(pos / (uint64_t)a.page_size);
-      ok = r >= 0 && r < a.n_req && page_idx < a.ld_pt;
+      const uint32_t ps = (uint32_t)a.page_size;
+      const uint32_t page_idx = pos / ps;
+      ok = r >= 0 && r < a.n_req && (int64_t)page_idx < a.ld_pt;
       if (ok) {
         const int64_t page = a.page_table[(int64_t)r * a.ld_pt + page_idx];
-        row = page * (a.page_size / kBlock) + (int64_t)(pos % (uint64_t)a.page_size) / kBlock;
+        row = page * (int64_t)(ps / kBlock) + (int64_t)((pos - page_idx * ps) / kBlock);
         ok = page >= 0;
       }
     }
@@ -100,23 +114,17 @@ compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
     }
 
     // FP32 block mean, summed in token order: ((k0 + k1) + k2) + k3, * 0.25.
-    const __nv_bfloat16* src = a.raw + blk * (kBlock * kDim);
     float lo[8], hi[8];
-    {
-      uint4 v0 = ld_stream_16(src + 8 * lane8);
-      uint4 w0 = ld_stream_16(src + 64 + 8 * lane8);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t x = (&v0.x)[e], y = (&w0.x)[e];
-        float2 fx = bf16x2_to_float2(x), fy = bf16x2_to_float2(y);
-        lo[2 * e] = fx.x; lo[2 * e + 1] = fx.y;
-        hi[2 * e] = fy.x; hi[2 * e + 1] = fy.y;
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 fx = bf16x2_to_float2((&vlo[0].x)[e]), fy = bf16x2_to_float2((&vhi[0].x)[e]);
+      lo[2 * e] = fx.x; lo[2 * e + 1] = fx.y;
+      hi[2 * e] = fy.x; hi[2 * e + 1] = fy.y;
     }
 #pragma unroll
     for (int k = 1; k < kBlock; ++k) {
-      accumulate_bf16x8(lo, ld_stream_16(src + k * kDim + 8 * lane8));
-      accumulate_bf16x8(hi, ld_stream_16(src + k * kDim + 64 + 8 * lane8));
+      accumulate_bf16x8(lo, vlo[k]);
+      accumulate_bf16x8(hi, vhi[k]);
     }
     float ss = 0.f;
 #pragma unroll
@@ -140,7 +148,7 @@ compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
       float r_lo[2], r_hi[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint64_t ph = pos * turn_frac[e + h];            // turns mod 1, wraps
+        const uint64_t ph = (uint64_t)pos * turn_frac[e + h];  // turns mod 1, wraps
         const int32_t top = (int32_t)(ph >> 32);               // signed: [-1/2, 1/2) turn
         const float y = (float)top * 4.656612873077392578125e-10f;  // * 2^-31: units of pi
         float s, c;

@@ -14,6 +14,7 @@
 #include "score_decode.cuh"
 #include "score_tc.cuh"
 #include "select.cuh"
+#include "select_resident.cuh"
 
 using namespace qsa;
 
@@ -31,6 +32,11 @@ constexpr int kSelListCap = 6144;
 constexpr int kSelPtStage = 2048;
 constexpr int kSelMaxSmem = kSelFixedBytes + kSelPtStage * 4 + kSelListCap * 8 +
                             kSelResidentCap * 4;
+// Rows of up to kRsMaxRow entries take the shared-memory-resident kernel;
+// its candidate list gets what the row, page table and output leave of
+// kRsMaxSmem (at least 2 * kMaxK entries, at most kRsListMax).
+constexpr int kRsMaxSmem = 227 * 1024;
+constexpr int kRsListMax = 8192;
 
 struct DeviceInfo {
   bool ready = false;
@@ -54,6 +60,10 @@ qsa_status device_info(DeviceInfo** out) {
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(select_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_resident_kernel<kModeTopk>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRsMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_resident_kernel<kModeQsa>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRsMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScoreSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -94,6 +104,25 @@ RopeTurns rope_turns(double base) {
   return e.turns;
 }
 
+// Launch with programmatic stream serialisation: the grid may become
+// resident before the previous kernel on the stream finishes; every kernel
+// launched this way executes griddepcontrol.wait before reading its inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 qsa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
@@ -102,9 +131,28 @@ qsa_status launch_status() {
 // candidates: resident rows (<= kSelResidentCap) live in shared memory, longer
 // rows stream through the bulk-copy ring.
 void plan_select(SelectArgs& a) {
+  a.pt_cap = kSelPtStage;
+  if (a.n_max <= kRsMaxRow) {
+    // resident kernel: [fixed][keys, whole chunks of 4096][page table]
+    // [selected][candidate keys][candidate indices]
+    a.resident = 2;
+    int off = kRsFixedBytes;
+    a.off_row = off;
+    off += ((a.n_max + kRsChunk - 1) / kRsChunk) * kRsChunk * 4;
+    a.off_pt = off;
+    off += a.pt_cap * 4;
+    a.off_sel = off;
+    off += ((a.k + 3) & ~3) * 4;
+    int cap = ((kRsMaxSmem - off) / 8) & ~3;
+    if (cap > kRsListMax) cap = kRsListMax;
+    a.list_cap = cap;
+    a.off_lkey = off;
+    off += cap * 4;
+    a.off_list = off;
+    return;
+  }
   a.resident = a.n_max <= kSelResidentCap;
   a.list_cap = kSelListCap;
-  a.pt_cap = kSelPtStage;
   int off = kSelFixedBytes;
   a.off_pt = off;
   off += a.pt_cap * 4;
@@ -116,6 +164,7 @@ void plan_select(SelectArgs& a) {
 }
 
 size_t select_smem_bytes(const SelectArgs& a) {
+  if (a.resident == 2) return (size_t)a.off_list + (size_t)a.list_cap * 4;
   const size_t row = a.resident ? (size_t)((a.n_max + 3) & ~3) * 4 : (size_t)kSelRing * kSelPiece * 4;
   return (size_t)a.off_row + row;
 }
@@ -137,7 +186,9 @@ qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  if (cudaLaunchKernelEx(&cfg, select_kernel<kMode>, a) != cudaSuccess) {
+  const cudaError_t e = a.resident == 2 ? cudaLaunchKernelEx(&cfg, select_resident_kernel<kMode>, a)
+                                         : cudaLaunchKernelEx(&cfg, select_kernel<kMode>, a);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
   }
@@ -195,8 +246,10 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   t.tiles_per_cta = (int32_t)((n_kt + x_ctas - 1) / x_ctas);
   dim3 grid((unsigned)((n_kt + t.tiles_per_cta - 1) / t.tiles_per_cta), (unsigned)row_tiles,
             (unsigned)s.n_req);
-  score_tc_kernel<<<grid, kTcThreads, smem, stream>>>(t);
-  if (qsa_status e = launch_status()) return e;
+  if (launch_pdl(score_tc_kernel, grid, dim3(kTcThreads), smem, stream, t) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
   if (s.n_fill > 0) {
     fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
                                                               s.n_fill);
@@ -240,8 +293,11 @@ qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream) {
     const int64_t tiles = (int64_t)s.n_req * ((cols + kScoreTile - 1) / kScoreTile);
     if (tiles > INT32_MAX) return QSA_ERR_UNSUPPORTED;
     const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)sm_count);
-    score_decode_kernel<<<(unsigned)grid, kScoreThreads, kScoreSmem, stream>>>(s);
-    if (qsa_status e = launch_status()) return e;
+    if (launch_pdl(score_decode_kernel, dim3((unsigned)grid), dim3(kScoreThreads), kScoreSmem, stream, s) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return QSA_ERR_CUDA;
+    }
   }
   return QSA_OK;
 }

@@ -124,6 +124,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 score_decode_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char score_smem_raw[];
   ScoreShared& sh = *reinterpret_cast<ScoreShared*>(score_smem_raw);
+  // Launched with programmatic serialisation: nothing is read before the
+  // previous grid on the stream has finished, and the dependent selection
+  // may only start once that holds here.
+  pdl_wait_primary();
   if (a.trigger_dependents) pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

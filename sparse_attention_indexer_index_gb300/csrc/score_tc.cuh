@@ -195,6 +195,10 @@ score_tc_kernel(TcArgs a) {
   int* s_nb = s_fail + 1;               // [rows_per_tile]
   int32_t* pt_s = s_nb + a.rows_per_tile;  // [kTcPtStage]
 
+  // Launched with programmatic serialisation: nothing is read before the
+  // previous grid on the stream has finished, and the dependent selection
+  // may only start once that holds here.
+  pdl_wait_primary();
   if (a.trigger_dependents) pdl_launch_dependents();
 
   const int r = blockIdx.z;

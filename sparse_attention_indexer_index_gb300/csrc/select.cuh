@@ -67,10 +67,10 @@ struct SelectArgs {
   int32_t n_max;                // host bound of a row's candidates
   int32_t vec_ok;               // rows are 16-byte aligned
   int32_t wait_primary;         // wait for the producing grid (PDL)
-  int32_t resident;             // rows fit in shared memory (n_max <= kSelResidentCap)
+  int32_t resident;             // 1: rows fit in shared memory (n_max <= kSelResidentCap); 2: select_resident_kernel
   int32_t list_cap;             // entries of the candidate list
   int32_t pt_cap;               // page-table entries staged in shared memory
-  int32_t off_pt, off_list, off_lkey, off_row;  // dynamic shared memory layout (bytes)
+  int32_t off_pt, off_list, off_lkey, off_row, off_sel;  // dynamic shared memory layout (bytes)
   // token top-k mode
   const int32_t* n_valid;       // [n_rows] or nullptr (all rows n_max)
   const int32_t* row_req;       // [n_rows] or nullptr (row t -> table row t)
