@@ -2,6 +2,7 @@
 // checks, launch shapes, and launches on the caller's stream.  Declarations
 // and the contract of every call are in include/qsa.h.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
@@ -66,6 +67,10 @@ qsa_status device_info(DeviceInfo** out) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRsMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScoreSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_cpasync_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_cpasync_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -195,6 +200,77 @@ qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream) {
   return QSA_OK;
 }
 
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (the library does not link libcuda directly).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The compressed-key pool as a 2-D tensor [pool_rows][128] BF16, boxes of
+// 64 x box_rows with the 128-byte swizzle (one K-half of box_rows keys).
+bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t pool_rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)pool_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TMA scorer (pages whose compressed rows form whole 8-row swizzle atoms).
+// Returns QSA_ERR_UNSUPPORTED when the layout does not allow it, so that the
+// caller takes the cp.async kernel.
+qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t n_req, int sm_count,
+                             cudaStream_t stream) {
+  const int kpp = t.page_size / kBlock;
+  int R = 0;
+  for (int c = kTcM; c >= 8; c >>= 1)
+    if (kpp % c == 0) {
+      R = c;
+      break;
+    }
+  if (R == 0 || t.pool_rows <= 0 || t.pool_rows > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (!encode_pool_map(&map, t.pool, t.pool_rows, R)) return QSA_ERR_UNSUPPORTED;
+  t.box_rows = R;
+  int cols = 32;
+  while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
+  t.tmem_cols = cols;
+  // one CTA per SM (the key ring takes most of shared memory); key tiles per
+  // CTA: about one wave of CTAs in total
+  const int64_t x_ctas = std::max<int64_t>(1, std::min<int64_t>(n_kt, sm_count / (row_tiles * n_req)));
+  t.tiles_per_cta = (int32_t)((n_kt + x_ctas - 1) / x_ctas);
+  t.pt_cap = (int32_t)std::min<int64_t>(kTcPtStage, (int64_t)t.tiles_per_cta * kTcM / kpp + 2);
+  const size_t fixed = 1024 + 2 * (size_t)t.n_cols * 128 + (2 * kTcMaxStages + 4) * 8 + sizeof(TmCtl) +
+                       4 * (size_t)t.rows_per_tile + 4 * (size_t)t.pt_cap;
+  t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / (2 * kTcHalf));
+  if (t.stages < 2) return QSA_ERR_UNSUPPORTED;
+  const size_t smem = fixed + (size_t)t.stages * 2 * kTcHalf;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tc_kernel, kTmThreads, smem) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)((n_kt + t.tiles_per_cta - 1) / t.tiles_per_cta), (unsigned)row_tiles, (unsigned)n_req);
+  if (launch_pdl(score_tc_kernel, grid, dim3(kTmThreads), smem, stream, t, map) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
 // Tensor-core scorer for requests with several rows: tiles of 128 keys x up
 // to 64 rows (N = 4 * rows, multiple of 16), a group of key tiles per CTA
 // when rows are plentiful (prefill), one otherwise (decode verify).  The
@@ -227,6 +303,13 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
   const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
   if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
+  qsa_status tma = launch_scores_tma(t, n_kt, row_tiles, s.n_req, sm_count, stream);
+  if (tma == QSA_OK && s.n_fill > 0) {
+    fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
+                                                              s.n_fill);
+    return launch_status();
+  }
+  if (tma != QSA_ERR_UNSUPPORTED) return tma;
   // key-ring stages: as many 32 KB stages as fit beside B and the rest
   const size_t fixed = 1024 + 2 * (size_t)t.n_cols * 128 + 32 + 4 * (size_t)t.rows_per_tile +
                        4 * (size_t)kTcPtStage;
@@ -236,7 +319,8 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   // resident CTAs per SM (shared memory bound; with the 4-stage ring this is
   // one) must never ask for more than the 512 TMEM columns
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tc_kernel, kTcThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tc_cpasync_kernel, kTcThreads, smem) !=
+      cudaSuccess)
     return QSA_ERR_CUDA;
   if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
   // Key tiles per CTA: about one wave of CTAs in total, consecutive tiles of
@@ -246,7 +330,7 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   t.tiles_per_cta = (int32_t)((n_kt + x_ctas - 1) / x_ctas);
   dim3 grid((unsigned)((n_kt + t.tiles_per_cta - 1) / t.tiles_per_cta), (unsigned)row_tiles,
             (unsigned)s.n_req);
-  if (launch_pdl(score_tc_kernel, grid, dim3(kTcThreads), smem, stream, t) != cudaSuccess) {
+  if (launch_pdl(score_tc_cpasync_kernel, grid, dim3(kTcThreads), smem, stream, t) != cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
   }

@@ -24,6 +24,8 @@
 // Every wait is bounded (a timeout latches kFaultWait and the CTA frees its
 // tensor memory before leaving).
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace qsa {
@@ -54,6 +56,8 @@ struct TcArgs {
   int32_t tiles_per_cta;        // key tiles walked by one CTA
   int32_t stages;               // key-ring stages (3..kTcMaxStages)
   int32_t trigger_dependents;
+  int32_t box_rows;             // TMA kernel: pool rows per tensor-map box (8..128, divides page_size/4)
+  int32_t pt_cap;               // TMA kernel: page-table entries staged in shared memory
 };
 
 // ---------------------------------------------------------------------------
@@ -120,6 +124,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+        "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -181,7 +194,7 @@ __device__ __forceinline__ void tc_load_keys(const TcArgs& a, int r, int kt, int
 }
 
 __global__ void __launch_bounds__(kTcThreads)
-score_tc_kernel(TcArgs a) {
+score_tc_cpasync_kernel(TcArgs a) {
   extern __shared__ __align__(16) unsigned char tc_smem_raw[];
   // layout from the first 1024-byte boundary (the swizzle atoms need it):
   // [A stages x 32 KB][B: 2 x N x 128 B][2 mbarriers][TMEM address][fail flag][row lengths][page table]
@@ -349,6 +362,304 @@ score_tc_kernel(TcArgs a) {
   cp_async_wait<0>();
   __syncthreads();
   if (threadIdx.x < 32) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA-fed, warp-specialised variant (pages of a multiple of 32 tokens, so
+// that a page's compressed keys form whole 8-row swizzle atoms).
+//
+// A page of P tokens holds P/4 consecutive pool rows, so the key tile of 128
+// blocks is 128*4/P contiguous runs of pool rows.  Each run is one
+// tensor-map box of 64 BF16 x box_rows per K-half, which the TMA engine
+// writes straight into the 128-byte-swizzled K-major layout the MMA reads
+// (the box's destination is 1024-byte aligned, so its swizzle phase is the
+// tile's).  Roles:
+//   warp 0      producer: looks up the pages of a tile (one lane per run)
+//               and issues its boxes on the stage's `full` barrier;
+//   warp 1      MMA issuer (one lane) and TMEM owner: waits `full`, issues
+//               the 8 K-steps into one of two TMEM accumulators, commits to
+//               the stage's `empty` barrier and the accumulator's `acc_full`;
+//   warps 2..9  epilogue: two warps per TMEM lane quarter split the column
+//               chunks, read the accumulator, apply ReLU / head sum / scale,
+//               store coalesced scores, and release `acc_empty`.
+// Every wait is bounded; a timeout latches kFaultWait and sets a shared
+// abort flag that ends the other roles' waits too, and the CTA drains its
+// outstanding copies and MMAs (again bounded) before freeing tensor memory.
+// ---------------------------------------------------------------------------
+constexpr int kTmWarps = 10;
+constexpr int kTmThreads = 32 * kTmWarps;
+constexpr int kTmEpiWarps = 8;
+
+struct TmCtl {
+  int abort;
+  int issued;     // tiles whose copies were issued
+  int consumed;   // tiles whose copies the MMA issuer saw land
+  int mma_done;   // tiles whose MMAs were committed
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool tm_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > 200000000ull) {
+      *abort = 1;
+      raise_fault(kFaultWait);
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kTmThreads, 1)
+score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
+  extern __shared__ __align__(16) unsigned char tm_smem_raw[];
+  // [A stages x 32 KB][B: 2 x N x 128 B][barriers][control][row lengths][page table]
+  unsigned char* base = tm_smem_raw + ((1024u - (smem_u32(tm_smem_raw) & 1023u)) & 1023u);
+  const int S = a.stages;
+  const int N = a.n_cols;
+  auto abuf = [&](int stage) { return base + (size_t)stage * 2 * kTcHalf; };
+  unsigned char* bbuf = base + (size_t)S * 2 * kTcHalf;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bbuf + 2 * N * 128);  // [S]
+  uint64_t* empty = full + S;                                         // [S]
+  uint64_t* acc_full = empty + S;                                     // [2]
+  uint64_t* acc_empty = acc_full + 2;                                 // [2]
+  TmCtl* ctl = reinterpret_cast<TmCtl*>(acc_empty + 2);
+  int* s_nb = reinterpret_cast<int*>(ctl + 1);  // [rows_per_tile]
+  int32_t* pt_s = s_nb + a.rows_per_tile;       // [pt_cap]
+  volatile int* abort = &ctl->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Launched with programmatic serialisation: nothing is read before the
+  // previous grid on the stream has finished, and the dependent selection
+  // may only start once that holds here.
+  pdl_wait_primary();
+  if (a.trigger_dependents) pdl_launch_dependents();
+  if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pool_map)) : "memory");
+
+  const int r = blockIdx.z;
+  const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
+  if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
+    return;
+  }
+  if (row1 - row0 > (int)gridDim.y * a.rows_per_tile) {  // more rows than max_rows_per_req promised
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
+  }
+  const int t0 = row0 + blockIdx.y * a.rows_per_tile;
+  const int t1 = min(row1, t0 + a.rows_per_tile);
+  if (t0 >= t1) return;
+  const int nrows = t1 - t0;
+  if (threadIdx.x < nrows) {
+    int L = __ldg(a.row_len + t0 + threadIdx.x);
+    if (L < 0 || L > a.max_len) { raise_fault(kFaultGrouping); L = 0; }
+    s_nb[threadIdx.x] = L / kBlock;
+  }
+  __syncthreads();
+  int nb_tile = 0;
+  for (int i = 0; i < nrows; ++i) nb_tile = max(nb_tile, s_nb[i]);
+  const int n_kt = (nb_tile + kTcM - 1) / kTcM;
+  const int kt0 = blockIdx.x * a.tiles_per_cta;
+  const int kt1 = min(n_kt, kt0 + a.tiles_per_cta);
+  if (kt0 >= kt1) return;
+  const int n_local = kt1 - kt0;
+
+  // ---- page-table entries of this CTA's key range, staged once ------------
+  const int kpp = a.page_size / kBlock;
+  const int pt0 = (kt0 * kTcM) / kpp;
+  int pt_n = min((kt1 * kTcM - 1) / kpp + 1 - pt0, a.pt_cap);
+  if (pt_n > a.ld_pt - pt0) pt_n = (int)(a.ld_pt - pt0);
+  if (pt_n < 0) pt_n = 0;
+  const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
+  for (int i = threadIdx.x; i < pt_n; i += kTmThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
+
+  // ---- query rows -> B (zero columns beyond 4 * nrows) ---------------------
+  const int valid_cols = 4 * nrows;
+  for (int i = threadIdx.x; i < N * 16; i += kTmThreads) {
+    const int col = i >> 4, c = i & 15;
+    const bool ok = col < valid_cols;
+    const __nv_bfloat16* src = ok ? a.q + ((int64_t)t0 * kHeads + col) * kDim + c * 8 : a.q;
+    cp_async_16(bbuf + sw128_offset(col, c, N), src, ok ? 16u : 0u);
+  }
+  cp_async_commit();
+
+  // ---- barriers and tensor memory -------------------------------------------
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kTmEpiWarps);
+    }
+    ctl->abort = 0;
+    ctl->issued = 0;
+    ctl->consumed = 0;
+    ctl->mma_done = 0;
+    fence_mbar_init();
+  }
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    // ---- producer: one lane per run of box_rows pool rows ------------------
+    const int R = a.box_rows;
+    const int runs = kTcM / R;
+    int i = 0;
+    for (; i < n_local; ++i) {
+      const int st = i % S;
+      if (i >= S) {
+        const bool ok = lane == 0 ? tm_wait(&empty[st], (uint32_t)((i / S) - 1) & 1u, abort) : true;
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      }
+      const int b = (kt0 + i) * kTcM + lane * R;  // first block of this lane's run
+      bool valid = false;
+      int prow = 0;
+      if (lane < runs && b < nb_tile) {
+        const int page_idx = b / kpp;
+        if (page_idx < a.ld_pt) {
+          const int64_t page = (page_idx >= pt0 && page_idx < pt0 + pt_n) ? pt_s[page_idx - pt0]
+                                                                            : __ldg(pt_row + page_idx);
+          const int64_t pr = page * kpp + (b - page_idx * kpp);
+          if (page >= 0 && pr < a.pool_rows) {
+            valid = true;
+            prow = (int)pr;
+            // visible rows of the run past the pool's end read as zero
+            if (pr + min(R, nb_tile - b) > a.pool_rows) raise_fault(kFaultPool);
+          } else {
+            raise_fault(kFaultPool);
+          }
+        } else {
+          raise_fault(kFaultIndex);
+        }
+      }
+      const unsigned vm = __ballot_sync(0xffffffffu, valid);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(vm) * 2u * (uint32_t)R * 128u);
+      __syncwarp();
+      if (valid) {
+        unsigned char* dst = abuf(st) + lane * R * 128;
+        tma_load_2d(dst, &pool_map, 0, prow, &full[st]);
+        tma_load_2d(dst + kTcHalf, &pool_map, 64, prow, &full[st]);
+      }
+    }
+    if (lane == 0) ctl->issued = i;
+  } else if (warp == 1) {
+    // ---- MMA issuer ---------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kTcM, N);
+      const uint32_t b_base = smem_u32(bbuf);
+      int i = 0;
+      for (; i < n_local; ++i) {
+        const int st = i % S, acc = i & 1;
+        if (!tm_wait(&full[st], (uint32_t)(i / S) & 1u, abort)) break;
+        ctl->consumed = i + 1;
+        if (i >= 2 && !tm_wait(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(abuf(st));
+        const uint32_t d = tmem + (uint32_t)(acc * N);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (uint32_t)(k >> 2);          // K-half index
+          const uint32_t within = (uint32_t)((k & 3) * 32);  // bytes along the 128-byte row
+          const uint64_t ad = umma_desc_sw128(a_base + koff * kTcHalf + within);
+          const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(N * 128) + within);
+          umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&empty[st]);
+        umma_commit(&acc_full[acc]);
+        ctl->mma_done = i + 1;
+      }
+    }
+  } else {
+    // ---- epilogue: warp w reads TMEM lane quarter w % 4 (keys 32(w%4) ..
+    // +31) and the column chunks of its half ---------------------------------
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    for (int i = 0; i < n_local; ++i) {
+      const int acc = i & 1;
+      const bool ok = __all_sync(0xffffffffu, tm_wait(&acc_full[acc], (uint32_t)(i >> 1) & 1u, abort));
+      if (!ok) break;
+      tc_fence_after();
+      const int b = (kt0 + i) * kTcM + quarter * 32 + lane;
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
+      for (int c0 = 32 * half; c0 < N; c0 += 64) {
+        uint32_t v[32];
+        int ncols = 32;
+        if (N - c0 >= 32) {
+          tmem_ld_32cols(taddr + (uint32_t)c0, v);
+        } else {
+          uint32_t w16[16];
+          tmem_ld_16cols(taddr + (uint32_t)c0, w16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = w16[e];
+          ncols = 16;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int tr = c0 / 4 + j;  // row within the tile
+          if (4 * j < ncols && tr < nrows && b < s_nb[tr]) {
+            float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
+            sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
+            sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
+            sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
+            a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = sc * kScoreScale;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) {
+    // Drain before the shared and tensor memory are released: copies issued
+    // but never seen landing, and the last committed MMAs.
+    for (int j = ctl->consumed; j < ctl->issued; ++j) {
+      const uint64_t t_start = global_timer_ns();
+      while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1u) && global_timer_ns() - t_start < 20000000ull) {
+      }
+    }
+    for (int j = max(0, ctl->mma_done - 2); j < ctl->mma_done; ++j) {
+      const uint64_t t_start = global_timer_ns();
+      while (!mbar_try_wait(&acc_full[j & 1], (uint32_t)(j >> 1) & 1u) &&
+             global_timer_ns() - t_start < 20000000ull) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
                  : "memory");
   }
