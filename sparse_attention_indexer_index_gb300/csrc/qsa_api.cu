@@ -216,11 +216,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The compressed-key pool as a 2-D tensor [pool_rows][128] BF16, boxes of
-// 64 x box_rows with the 128-byte swizzle (one K-half of box_rows keys).
-bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t pool_rows, int box_rows) {
+// The compressed-key pool for the TMA scorer, with the 128-byte swizzle.
+// 4-D view (pool_rows a multiple of 8): [row / 8][K-half][row % 8][64 BF16],
+// one box of box_rows / 8 groups covers a run of box_rows keys, both
+// K-halves, landing as [group][K-half][8 rows][128 B].  2-D view otherwise:
+// [pool_rows][128 BF16], one box of 64 x box_rows per K-half.
+bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t pool_rows, int box_rows, bool four_d) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
+  if (four_d) {
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(pool_rows / 8)};
+    const cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, 128, (cuuint64_t)kDim * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)pool_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
@@ -244,7 +256,11 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
     }
   if (R == 0 || t.pool_rows <= 0 || t.pool_rows > INT32_MAX) return QSA_ERR_UNSUPPORTED;
   CUtensorMap map;
-  if (!encode_pool_map(&map, t.pool, t.pool_rows, R)) return QSA_ERR_UNSUPPORTED;
+  t.box4d = t.pool_rows % 8 == 0 ? 1 : 0;
+  if (!encode_pool_map(&map, t.pool, t.pool_rows, R, t.box4d != 0)) {
+    t.box4d = 0;
+    if (!encode_pool_map(&map, t.pool, t.pool_rows, R, false)) return QSA_ERR_UNSUPPORTED;
+  }
   t.box_rows = R;
   int cols = 32;
   while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators

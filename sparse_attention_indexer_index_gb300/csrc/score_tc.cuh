@@ -58,6 +58,7 @@ struct TcArgs {
   int32_t trigger_dependents;
   int32_t box_rows;             // TMA kernel: pool rows per tensor-map box (8..128, divides page_size/4)
   int32_t pt_cap;               // TMA kernel: page-table entries staged in shared memory
+  int32_t box4d;                // TMA kernel: 4-D view, one box per run covers both K-halves
 };
 
 // ---------------------------------------------------------------------------
@@ -97,12 +98,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 // K-major, 128-byte swizzle shared-memory matrix descriptor: start address,
-// stride between 8-row groups = 1024 B, descriptor version 1, layout 2.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+// stride between 8-row atoms (1024 B when the atoms of one K-half are packed,
+// 2048 B when the two K-halves of each 8 rows alternate), descriptor
+// version 1, layout 2.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t sbo_bytes = 1024) {
   uint64_t d = 0;
   d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);        // start address
   d |= (uint64_t)1 << 16;                               // leading byte offset (unused, 16 B)
-  d |= (uint64_t)(1024 >> 4) << 32;                     // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)(sbo_bytes >> 4) << 32;                // stride byte offset: between 8-row atoms
   d |= (uint64_t)1 << 46;                               // descriptor version
   d |= (uint64_t)2 << 61;                               // 128-byte swizzle
   return d;
@@ -408,6 +411,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int g, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(g), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -564,9 +574,13 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
       if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(vm) * 2u * (uint32_t)R * 128u);
       __syncwarp();
       if (valid) {
-        unsigned char* dst = abuf(st) + lane * R * 128;
-        tma_load_2d(dst, &pool_map, 0, prow, &full[st]);
-        tma_load_2d(dst + kTcHalf, &pool_map, 64, prow, &full[st]);
+        if (a.box4d) {  // [run][8-row group][K-half][8 rows][128 B]
+          tma_load_4d(abuf(st) + lane * R * 256, &pool_map, prow >> 3, &full[st]);
+        } else {        // [K-half][128 rows][128 B]
+          unsigned char* dst = abuf(st) + lane * R * 128;
+          tma_load_2d(dst, &pool_map, 0, prow, &full[st]);
+          tma_load_2d(dst + kTcHalf, &pool_map, 64, prow, &full[st]);
+        }
       }
     }
     if (lane == 0) ctl->issued = i;
@@ -575,6 +589,8 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(kTcM, N);
       const uint32_t b_base = smem_u32(bbuf);
+      const uint32_t a_half = a.box4d ? 1024u : (uint32_t)kTcHalf;  // offset of K-half 1
+      const uint32_t a_sbo = a.box4d ? 2048u : 1024u;
       int i = 0;
       for (; i < n_local; ++i) {
         const int st = i % S, acc = i & 1;
@@ -588,7 +604,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (uint32_t)(k >> 2);          // K-half index
           const uint32_t within = (uint32_t)((k & 3) * 32);  // bytes along the 128-byte row
-          const uint64_t ad = umma_desc_sw128(a_base + koff * kTcHalf + within);
+          const uint64_t ad = umma_desc_sw128(a_base + koff * a_half + within, a_sbo);
           const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(N * 128) + within);
           umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
@@ -660,6 +676,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   __syncthreads();
   tc_fence_after();
   if (warp == 1) {
+    __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
                  : "memory");
   }
