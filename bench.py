@@ -266,6 +266,47 @@ def scores_only(g: Gpu, st):
                        w.max_len, w.max_rows_per_req, scores=st["scores"])
 
 
+def compress_only(g: Gpu, st):
+    w = st["w"]
+    g.qsa.compress_keys(st["new_raw"], st["new_id"], st["pool"], block_req=st["new_req"],
+                        page_table=st["pt"], page_size=w.page_size, rope_base=w.rope_base)
+
+
+def select_only(g: Gpu, st):
+    """The selection half of the fused call on the scores left in st["scores"]
+    by scores_only (the kernel the fused call runs after the scorer)."""
+    w = st["w"]
+    g.qsa.select_blocks(st["scores"], st["rrs"], st["row_len"], st["pt"], w.page_size, w.max_len,
+                        k_blk=w.k_blk, out_slots=st["slots"])
+
+
+def kernel_names(w):
+    """Kernels the library dispatches to for this workload (the launch rules
+    of qsa_api.cu: requests with 2+ rows use the tensor-core scorer, fed by
+    TMA when a page holds a multiple of 8 compressed keys; rows of up to
+    32768 blocks take the shared-memory-resident selection)."""
+    if w.max_rows_per_req >= 2:
+        score = "score_tc_kernel" if (w.page_size // 4) % 8 == 0 else "score_tc_cpasync_kernel"
+    else:
+        score = "score_decode_kernel"
+    select = "select_resident_kernel" if w.max_len // 4 <= 32768 else "select_kernel"
+    return {"compress": "compress_keys_kernel", "score": score, "select": select}
+
+
+def kernel_bytes(w, new_blocks):
+    """Algorithmic HBM bytes per launch of each kernel of the step.
+    compress: per new block 4 raw keys read (1 KB), one key written (256 B),
+      its id, request and page-table entry (12 B);
+    score: decode_bytes' keys + q + page table + the FP32 scores written;
+    select: the FP32 scores read, the page-table entries of the context, the
+      slot rows written."""
+    by = decode_bytes(w)
+    n_new = new_blocks * w.n_req
+    return {"compress": n_new * (4 * 256 + 256 + 12),
+            "score": by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"],
+            "select": by["scores_fp32"] + by["page_table"] + by["slots"]}
+
+
 def decode_bytes(w):
     """Algorithmic HBM bytes of one fused indexer call: every visible
     compressed key of a request read once (256 B), the query rows (1 KB
@@ -363,7 +404,7 @@ def bench_variant_prefill(g, w, iters, warmup, peaks):
             "rows_per_s": w.n_rows / (ms * 1e-3), "flop": flop,
             "TFLOPs": flop / (ms * 1e-3) / 1e12,
             "frac_tensor": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
-            "path": "cuda-core scorer (tensor-core prefill scorer not yet built)"}
+            "path": "tensor-core scorer (tcgen05 MMA, TMA-fed key tiles) + resident-row selection"}
 
 
 def cpu_oracle_rate(w, budget_s=10.0):
@@ -492,12 +533,23 @@ def main():
     ms = aggregate_time(local_ms, ws, device)
     value = ws * w.n_rows / (ms * 1e-3)
 
-    # ---- dominant kernel of the step: the scorer, timed the same way -----
-    t_score = g.timed(lambda: scores_only(g, st), args.steps, args.warmup)
+    # ---- each kernel of the step alone, timed the same way; the roofline
+    # object describes the one that takes longest -------------------------
+    names = kernel_names(w)
+    kbytes = kernel_bytes(w, new_blocks)
+    scores_only(g, st)  # the selection below reads these scores
+    kms = {
+        "compress": statistics.mean(g.timed(lambda: compress_only(g, st), args.steps, args.warmup)),
+        "score": statistics.mean(g.timed(lambda: scores_only(g, st), args.steps, args.warmup)),
+        "select": statistics.mean(g.timed(lambda: select_only(g, st), args.steps, args.warmup)),
+    }
+    kernels = {names[k]: {"us_per_launch": 1e3 * v, "alg_bytes_per_launch": kbytes[k],
+                          "achieved_GBps": kbytes[k] / (v * 1e-3) / 1e9,
+                          "frac": kbytes[k] / (v * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+               for k, v in kms.items()}
+    dom = max(kms, key=kms.get)
+    achieved = kbytes[dom] / (kms[dom] * 1e-3) / 1e9
     by = decode_bytes(w)
-    score_bytes = by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"]
-    score_ms = statistics.mean(t_score)
-    achieved = score_bytes / (score_ms * 1e-3) / 1e9
     step_bytes = by["keys"] + by["q"] + by["page_table"] + by["slots"]
 
     # ---- end to end through the API with host buffers ---------------------
@@ -519,12 +571,15 @@ def main():
         "step_alg_bytes": step_bytes,
         "step_alg_GBps": step_bytes / (ms * 1e-3) / 1e9,
         "step_frac_hbm": step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-        "roofline": {"bound": "hbm", "kernel": "score_decode_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": captured_traffic("score_decode_kernel", w.name),
-                     "alg_bytes_per_launch": score_bytes,
-                     "us_per_launch": 1e3 * score_ms,
+                     "traffic": captured_traffic(names[dom], w.name),
+                     "alg_bytes_per_launch": kbytes[dom],
+                     "us_per_launch": 1e3 * kms[dom],
+                     "timing": "CUDA events around the kernel's own API call replayed from a CUDA "
+                               "graph, L2 flushed before each launch, mean over the timed launches",
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "kernels": kernels,
         "e2e": {"value": ws * w.n_rows / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "how": "eager Python API calls per step, pinned host buffers, no graph"},

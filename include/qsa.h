@@ -178,6 +178,27 @@ qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_
                             int32_t* out_pos, int32_t* out_slots, void* stream);
 
 /* ---------------------------------------------------------------------
+ * Top-k_blk blocks of given block scores, expanded and translated, one
+ * call  ([QSA] 512-block selection, 4 token positions per block followed by
+ * the pending tokens; [TOPK] selection fused with the page-table transform).
+ * The selection half of qsa_indexer_select, for scores that come from
+ * elsewhere (qsa_index_scores, or another scorer).
+ *
+ *   scores     [n_rows][ld_scores] FP32; the candidates of row t are its
+ *              entries b < row_len[t]/4.  ld_scores >= max_len/4.
+ *   out_blocks [n_rows][k_blk] or NULL: the selected block ids, ascending,
+ *              -1 after the first min(k_blk, row_len/4).
+ *   out_pos    [n_rows][4*k_blk+3] or NULL: token positions.
+ *   out_slots  [n_rows][4*k_blk+3]: physical KV slots, -1 padded.
+ * Order and ties as in topk_select.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_req,
+                             const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                             int32_t max_len, const int32_t* page_table, int64_t ld_pt,
+                             int32_t page_size, int32_t k_blk, int32_t* out_blocks, int32_t* out_pos,
+                             int32_t* out_slots, void* stream);
+
+/* ---------------------------------------------------------------------
  * The fused decode path: score -> top-k_blk blocks -> expand -> slots, one
  * call  ([QSA] score equation and 512-block selection; [TOPK] selection
  * fused with the page-table transform).

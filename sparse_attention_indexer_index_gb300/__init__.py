@@ -52,6 +52,8 @@ def lib():
             "topk_select_workspace_size": (sz, [i32, i32, i32]),
             "topk_select": (ctypes.c_int, [p, i64, p, i32, i32, i32, p, i64, p, i32, p, p, p, sz, p]),
             "qsa_expand_slots": (ctypes.c_int, [p, i32, i32, p, i32, p, p, i64, i32, p, p, p]),
+            "qsa_select_blocks": (ctypes.c_int, [p, i64, i32, p, i32, p, i32, p, i64, i32, i32, p, p, p,
+                                                 p]),
             "qsa_indexer_select_workspace_size": (sz, [i32, i32, i32]),
             "qsa_indexer_select": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                   i32, p, p, p, p, i64, p, sz, p]),
@@ -204,6 +206,34 @@ def expand_slots(sel_blocks, req_row_start, row_len, page_table, page_size, want
         _ptr(page_table), page_table.shape[1], int(page_size), _ptr(pos), _ptr(slots),
         _stream(stream)))
     return pos, slots
+
+
+def select_blocks(scores, req_row_start, row_len, page_table, page_size, max_len, k_blk=512,
+                  want_blocks=False, want_pos=False, out_slots=None, stream=None):
+    """Top-k_blk blocks of given scores -> expand -> slots.
+    Returns dict(slots, blocks?, pos?)."""
+    torch = _torch()
+    _dev(scores, torch.float32, "scores", 2)
+    _dev(req_row_start, torch.int32, "req_row_start", 1)
+    _dev(row_len, torch.int32, "row_len", 1)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_rows = row_len.numel()
+    dev = scores.device
+    w = out_width(k_blk)
+    if out_slots is None:
+        out_slots = torch.empty((n_rows, w), dtype=torch.int32, device=dev)
+    blocks = torch.empty((n_rows, k_blk), dtype=torch.int32, device=dev) if want_blocks else None
+    pos = torch.empty((n_rows, w), dtype=torch.int32, device=dev) if want_pos else None
+    _check("qsa_select_blocks", lib().qsa_select_blocks(
+        _ptr(scores), scores.shape[1], req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+        _ptr(row_len), int(max_len), _ptr(page_table), page_table.shape[1], int(page_size), int(k_blk),
+        _ptr(blocks), _ptr(pos), _ptr(out_slots), _stream(stream)))
+    out = {"slots": out_slots}
+    if blocks is not None:
+        out["blocks"] = blocks
+    if pos is not None:
+        out["pos"] = pos
+    return out
 
 
 def indexer_select_workspace_size(n_rows, max_len, k_blk=512) -> int:

@@ -538,6 +538,41 @@ qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_
   return launch_status();
 }
 
+qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_req,
+                             const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                             int32_t max_len, const int32_t* page_table, int64_t ld_pt,
+                             int32_t page_size, int32_t k_blk, int32_t* out_blocks, int32_t* out_pos,
+                             int32_t* out_slots, void* stream) {
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+  const int32_t nb_max = max_len / kBlock;
+  if (!out_slots || (nb_max > 0 && !scores) || ld_scores < nb_max) return QSA_ERR_INVALID_ARG;
+  if (scores && !aligned4(scores)) return QSA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  SelectArgs a{};
+  a.scores = scores;
+  a.ld = ld_scores;
+  a.n_rows = n_rows;
+  a.k = k_blk;
+  a.n_max = nb_max;
+  plan_select(a);
+  a.vec_ok = scores && aligned16(scores) && (ld_scores % 4 == 0);
+  a.wait_primary = 0;
+  a.n_req = n_req;
+  a.req_row_start = req_row_start;
+  a.row_len = row_len;
+  a.out_idx = out_blocks;
+  a.out_pos = out_pos;
+  a.out_xslots = out_slots;
+  a.page_table = page_table;
+  a.ld_pt = ld_pt;
+  a.page_size = page_size;
+  return launch_select<kModeQsa>(a, false, static_cast<cudaStream_t>(stream));
+}
+
 size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_t k_blk) {
   (void)k_blk;
   if (n_rows <= 0 || max_len <= 0) return 0;

@@ -99,3 +99,15 @@ def test_zero_rows_are_a_no_op(L):
     assert L.topk_select(None, 0, None, 0, 0, 8, None, 0, None, 0, None, None, None, 0, None) == 0
     assert L.qsa_indexer_select(None, None, 0, 0, None, 0, None, 0, 0, None, 0, 64, 512, None, None,
                                 None, None, 0, None, 0, None) == 0
+
+
+def test_select_blocks_rejects_bad_arguments(L):
+    rrs = FAKE
+    # k_blk out of range
+    assert L.qsa_select_blocks(FAKE, 8, 1, rrs, 1, FAKE, 32, FAKE, 1, 64, 0, None, None, FAKE, None) == -2
+    # no output slots
+    assert L.qsa_select_blocks(FAKE, 8, 1, rrs, 1, FAKE, 32, FAKE, 1, 64, 4, None, None, None, None) == -1
+    # leading dimension shorter than max_len / 4
+    assert L.qsa_select_blocks(FAKE, 4, 1, rrs, 1, FAKE, 32, FAKE, 1, 64, 4, None, None, FAKE, None) == -1
+    # page size not a multiple of 4
+    assert L.qsa_select_blocks(FAKE, 8, 1, rrs, 1, FAKE, 32, FAKE, 1, 6, 4, None, None, FAKE, None) == -2

@@ -61,3 +61,24 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "rows/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_names_follow_the_dispatch_rules():
+    import bench
+    from workloads import c2_verify, c3_batched
+    n2 = bench.kernel_names(c2_verify(0))  # 6 rows per request, 64-token pages
+    assert n2 == {"compress": "compress_keys_kernel", "score": "score_tc_kernel",
+                  "select": "select_resident_kernel"}
+    n3 = bench.kernel_names(c3_batched(0))  # one row per request
+    assert n3["score"] == "score_decode_kernel"
+
+
+def test_kernel_bytes_c2():
+    import bench
+    from workloads import c2_verify
+    w = c2_verify(0)
+    kb = bench.kernel_bytes(w, 2)
+    nb = [int(L) // 4 for L in w.row_len]
+    assert kb["compress"] == 2 * (4 * 256 + 256 + 12)
+    assert kb["select"] == 4 * sum(nb) + 4 * (80000 // 64) + 6 * 4 * (4 * 512 + 3)
+    assert kb["score"] == 256 * max(nb) + 1024 * 6 + 4 * (80000 // 64) + 4 * sum(nb)

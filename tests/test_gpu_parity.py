@@ -330,3 +330,24 @@ def test_fused_workspace_path_matches_scores_out_path(qsa):
     a = qsa.indexer_select(*args, k_blk=512, scores_out=torch.empty((w.n_rows, ld), device="cuda"))
     b = qsa.indexer_select(*args, k_blk=512)
     assert torch.equal(a["slots"], b["slots"])
+
+
+@pytest.mark.parametrize("case", ["ragged_small", "c2_verify"])
+def test_select_blocks_parity(qsa, case):
+    """The selection half alone (scores given): bit-exact against the
+    oracle's top-k and expansion on the same FP32 scores, including rows with
+    fewer visible blocks than k and every pending-token count."""
+    if case == "ragged_small":
+        w = decode_workload(54, [[1, 5, 9], [2051, 4096, 7001, 20_002]], page_size=64, k_blk=512)
+    else:
+        w = c2_verify(0)
+    rng = np.random.default_rng(11)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    s = rng.standard_normal((w.n_rows, ld)).astype(np.float32)
+    out = qsa.select_blocks(to_dev(s), to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table),
+                            w.page_size, w.max_len, k_blk=w.k_blk, want_blocks=True, want_pos=True)
+    sel_ref, _ = oracle.topk(s, w.k_blk, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
