@@ -280,16 +280,22 @@ def select_only(g: Gpu, st):
                         k_blk=w.k_blk, out_slots=st["slots"])
 
 
-def kernel_names(w):
+def kernel_names(w, sm_count=152):
     """Kernels the library dispatches to for this workload (the launch rules
     of qsa_api.cu: requests with 2+ rows use the tensor-core scorer, fed by
     TMA when a page holds a multiple of 8 compressed keys; rows of up to
-    32768 blocks take the shared-memory-resident selection)."""
+    32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
+    shared-memory-resident single-CTA selection otherwise)."""
     if w.max_rows_per_req >= 2:
         score = "score_tc_kernel" if (w.page_size // 4) % 8 == 0 else "score_tc_cpasync_kernel"
     else:
         score = "score_decode_kernel"
-    select = "select_resident_kernel" if w.max_len // 4 <= 32768 else "select_kernel"
+    if w.max_len // 4 > 32768:
+        select = "select_kernel"
+    elif w.n_rows * 8 <= sm_count:
+        select = "select_cluster_kernel"
+    else:
+        select = "select_resident_kernel"
     return {"compress": "compress_keys_kernel", "score": score, "select": select}
 
 
@@ -535,7 +541,7 @@ def main():
 
     # ---- each kernel of the step alone, timed the same way; the roofline
     # object describes the one that takes longest -------------------------
-    names = kernel_names(w)
+    names = kernel_names(w, torch.cuda.get_device_properties(device).multi_processor_count)
     kbytes = kernel_bytes(w, new_blocks)
     scores_only(g, st)  # the selection below reads these scores
     kms = {

@@ -16,6 +16,7 @@
 #include "score_tc.cuh"
 #include "select.cuh"
 #include "select_resident.cuh"
+#include "select_cluster.cuh"
 
 using namespace qsa;
 
@@ -38,6 +39,10 @@ constexpr int kSelMaxSmem = kSelFixedBytes + kSelPtStage * 4 + kSelListCap * 8 +
 // kRsMaxSmem (at least 2 * kMaxK entries, at most kRsListMax).
 constexpr int kRsMaxSmem = 227 * 1024;
 constexpr int kRsListMax = 8192;
+// Few rows: one cluster of C CTAs per row (select_cluster_kernel), with a
+// candidate list of kScListCap entries in the leader.
+constexpr int kScListCap = 8192;
+constexpr int kScSmem = kScFixedBytes + 2 * kScListCap * 4 + kSelPtStage * 4 + kMaxK * 4;
 
 struct DeviceInfo {
   bool ready = false;
@@ -65,6 +70,10 @@ qsa_status device_info(DeviceInfo** out) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRsMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(select_resident_kernel<kModeQsa>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRsMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_cluster_kernel<kModeTopk, 4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(select_cluster_kernel<kModeQsa, 4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kScoreSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_cpasync_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -174,9 +183,63 @@ size_t select_smem_bytes(const SelectArgs& a) {
   return (size_t)a.off_row + row;
 }
 
+// Cluster selection for launches with few rows: 8 CTAs per row when
+// rows * 8 <= SMs.  Returns QSA_ERR_UNSUPPORTED when the single-CTA kernels
+// should run instead.
 template <int kMode>
-qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream) {
+qsa_status launch_select_cluster(const SelectArgs& args, bool pdl, int sm_count, cudaStream_t stream) {
+  if (args.n_max > kRsMaxRow) return QSA_ERR_UNSUPPORTED;
+  // one cluster of 8 CTAs per row when the rows leave that many SMs; with
+  // more rows the single-CTA kernels keep the GPU busy as well
+  const int C = 8;
+  if ((int64_t)args.n_rows * C > sm_count) return QSA_ERR_UNSUPPORTED;
+  SelectArgs a = args;
+  int off = kScFixedBytes;
+  a.list_cap = kScListCap;
+  a.off_lkey = off;
+  off += kScListCap * 4;
+  a.off_list = off;
+  off += kScListCap * 4;
+  a.off_pt = off;
+  a.pt_cap = kSelPtStage;
+  off += kSelPtStage * 4;
+  a.off_sel = off;
+  off += ((a.k + 3) & ~3) * 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.n_rows * C), 1, 1);
+  cfg.blockDim = dim3(kScThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)off;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)C;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e;
+  e = cudaLaunchKernelEx(&cfg, select_cluster_kernel<kMode, 4>, a);  // slices of <= 4096 = 1024 x 4
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
+template <int kMode>
+qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count = 0) {
   if (a.n_rows == 0) return QSA_OK;
+  if (sm_count > 0) {
+    const qsa_status st = launch_select_cluster<kMode>(a, pdl, sm_count, stream);
+    if (st != QSA_ERR_UNSUPPORTED) return st;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_rows, 1, 1);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
@@ -517,7 +580,7 @@ qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, 
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size > 0 ? page_size : 1;
-  if (qsa_status st = launch_select<kModeTopk>(a, false, static_cast<cudaStream_t>(stream)))
+  if (qsa_status st = launch_select<kModeTopk>(a, false, static_cast<cudaStream_t>(stream), d->sm_count))
     return st;
   return QSA_OK;
 }
@@ -570,7 +633,7 @@ qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_r
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
-  return launch_select<kModeQsa>(a, false, static_cast<cudaStream_t>(stream));
+  return launch_select<kModeQsa>(a, false, static_cast<cudaStream_t>(stream), d->sm_count);
 }
 
 size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_t k_blk) {
@@ -635,7 +698,7 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
-  return launch_select<kModeQsa>(a, nb_max > 0, st);
+  return launch_select<kModeQsa>(a, nb_max > 0, st, d->sm_count);
 }
 
 }  // extern "C"
@@ -722,5 +785,5 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
-  return launch_select<kModeQsa>(a, nb_max > 0, st);
+  return launch_select<kModeQsa>(a, nb_max > 0, st, d->sm_count);
 }

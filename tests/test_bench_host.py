@@ -68,9 +68,9 @@ def test_kernel_names_follow_the_dispatch_rules():
     from workloads import c2_verify, c3_batched
     n2 = bench.kernel_names(c2_verify(0))  # 6 rows per request, 64-token pages
     assert n2 == {"compress": "compress_keys_kernel", "score": "score_tc_kernel",
-                  "select": "select_resident_kernel"}
-    n3 = bench.kernel_names(c3_batched(0))  # one row per request
-    assert n3["score"] == "score_decode_kernel"
+                  "select": "select_cluster_kernel"}
+    n3 = bench.kernel_names(c3_batched(0))  # one row per request, 32 rows
+    assert n3["score"] == "score_decode_kernel" and n3["select"] == "select_resident_kernel"
 
 
 def test_kernel_bytes_c2():

@@ -132,7 +132,7 @@ def test_topk_parity_ragged(qsa, dist, k):
     run_topk(qsa, topk_workload(31, 9, 6000, k=k, dist=dist, ragged=True), k)
 
 
-@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (200, 3000),
+@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (40, 20_000), (200, 3000),
                                       (5, 32_768), (2, 32_772)])
 def test_topk_parity_row_lengths(qsa, n_rows, n):
     """Rows kept in shared memory (<= 32,768 scores) and rows streamed through
@@ -169,6 +169,26 @@ def test_topk_heavy_ties_take_the_full_row_path(qsa, n):
     s[2] = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)  # one top-bits bin
     s[3] = rng.standard_normal(n).astype(np.float32)        # ordinary row beside them
     nv = np.full(4, n, np.int32)
+    for k in [512, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
+@pytest.mark.parametrize("n", [20_000, 32_768])
+def test_topk_hard_rows_many_rows(qsa, n):
+    """The same hard rows (all equal, three values, one top-bits bin, the
+    sample planted with the largest values) in a launch of 24 rows, which
+    takes the single-CTA selection instead of one cluster per row."""
+    rng = np.random.default_rng(n + 7)
+    base = np.zeros((4, n), np.float32)
+    base[0] = 1.5
+    base[1] = rng.integers(0, 3, size=n).astype(np.float32)
+    base[2] = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)
+    base[3] = (rng.standard_normal(n) * 0.01).astype(np.float32)
+    base[3, (np.arange(1024, dtype=np.int64) * n) // 1024] = 100.0
+    s = np.concatenate([base] * 5 + [rng.standard_normal((4, n)).astype(np.float32)])
+    nv = np.full(s.shape[0], n, np.int32)
     for k in [512, 2048]:
         idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
         ref, _ = oracle.topk(s, k, n_valid=nv)
