@@ -283,13 +283,15 @@ def select_only(g: Gpu, st):
 def kernel_names(w, sm_count=152):
     """Kernels the library dispatches to for this workload (the launch rules
     of qsa_api.cu: requests with 2+ rows use the tensor-core scorer, fed by
-    TMA when a page holds a multiple of 8 compressed keys; rows of up to
+    TMA when a page holds a multiple of 8 compressed keys; one-row requests
+    use the balanced tensor-core scorer on such pages; rows of up to
     32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
     shared-memory-resident single-CTA selection otherwise)."""
+    tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0
     if w.max_rows_per_req >= 2:
-        score = "score_tc_kernel" if (w.page_size // 4) % 8 == 0 else "score_tc_cpasync_kernel"
+        score = "score_tc_kernel" if tma else "score_tc_cpasync_kernel"
     else:
-        score = "score_decode_kernel"
+        score = "score_tcb_kernel" if tma else "score_decode_kernel"
     if w.max_len // 4 > 32768:
         select = "select_kernel"
     elif w.n_rows * 8 <= sm_count:

@@ -82,6 +82,10 @@ qsa_status device_info(DeviceInfo** out) {
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return QSA_ERR_CUDA;
@@ -350,6 +354,104 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
   return QSA_OK;
 }
 
+// The query rows as a 2-D tensor [n_rows * 4][128] BF16 for the balanced
+// scorer's B operand: boxes of 64 x n_cols with the 128-byte swizzle (one
+// K-half of the n_cols query heads starting at a row tile's first head).
+bool encode_q_map(CUtensorMap* m, const void* q, int32_t n_rows, int n_cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)n_rows * kHeads};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)n_cols};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Balanced tensor-core scorer for decode batches (one row per request,
+// TMA-compatible pages): the key tiles of all requests split evenly over one
+// CTA per SM.  QSA_ERR_UNSUPPORTED: take another path.
+qsa_status launch_scores_balanced(const ScoreArgs& s, int max_rows_per_req, int sm_count,
+                                  cudaStream_t stream) {
+  const int64_t nb_max = s.max_len / kBlock;
+  if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
+  // Measured: with several rows per request the per-stage query block costs
+  // more than the balance gains (the per-request kernel is faster there).
+  if (max_rows_per_req != 1 || (int64_t)s.n_req > kTbMaxGroups) return QSA_ERR_UNSUPPORTED;
+  const int kpp = s.page_size / kBlock;
+  int R = 0;
+  for (int c = kTcM; c >= 8; c >>= 1)
+    if (kpp % c == 0) {
+      R = c;
+      break;
+    }
+  if (R == 0 || s.pool_rows <= 0 || s.pool_rows > INT32_MAX || s.pool_rows % 8 != 0) return QSA_ERR_UNSUPPORTED;
+  if ((int64_t)s.n_rows * kHeads > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  TcArgs t{};
+  t.q = s.q;
+  t.pool = s.pool;
+  t.pool_rows = s.pool_rows;
+  t.n_req = s.n_req;
+  t.req_row_start = s.req_row_start;
+  t.n_rows = s.n_rows;
+  t.row_len = s.row_len;
+  t.max_len = s.max_len;
+  t.page_table = s.page_table;
+  t.ld_pt = s.ld_pt;
+  t.page_size = s.page_size;
+  t.scores = s.scores;
+  t.ld_scores = s.ld_scores;
+  t.rows_per_tile = max_rows_per_req;
+  t.n_cols = ((4 * t.rows_per_tile) + 15) & ~15;
+  int cols = 32;
+  while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
+  t.tmem_cols = cols;
+  t.trigger_dependents = s.trigger_dependents;
+  t.box_rows = R;
+  t.box4d = 1;
+  t.row_tiles = 1;
+  t.n_groups = s.n_req;
+  CUtensorMap pool_map, q_map;
+  if (!encode_pool_map(&pool_map, t.pool, t.pool_rows, R, true) || !encode_q_map(&q_map, t.q, s.n_rows, t.n_cols))
+    return QSA_ERR_UNSUPPORTED;
+  const size_t stage_bytes = ((size_t)2 * kTcHalf + 2 * (size_t)t.n_cols * 128 + 1023) & ~(size_t)1023;
+  const size_t fixed = 1024 + (2 * kTcMaxStages + 4) * 8 + kTcMaxStages * sizeof(TbDesc) + sizeof(TbCtl) +
+                       4 * (4 * (size_t)t.n_groups + 1);
+  t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / stage_bytes);
+  if (t.stages < 3) return QSA_ERR_UNSUPPORTED;
+  const size_t smem = fixed + (size_t)t.stages * stage_bytes;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tcb_kernel, kTmThreads, smem) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
+  const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + kTcM - 1) / kTcM);
+  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(tiles_max, sm_count));
+  if (launch_pdl(score_tcb_kernel, dim3((unsigned)ctas), dim3(kTmThreads), smem, stream, t, pool_map, q_map) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  if (s.n_fill > 0) {
+    fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
+                                                              s.n_fill);
+    return launch_status();
+  }
+  return QSA_OK;
+}
+
+// Scorer dispatch: the balanced tensor-core kernel for decode batches, the
+// per-request tensor-core kernel for requests with several rows, the CUDA-
+// core streaming kernel otherwise.
+qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream);
+qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream);
+qsa_status launch_scorer(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
+  const qsa_status b = launch_scores_balanced(s, max_rows_per_req, sm_count, stream);
+  if (b != QSA_ERR_UNSUPPORTED) return b;
+  return max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, sm_count, stream)
+                                        : launch_scores(s, sm_count, stream);
+}
+
 // Tensor-core scorer for requests with several rows: tiles of 128 keys x up
 // to 64 rows (N = 4 * rows, multiple of 16), a group of key tiles per CTA
 // when rows are plentiful (prefill), one otherwise (decode verify).  The
@@ -541,9 +643,7 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld_scores, n_fill, 0};
-  if (max_rows_per_req >= kTcMinRows)
-    return launch_scores_tc(s, max_rows_per_req, d->sm_count, static_cast<cudaStream_t>(stream));
-  return launch_scores(s, d->sm_count, static_cast<cudaStream_t>(stream));
+  return launch_scorer(s, max_rows_per_req, d->sm_count, static_cast<cudaStream_t>(stream));
 }
 
 size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k) {
@@ -676,8 +776,7 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld, 0, 1};
-  if (qsa_status e = max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, d->sm_count, st)
-                                                     : launch_scores(s, d->sm_count, st))
+  if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
     return e;
 
   SelectArgs a{};
@@ -763,8 +862,7 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld, 0, 1};
-  if (qsa_status e = max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, d->sm_count, st)
-                                                     : launch_scores(s, d->sm_count, st))
+  if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
     return e;
 
   SelectArgs a{};

@@ -70,7 +70,7 @@ def test_kernel_names_follow_the_dispatch_rules():
     assert n2 == {"compress": "compress_keys_kernel", "score": "score_tc_kernel",
                   "select": "select_cluster_kernel"}
     n3 = bench.kernel_names(c3_batched(0))  # one row per request, 32 rows
-    assert n3["score"] == "score_decode_kernel" and n3["select"] == "select_resident_kernel"
+    assert n3["score"] == "score_tcb_kernel" and n3["select"] == "select_resident_kernel"
 
 
 def test_kernel_bytes_c2():

@@ -51,6 +51,8 @@ SMALL_DECODE = [
     ("multi_request", [[37, 40, 41], [9], [1030, 1031], [4096 * 4 + 3]], 16),
     ("tiny_pages", [[77, 78], [130]], 4),
     ("ten_rows", [[2000 + i for i in range(10)], [513]], 32),
+    # one row per request on 16-token pages: the CUDA-core streaming scorer
+    ("one_row_small_pages", [[1002], [4001], [77], [9000]], 16),
 ]
 
 
