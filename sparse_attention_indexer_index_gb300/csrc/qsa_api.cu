@@ -80,13 +80,17 @@ qsa_status device_info(DeviceInfo** out) {
                              kTcMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_cpasync_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-        cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(score_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-        cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(score_tc_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return QSA_ERR_CUDA;
     d.ready = true;
@@ -342,12 +346,17 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
   t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / (2 * kTcHalf));
   if (t.stages < 2) return QSA_ERR_UNSUPPORTED;
   const size_t smem = fixed + (size_t)t.stages * 2 * kTcHalf;
+  // wide tiles (prefill) get 16 epilogue warps, narrow ones 8
+  const bool wide = t.n_cols >= 128;
+  const int threads = wide ? 32 * (2 + 16) : 32 * (2 + 8);
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tc_kernel, kTmThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, wide ? score_tc_kernel<16> : score_tc_kernel<8>, threads,
+                                                    smem) != cudaSuccess)
     return QSA_ERR_CUDA;
   if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
   dim3 grid((unsigned)((n_kt + t.tiles_per_cta - 1) / t.tiles_per_cta), (unsigned)row_tiles, (unsigned)n_req);
-  if (launch_pdl(score_tc_kernel, grid, dim3(kTmThreads), smem, stream, t, map) != cudaSuccess) {
+  if (launch_pdl(wide ? score_tc_kernel<16> : score_tc_kernel<8>, grid, dim3(threads), smem, stream, t, map) !=
+      cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
   }

@@ -387,9 +387,10 @@ score_tc_cpasync_kernel(TcArgs a) {
 //   warp 1      MMA issuer (one lane) and TMEM owner: waits `full`, issues
 //               the 8 K-steps into one of two TMEM accumulators, commits to
 //               the stage's `empty` barrier and the accumulator's `acc_full`;
-//   warps 2..9  epilogue: two warps per TMEM lane quarter split the column
-//               chunks, read the accumulator, apply ReLU / head sum / scale,
-//               store coalesced scores, and release `acc_empty`.
+//   warps 2..    epilogue (8, or 16 for wide prefill tiles): two or four
+//               warps per TMEM lane quarter split the column chunks, read the
+//               accumulator, apply ReLU / head sum / scale, store coalesced
+//               scores, and release `acc_empty`.
 // Every wait is bounded; a timeout latches kFaultWait and sets a shared
 // abort flag that ends the other roles' waits too, and the CTA drains its
 // outstanding copies and MMAs (again bounded) before freeing tensor memory.
@@ -438,8 +439,13 @@ __device__ __forceinline__ bool tm_wait(uint64_t* bar, uint32_t parity, volatile
   return true;
 }
 
-__global__ void __launch_bounds__(kTmThreads, 1)
+// kEpi: epilogue warps, 8 or 16 (4 per TMEM lane quarter, each taking a
+// quarter of the column chunks; wide tiles -- prefill, N = 256 -- need 16 to
+// keep up with the MMA).
+template <int kEpi>
+__global__ void __launch_bounds__(32 * (2 + kEpi), 1)
 score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
+  constexpr int kThreads = 32 * (2 + kEpi);
   extern __shared__ __align__(16) unsigned char tm_smem_raw[];
   // [A stages x 32 KB][B: 2 x N x 128 B][barriers][control][row lengths][page table]
   unsigned char* base = tm_smem_raw + ((1024u - (smem_u32(tm_smem_raw) & 1023u)) & 1023u);
@@ -498,11 +504,11 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   if (pt_n > a.ld_pt - pt0) pt_n = (int)(a.ld_pt - pt0);
   if (pt_n < 0) pt_n = 0;
   const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
-  for (int i = threadIdx.x; i < pt_n; i += kTmThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
+  for (int i = threadIdx.x; i < pt_n; i += kThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
 
   // ---- query rows -> B (zero columns beyond 4 * nrows) ---------------------
   const int valid_cols = 4 * nrows;
-  for (int i = threadIdx.x; i < N * 16; i += kTmThreads) {
+  for (int i = threadIdx.x; i < N * 16; i += kThreads) {
     const int col = i >> 4, c = i & 15;
     const bool ok = col < valid_cols;
     const __nv_bfloat16* src = ok ? a.q + ((int64_t)t0 * kHeads + col) * kDim + c * 8 : a.q;
@@ -525,7 +531,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kTmEpiWarps);
+      mbar_init(&acc_empty[i], kEpi);
     }
     ctl->abort = 0;
     ctl->issued = 0;
@@ -619,7 +625,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
     // ---- epilogue: warp w reads TMEM lane quarter w % 4 (keys 32(w%4) ..
     // +31) and the column chunks of its half ---------------------------------
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int cgroup = (warp - 2) >> 2;  // 0 .. kEpi/4 - 1
     for (int i = 0; i < n_local; ++i) {
       const int acc = i & 1;
       const bool ok = __all_sync(0xffffffffu, tm_wait(&acc_full[acc], (uint32_t)(i >> 1) & 1u, abort));
@@ -627,7 +633,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
       tc_fence_after();
       const int b = (kt0 + i) * kTcM + quarter * 32 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
-      for (int c0 = 32 * half; c0 < N; c0 += 64) {
+      for (int c0 = 32 * cgroup; c0 < N; c0 += 32 * (kEpi / 4)) {
         uint32_t v[32];
         int ncols = 32;
         if (N - c0 >= 32) {
