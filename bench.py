@@ -288,10 +288,13 @@ def kernel_names(w, sm_count=152):
     32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
     shared-memory-resident single-CTA selection otherwise)."""
     tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0
-    if w.max_rows_per_req >= 2:
+    balanced = tma and w.max_rows_per_req == 1
+    if balanced:
+        score = "score_tcb_kernel"
+    elif w.max_rows_per_req >= 2:
         score = "score_tc_kernel" if tma else "score_tc_cpasync_kernel"
     else:
-        score = "score_tcb_kernel" if tma else "score_decode_kernel"
+        score = "score_decode_kernel"
     if w.max_len // 4 > 32768:
         select = "select_kernel"
     elif w.n_rows * 8 <= sm_count:

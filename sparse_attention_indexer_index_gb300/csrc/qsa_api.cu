@@ -385,8 +385,8 @@ qsa_status launch_scores_balanced(const ScoreArgs& s, int max_rows_per_req, int 
                                   cudaStream_t stream) {
   const int64_t nb_max = s.max_len / kBlock;
   if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
-  // Measured: with several rows per request the per-stage query block costs
-  // more than the balance gains (the per-request kernel is faster there).
+  // Measured: requests with several rows run faster on the per-request
+  // kernel (its tiles already spread over the grid, and it starts sooner).
   if (max_rows_per_req != 1 || (int64_t)s.n_req > kTbMaxGroups) return QSA_ERR_UNSUPPORTED;
   const int kpp = s.page_size / kBlock;
   int R = 0;
@@ -425,7 +425,7 @@ qsa_status launch_scores_balanced(const ScoreArgs& s, int max_rows_per_req, int 
   if (!encode_pool_map(&pool_map, t.pool, t.pool_rows, R, true) || !encode_q_map(&q_map, t.q, s.n_rows, t.n_cols))
     return QSA_ERR_UNSUPPORTED;
   const size_t stage_bytes = ((size_t)2 * kTcHalf + 2 * (size_t)t.n_cols * 128 + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + (2 * kTcMaxStages + 4) * 8 + kTcMaxStages * sizeof(TbDesc) + sizeof(TbCtl) +
+  const size_t fixed = 1024 + (2 * kTcMaxStages + 6) * 8 + kTcMaxStages * sizeof(TbDesc) + sizeof(TbCtl) +
                        4 * (4 * (size_t)t.n_groups + 1);
   t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / stage_bytes);
   if (t.stages < 3) return QSA_ERR_UNSUPPORTED;

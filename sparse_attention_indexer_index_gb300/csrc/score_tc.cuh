@@ -695,19 +695,21 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
 // requests): the key tiles of all (request, row tile) groups form one list
 // that the CTAs split evenly (one CTA per SM), so a CTA crosses requests.
 // Every ring stage carries its own query rows (B operand, via a second
-// tensor map over q) and a small descriptor of its tile, so a change of
-// request costs nothing in the pipeline.  The page-table entries of a tile
-// are fetched kTbPtAhead tiles ahead (cp.async into a small ring): while HBM
-// is saturated a scattered 4-byte load takes microseconds.  A stage is
-// released when its MMAs completed and every epilogue warp has read its
-// descriptor.  Roles as in score_tc_kernel.
+// tensor map over q, loaded only when the stage last held another group's
+// rows) and a small descriptor of its tile, so a change of request costs
+// nothing in the pipeline.  The page-table entries of a tile are fetched
+// kTbPtAhead tiles ahead (cp.async into a small ring): while HBM is
+// saturated a scattered 4-byte load takes microseconds.  A stage is released
+// when its MMAs complete; the MMA thread hands the tile's descriptor to the
+// epilogue through a per-accumulator slot and barrier.  Roles as in
+// score_tc_kernel.
 // ---------------------------------------------------------------------------
 constexpr int kTbMaxRowsPerTile = 16;  // N <= 64 columns: B of a stage <= 16 KB
 constexpr int kTbMaxGroups = 2048;
 constexpr int kTbPtAhead = 8;
 
 struct TbDesc {
-  int t0, nrows, kt, pad;
+  int t0, nrows, kt, nb;  // first row, rows, key tile, visible blocks (max over the rows)
 };
 struct TbCtl {
   int abort;
@@ -717,13 +719,15 @@ struct TbCtl {
   uint32_t tmem;
   int wsum[kTmWarps];
   int32_t pt_ring[kTbPtAhead + 1][16];  // page entries of upcoming tiles (<= 16 runs each)
+  int b_group[kTcMaxStages];            // group whose query rows a stage's B holds (-1: none)
+  TbDesc desc_acc[2];                   // descriptor of the tile in each accumulator
 };
 
 __global__ void __launch_bounds__(kTmThreads, 1)
 score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
                  const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ __align__(16) unsigned char tb_smem_raw[];
-  // [stages x (A 32 KB | B 2 x N x 128 B)][full][empty][acc_full][acc_empty][descs][control]
+  // [stages x (A 32 KB | B 2 x N x 128 B)][full][empty][acc_full][acc_empty][desc_ready][descs][control]
   // [group prefix][group first row][group rows][group blocks]
   unsigned char* base = tb_smem_raw + ((1024u - (smem_u32(tb_smem_raw) & 1023u)) & 1023u);
   const int S = a.stages;
@@ -735,7 +739,8 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
   uint64_t* empty = full + S;                                                    // [S]
   uint64_t* acc_full = empty + S;                                                // [2]
   uint64_t* acc_empty = acc_full + 2;                                            // [2]
-  TbDesc* desc = reinterpret_cast<TbDesc*>(acc_empty + 2);                       // [S]
+  uint64_t* desc_ready = acc_empty + 2;                                          // [2]
+  TbDesc* desc = reinterpret_cast<TbDesc*>(desc_ready + 2);                      // [S]
   TbCtl* ctl = reinterpret_cast<TbCtl*>(desc + S);
   int* g_pre = reinterpret_cast<int*>(ctl + 1);  // [G + 1] key tiles before group g
   int* g_t0 = g_pre + a.n_groups + 1;            // [G] first row of group g
@@ -824,16 +829,18 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + kTmEpiWarps);  // MMA commit + every epilogue warp read the descriptor
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kTmEpiWarps);
+      mbar_init(&desc_ready[i], 1);
     }
     ctl->abort = 0;
     ctl->issued = 0;
     ctl->consumed = 0;
     ctl->mma_done = 0;
+    for (int i = 0; i < kTcMaxStages; ++i) ctl->b_group[i] = -1;
     fence_mbar_init();
   }
   tc_fence_before();
@@ -843,7 +850,9 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
 
   if (warp == 0) {
     // ---- producer: key runs (one 4-D box per run), the group's query rows
-    // (two 2-D boxes), the stage descriptor ----------------------------------
+    // (two 2-D boxes, only when the stage's B holds another group's rows:
+    // the previous MMAs on the stage are complete once `empty` fired), the
+    // stage descriptor --------------------------------------------------------
     const int R = a.box_rows;
     const int runs = kTcM / R;  // <= 16
     int g_ahead = g_first;
@@ -905,11 +914,16 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
         desc[st].t0 = g_t0[g];
         desc[st].nrows = g_nr[g];
         desc[st].kt = kt;
+        desc[st].nb = nb_tile;
+        const bool load_b = ctl->b_group[st] != g;
         mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(vm) * 2u * (uint32_t)R * 128u +
-                                             2u * (uint32_t)N * 128u);
-        unsigned char* bdst = bbuf(st);
-        tma_load_2d(bdst, &q_map, 0, g_t0[g] * kHeads, &full[st]);
-        tma_load_2d(bdst + N * 128, &q_map, 64, g_t0[g] * kHeads, &full[st]);
+                                             (load_b ? 2u * (uint32_t)N * 128u : 0u));
+        if (load_b) {
+          ctl->b_group[st] = g;
+          unsigned char* bdst = bbuf(st);
+          tma_load_2d(bdst, &q_map, 0, g_t0[g] * kHeads, &full[st]);
+          tma_load_2d(bdst + N * 128, &q_map, 64, g_t0[g] * kHeads, &full[st]);
+        }
       }
       __syncwarp();
       if (valid) tma_load_4d(abuf(st) + lane * R * 256, &pool_map, prow >> 3, &full[st]);
@@ -926,6 +940,10 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
         if (!tm_wait(&full[st], (uint32_t)(i / S) & 1u, abort)) break;
         ctl->consumed = i + 1;
         if (i >= 2 && !tm_wait(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, abort)) break;
+        // hand the tile's descriptor to the epilogue (its previous reader of
+        // this accumulator is done: acc_empty above)
+        ctl->desc_acc[acc] = desc[st];
+        mbar_arrive(&desc_ready[acc]);
         tc_fence_after();
         const uint32_t a_base = smem_u32(abuf(st)), b_base = smem_u32(bbuf(st));
         const uint32_t d = tmem + (uint32_t)(acc * N);
@@ -948,16 +966,14 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
     const int half = (warp - 2) >> 2;
     for (int i = 0; i < n_items; ++i) {
       const int st = i % S, acc = i & 1;
-      // acc_full completes through the tensor core; the stage's own `full`
-      // phase (done, and not reopened before this warp releases the stage)
-      // orders the producer's descriptor write before the read below
-      const bool ok = __all_sync(0xffffffffu, tm_wait(&acc_full[acc], (uint32_t)(i >> 1) & 1u, abort) &&
-                                                  tm_wait(&full[st], (uint32_t)(i / S) & 1u, abort));
+      // the descriptor comes through desc_ready (a plain arrive by the MMA
+      // thread, which read it after `full`); acc_full completes through the
+      // tensor core
+      const bool ok = __all_sync(0xffffffffu, tm_wait(&desc_ready[acc], (uint32_t)(i >> 1) & 1u, abort) &&
+                                                  tm_wait(&acc_full[acc], (uint32_t)(i >> 1) & 1u, abort));
       if (!ok) break;
       tc_fence_after();
-      const TbDesc dd = desc[st];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the descriptor
+      const TbDesc dd = ctl->desc_acc[acc];
       const int b = dd.kt * kTcM + quarter * 32 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
       for (int c0 = 32 * half; c0 < N; c0 += 64) {
@@ -975,8 +991,9 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int tr = c0 / 4 + j;  // row within the tile
-          if (4 * j < ncols && tr < dd.nrows) {
-            const int L = __ldg(a.row_len + dd.t0 + tr);
+          if (4 * j < ncols && tr < dd.nrows && b < dd.nb) {
+            // one row: its visible blocks are the group's; several: its own
+            const int L = dd.nrows == 1 ? kBlock * dd.nb : __ldg(a.row_len + dd.t0 + tr);
             if (L >= 0 && L <= a.max_len && b < L / kBlock) {
               float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
               sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
