@@ -65,6 +65,8 @@ def _load():
                 "oracle_expand_row": (None, [p, i64, i64, p, i64, p, p]),
                 "oracle_expand": (None, [p, i64, i64, p, p, p, i64, i64, p, p]),
                 "oracle_indexer_select": (None, [p, p, i64, p, p, p, i64, i64, i64, p, i64, p, p, p]),
+                "oracle_indexshare_row": (ctypes.c_int, [p, i64, i64, i64, i64, p, i64, p, p]),
+                "oracle_indexshare": (ctypes.c_int, [p, p, i64, p, i64, i64, i64, p, p, p, i64, i64, p, p]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -233,3 +235,40 @@ def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, k_blk
                                   _ptr(pt), pt.shape[-1], int(page_size), int(k_blk),
                                   _ptr(scores), ld, _ptr(blocks), _ptr(pos), _ptr(slots))
     return {"scores": scores, "blocks": blocks, "pos": pos, "slots": slots}
+
+
+# ---------------------------------------------------------------- IndexShare
+def indexshare_width(k_blk: int, n_extra: int) -> int:
+    """Entries per reused row: the expanded width plus the drafted columns."""
+    return out_width(k_blk) + n_extra
+
+
+def indexshare_row(cap_sel, cap_len, n_extra, L, pt_row, page_size):
+    """Returns (pos, slots, flags) of one draft row reading a captured row."""
+    cap_sel = _c(cap_sel, np.int32)
+    pt_row = _c(pt_row, np.int32)
+    w = indexshare_width(cap_sel.size, n_extra)
+    pos = np.empty(w, np.int32)
+    slots = np.empty(w, np.int32)
+    f = _load().oracle_indexshare_row(_ptr(cap_sel), cap_sel.size, int(cap_len), int(n_extra), int(L),
+                                      _ptr(pt_row), int(page_size), _ptr(pos), _ptr(slots))
+    return pos, slots, int(f)
+
+
+def indexshare(cap_sel, cap_len, cap_row, n_extra, req_row_start, row_len, page_table, page_size):
+    """cap_sel [n_cap][k_blk], cap_len [n_cap], cap_row [n_req].  Returns
+    (pos, slots, flags) for every row."""
+    cap_sel = _c(cap_sel, np.int32)
+    n_cap, k_blk = cap_sel.shape
+    cl = _c(cap_len, np.int32)
+    cr = _c(cap_row, np.int32)
+    rrs = _c(req_row_start, np.int32)
+    rl = _c(row_len, np.int32)
+    pt = _c(page_table, np.int32)
+    w = indexshare_width(k_blk, n_extra)
+    pos = np.empty((rl.size, w), np.int32)
+    slots = np.empty((rl.size, w), np.int32)
+    f = _load().oracle_indexshare(_ptr(cap_sel), _ptr(cl), n_cap, _ptr(cr), k_blk, int(n_extra),
+                                  rrs.size - 1, _ptr(rrs), _ptr(rl), _ptr(pt), pt.shape[-1],
+                                  int(page_size), _ptr(pos), _ptr(slots))
+    return pos, slots, int(f)

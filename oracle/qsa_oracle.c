@@ -19,6 +19,10 @@
  *  [SMLA] "vllm-sparse-mla-blackwell" (shadowgraph.io), section "Design notes
  *         worth knowing" -- the consumer masks on index >= 0, so -1 is the
  *         empty-entry sentinel.
+ *  [QSA] also, section "IndexShare MTP: reusing the QSA selection across
+ *         draft steps" -- the selection of the draft-extend row is kept for
+ *         the whole MTP iteration and read together with the positions
+ *         drafted since; the draft steps run no indexer.
  *
  * Every floating-point step that the pages leave open is done in FP64 and
  * rounded once at the end, except the block mean, which [QSA] fixes as FP32.
@@ -269,6 +273,79 @@ void oracle_expand(const int32_t* sel, int64_t k_blk, int64_t n_req, const int32
     for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t)
       oracle_expand_row(sel + t * k_blk, k_blk, row_len[t], page_table + r * ld_pt, page_size,
                         out_pos + t * width, out_slots + t * width);
+}
+
+/* ---------- IndexShare reuse ([QSA], section "IndexShare MTP: reusing the
+ * QSA selection across draft steps") ------------------------------------- */
+
+/* The selection kept at a request's draft-extend row (the last row the target
+ * accepted; it saw cap_len tokens and kept the blocks cap_sel[0..k_blk))
+ * serves every later draft row of that request, which runs no scorer and no
+ * top-k of its own.  A row that sees L tokens reads, in ascending order:
+ *   - the positions 4b..4b+3 of each captured block b, those below L;
+ *   - every position from 4*floor(cap_len/4) up to L-1: the capture's own
+ *     pending tokens, then every token drafted since;
+ * then -1 up to the width 4*k_blk + 3 + n_extra (n_extra: the drafted
+ * positions the caller leaves room for).  A captured block that was not
+ * complete at the capture (b >= floor(cap_len/4)) is skipped: its positions
+ * belong to the second part.  Slots are the page-table images of the
+ * positions.  Returns a bit set: 1 = the list did not fit and was cut at the
+ * width, 2 = a captured block was skipped. */
+int oracle_indexshare_row(const int32_t* cap_sel, int64_t k_blk, int64_t cap_len,
+                          int64_t n_extra, int64_t L, const int32_t* pt_row, int64_t page_size,
+                          int32_t* out_pos, int32_t* out_slots) {
+  int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;
+  int64_t nb0 = cap_len / QSA_C;
+  int64_t w = 0;
+  int flags = 0;
+  for (int64_t j = 0; j < k_blk; ++j) {
+    int64_t b = cap_sel[j];
+    if (b < 0) continue;
+    if (b >= nb0) {
+      flags |= 2;
+      continue;
+    }
+    for (int c = 0; c < QSA_C; ++c) {
+      int64_t p = QSA_C * b + c;
+      if (p >= L) continue;
+      if (w < width) out_pos[w++] = (int32_t)p;
+      else flags |= 1;
+    }
+  }
+  for (int64_t p = QSA_C * nb0; p < L; ++p) {
+    if (w < width) out_pos[w++] = (int32_t)p;
+    else flags |= 1;
+  }
+  for (; w < width; ++w) out_pos[w] = -1;
+  for (int64_t j = 0; j < width; ++j)
+    out_slots[j] = out_pos[j] < 0 ? -1 : (int32_t)oracle_slot_of(pt_row, out_pos[j], page_size);
+  return flags;
+}
+
+/* Every row t of request r reads the captured row cap_row[r] of cap_sel
+ * ([n_cap][k_blk], row lengths cap_len[n_cap]).  A request whose cap_row is
+ * outside [0, n_cap) gets a row of -1 and flag 4.  Returns the OR of the
+ * rows' flags. */
+int oracle_indexshare(const int32_t* cap_sel, const int32_t* cap_len, int64_t n_cap,
+                      const int32_t* cap_row, int64_t k_blk, int64_t n_extra, int64_t n_req,
+                      const int32_t* req_row_start, const int32_t* row_len,
+                      const int32_t* page_table, int64_t ld_pt, int64_t page_size,
+                      int32_t* out_pos, int32_t* out_slots) {
+  int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;
+  int flags = 0;
+  for (int64_t r = 0; r < n_req; ++r)
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t) {
+      int64_t c = cap_row[r];
+      if (c < 0 || c >= n_cap) {
+        for (int64_t j = 0; j < width; ++j) out_pos[t * width + j] = out_slots[t * width + j] = -1;
+        flags |= 4;
+        continue;
+      }
+      flags |= oracle_indexshare_row(cap_sel + c * k_blk, k_blk, cap_len[c], n_extra, row_len[t],
+                                     page_table + r * ld_pt, page_size, out_pos + t * width,
+                                     out_slots + t * width);
+    }
+  return flags;
 }
 
 /* ---------- the whole decode path: score -> top-k blocks -> slots ------- */

@@ -376,3 +376,96 @@ def test_indexer_select_composition_and_padding():
         assert np.array_equal(out["blocks"][t], want)
         _check_invariants(out["scores"][t], nb, 512, out["blocks"][t])
         assert ((out["blocks"][t] == -1).sum() > 0) == (nb < 512)
+
+
+# ------------------------------------------------------------ IndexShare reuse
+# Qwen3.8-Flash-Next day-0 write-up, section "IndexShare MTP: reusing the QSA
+# selection across draft steps": draft rows read the draft-extend row's
+# selection plus the positions drafted since, without a scorer or top-k.
+def test_indexshare_hand_example():
+    g = json.load(open(os.path.join(GOLDEN, "indexshare_3block.json")))
+    pt = np.array(g["page_table"], np.int32)
+    for row in g["rows"]:
+        pos, slots, flags = oracle.indexshare_row(g["cap_blocks"], g["cap_len"], g["n_extra"], row["L"], pt,
+                                                  g["page_size"])
+        assert pos.tolist() == row["positions"], row["L"]
+        assert slots.tolist() == row["slots"], row["L"]
+        assert flags == row["flags"], row["L"]
+
+
+def _captured(seed, k_blk, cap_len):
+    """A captured selection as the selection step makes it: top-k of random
+    scores over the capture's complete blocks."""
+    nb0 = cap_len // 4
+    s = np.random.default_rng(seed).standard_normal(max(nb0, 1)).astype(np.float32)
+    return oracle.topk_row(s[:nb0], k_blk)
+
+
+@pytest.mark.parametrize("cap_len", [0, 3, 4, 13, 14, 15, 16, 2047, 2048, 2051, 5000])
+def test_indexshare_without_new_blocks_is_the_plain_expansion(cap_len):
+    """While no block completes after the capture, the reused row is exactly
+    the expansion of the captured blocks at the row's own length."""
+    k_blk, P = 512, 16
+    pt = np.random.default_rng(cap_len).permutation(cap_len // P + 4).astype(np.int32)
+    sel = _captured(cap_len, k_blk, cap_len)
+    for L in range(cap_len, 4 * (cap_len // 4) + 4):
+        pos, slots, flags = oracle.indexshare_row(sel, cap_len, 0, L, pt, P)
+        epos, eslots = oracle.expand_row(sel, L, pt, P)
+        assert flags == 0
+        assert np.array_equal(pos, epos) and np.array_equal(slots, eslots)
+
+
+@pytest.mark.parametrize("cap_len,n_extra", [(14, 3), (16, 1), (2049, 6), (8000, 4), (8003, 9)])
+def test_indexshare_equals_expansion_with_every_new_block_kept(cap_len, n_extra):
+    """Blocks completed after the capture are visible in full: the reused
+    list equals the plain expansion at the row's length of the captured
+    blocks plus every block completed since (a wider selection)."""
+    k_blk, P = 512, 64
+    L_max = cap_len + n_extra
+    pt = np.random.default_rng(cap_len + 7).permutation(L_max // P + 2).astype(np.int32)
+    sel = _captured(cap_len + 1, k_blk, cap_len)
+    nb0 = cap_len // 4
+    for L in range(cap_len, L_max + 1):
+        pos, slots, flags = oracle.indexshare_row(sel, cap_len, n_extra, L, pt, P)
+        assert flags == 0 and pos.size == 4 * k_blk + 3 + n_extra
+        new = np.arange(nb0, L // 4, dtype=np.int32)
+        wide = np.concatenate([sel[sel >= 0], new]).astype(np.int32)
+        epos, eslots = oracle.expand_row(wide, L, pt, P)
+        n = int((pos >= 0).sum())
+        assert n == int((epos >= 0).sum())
+        assert np.array_equal(pos[:n], epos[:n]) and np.array_equal(slots[:n], eslots[:n])
+        assert (pos[n:] == -1).all() and (slots[n:] == -1).all()
+
+
+def test_indexshare_row_before_capture_sees_only_its_past():
+    """A row earlier than the capture keeps only the captured positions
+    below its own length (ascending, -1 at the tail)."""
+    k_blk, P, cap_len = 64, 16, 1000
+    pt = np.arange(cap_len // P + 2, dtype=np.int32)[::-1].copy()
+    sel = _captured(3, k_blk, cap_len)
+    full, _ = oracle.expand_row(sel, cap_len, pt, P)
+    for L in [0, 1, 5, 100, 401, 997, 999]:
+        pos, slots, flags = oracle.indexshare_row(sel, cap_len, 2, L, pt, P)
+        want = [int(p) for p in full if 0 <= p < L]
+        n = len(want)
+        assert flags == 0 and pos[:n].tolist() == want and (pos[n:] == -1).all()
+
+
+def test_indexshare_flags_and_request_mapping():
+    P = 4
+    pt = np.array([[2, 0, 3, 1, 5, 6], [1, 2, 3, 4, 5, 0]], np.int32)
+    # a captured block that was not complete at the capture is skipped
+    pos, _, flags = oracle.indexshare_row([0, 3], 14, 3, 16, pt[0], P)
+    assert flags == 2 and pos.tolist()[:8] == [0, 1, 2, 3, 12, 13, 14, 15]
+    # request -> captured row, rows of a request share it; a bad cap_row gives -1
+    cap = np.array([[0, 2], [1, -1]], np.int32)
+    cap_len = np.array([14, 9], np.int32)
+    rrs = np.array([0, 2, 3], np.int32)
+    row_len = np.array([15, 17, 11], np.int32)
+    pos, slots, flags = oracle.indexshare(cap, cap_len, [0, 1], 3, rrs, row_len, pt, P)
+    assert flags == 0
+    assert pos[0].tolist() == [0, 1, 2, 3, 8, 9, 10, 11, 12, 13, 14, -1, -1, -1]
+    assert pos[2].tolist() == [4, 5, 6, 7, 8, 9, 10] + [-1] * 7
+    assert slots[2].tolist() == [8, 9, 10, 11, 12, 13, 14] + [-1] * 7
+    pos, slots, flags = oracle.indexshare(cap, cap_len, [0, 2], 3, rrs, row_len, pt, P)
+    assert flags == 4 and (pos[2] == -1).all() and (slots[2] == -1).all()

@@ -49,6 +49,13 @@ MUTANTS = {
     "expand_block_not_times_4": (
         "out_pos[w++] = QSA_C * sel[j] + c;", "out_pos[w++] = sel[j] + c;"),
     "bf16_truncates": ("double r = nearbyint(x / q) * q;", "double r = trunc(x / q) * q;"),
+    "indexshare_tail_from_cap_len": (
+        "for (int64_t p = QSA_C * nb0; p < L; ++p) {", "for (int64_t p = cap_len; p < L; ++p) {"),
+    "indexshare_no_causal_cut": ("      if (p >= L) continue;\n", ""),
+    "indexshare_incomplete_block_kept": ("    if (b >= nb0) {\n      flags |= 2;\n      continue;\n    }\n", ""),
+    "indexshare_no_drafted_columns": (
+        "int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;\n  int64_t nb0",
+        "int64_t width = QSA_C * k_blk + (QSA_C - 1);\n  int64_t nb0"),
 }
 
 
