@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (c1_decode, c2_batched, c2_verify, c3_batched, c4_dsa_topk,  # noqa: E402
+from workloads import (c1_decode, c2_batched, c2_verify, c3_batched, c4_dsa_topk, indexshare_mtp,  # noqa: E402
                        c5_prefill)
 
 METRIC = "indexer+top-k query rows/sec at L=80k decode; achieved HBM GB/s vs roofline"
@@ -402,6 +402,49 @@ def bench_variant_topk(g, w, iters, warmup, peaks):
             "dup_fraction": w.dup_fraction}
 
 
+def bench_variant_indexshare(g, w, iters, warmup, peaks):
+    """One draft step of an MTP iteration with IndexShare: each request's
+    draft row reads the selection kept at its draft-extend row
+    (qsa_indexshare_slots) instead of running the indexer.  The indexer call
+    the same draft rows would otherwise make is timed beside it."""
+    torch, qsa = g.torch, g.qsa
+    ext_rows = w.req_row_start[:-1]
+    ext_len = np.ascontiguousarray(w.row_len[ext_rows])
+    d_rows = ext_rows + 1  # the first draft step: position L0 + 1
+    d_len = np.ascontiguousarray(w.row_len[d_rows])
+    n_req = w.n_req
+    st = setup_decode(g, w, 0)
+    rrs1 = g.h2d(np.arange(n_req + 1, dtype=np.int32))
+    pt = st["pt"]
+    ext = qsa.indexer_select(g.bf16(w.q[ext_rows]), st["pool"], rrs1, g.h2d(ext_len), pt, w.page_size,
+                             int(ext_len.max()), 1, k_blk=w.k_blk, want_blocks=True)
+    kept, kept_len = ext["blocks"], g.h2d(ext_len)
+    cap_row = g.h2d(np.arange(n_req, dtype=np.int32))
+    n_extra = int(w.max_rows_per_req)  # the draft depth + 1
+    d_len_t = g.h2d(d_len)
+    out = torch.empty((n_req, qsa.indexshare_width(w.k_blk, n_extra)), dtype=torch.int32, device=g.dev)
+    t_share = g.timed(lambda: qsa.indexshare_slots(kept, kept_len, cap_row, n_extra, rrs1, d_len_t, pt,
+                                                   w.page_size, want_pos=False, out_slots=out),
+                      iters, warmup)
+    q_d = g.bf16(w.q[d_rows])
+    ws = torch.empty(qsa.indexer_select_workspace_size(n_req, int(d_len.max()), w.k_blk), dtype=torch.uint8,
+                     device=g.dev)
+    slots = torch.empty((n_req, 4 * w.k_blk + 3), dtype=torch.int32, device=g.dev)
+    t_full = g.timed(lambda: qsa.indexer_select(q_d, st["pool"], rrs1, d_len_t, pt, w.page_size,
+                                                int(d_len.max()), 1, k_blk=w.k_blk, workspace=ws,
+                                                out_slots=slots), iters, warmup)
+    ms, ms_full = statistics.mean(t_share), statistics.mean(t_full)
+    width = 4 * w.k_blk + 3 + n_extra
+    # kept blocks and row lengths read, one page-table entry per kept block
+    # and per tail page, the slot rows written
+    alg = n_req * (4 * w.k_blk + 8 + 4 * w.k_blk + 4 * width)
+    del st
+    return {"workload": w.name + "_draft_step", "rows": n_req, "us_per_call": 1e3 * ms,
+            "rows_per_s": n_req / (ms * 1e-3), "alg_bytes": alg, "alg_GBps": alg / (ms * 1e-3) / 1e9,
+            "indexer_us_same_rows": 1e3 * ms_full, "indexer_over_indexshare": ms_full / ms,
+            "kernel": "indexshare_kernel"}
+
+
 def bench_variant_prefill(g, w, iters, warmup, peaks):
     st = setup_decode(g, w, 0)
     t = g.timed(lambda: g.qsa.indexer_select(st["q"], st["pool"], st["rrs"], st["row_len"], st["pt"],
@@ -609,6 +652,7 @@ def main():
             "c4_dsa_topk_relu4": bench_variant_topk(g, c4_dsa_topk(0, "relu4"), it, args.warmup, peaks),
             "c4_dsa_topk_fp16dup": bench_variant_topk(g, c4_dsa_topk(0, "fp16dup"), it, args.warmup, peaks),
             "c5_prefill_4096rows": bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
+            "indexshare_32req_draft": bench_variant_indexshare(g, indexshare_mtp(0), it, args.warmup, peaks),
         }
     if rank == 0:
         if args.cpu_budget > 0:

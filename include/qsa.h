@@ -91,7 +91,8 @@ int qsa_version(void);
  * device-side bounds checks of earlier calls, optionally clears it, and
  * returns QSA_OK or QSA_ERR_DEVICE_FAULT.  *h_bits (may be NULL) receives the
  * word: bit 0 row/page index out of range, bit 1 pool row out of range,
- * bit 2 a bounded wait expired, bit 3 inconsistent row grouping. */
+ * bit 2 a bounded wait expired, bit 3 inconsistent row grouping, bit 4 an
+ * output row too narrow for its entries (qsa_indexshare_slots). */
 qsa_status qsa_device_status(void* stream, int clear, uint32_t* h_bits);
 
 /* ---------------------------------------------------------------------
@@ -176,6 +177,39 @@ qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_
                             const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
                             const int32_t* page_table, int64_t ld_pt, int32_t page_size,
                             int32_t* out_pos, int32_t* out_slots, void* stream);
+
+/* ---------------------------------------------------------------------
+ * IndexShare reuse of a kept selection  ([QSA], section "IndexShare MTP:
+ * reusing the QSA selection across draft steps": the QSA selection computed
+ * at the draft-extend pass over the tokens the target just accepted is kept
+ * for the whole MTP iteration; each draft decode step skips the indexer and
+ * reads that frozen selection plus the positions drafted since, so the draft
+ * still sees its own in-flight tokens).
+ *
+ *   cap_blocks [n_cap][k_blk]: kept block ids, e.g. out_blocks of the
+ *              draft-extend call (ascending, -1 padded; any order is read
+ *              as given, -1 entries skipped).
+ *   cap_len    [n_cap]: tokens the kept row saw (its row_len).
+ *   cap_row    [n_req]: which kept row serves request r (its last accepted
+ *              row).  Rows of request r are the draft rows of this step.
+ *   n_extra    drafted columns to reserve, 0 <= n_extra <= 65536 (the MTP
+ *              depth N + 1 covers a whole iteration).
+ *   out_pos    [n_rows][4*k_blk+3+n_extra] or NULL: token positions.
+ *   out_slots  [n_rows][4*k_blk+3+n_extra]: physical KV slots.
+ *
+ * Row t of request r, seeing L = row_len[t] tokens, with c = cap_row[r] and
+ * nb0 = cap_len[c]/4: the positions 4b..4b+3 (those below L) of each kept
+ * block b, in the order given, then every position 4*nb0 .. L-1 (the kept
+ * row's pending tokens and every token drafted since), then -1.  Device
+ * faults: a kept block b >= nb0 is skipped (bit 0); c outside [0, n_cap)
+ * gives a row of -1 (bit 0); a list longer than the row is cut at the width
+ * (bit 4).  No scores are read and nothing is selected.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_indexshare_slots(const int32_t* cap_blocks, const int32_t* cap_len, int32_t n_cap,
+                                const int32_t* cap_row, int32_t k_blk, int32_t n_extra, int32_t n_req,
+                                const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                                const int32_t* page_table, int64_t ld_pt, int32_t page_size,
+                                int32_t* out_pos, int32_t* out_slots, void* stream);
 
 /* ---------------------------------------------------------------------
  * Top-k_blk blocks of given block scores, expanded and translated, one

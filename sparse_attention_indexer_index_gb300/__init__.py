@@ -19,6 +19,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
+    "select_blocks", "indexshare_slots", "indexshare_width",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -54,6 +55,8 @@ def lib():
             "qsa_expand_slots": (ctypes.c_int, [p, i32, i32, p, i32, p, p, i64, i32, p, p, p]),
             "qsa_select_blocks": (ctypes.c_int, [p, i64, i32, p, i32, p, i32, p, i64, i32, i32, p, p, p,
                                                  p]),
+            "qsa_indexshare_slots": (ctypes.c_int, [p, p, i32, p, i32, i32, i32, p, i32, p, p, i64, i32,
+                                                    p, p, p]),
             "qsa_indexer_select_workspace_size": (sz, [i32, i32, i32]),
             "qsa_indexer_select": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                   i32, p, p, p, p, i64, p, sz, p]),
@@ -206,6 +209,40 @@ def expand_slots(sel_blocks, req_row_start, row_len, page_table, page_size, want
         _ptr(page_table), page_table.shape[1], int(page_size), _ptr(pos), _ptr(slots),
         _stream(stream)))
     return pos, slots
+
+
+def indexshare_width(k_blk: int, n_extra: int) -> int:
+    """Entries per reused row: the expanded width plus the drafted columns."""
+    return out_width(k_blk) + int(n_extra)
+
+
+def indexshare_slots(cap_blocks, cap_len, cap_row, n_extra, req_row_start, row_len, page_table,
+                     page_size, want_pos=True, out_slots=None, stream=None):
+    """Draft rows read a kept selection (IndexShare): cap_blocks [n_cap][k]
+    with cap_len [n_cap]; request r reads kept row cap_row[r].
+    Returns (positions or None, slots) [n_rows][4k+3+n_extra]."""
+    torch = _torch()
+    _dev(cap_blocks, torch.int32, "cap_blocks", 2)
+    _dev(cap_len, torch.int32, "cap_len", 1)
+    _dev(cap_row, torch.int32, "cap_row", 1)
+    _dev(req_row_start, torch.int32, "req_row_start", 1)
+    _dev(row_len, torch.int32, "row_len", 1)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_cap, k = cap_blocks.shape
+    if cap_len.numel() != n_cap or cap_row.numel() != req_row_start.numel() - 1:
+        raise ValueError("cap_len must have n_cap entries and cap_row one per request")
+    n_rows = row_len.numel()
+    w = indexshare_width(k, n_extra)
+    dev = cap_blocks.device
+    if out_slots is None:
+        out_slots = torch.empty((n_rows, w), dtype=torch.int32, device=dev)
+    _dev(out_slots, torch.int32, "out_slots", 2)
+    pos = torch.empty((n_rows, w), dtype=torch.int32, device=dev) if want_pos else None
+    _check("qsa_indexshare_slots", lib().qsa_indexshare_slots(
+        _ptr(cap_blocks), _ptr(cap_len), n_cap, _ptr(cap_row), k, int(n_extra),
+        req_row_start.numel() - 1, _ptr(req_row_start), n_rows, _ptr(row_len), _ptr(page_table),
+        page_table.shape[1], int(page_size), _ptr(pos), _ptr(out_slots), _stream(stream)))
+    return pos, out_slots
 
 
 def select_blocks(scores, req_row_start, row_len, page_table, page_size, max_len, k_blk=512,

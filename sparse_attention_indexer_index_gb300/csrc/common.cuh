@@ -15,6 +15,7 @@ constexpr int kDim = 128;          // index head dim
 constexpr int kHeads = 4;          // index query heads
 constexpr int kBlock = 4;          // raw keys per compressed block (c4)
 constexpr int kMaxK = 2048;        // largest k a selection supports
+constexpr int kMaxShareExtra = 1 << 16;  // drafted columns a reused row may reserve
 // 1/sqrt(128) rounded to FP32.
 constexpr float kScoreScale = 0.08838834764831845f;
 
@@ -23,6 +24,7 @@ constexpr unsigned kFaultIndex = 1u;      // row / page index out of range
 constexpr unsigned kFaultPool = 2u;       // pool row out of range
 constexpr unsigned kFaultWait = 4u;       // a bounded wait expired
 constexpr unsigned kFaultGrouping = 8u;   // inconsistent row grouping / lengths
+constexpr unsigned kFaultCapacity = 16u;  // an output row too narrow for its entries
 
 // Device fault word of this translation unit (internal linkage: every
 // translation unit that launches kernels has its own and exposes a host

@@ -710,6 +710,25 @@ qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_
   return launch_status();
 }
 
+qsa_status qsa_indexshare_slots(const int32_t* cap_blocks, const int32_t* cap_len, int32_t n_cap,
+                               const int32_t* cap_row, int32_t k_blk, int32_t n_extra, int32_t n_req,
+                               const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                               const int32_t* page_table, int64_t ld_pt, int32_t page_size,
+                               int32_t* out_pos, int32_t* out_slots, void* stream) {
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (n_extra < 0 || n_cap < 0) return QSA_ERR_INVALID_ARG;
+  if (n_extra > kMaxShareExtra) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, 0)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (!cap_row || !out_slots || !page_table || ld_pt < 1 || page_size <= 0) return QSA_ERR_INVALID_ARG;
+  if (n_cap > 0 && (!cap_blocks || !cap_len)) return QSA_ERR_INVALID_ARG;
+  if (page_size % kBlock != 0) return QSA_ERR_UNSUPPORTED;
+  ShareArgs a{cap_blocks, cap_len, n_cap, cap_row, k_blk, n_extra, n_req, req_row_start, n_rows,
+              row_len, page_table, ld_pt, page_size, out_pos, out_slots};
+  indexshare_kernel<<<(unsigned)n_rows, kExpThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
 qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_req,
                              const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
                              int32_t max_len, const int32_t* page_table, int64_t ld_pt,

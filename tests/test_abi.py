@@ -111,3 +111,20 @@ def test_select_blocks_rejects_bad_arguments(L):
     assert L.qsa_select_blocks(FAKE, 4, 1, rrs, 1, FAKE, 32, FAKE, 1, 64, 4, None, None, FAKE, None) == -1
     # page size not a multiple of 4
     assert L.qsa_select_blocks(FAKE, 8, 1, rrs, 1, FAKE, 32, FAKE, 1, 6, 4, None, None, FAKE, None) == -2
+
+
+def test_indexshare_rejects_bad_arguments(L):
+    f = L.qsa_indexshare_slots
+    # k_blk out of range; too many drafted columns
+    assert f(FAKE, FAKE, 1, FAKE, 0, 3, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, FAKE, None) == -2
+    assert f(FAKE, FAKE, 1, FAKE, 512, (1 << 16) + 1, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, FAKE, None) == -2
+    # negative drafted columns; no output slots; no request -> kept-row map
+    assert f(FAKE, FAKE, 1, FAKE, 512, -1, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, FAKE, None) == -1
+    assert f(FAKE, FAKE, 1, FAKE, 512, 3, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, None, None) == -1
+    assert f(FAKE, FAKE, 1, None, 512, 3, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, FAKE, None) == -1
+    # kept rows announced but not given
+    assert f(None, FAKE, 1, FAKE, 512, 3, 1, FAKE, 1, FAKE, FAKE, 4, 64, None, FAKE, None) == -1
+    # page size not a multiple of 4
+    assert f(FAKE, FAKE, 1, FAKE, 512, 3, 1, FAKE, 1, FAKE, FAKE, 4, 62, None, FAKE, None) == -2
+    # no rows: nothing to do
+    assert f(None, None, 0, None, 512, 3, 0, None, 0, None, None, 0, 64, None, None, None) == 0

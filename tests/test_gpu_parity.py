@@ -11,7 +11,7 @@ import pytest
 import oracle
 from gpu_util import bf16_dev, bf16_host, score_tolerance, to_dev
 from workloads import (c1_decode, c2_verify, c2_batched, c3_batched, c4_dsa_topk, c5_prefill,
-                       decode_workload, topk_workload, TOPK_DISTS)
+                       decode_workload, indexshare_mtp, topk_workload, TOPK_DISTS)
 
 pytestmark = pytest.mark.gpu
 
@@ -373,3 +373,98 @@ def test_select_blocks_parity(qsa, case):
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
     assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
     assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+# ----------------------------------------------------------------- IndexShare
+def _dev_fault_bits(flags):
+    """Oracle flags -> device fault bits (1: cut at the width -> bit 4;
+    2: kept block incomplete at the capture, 4: kept row out of range -> bit 0)."""
+    return (16 if flags & 1 else 0) | (1 if flags & 6 else 0)
+
+
+@pytest.mark.parametrize("P", [4, 16, 64])
+def test_indexshare_parity_kept_selections(qsa, P):
+    """Draft rows reading kept selections: rows before, at and after the
+    capture, every cap_len mod 4, kept rows with fewer blocks than k, kept
+    rows shared by several requests, several rows per request."""
+    rng = np.random.default_rng(100 + P)
+    k, n_extra = 512, 5
+    cap_len = np.array([0, 3, 4, 9, 2050, 2051, 2052, 2053, 7001, 20_000], np.int32)
+    cap = np.full((cap_len.size, k), -1, np.int32)
+    for c, L0 in enumerate(cap_len):
+        nb0 = int(L0) // 4
+        if nb0:
+            cap[c] = oracle.topk_row(rng.standard_normal(nb0).astype(np.float32), k)
+    cap_row = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 9, 4], np.int32)
+    rows = []
+    for r, c in enumerate(cap_row):
+        L0 = int(cap_len[c])
+        rows.append([max(0, L0 - 3), L0, L0 + 1, L0 + 3, L0 + n_extra] if r % 2 == 0 else [L0 + 2])
+    row_len = np.array([x for rr in rows for x in rr], np.int32)
+    rrs = np.concatenate([[0], np.cumsum([len(rr) for rr in rows])]).astype(np.int32)
+    ctx = max(int(row_len.max()), 1)
+    pt = np.stack([rng.permutation(ctx // P + 8) for _ in rows]).astype(np.int32)
+    pos, slots = qsa.indexshare_slots(to_dev(cap), to_dev(cap_len), to_dev(cap_row), n_extra, to_dev(rrs),
+                                      to_dev(row_len), to_dev(pt), P)
+    rpos, rslots, flags = oracle.indexshare(cap, cap_len, cap_row, n_extra, rrs, row_len, pt, P)
+    assert flags == 0
+    assert np.array_equal(pos.cpu().numpy(), rpos)
+    assert np.array_equal(slots.cpu().numpy(), rslots)
+
+
+def test_indexshare_parity_faults(qsa):
+    """Rows whose list does not fit, kept blocks incomplete at the capture
+    and a kept row out of range: the same output as the oracle, and the
+    device fault bits set."""
+    P, k, n_extra = 16, 8, 2
+    cap = np.array([[0, 3, 5, 9, -1, -1, -1, -1], [1, 2, 40, -1, -1, -1, -1, -1]], np.int32)
+    cap_len = np.array([41, 30], np.int32)
+    pt = np.arange(16, dtype=np.int32)[None, :].repeat(3, 0)[:, ::-1].copy()
+    for cap_row, row_len, want_flags in [
+        ([0, 0, 0], [45, 60, 100], 1),       # tails of 5, 20 and 60 positions, room for 21
+        ([1, 1, 1], [30, 31, 33], 2),        # block 40 was not complete at L = 30
+        ([0, 2, 0], [41, 41, 41], 4),        # request 1 points past the kept rows
+    ]:
+        rrs = np.arange(4, dtype=np.int32)
+        cr, rl = np.array(cap_row, np.int32), np.array(row_len, np.int32)
+        pos, slots = qsa.indexshare_slots(to_dev(cap), to_dev(cap_len), to_dev(cr), n_extra, to_dev(rrs),
+                                          to_dev(rl), to_dev(pt), P)
+        rpos, rslots, flags = oracle.indexshare(cap, cap_len, cr, n_extra, rrs, rl, pt, P)
+        assert flags == want_flags
+        assert qsa.device_status(clear=True) == _dev_fault_bits(flags)
+        assert np.array_equal(pos.cpu().numpy(), rpos)
+        assert np.array_equal(slots.cpu().numpy(), rslots)
+
+
+def test_indexshare_after_fused_draft_extend(qsa):
+    """One MTP iteration: the fused indexer runs on each request's
+    draft-extend row, its selection is kept, and the draft rows read it
+    (positions up to 3 tokens past the capture, pending counts 0-3, rows with
+    fewer visible blocks than k)."""
+    import torch
+    w = indexshare_mtp(3, n_req=6, lo=1000, hi=30_000, n_draft=3, page_size=64)
+    n_draft = 3
+    ext_rows = w.req_row_start[:-1]
+    ext_len = w.row_len[ext_rows].copy()
+    pool = gpu_pool(qsa, w)
+    ext_rrs = np.arange(w.n_req + 1, dtype=np.int32)
+    ld = (int(ext_len.max()) // 4 + 3) // 4 * 4
+    scores = torch.empty((w.n_req, ld), device="cuda")
+    ext = qsa.indexer_select(bf16_dev(w.q[ext_rows]), pool, to_dev(ext_rrs), to_dev(ext_len),
+                             to_dev(w.page_table), w.page_size, int(ext_len.max()), 1, k_blk=512,
+                             want_blocks=True, scores_out=scores)
+    kept = ext["blocks"]
+    sel_ref, _ = oracle.topk(scores.cpu().numpy(), 512, n_valid=ext_len // 4)
+    assert np.array_equal(kept.cpu().numpy(), sel_ref)
+    # the draft rows of this iteration: request r's rows after its first
+    draft = np.concatenate([np.arange(w.req_row_start[r] + 1, w.req_row_start[r + 1]) for r in range(w.n_req)])
+    d_len = w.row_len[draft]
+    d_rrs = np.arange(0, w.n_req * n_draft + 1, n_draft, dtype=np.int32)
+    cap_row = np.arange(w.n_req, dtype=np.int32)
+    pos, slots = qsa.indexshare_slots(kept, to_dev(ext_len), to_dev(cap_row), n_draft + 1, to_dev(d_rrs),
+                                      to_dev(d_len), to_dev(w.page_table), w.page_size)
+    rpos, rslots, flags = oracle.indexshare(sel_ref, ext_len, cap_row, n_draft + 1, d_rrs, d_len,
+                                            w.page_table, w.page_size)
+    assert flags == 0
+    assert np.array_equal(pos.cpu().numpy(), rpos)
+    assert np.array_equal(slots.cpu().numpy(), rslots)

@@ -20,7 +20,7 @@ D, H, C = 128, 4, 4
 __all__ = [
     "D", "H", "C", "bf16_bits", "normal_bf16", "DecodeWorkload", "decode_workload",
     "TopkWorkload", "topk_workload", "c1_decode", "c2_verify", "c2_batched", "c3_batched",
-    "c4_dsa_topk", "c5_prefill", "TOPK_DISTS",
+    "c4_dsa_topk", "c5_prefill", "indexshare_mtp", "TOPK_DISTS",
 ]
 
 
@@ -148,6 +148,18 @@ def c3_batched(seed: int = 0, n_req: int = 32, lo: int = 4096, hi: int = 131_072
     rng = np.random.default_rng(seed + 1_000_003)
     lens = rng.integers(lo, hi, size=n_req, endpoint=True)
     return decode_workload(seed, [[int(L)] for L in lens], name=f"decode_batched_{n_req}req")
+
+
+def indexshare_mtp(seed: int = 0, n_req: int = 32, lo: int = 4096, hi: int = 131_072, n_draft: int = 3,
+                   page_size: int = 64) -> DecodeWorkload:
+    """One MTP iteration per request: the draft-extend row at L0 (the last
+    token the target accepted; L0 uniform in [lo, hi]) followed by the
+    n_draft draft rows L0+1 .. L0+n_draft.  Rows of request r: its draft-extend
+    row first.  The page table covers the drafted positions."""
+    rng = np.random.default_rng(seed + 9000)
+    L0 = rng.integers(lo, hi + 1, size=n_req)
+    return decode_workload(seed, [[int(l) + j for j in range(n_draft + 1)] for l in L0],
+                           page_size=page_size, name=f"indexshare_{n_req}req_{n_draft}draft")
 
 
 def c5_prefill(seed: int = 0, L: int = 131_072, n_rows: int = 4096) -> DecodeWorkload:
