@@ -286,7 +286,9 @@ def kernel_names(w, sm_count=152):
     TMA when a page holds a multiple of 8 compressed keys; one-row requests
     use the balanced tensor-core scorer on such pages; rows of up to
     32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
-    shared-memory-resident single-CTA selection otherwise)."""
+    shared-memory-resident single-CTA selection otherwise; longer rows a
+    cluster of 2-16 CTAs per row when rows * 2 <= SMs, one streaming CTA per
+    row otherwise)."""
     tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0
     balanced = tma and w.max_rows_per_req == 1
     if balanced:
@@ -296,7 +298,7 @@ def kernel_names(w, sm_count=152):
     else:
         score = "score_decode_kernel"
     if w.max_len // 4 > 32768:
-        select = "select_kernel"
+        select = "select_long_kernel" if w.n_rows * 2 <= sm_count else "select_kernel"
     elif w.n_rows * 8 <= sm_count:
         select = "select_cluster_kernel"
     else:
@@ -384,6 +386,13 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     return res
 
 
+def topk_kernel_name(n_rows, n, sm_count=152):
+    """The selection kernel topk_select runs for n_rows rows of n scores."""
+    if n > 32768:
+        return "select_long_kernel" if n_rows * 2 <= sm_count else "select_kernel"
+    return "select_cluster_kernel" if n_rows * 8 <= sm_count else "select_resident_kernel"
+
+
 def bench_variant_topk(g, w, iters, warmup, peaks):
     torch, qsa = g.torch, g.qsa
     s = g.h2d(w.scores)
@@ -399,7 +408,8 @@ def bench_variant_topk(g, w, iters, warmup, peaks):
     return {"workload": w.name, "rows": int(s.shape[0]), "us_per_call": 1e3 * ms,
             "rows_per_s": s.shape[0] / (ms * 1e-3), "alg_bytes": alg,
             "alg_GBps": alg / (ms * 1e-3) / 1e9, "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "dup_fraction": w.dup_fraction}
+            "dup_fraction": w.dup_fraction,
+            "kernel": topk_kernel_name(int(s.shape[0]), int(w.n_valid.max()))}
 
 
 def bench_variant_indexshare(g, w, iters, warmup, peaks):
@@ -651,6 +661,11 @@ def main():
             "c4_dsa_topk_normal": bench_variant_topk(g, c4_dsa_topk(0, "normal"), it, args.warmup, peaks),
             "c4_dsa_topk_relu4": bench_variant_topk(g, c4_dsa_topk(0, "relu4"), it, args.warmup, peaks),
             "c4_dsa_topk_fp16dup": bench_variant_topk(g, c4_dsa_topk(0, "fp16dup"), it, args.warmup, peaks),
+            # the verify shape of the TopK-V2 latency figure (6 rows) at 80K and 1M tokens
+            "dsa_topk_verify_6x80000": bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6), it, args.warmup,
+                                                          peaks),
+            "dsa_topk_verify_6x1M": bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6, n=1_000_000), it,
+                                                       args.warmup, peaks),
             "c5_prefill_4096rows": bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
             "indexshare_32req_draft": bench_variant_indexshare(g, indexshare_mtp(0), it, args.warmup, peaks),
         }

@@ -17,6 +17,7 @@
 #include "select.cuh"
 #include "select_resident.cuh"
 #include "select_cluster.cuh"
+#include "select_long.cuh"
 
 using namespace qsa;
 
@@ -44,9 +45,15 @@ constexpr int kRsListMax = 8192;
 constexpr int kScListCap = 8192;
 constexpr int kScSmem = kScFixedBytes + 2 * kScListCap * 4 + kSelPtStage * 4 + kMaxK * 4;
 
+// Long rows (more than kRsMaxRow entries) with few rows: one cluster of
+// 2..16 CTAs per row (select_long_kernel), each CTA keeping as much of its
+// slice in shared memory as kSlSmem leaves.
+constexpr int kSlSmem = 227 * 1024;
+
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
+  int sl_clusters[5] = {0, 0, 0, 0, 0};  // co-resident clusters of 1, 2, 4, 8, 16 long-row CTAs
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -93,6 +100,34 @@ qsa_status device_info(DeviceInfo** out) {
         cudaFuncSetAttribute(score_tc_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return QSA_ERR_CUDA;
+    for (int m = 0; m < 2; ++m) {
+      void (*kern)(SelectArgs) = m == 0 ? select_long_kernel<kModeTopk> : select_long_kernel<kModeQsa>;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlSmem) != cudaSuccess)
+        return QSA_ERR_CUDA;
+      // clusters of 16 are beyond the portable size; without the opt-in the
+      // 16-CTA plan is simply never taken
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaGetLastError();
+    }
+    for (int e = 1; e <= 4; ++e) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1u << e, 1, 1);
+      cfg.blockDim = dim3(kSlThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSlSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1u << e;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, select_long_kernel<kModeTopk>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        nc = 0;
+      }
+      d.sl_clusters[e] = nc;
+    }
     d.ready = true;
   }
   *out = &d;
@@ -241,9 +276,55 @@ qsa_status launch_select_cluster(const SelectArgs& args, bool pdl, int sm_count,
   return QSA_OK;
 }
 
+// Long rows: a cluster of C CTAs per row, C the largest of 16, 8, 4, 2 with
+// rows * C <= SMs (and such clusters schedulable).  QSA_ERR_UNSUPPORTED: one
+// CTA per row (select_kernel) instead.
+template <int kMode>
+qsa_status launch_select_long(const SelectArgs& args, bool pdl, cudaStream_t stream) {
+  if (args.n_max <= kRsMaxRow) return QSA_ERR_UNSUPPORTED;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  int e = 4;
+  while (e >= 1 && ((int64_t)args.n_rows << e > d->sm_count || d->sl_clusters[e] < 1)) --e;
+  if (e < 1) return QSA_ERR_UNSUPPORTED;
+  const int C = 1 << e;
+  SelectArgs a = args;
+  const int64_t S = (((int64_t)a.n_max + C - 1) / C + 3) & ~int64_t(3);
+  const int64_t cap = ((kSlSmem - kSlFixedBytes) / 4) & ~3;
+  a.list_cap = (int32_t)std::min(S, cap);  // slice entries kept in shared memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.n_rows * C), 1, 1);
+  cfg.blockDim = dim3(kSlThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)kSlFixedBytes + (size_t)a.list_cap * 4;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)C;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, select_long_kernel<kMode>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
 template <int kMode>
 qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count = 0) {
   if (a.n_rows == 0) return QSA_OK;
+  {
+    const qsa_status st = launch_select_long<kMode>(a, pdl, stream);
+    if (st != QSA_ERR_UNSUPPORTED) return st;
+  }
   if (sm_count > 0) {
     const qsa_status st = launch_select_cluster<kMode>(a, pdl, sm_count, stream);
     if (st != QSA_ERR_UNSUPPORTED) return st;

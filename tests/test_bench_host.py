@@ -82,3 +82,12 @@ def test_kernel_bytes_c2():
     assert kb["compress"] == 2 * (4 * 256 + 256 + 12)
     assert kb["select"] == 4 * sum(nb) + 4 * (80000 // 64) + 6 * 4 * (4 * 512 + 3)
     assert kb["score"] == 256 * max(nb) + 1024 * 6 + 4 * (80000 // 64) + 4 * sum(nb)
+
+
+def test_long_rows_take_the_cluster_selection():
+    import bench
+    assert bench.topk_kernel_name(6, 80_000) == "select_long_kernel"
+    assert bench.topk_kernel_name(64, 80_000) == "select_long_kernel"
+    assert bench.topk_kernel_name(100, 80_000) == "select_kernel"
+    assert bench.topk_kernel_name(6, 20_000) == "select_cluster_kernel"
+    assert bench.topk_kernel_name(64, 20_000) == "select_resident_kernel"

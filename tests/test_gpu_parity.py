@@ -203,6 +203,45 @@ def test_topk_parity_dsa_full_size(qsa, dist):
     run_topk(qsa, c4_dsa_topk(0, dist))
 
 
+@pytest.mark.parametrize("dist", TOPK_DISTS)
+def test_topk_long_rows_1m_verify_shape(qsa, dist):
+    """6 rows of 1,000,000 FP32 scores (long-context verify step), k = 2048,
+    with slots: one cluster of 16 CTAs per row, slices larger than shared
+    memory (the rest re-read from L2)."""
+    run_topk(qsa, topk_workload(61, 6, 1_000_000, k=2048, dist=dist))
+
+
+@pytest.mark.parametrize("k", [1, 777, 2048])
+def test_topk_long_rows_ragged(qsa, k):
+    """12 long rows of ragged valid lengths (some no longer than k, one
+    empty) in one launch: clusters of 8 CTAs, empty slices in the last CTAs
+    of short rows."""
+    w = topk_workload(62, 12, 300_000, k=k, dist="normal")
+    w.n_valid[:] = [300_000, 299_999, 33_001, 150_003, 2048, 777, 0, 5, 64_000, 131_071, 40_000, 250_001]
+    run_topk(qsa, w, k)
+
+
+def test_topk_long_rows_heavy_ties(qsa):
+    """Long rows where the k-th key is shared by most of the row: all equal,
+    three values, one top-bits bin, +-0 and NaN mixed in; the radix levels
+    run to the full key and the equal entries are taken by index."""
+    rng = np.random.default_rng(63)
+    n = 200_000
+    s = np.zeros((5, n), np.float32)
+    s[0] = 1.5
+    s[1] = rng.integers(0, 3, size=n).astype(np.float32)
+    s[2] = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)
+    s[3] = np.where(rng.random(n) < 0.5, np.float32(0.0), np.float32(-0.0))
+    s[3, ::7] = np.nan
+    s[4] = rng.standard_normal(n).astype(np.float32)
+    s[4, -3000:] = np.inf
+    nv = np.full(5, n, np.int32)
+    for k in [512, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
 def test_topk_special_rows(qsa):
     import torch
     n = 5000
@@ -468,3 +507,26 @@ def test_indexshare_after_fused_draft_extend(qsa):
     assert flags == 0
     assert np.array_equal(pos.cpu().numpy(), rpos)
     assert np.array_equal(slots.cpu().numpy(), rslots)
+
+
+def test_select_blocks_long_context(qsa):
+    """Block selection for rows past 131,072 tokens (more than 32,768
+    blocks, up to a 1M-token context): the long-row cluster kernel in QSA
+    mode, with every pending-token count and slot translation."""
+    P = 64
+    row_len = np.array([1_000_003, 524_289, 131_074, 400_000], np.int32)
+    rrs = np.array([0, 1, 2, 4], np.int32)  # the last request has two rows
+    rng = np.random.default_rng(12)
+    ld_pt = (int(row_len.max()) + P - 1) // P
+    page_table = rng.permutation(3 * ld_pt).astype(np.int32).reshape(3, ld_pt)
+    max_len = int(row_len.max())
+    ld = (max_len // 4 + 3) // 4 * 4
+    s = (rng.standard_normal((row_len.size, ld)) * 0.1).astype(np.float32)
+    s[1, ::5] = 0.25  # many exact ties in one row
+    out = qsa.select_blocks(to_dev(s), to_dev(rrs), to_dev(row_len), to_dev(page_table), P, max_len, k_blk=512,
+                            want_blocks=True, want_pos=True)
+    sel_ref, _ = oracle.topk(s, 512, n_valid=row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, rrs, row_len, page_table, P)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
