@@ -533,6 +533,25 @@ WORKLOADS = {
 }
 
 
+def variant_table(g, it, warmup, peaks):
+    """The secondary workloads of the JSON line: name -> a call measuring it."""
+    return {
+        "c1_decode_L8192": lambda: bench_variant_decode(g, c1_decode(0), 1, it, warmup, peaks),
+        "c2_b32_verify_x32": lambda: bench_variant_decode(g, c2_batched(0), 2, it, warmup, peaks),
+        "c3_batched_32req": lambda: bench_variant_decode(g, c3_batched(0), 1, it, warmup, peaks),
+        "c4_dsa_topk_normal": lambda: bench_variant_topk(g, c4_dsa_topk(0, "normal"), it, warmup, peaks),
+        "c4_dsa_topk_relu4": lambda: bench_variant_topk(g, c4_dsa_topk(0, "relu4"), it, warmup, peaks),
+        "c4_dsa_topk_fp16dup": lambda: bench_variant_topk(g, c4_dsa_topk(0, "fp16dup"), it, warmup, peaks),
+        # the verify shape of the TopK-V2 latency figure (6 rows) at 80K and 1M tokens
+        "dsa_topk_verify_6x80000": lambda: bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6), it, warmup,
+                                                              peaks),
+        "dsa_topk_verify_6x1M": lambda: bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6, n=1_000_000), it,
+                                                           warmup, peaks),
+        "c5_prefill_4096rows": lambda: bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
+        "indexshare_32req_draft": lambda: bench_variant_indexshare(g, indexshare_mtp(0), it, warmup, peaks),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,6 +561,8 @@ def main():
     ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS),
                     help="decode workload of the primary line (default: the 6-row verify step)")
     ap.add_argument("--no-variants", action="store_true", help="primary workload only")
+    ap.add_argument("--variant", default=None,
+                    help="measure this one secondary workload only and print its line")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time (0: skip)")
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of untimed steps run under the clock sampler before timing")
@@ -552,6 +573,13 @@ def main():
         return run_reference(args)
 
     import torch
+    if args.variant is not None:
+        g = Gpu(torch.device("cuda", 0))
+        fns = variant_table(g, max(10, min(args.steps, 30)), args.warmup, load_peaks())
+        if args.variant not in fns:
+            raise SystemExit(f"unknown variant {args.variant}; one of {sorted(fns)}")
+        print(json.dumps({"variant": args.variant, **fns[args.variant]()}))
+        return 0
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
@@ -654,21 +682,7 @@ def main():
     del st
     if rank == 0 and not args.no_variants:
         it = max(10, min(args.steps, 30))
-        out["variants"] = {
-            "c1_decode_L8192": bench_variant_decode(g, c1_decode(0), 1, it, args.warmup, peaks),
-            "c2_b32_verify_x32": bench_variant_decode(g, c2_batched(0), 2, it, args.warmup, peaks),
-            "c3_batched_32req": bench_variant_decode(g, c3_batched(0), 1, it, args.warmup, peaks),
-            "c4_dsa_topk_normal": bench_variant_topk(g, c4_dsa_topk(0, "normal"), it, args.warmup, peaks),
-            "c4_dsa_topk_relu4": bench_variant_topk(g, c4_dsa_topk(0, "relu4"), it, args.warmup, peaks),
-            "c4_dsa_topk_fp16dup": bench_variant_topk(g, c4_dsa_topk(0, "fp16dup"), it, args.warmup, peaks),
-            # the verify shape of the TopK-V2 latency figure (6 rows) at 80K and 1M tokens
-            "dsa_topk_verify_6x80000": bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6), it, args.warmup,
-                                                          peaks),
-            "dsa_topk_verify_6x1M": bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6, n=1_000_000), it,
-                                                       args.warmup, peaks),
-            "c5_prefill_4096rows": bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
-            "indexshare_32req_draft": bench_variant_indexshare(g, indexshare_mtp(0), it, args.warmup, peaks),
-        }
+        out["variants"] = {name: fn() for name, fn in variant_table(g, it, args.warmup, peaks).items()}
     if rank == 0:
         if args.cpu_budget > 0:
             out["cpu_baseline"] = cpu_oracle_rate(w, args.cpu_budget)
