@@ -67,6 +67,8 @@ def _load():
                 "oracle_indexer_select": (None, [p, p, i64, p, p, p, i64, i64, i64, p, i64, p, p, p]),
                 "oracle_indexshare_row": (ctypes.c_int, [p, i64, i64, i64, i64, p, i64, p, p]),
                 "oracle_indexshare": (ctypes.c_int, [p, p, i64, p, i64, i64, i64, p, p, p, i64, i64, p, p]),
+                "oracle_sparse_attn_row": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, p, i64, d, p, p]),
+                "oracle_sparse_attn": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, i64, p, i64, i64, d, p, p]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -272,3 +274,22 @@ def indexshare(cap_sel, cap_len, cap_row, n_extra, req_row_start, row_len, page_
                                   rrs.size - 1, _ptr(rrs), _ptr(rl), _ptr(pt), pt.shape[-1],
                                   int(page_size), _ptr(pos), _ptr(slots))
     return pos, slots, int(f)
+
+
+# ---------------------------------------------------------------- sparse attention
+def sparse_attn(q, k, v, slots, scale):
+    """q [n_rows][H_q][d] u16, k/v [n_slots][H_kv][d] u16, slots [n_rows][n_idx]
+    int32 (-1 masked).  Returns (out [n_rows][H_q][d] f32, lse [n_rows][H_q]
+    f32, flags)."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sl = _c(slots, np.int32)
+    n_rows, h_q, d = q.shape
+    n_slots, h_kv, _ = k.shape
+    n_idx = sl.shape[1]
+    out = np.empty((n_rows, h_q, d), np.float32)
+    lse = np.empty((n_rows, h_q), np.float32)
+    f = _load().oracle_sparse_attn(_ptr(q), _ptr(k), _ptr(v), n_slots, n_rows, h_q, h_kv, d, _ptr(sl),
+                                   n_idx, n_idx, float(scale), _ptr(out), _ptr(lse))
+    return out, lse, int(f)

@@ -19,6 +19,8 @@
  *  [SMLA] "vllm-sparse-mla-blackwell" (shadowgraph.io), section "Design notes
  *         worth knowing" -- the consumer masks on index >= 0, so -1 is the
  *         empty-entry sentinel.
+ *  [QSA] also: the compressed keys only index; softmax and value
+ *         aggregation read the original K/V at the selected positions.
  *  [QSA] also, section "IndexShare MTP: reusing the QSA selection across
  *         draft steps" -- the selection of the draft-extend row is kept for
  *         the whole MTP iteration and read together with the positions
@@ -346,6 +348,74 @@ int oracle_indexshare(const int32_t* cap_sel, const int32_t* cap_len, int64_t n_
                                      out_slots + t * width);
     }
   return flags;
+}
+
+/* ---------- sparse attention over the selected slots ([QSA]; [SMLA]) ----- */
+
+/* [QSA], section "Qwen sparse attention (QSA)": the compressed keys only
+ * index; the final softmax and value aggregation read the original,
+ * uncompressed K/V at the selected positions (sparse GQA).  [SMLA], "Design
+ * notes worth knowing": the only mask is index >= 0, and a token whose whole
+ * selection is masked must not come out as NaN.
+ * One row: query q [H_q][d], query head h reads KV head h / (H_q / H_kv);
+ * slots[0..n_idx) index the caches k, v [n_slots][H_kv][d]; entries < 0 are
+ * skipped.  out[h] = sum_j softmax_j(scale <q_h, k_j>) v_j in FP64, rounded
+ * to FP32 once; lse[h] = log sum_j exp(scale <q_h, k_j>).  With no valid
+ * entry: out = 0, lse = -inf.  Returns 1 if an entry >= n_slots was skipped. */
+int oracle_sparse_attn_row(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t n_slots,
+                           int64_t h_q, int64_t h_kv, int64_t d, const int32_t* slots,
+                           int64_t n_idx, double scale, float* out, float* lse) {
+  int64_t group = h_q / h_kv;
+  int bad = 0;
+  double* logit = (double*)malloc((size_t)(n_idx > 0 ? n_idx : 1) * sizeof(double));
+  double* acc = (double*)malloc((size_t)d * sizeof(double));
+  for (int64_t h = 0; h < h_q; ++h) {
+    int64_t g = h / group;
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < n_idx; ++j) {
+      logit[j] = -INFINITY;
+      int64_t s = slots[j];
+      if (s < 0) continue;
+      if (s >= n_slots) {
+        bad = 1;
+        continue;
+      }
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e)
+        dot += oracle_bf16_to_double(q[h * d + e]) * oracle_bf16_to_double(k[(s * h_kv + g) * d + e]);
+      logit[j] = scale * dot;
+      if (logit[j] > mx) mx = logit[j];
+    }
+    for (int64_t e = 0; e < d; ++e) acc[e] = 0.0;
+    double sum = 0.0;
+    if (mx > -INFINITY) {
+      for (int64_t j = 0; j < n_idx; ++j) {
+        if (logit[j] == -INFINITY) continue;
+        double w = exp(logit[j] - mx);
+        sum += w;
+        int64_t s = slots[j];
+        for (int64_t e = 0; e < d; ++e) acc[e] += w * oracle_bf16_to_double(v[(s * h_kv + g) * d + e]);
+      }
+    }
+    for (int64_t e = 0; e < d; ++e) out[h * d + e] = sum > 0.0 ? (float)(acc[e] / sum) : 0.0f;
+    if (lse) lse[h] = sum > 0.0 ? (float)(mx + log(sum)) : -INFINITY;
+  }
+  free(logit);
+  free(acc);
+  return bad;
+}
+
+/* Every row t: q[t], slots[t][0..n_idx) (leading dimension ld_slots),
+ * out[t] [H_q][d], lse[t] [H_q] (lse may be NULL).  Returns the OR of the
+ * rows' flags. */
+int oracle_sparse_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t n_slots,
+                       int64_t n_rows, int64_t h_q, int64_t h_kv, int64_t d, const int32_t* slots,
+                       int64_t ld_slots, int64_t n_idx, double scale, float* out, float* lse) {
+  int bad = 0;
+  for (int64_t t = 0; t < n_rows; ++t)
+    bad |= oracle_sparse_attn_row(q + t * h_q * d, k, v, n_slots, h_q, h_kv, d, slots + t * ld_slots,
+                                  n_idx, scale, out + t * h_q * d, lse ? lse + t * h_q : NULL);
+  return bad;
 }
 
 /* ---------- the whole decode path: score -> top-k blocks -> slots ------- */

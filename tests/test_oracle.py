@@ -469,3 +469,91 @@ def test_indexshare_flags_and_request_mapping():
     assert slots[2].tolist() == [8, 9, 10, 11, 12, 13, 14] + [-1] * 7
     pos, slots, flags = oracle.indexshare(cap, cap_len, [0, 2], 3, rrs, row_len, pt, P)
     assert flags == 4 and (pos[2] == -1).all() and (slots[2] == -1).all()
+
+
+# ------------------------------------------------------------ sparse attention
+# Qwen3.8-Flash-Next write-up, "Qwen sparse attention (QSA)": softmax and
+# value aggregation over the original K/V at the selected positions;
+# vllm-sparse-mla-blackwell, "Design notes worth knowing": the only mask is
+# index >= 0, and a fully masked token must not give NaN.
+def _attn_case(n_slots=12, h_q=8, h_kv=2, d=128, seed=0):
+    rng = np.random.default_rng(seed)
+    q = normal_bf16(rng, (1, h_q, d))
+    k = normal_bf16(rng, (n_slots, h_kv, d))
+    v = normal_bf16(rng, (n_slots, h_kv, d))
+    return q, k, v
+
+
+def _b2f(x):
+    return oracle.bf16_to_float(x)
+
+
+def test_attn_single_slot_returns_its_value_row_per_kv_head():
+    q, k, v = _attn_case(h_q=8, h_kv=2)
+    out, lse, f = oracle.sparse_attn(q, k, v, np.array([[-1, 5, -1]], np.int32), 0.3)
+    assert f == 0
+    for h in range(8):  # query heads 0-3 read KV head 0, 4-7 KV head 1
+        assert np.array_equal(out[0, h], _b2f(v[5, h // 4]).astype(np.float32))
+
+
+def test_attn_identical_keys_average_the_values():
+    q, k, v = _attn_case(h_q=4, h_kv=1)
+    k[:] = k[0]
+    slots = np.array([[0, 3, 7, -1, 9]], np.int32)
+    out, lse, _ = oracle.sparse_attn(q, k, v, slots, 0.125)
+    mean = _b2f(v[[0, 3, 7, 9], 0]).mean(axis=0)
+    for h in range(4):
+        np.testing.assert_allclose(out[0, h], mean, rtol=1e-6, atol=1e-7)
+        dot = float(_b2f(q[0, h]) @ _b2f(k[0, 0]))
+        assert abs(lse[0, h] - (0.125 * dot + math.log(4))) < 1e-5 * (1 + abs(dot))
+
+
+def test_attn_two_slots_closed_form_and_large_logits():
+    """q = a e0, k1 = e0, k2 = e0 * (a - 1) / a: logits differ by scale, so
+    the weights are sigmoid(scale) and 1 - sigmoid(scale) -- also with logits
+    near 1600, far past FP64 exp overflow without the max subtraction."""
+    d = 128
+    for a, scale in [(2.0, 0.5), (40.0, 1.0)]:
+        q = np.zeros((1, 1, d), np.uint16)
+        k = np.zeros((2, 1, d), np.uint16)
+        q[0, 0, 0] = oracle.bf16_round(a)
+        k[0, 0, 0] = oracle.bf16_round(a)
+        k[1, 0, 0] = oracle.bf16_round(a - 1.0)
+        rng = np.random.default_rng(3)
+        v = normal_bf16(rng, (2, 1, d))
+        out, lse, _ = oracle.sparse_attn(q, k, v, np.array([[0, 1]], np.int32), scale)
+        w1 = 1.0 / (1.0 + math.exp(-scale * a))  # logit gap = scale * a * (a - (a - 1))
+        want = w1 * _b2f(v[0, 0]) + (1 - w1) * _b2f(v[1, 0])
+        np.testing.assert_allclose(out[0, 0], want, rtol=1e-6, atol=1e-7)
+        top = scale * a * a
+        assert abs(lse[0, 0] - (top + math.log(1 + math.exp(-scale * a)))) < 1e-6 * max(1.0, top)
+
+
+def test_attn_zero_query_and_fully_masked_row():
+    q, k, v = _attn_case(h_q=2, h_kv=1)
+    q[:] = 0
+    slots = np.array([[2, 4, 6], [-1, -1, -1]], np.int32)
+    out, lse, _ = oracle.sparse_attn(np.concatenate([q, q]), k, v, slots, 1.0)
+    np.testing.assert_allclose(out[0, 0], _b2f(v[[2, 4, 6], 0]).mean(axis=0), rtol=1e-6, atol=1e-7)
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+    assert not np.isnan(out).any()
+
+
+def test_attn_permutation_and_duplicates():
+    q, k, v = _attn_case(h_q=8, h_kv=2, seed=4)
+    a = np.array([[1, -1, 3, 8, -1, 10]], np.int32)
+    b = np.array([[10, 8, -1, -1, 1, 3]], np.int32)
+    oa, la, _ = oracle.sparse_attn(q, k, v, a, 0.1)
+    ob, lb, _ = oracle.sparse_attn(q, k, v, b, 0.1)
+    np.testing.assert_allclose(oa, ob, rtol=1e-6, atol=1e-7)
+    # the same slot twice is the same softmax average as once
+    o1, _, _ = oracle.sparse_attn(q, k, v, np.array([[7]], np.int32), 0.1)
+    o2, l2, _ = oracle.sparse_attn(q, k, v, np.array([[7, 7]], np.int32), 0.1)
+    np.testing.assert_allclose(o1, o2, rtol=1e-6, atol=1e-7)
+
+
+def test_attn_slot_past_the_cache_is_flagged_and_skipped():
+    q, k, v = _attn_case(n_slots=4, h_q=2, h_kv=1)
+    out, lse, f = oracle.sparse_attn(q, k, v, np.array([[4, 1]], np.int32), 0.2)
+    o1, _, _ = oracle.sparse_attn(q, k, v, np.array([[1]], np.int32), 0.2)
+    assert f == 1 and np.array_equal(out, o1)

@@ -53,6 +53,13 @@ MUTANTS = {
         "for (int64_t p = QSA_C * nb0; p < L; ++p) {", "for (int64_t p = cap_len; p < L; ++p) {"),
     "indexshare_no_causal_cut": ("      if (p >= L) continue;\n", ""),
     "indexshare_incomplete_block_kept": ("    if (b >= nb0) {\n      flags |= 2;\n      continue;\n    }\n", ""),
+    "attn_kv_head_modulo": ("int64_t g = h / group;", "int64_t g = h % h_kv;"),
+    "attn_no_max_subtraction": ("double w = exp(logit[j] - mx);", "double w = exp(logit[j]);"),
+    "attn_mask_reads_slot_0": ("      if (s < 0) continue;\n      if (s >= n_slots) {",
+                               "      if (s < 0) s = 0;\n      if (s >= n_slots) {"),
+    "attn_nan_when_all_masked": ("out[h * d + e] = sum > 0.0 ? (float)(acc[e] / sum) : 0.0f;",
+                                 "out[h * d + e] = (float)(acc[e] / sum);"),
+    "attn_no_scale": ("      logit[j] = scale * dot;", "      logit[j] = dot;"),
     "indexshare_no_drafted_columns": (
         "int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;\n  int64_t nb0",
         "int64_t width = QSA_C * k_blk + (QSA_C - 1);\n  int64_t nb0"),
