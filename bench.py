@@ -533,6 +533,45 @@ WORKLOADS = {
 }
 
 
+def bench_variant_attn(g, w, iters, warmup, peaks, h_q=16, h_kv=2, d=256):
+    """Sparse attention over the slots the fused indexer selects for w's
+    rows (synthetic BF16 K/V cache covering every slot of the page pool,
+    drawn on the device from a seeded generator): the consumer of the
+    selection.  Timed alone; the indexer + attention pair timed too."""
+    torch, qsa = g.torch, g.qsa
+    st = setup_decode(g, w, 0)
+    qsa.indexer_select(st["q"], st["pool"], st["rrs"], st["row_len"], st["pt"], w.page_size, w.max_len,
+                       w.max_rows_per_req, k_blk=w.k_blk, workspace=st["ws"], out_slots=st["slots"])
+    n_slots = w.n_pages * w.page_size
+    gen = torch.Generator(device=g.dev)
+    gen.manual_seed(1234)
+    k = torch.randn((n_slots, h_kv, d), generator=gen, device=g.dev).to(torch.bfloat16)
+    v = torch.randn((n_slots, h_kv, d), generator=gen, device=g.dev).to(torch.bfloat16)
+    qa = torch.randn((w.n_rows, h_q, d), generator=gen, device=g.dev).to(torch.bfloat16)
+    slots = st["slots"]
+    out = torch.empty((w.n_rows, h_q, d), dtype=torch.float32, device=g.dev)
+    lse = torch.empty((w.n_rows, h_q), dtype=torch.float32, device=g.dev)
+    n_idx = slots.shape[1]
+    ws = torch.empty(max(1, qsa.lib().qsa_sparse_attn_workspace_size(w.n_rows, h_q, d, n_idx)),
+                     dtype=torch.uint8, device=g.dev)
+    fn = lambda: qsa.sparse_attn(qa, k, v, slots, d ** -0.5, out=out, lse=lse, workspace=ws)
+    t_attn = g.timed(fn, iters, warmup)
+    both = lambda: (qsa.indexer_select(st["q"], st["pool"], st["rrs"], st["row_len"], st["pt"], w.page_size,
+                                       w.max_len, w.max_rows_per_req, k_blk=w.k_blk, workspace=st["ws"],
+                                       out_slots=slots), fn())
+    t_both = g.timed(both, iters, warmup)
+    valid = int((slots >= 0).sum().item())
+    # K and V rows of every valid entry, the queries, the slot rows, the outputs
+    alg = valid * h_kv * d * 2 * 2 + w.n_rows * h_q * d * 2 + slots.numel() * 4 + w.n_rows * h_q * (d + 1) * 4
+    ms, ms_both = statistics.mean(t_attn), statistics.mean(t_both)
+    del st
+    return {"workload": w.name + f"_attn_h{h_q}kv{h_kv}d{d}", "rows": w.n_rows, "us_per_call": 1e3 * ms,
+            "rows_per_s": w.n_rows / (ms * 1e-3), "alg_bytes": alg, "alg_GBps": alg / (ms * 1e-3) / 1e9,
+            "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "indexer_plus_attn_us": 1e3 * ms_both,
+            "kernel": "sparse_attn_kernel<8, 256> + sparse_attn_merge_kernel<256>",
+            "kv": "synthetic BF16 N(0,1), 16 query / 2 KV heads, head dim 256 (the pages give no shape)"}
+
+
 def variant_table(g, it, warmup, peaks):
     """The secondary workloads of the JSON line: name -> a call measuring it."""
     return {
@@ -549,6 +588,7 @@ def variant_table(g, it, warmup, peaks):
                                                            warmup, peaks),
         "c5_prefill_4096rows": lambda: bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
         "indexshare_32req_draft": lambda: bench_variant_indexshare(g, indexshare_mtp(0), it, warmup, peaks),
+        "sparse_attn_32req": lambda: bench_variant_attn(g, c3_batched(0), it, warmup, peaks),
     }
 
 

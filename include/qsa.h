@@ -212,6 +212,38 @@ qsa_status qsa_indexshare_slots(const int32_t* cap_blocks, const int32_t* cap_le
                                 int32_t* out_pos, int32_t* out_slots, void* stream);
 
 /* ---------------------------------------------------------------------
+ * Sparse attention over the selected slots  ([QSA]: the compressed keys only
+ * index; the final softmax and value aggregation read the original,
+ * uncompressed K/V at the selected positions -- sparse GQA over at most
+ * 2051 positions.  [SMLA]: the only mask is index >= 0, and a token whose
+ * whole selection is masked must not give NaN).
+ *
+ *   q          [n_rows][h_q][head_dim] BF16 queries (16-byte aligned).
+ *   k_cache, v_cache  [n_slots][h_kv][head_dim] BF16: the K and V rows of
+ *              every physical KV slot (16-byte aligned).
+ *   slots      [n_rows][ld_slots] int32: entries 0 .. n_idx-1 of each row
+ *              are read (e.g. out_slots of qsa_indexer_select or
+ *              qsa_indexshare_slots); entries < 0 are skipped.
+ *   scale      softmax scale (e.g. 1/sqrt(head_dim)).
+ *   out        [n_rows][h_q][head_dim] FP32.
+ *   lse        [n_rows][h_q] FP32 or NULL: log sum_j exp(scale <q_h, k_j>).
+ *   workspace  qsa_sparse_attn_workspace_size(n_rows, h_q, head_dim, n_idx)
+ *              bytes (16-byte aligned; 0 bytes when n_idx <= 256).
+ *
+ * Query head h reads KV head h / (h_q / h_kv).  For each row and query head:
+ * out = sum_j softmax_j(scale <q_h, k_j>) v_j over the valid entries, FP32
+ * arithmetic on BF16 inputs.  A row with no valid entry gets out = 0 and
+ * lse = -inf.  Supported: h_q / h_kv a power of two, up to 16 with
+ * head_dim 128, up to 8 with head_dim 256 (else QSA_ERR_UNSUPPORTED).
+ * A slot >= n_slots is skipped and latches device fault bit 0.
+ * ------------------------------------------------------------------- */
+size_t qsa_sparse_attn_workspace_size(int32_t n_rows, int32_t h_q, int32_t head_dim, int32_t n_idx);
+qsa_status qsa_sparse_attn(const void* q, const void* k_cache, const void* v_cache, int64_t n_slots,
+                           int32_t n_rows, int32_t h_q, int32_t h_kv, int32_t head_dim,
+                           const int32_t* slots, int64_t ld_slots, int32_t n_idx, float scale, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------
  * Top-k_blk blocks of given block scores, expanded and translated, one
  * call  ([QSA] 512-block selection, 4 token positions per block followed by
  * the pending tokens; [TOPK] selection fused with the page-table transform).

@@ -19,7 +19,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
-    "select_blocks", "indexshare_slots", "indexshare_width",
+    "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -57,6 +57,9 @@ def lib():
                                                  p]),
             "qsa_indexshare_slots": (ctypes.c_int, [p, p, i32, p, i32, i32, i32, p, i32, p, p, i64, i32,
                                                     p, p, p]),
+            "qsa_sparse_attn_workspace_size": (sz, [i32, i32, i32, i32]),
+            "qsa_sparse_attn": (ctypes.c_int, [p, p, p, i64, i32, i32, i32, i32, p, i64, i32,
+                                               ctypes.c_float, p, p, p, sz, p]),
             "qsa_indexer_select_workspace_size": (sz, [i32, i32, i32]),
             "qsa_indexer_select": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                   i32, p, p, p, p, i64, p, sz, p]),
@@ -243,6 +246,39 @@ def indexshare_slots(cap_blocks, cap_len, cap_row, n_extra, req_row_start, row_l
         req_row_start.numel() - 1, _ptr(req_row_start), n_rows, _ptr(row_len), _ptr(page_table),
         page_table.shape[1], int(page_size), _ptr(pos), _ptr(out_slots), _stream(stream)))
     return pos, out_slots
+
+
+def sparse_attn(q, k_cache, v_cache, slots, scale=None, n_idx=None, out=None, lse=None, want_lse=True,
+                workspace=None, stream=None):
+    """Softmax attention of q [n_rows][h_q][d] over the K/V rows
+    [n_slots][h_kv][d] (bf16) at slots [n_rows][w] (int32, -1 skipped).
+    Returns (out [n_rows][h_q][d] float32, lse [n_rows][h_q] or None)."""
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
+    _dev(k_cache, torch.bfloat16, "k_cache", 3)
+    _dev(v_cache, torch.bfloat16, "v_cache", 3)
+    _dev(slots, torch.int32, "slots", 2)
+    n_rows, h_q, d = q.shape
+    n_slots, h_kv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or slots.shape[0] != n_rows:
+        raise ValueError("q, k_cache, v_cache and slots shapes disagree")
+    if n_idx is None:
+        n_idx = slots.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    dev = q.device
+    if out is None:
+        out = torch.empty((n_rows, h_q, d), dtype=torch.float32, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty((n_rows, h_q), dtype=torch.float32, device=dev)
+    ws_bytes = lib().qsa_sparse_attn_workspace_size(n_rows, h_q, d, int(n_idx))
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _check("qsa_sparse_attn", lib().qsa_sparse_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), n_slots, n_rows, h_q, h_kv, d, _ptr(slots), slots.shape[1],
+        int(n_idx), float(scale), _ptr(out), _ptr(lse if want_lse else None), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
+    return out, (lse if want_lse else None)
 
 
 def select_blocks(scores, req_row_start, row_len, page_table, page_size, max_len, k_blk=512,

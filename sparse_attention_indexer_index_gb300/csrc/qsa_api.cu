@@ -18,6 +18,7 @@
 #include "select_resident.cuh"
 #include "select_cluster.cuh"
 #include "select_long.cuh"
+#include "sparse_attn.cuh"
 
 using namespace qsa;
 
@@ -49,6 +50,18 @@ constexpr int kScSmem = kScFixedBytes + 2 * kScListCap * 4 + kSelPtStage * 4 + k
 // 2..16 CTAs per row (select_long_kernel), each CTA keeping as much of its
 // slice in shared memory as kSlSmem leaves.
 constexpr int kSlSmem = 227 * 1024;
+
+// Sparse attention instances: (query heads per KV head, head dim).
+template <int G, int D>
+bool set_attn_smem_one() {
+  return cudaFuncSetAttribute(sparse_attn_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(SaSmem<G, D>)) == cudaSuccess;
+}
+bool set_attn_smem() {
+  return set_attn_smem_one<1, 128>() && set_attn_smem_one<2, 128>() && set_attn_smem_one<4, 128>() &&
+         set_attn_smem_one<8, 128>() && set_attn_smem_one<16, 128>() && set_attn_smem_one<1, 256>() &&
+         set_attn_smem_one<2, 256>() && set_attn_smem_one<4, 256>() && set_attn_smem_one<8, 256>();
+}
 
 struct DeviceInfo {
   bool ready = false;
@@ -109,6 +122,7 @@ qsa_status device_info(DeviceInfo** out) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         cudaGetLastError();
     }
+    if (!set_attn_smem()) return QSA_ERR_CUDA;
     for (int e = 1; e <= 4; ++e) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1u << e, 1, 1);
@@ -657,6 +671,51 @@ qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream) {
   return QSA_OK;
 }
 
+template <int G, int D>
+qsa_status launch_attn_gd(const SaArgs& a, cudaStream_t stream) {
+  dim3 grid((unsigned)a.n_split, (unsigned)a.h_kv, (unsigned)a.n_rows);
+  sparse_attn_kernel<G, D><<<grid, kSaThreads, sizeof(SaSmem<G, D>), stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
+  if (a.n_split > 1) {
+    if (launch_pdl(sparse_attn_merge_kernel<D>, dim3((unsigned)((int64_t)a.n_rows * a.h_q)), dim3(D), 0,
+                   stream, a) != cudaSuccess) {
+      cudaGetLastError();
+      return QSA_ERR_CUDA;
+    }
+  }
+  return QSA_OK;
+}
+
+qsa_status launch_attn(const SaArgs& a, int group, int d, cudaStream_t stream) {
+  if (d == 128) {
+    switch (group) {
+      case 1: return launch_attn_gd<1, 128>(a, stream);
+      case 2: return launch_attn_gd<2, 128>(a, stream);
+      case 4: return launch_attn_gd<4, 128>(a, stream);
+      case 8: return launch_attn_gd<8, 128>(a, stream);
+      case 16: return launch_attn_gd<16, 128>(a, stream);
+      default: return QSA_ERR_UNSUPPORTED;
+    }
+  }
+  if (d == 256) {
+    switch (group) {
+      case 1: return launch_attn_gd<1, 256>(a, stream);
+      case 2: return launch_attn_gd<2, 256>(a, stream);
+      case 4: return launch_attn_gd<4, 256>(a, stream);
+      case 8: return launch_attn_gd<8, 256>(a, stream);
+      default: return QSA_ERR_UNSUPPORTED;
+    }
+  }
+  return QSA_ERR_UNSUPPORTED;
+}
+
+bool attn_shape_ok(int32_t h_q, int32_t h_kv, int32_t d) {
+  if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0) return false;
+  const int group = h_q / h_kv;
+  const bool pow2 = (group & (group - 1)) == 0;
+  return pow2 && ((d == 128 && group <= 16) || (d == 256 && group <= 8));
+}
+
 }  // namespace
 
 extern "C" {
@@ -808,6 +867,56 @@ qsa_status qsa_indexshare_slots(const int32_t* cap_blocks, const int32_t* cap_le
               row_len, page_table, ld_pt, page_size, out_pos, out_slots};
   indexshare_kernel<<<(unsigned)n_rows, kExpThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
+}
+
+size_t qsa_sparse_attn_workspace_size(int32_t n_rows, int32_t h_q, int32_t head_dim, int32_t n_idx) {
+  if (n_rows <= 0 || h_q <= 0 || head_dim <= 0 || n_idx <= kSaMaxChunk) return 0;
+  const int64_t n_split = ((int64_t)n_idx + kSaMinChunk - 1) / kSaMinChunk;
+  return (size_t)((int64_t)n_rows * h_q * n_split * (head_dim + 2) * 4) + 256;
+}
+
+qsa_status qsa_sparse_attn(const void* q, const void* k_cache, const void* v_cache, int64_t n_slots,
+                           int32_t n_rows, int32_t h_q, int32_t h_kv, int32_t head_dim,
+                           const int32_t* slots, int64_t ld_slots, int32_t n_idx, float scale, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_rows < 0 || n_idx < 0 || n_slots < 0 || ld_slots < n_idx) return QSA_ERR_INVALID_ARG;
+  if (!attn_shape_ok(h_q, h_kv, head_dim)) return QSA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return QSA_OK;
+  if (n_rows > 65535 || h_kv > 65535) return QSA_ERR_UNSUPPORTED;
+  if (!q || !out || (n_idx > 0 && (!k_cache || !v_cache || !slots))) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || (k_cache && !aligned16(k_cache)) || (v_cache && !aligned16(v_cache)) ||
+      !aligned4(out) || (lse && !aligned4(lse)))
+    return QSA_ERR_INVALID_ARG;
+  const size_t ws_need = qsa_sparse_attn_workspace_size(n_rows, h_q, head_dim, n_idx);
+  if (ws_need > 0 && (!workspace || workspace_bytes < ws_need)) return QSA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_need > 0 && !aligned16(workspace)) return QSA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  SaArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k_cache);
+  a.v = static_cast<const uint16_t*>(v_cache);
+  a.n_slots = n_slots;
+  a.n_rows = n_rows;
+  a.h_q = h_q;
+  a.h_kv = h_kv;
+  a.slots = slots;
+  a.ld_slots = ld_slots;
+  a.n_idx = n_idx;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  // entries per CTA: the largest of 256, 128, 64 that still gives two CTAs
+  // per SM; rows of at most 256 entries take one CTA per (row, KV head)
+  int chunk = kSaMaxChunk;
+  const int64_t units = (int64_t)n_rows * h_kv;
+  while (chunk > kSaMinChunk && units * (((int64_t)n_idx + chunk - 1) / chunk) < 2LL * d->sm_count) chunk >>= 1;
+  if (n_idx <= kSaMaxChunk) chunk = kSaMaxChunk;
+  a.chunk = chunk;
+  a.n_split = (int32_t)std::max<int64_t>(1, ((int64_t)n_idx + chunk - 1) / chunk);
+  if (a.n_split > 65535) return QSA_ERR_UNSUPPORTED;
+  if (a.n_split > 1) a.part = static_cast<float*>(workspace);  // n_split <= the size query's split
+  return launch_attn(a, h_q / h_kv, head_dim, static_cast<cudaStream_t>(stream));
 }
 
 qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_req,

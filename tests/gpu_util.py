@@ -43,3 +43,34 @@ def score_tolerance(q_bits, pool_bits, req_row_start, row_len, page_table, page_
 
 def pool_rows_of(page_table_row, nb, page_size):
     return np.array([oracle.pool_row(page_table_row, b, page_size) for b in range(nb)], np.int64)
+
+
+def attn_tolerance(q_bits, k_bits, v_bits, slots, scale, chunk=256):
+    """Per-element bound of the sparse-attention comparison [rows][h_q][d].
+    A logit is an FP32 sum of exact BF16 products: each lane adds d/32 of
+    them in order, then a 5-level butterfly adds the lanes, so its error is
+    at most (d/32 + 5) 2^-24 scale sum|q k|; the weights carry twice that
+    relative error plus 2^-22 for exp; a warp adds at most chunk/4 weighted
+    rows in order.  Bound on |out - out_ref|: that relative error times
+    max_j |v_j| (over the valid entries), plus 1e-6."""
+    q = oracle.bf16_to_float(q_bits)   # [rows][h_q][d]
+    k = oracle.bf16_to_float(k_bits)   # [n_slots][h_kv][d]
+    v = oracle.bf16_to_float(v_bits)
+    rows, h_q, d = q.shape
+    h_kv = k.shape[1]
+    g = h_q // h_kv
+    tol = np.zeros(q.shape)
+    gam = (d / 32 + 5) * 2.0 ** -24
+    for t in range(rows):
+        sl = slots[t]
+        sl = sl[(sl >= 0) & (sl < k.shape[0])]
+        if sl.size == 0:
+            tol[t] = 1e-6
+            continue
+        for h in range(h_q):
+            kk = k[sl, h // g]                       # [n][d]
+            L = abs(scale) * (np.abs(kk) @ np.abs(q[t, h])).max()
+            vmax = np.abs(v[sl, h // g]).max(axis=0)  # [d]
+            rel = 2 * gam * L + 2.0 ** -22 + (chunk / 4) * 2.0 ** -24 + 4e-6
+            tol[t, h] = rel * vmax + 1e-6
+    return tol

@@ -128,3 +128,24 @@ def test_indexshare_rejects_bad_arguments(L):
     assert f(FAKE, FAKE, 1, FAKE, 512, 3, 1, FAKE, 1, FAKE, FAKE, 4, 62, None, FAKE, None) == -2
     # no rows: nothing to do
     assert f(None, None, 0, None, 512, 3, 0, None, 0, None, None, 0, 64, None, None, None) == 0
+
+
+def test_sparse_attn_rejects_bad_arguments(L):
+    f = L.qsa_sparse_attn
+    c = ctypes.c_float(0.0625)
+    # group size 3, 32 (too many heads per KV head), head_dim 64
+    assert f(FAKE, FAKE, FAKE, 100, 1, 6, 2, 128, FAKE, 8, 8, c, FAKE, None, None, 0, None) == -2
+    assert f(FAKE, FAKE, FAKE, 100, 1, 32, 1, 128, FAKE, 8, 8, c, FAKE, None, None, 0, None) == -2
+    assert f(FAKE, FAKE, FAKE, 100, 1, 16, 1, 256, FAKE, 8, 8, c, FAKE, None, None, 0, None) == -2
+    assert f(FAKE, FAKE, FAKE, 100, 1, 8, 1, 64, FAKE, 8, 8, c, FAKE, None, None, 0, None) == -2
+    # entries beyond the leading dimension; misaligned q; no output
+    assert f(FAKE, FAKE, FAKE, 100, 1, 8, 1, 128, FAKE, 8, 9, c, FAKE, None, None, 0, None) == -1
+    assert f(ctypes.c_void_p(0x1002), FAKE, FAKE, 100, 1, 8, 1, 128, FAKE, 8, 8, c, FAKE, None, None, 0,
+             None) == -1
+    assert f(FAKE, FAKE, FAKE, 100, 1, 8, 1, 128, FAKE, 8, 8, c, None, None, None, 0, None) == -1
+    # a long row needs the workspace
+    need = L.qsa_sparse_attn_workspace_size(1, 8, 128, 2051)
+    assert need > 0 and L.qsa_sparse_attn_workspace_size(1, 8, 128, 256) == 0
+    assert f(FAKE, FAKE, FAKE, 100, 1, 8, 1, 128, FAKE, 2051, 2051, c, FAKE, None, None, 0, None) == -3
+    # no rows: nothing to do
+    assert f(None, None, None, 0, 0, 8, 1, 128, None, 0, 0, c, None, None, None, 0, None) == 0

@@ -11,7 +11,7 @@ import pytest
 import oracle
 from gpu_util import bf16_dev, bf16_host, score_tolerance, to_dev
 from workloads import (c1_decode, c2_verify, c2_batched, c3_batched, c4_dsa_topk, c5_prefill,
-                       decode_workload, indexshare_mtp, topk_workload, TOPK_DISTS)
+                       decode_workload, indexshare_mtp, normal_bf16, topk_workload, TOPK_DISTS)
 
 pytestmark = pytest.mark.gpu
 
@@ -530,3 +530,82 @@ def test_select_blocks_long_context(qsa):
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
     assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
     assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+# ----------------------------------------------------------------- sparse attention
+def _attn_check(qsa, q, k, v, slots, scale, faults=0):
+    import torch
+    from gpu_util import attn_tolerance
+    out, lse = qsa.sparse_attn(bf16_dev(q), bf16_dev(k), bf16_dev(v), to_dev(slots), scale)
+    ro, rl, f = oracle.sparse_attn(q, k, v, slots, scale)
+    assert qsa.device_status(clear=True) == faults
+    o = out.cpu().numpy().astype(np.float64)
+    tol = attn_tolerance(q, k, v, slots, scale)
+    err = np.abs(o - ro)
+    assert (err <= tol).all(), float((err / tol).max())
+    l = lse.cpu().numpy()
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(l), np.isneginf(rl))
+    assert np.abs(l[fin] - rl[fin]).max(initial=0.0) <= 1e-5 * (1 + np.abs(rl[fin]).max(initial=0.0))
+    return out
+
+
+@pytest.mark.parametrize("h_q,h_kv,d", [(16, 2, 256), (8, 2, 256), (4, 4, 256), (1, 1, 256), (16, 1, 128),
+                                        (8, 4, 128), (2, 1, 128)])
+def test_sparse_attn_parity_shapes(qsa, h_q, h_kv, d):
+    """Rows of 2051 entries (several chunks per row, merged) with masked
+    entries, duplicates, a fully masked row and a single-entry row."""
+    rng = np.random.default_rng(h_q * 1000 + h_kv * 10 + d)
+    n_slots, rows, w = 5000, 5, 2051
+    q = normal_bf16(rng, (rows, h_q, d))
+    k = normal_bf16(rng, (n_slots, h_kv, d))
+    v = normal_bf16(rng, (n_slots, h_kv, d))
+    slots = rng.integers(0, n_slots, size=(rows, w)).astype(np.int32)
+    slots[0, rng.random(w) < 0.3] = -1
+    slots[1, -300:] = -1
+    slots[2] = -1
+    slots[3] = -1
+    slots[3, 1234] = 77
+    slots[4, 100:200] = slots[4, 0]
+    _attn_check(qsa, q, k, v, slots, d ** -0.5)
+
+
+@pytest.mark.parametrize("w", [1, 31, 64, 256, 257, 700])
+def test_sparse_attn_parity_row_widths(qsa, w):
+    """One chunk per row (<= 256 entries) and the split path just past it."""
+    rng = np.random.default_rng(w)
+    q = normal_bf16(rng, (3, 8, 128))
+    k = normal_bf16(rng, (900, 1, 128))
+    v = normal_bf16(rng, (900, 1, 128))
+    slots = rng.integers(-1, 900, size=(3, w)).astype(np.int32)
+    _attn_check(qsa, q, k, v, slots, 0.1)
+
+
+def test_sparse_attn_slot_past_the_cache_is_flagged(qsa):
+    rng = np.random.default_rng(5)
+    q = normal_bf16(rng, (2, 8, 256))
+    k = normal_bf16(rng, (100, 1, 256))
+    v = normal_bf16(rng, (100, 1, 256))
+    slots = rng.integers(0, 100, size=(2, 300)).astype(np.int32)
+    slots[1, 7] = 100
+    _attn_check(qsa, q, k, v, slots, 0.0625, faults=1)
+
+
+def test_sparse_attn_after_the_fused_indexer(qsa):
+    """The end-to-end decode path: slots from qsa_indexer_select (top-512
+    blocks, pending tokens, -1 padding for short contexts) feed the sparse
+    attention over a synthetic paged K/V cache."""
+    import torch
+    w = decode_workload(71, [[20_003], [1500], [9000, 9001]], page_size=64, k_blk=512)
+    pool = gpu_pool(qsa, w)
+    out = qsa.indexer_select(bf16_dev(w.q), pool, to_dev(w.req_row_start), to_dev(w.row_len),
+                             to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, k_blk=512)
+    slots = out["slots"].cpu().numpy()
+    rng = np.random.default_rng(72)
+    n_slots = w.n_pages * w.page_size
+    h_q, h_kv, d = 16, 2, 256
+    qa = normal_bf16(rng, (w.n_rows, h_q, d))
+    k = normal_bf16(rng, (n_slots, h_kv, d))
+    v = normal_bf16(rng, (n_slots, h_kv, d))
+    assert (slots[1] == -1).sum() > 0  # the short context is padded
+    _attn_check(qsa, qa, k, v, slots, d ** -0.5)
