@@ -372,6 +372,7 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     st = setup_decode(g, w, new_blocks)
     t_step = g.timed(lambda: decode_step(g, st), iters, warmup)
     t_score = g.timed(lambda: scores_only(g, st), iters, warmup)
+    t_select = g.timed(lambda: select_only(g, st), iters, warmup)
     by = decode_bytes(w)
     alg = by["keys"] + by["q"] + by["page_table"] + by["slots"]
     ms = statistics.mean(t_step)
@@ -379,7 +380,8 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     res = {"workload": w.name, "rows": w.n_rows, "us_per_call": 1e3 * ms,
            "rows_per_s": w.n_rows / (ms * 1e-3), "alg_bytes": alg,
            "alg_GBps": alg / (ms * 1e-3) / 1e9, "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-           "score_kernel_us": 1e3 * ms_sc,
+           "score_kernel_us": 1e3 * ms_sc, "select_kernel_us": 1e3 * statistics.mean(t_select),
+           "kernels": kernel_names(w),
            "score_alg_GBps": (by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"]) /
                              (ms_sc * 1e-3) / 1e9}
     del st

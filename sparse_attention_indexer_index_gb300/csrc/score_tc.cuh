@@ -964,6 +964,9 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
     // ---- epilogue -------------------------------------------------------------
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
+    // row lengths of the current group's rows, lane j holding row t0 + j
+    // (reloaded only when the group changes)
+    int len_t0 = -1, my_len = 0;
     for (int i = 0; i < n_items; ++i) {
       const int st = i % S, acc = i & 1;
       // the descriptor comes through desc_ready (a plain arrive by the MMA
@@ -974,6 +977,10 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
       if (!ok) break;
       tc_fence_after();
       const TbDesc dd = ctl->desc_acc[acc];
+      if (dd.nrows > 1 && dd.t0 != len_t0) {
+        len_t0 = dd.t0;
+        my_len = lane < dd.nrows ? __ldg(a.row_len + dd.t0 + lane) : 0;
+      }
       const int b = dd.kt * kTcM + quarter * 32 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
       for (int c0 = 32 * half; c0 < N; c0 += 64) {
@@ -990,10 +997,11 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int tr = c0 / 4 + j;  // row within the tile
+          const int tr = c0 / 4 + j;  // row within the tile (warp-uniform)
+          // one row: its visible blocks are the group's; several: its own
+          const int Lr = dd.nrows == 1 ? kBlock * dd.nb : __shfl_sync(0xffffffffu, my_len, tr & 31);
           if (4 * j < ncols && tr < dd.nrows && b < dd.nb) {
-            // one row: its visible blocks are the group's; several: its own
-            const int L = dd.nrows == 1 ? kBlock * dd.nb : __ldg(a.row_len + dd.t0 + tr);
+            const int L = Lr;
             if (L >= 0 && L <= a.max_len && b < L / kBlock) {
               float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
               sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);

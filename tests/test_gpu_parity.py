@@ -177,11 +177,11 @@ def test_topk_heavy_ties_take_the_full_row_path(qsa, n):
         assert np.array_equal(idx.cpu().numpy(), ref), k
 
 
-@pytest.mark.parametrize("n", [20_000, 32_768])
-def test_topk_hard_rows_many_rows(qsa, n):
+@pytest.mark.parametrize("n,copies", [(20_000, 5), (32_768, 5), (20_000, 19)])
+def test_topk_hard_rows_many_rows(qsa, n, copies):
     """The same hard rows (all equal, three values, one top-bits bin, the
-    sample planted with the largest values) in a launch of 24 rows, which
-    takes the single-CTA selection instead of one cluster per row."""
+    sample planted with the largest values) in launches of 24 and 80 rows,
+    which take the single-CTA selection instead of one cluster per row."""
     rng = np.random.default_rng(n + 7)
     base = np.zeros((4, n), np.float32)
     base[0] = 1.5
@@ -189,7 +189,7 @@ def test_topk_hard_rows_many_rows(qsa, n):
     base[2] = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)
     base[3] = (rng.standard_normal(n) * 0.01).astype(np.float32)
     base[3, (np.arange(1024, dtype=np.int64) * n) // 1024] = 100.0
-    s = np.concatenate([base] * 5 + [rng.standard_normal((4, n)).astype(np.float32)])
+    s = np.concatenate([base] * copies + [rng.standard_normal((4, n)).astype(np.float32)])
     nv = np.full(s.shape[0], n, np.int32)
     for k in [512, 2048]:
         idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
