@@ -67,6 +67,7 @@ def _load():
                 "oracle_indexer_select": (None, [p, p, i64, p, p, p, i64, i64, i64, p, i64, p, p, p]),
                 "oracle_indexshare_row": (ctypes.c_int, [p, i64, i64, i64, i64, p, i64, p, p]),
                 "oracle_indexshare": (ctypes.c_int, [p, p, i64, p, i64, i64, i64, p, p, p, i64, i64, p, p]),
+                "oracle_append_keys": (None, [p, p, p, i64, p, p, i64, i64, d, p]),
                 "oracle_sparse_attn_row": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, p, i64, d, p, p]),
                 "oracle_sparse_attn": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, i64, p, i64, i64, d, p, p]),
             }
@@ -293,3 +294,18 @@ def sparse_attn(q, k, v, slots, scale):
     f = _load().oracle_sparse_attn(_ptr(q), _ptr(k), _ptr(v), n_slots, n_rows, h_q, h_kv, d, _ptr(sl),
                                    n_idx, n_idx, float(scale), _ptr(out), _ptr(lse))
     return out, lse, int(f)
+
+
+# ---------------------------------------------------------------- key path
+def append_keys(new_keys, req_tok_start, req_first_pos, ring, page_table, page_size, rope_base, pool):
+    """Appends raw keys per request (ring [n_req][4][128] u16 and pool
+    updated in place); returns (ring, pool)."""
+    nk = _c(new_keys, np.uint16)
+    rts = _c(req_tok_start, np.int32)
+    rfp = _c(req_first_pos, np.int32)
+    pt = _c(page_table, np.int32)
+    assert ring.dtype == np.uint16 and ring.flags.c_contiguous
+    assert pool.dtype == np.uint16 and pool.flags.c_contiguous
+    _load().oracle_append_keys(_ptr(nk), _ptr(rts), _ptr(rfp), rts.size - 1, _ptr(ring), _ptr(pt),
+                               pt.shape[-1], int(page_size), float(rope_base), _ptr(pool))
+    return ring, pool

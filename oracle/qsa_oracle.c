@@ -148,6 +148,45 @@ void oracle_compress(const uint16_t* raw, int64_t n_blocks, const int32_t* block
   }
 }
 
+/* ---------- key path of a decode step ([QSA]: the raw index keys of the
+ * incomplete block wait in a 4-slot ring per request; a completed block is
+ * compressed into the pool at full_slot/4) ------------------------------- */
+
+/* Request r appends the raw keys new_keys[req_tok_start[r] + i] at positions
+ * req_first_pos[r] + i, i < req_tok_start[r+1] - req_tok_start[r].  Every
+ * block b completed by these tokens (4b+3 among the positions) is compressed
+ * from its 4 raw keys -- those of this call where present, the ring's
+ * (ring[r][q mod 4], written by earlier calls) for the earlier positions --
+ * into pool row slot(4b)/4.  Then ring[r][p mod 4] takes the key of every
+ * appended position p, in order (later positions overwrite earlier ones).
+ * ring is [n_req][4][128] u16, updated in place. */
+void oracle_append_keys(const uint16_t* new_keys, const int32_t* req_tok_start,
+                        const int32_t* req_first_pos, int64_t n_req, uint16_t* ring,
+                        const int32_t* page_table, int64_t ld_pt, int64_t page_size,
+                        double rope_base, uint16_t* pool) {
+  uint16_t blk[QSA_C * QSA_D];
+  for (int64_t r = 0; r < n_req; ++r) {
+    int64_t n = req_tok_start[r + 1] - req_tok_start[r];
+    int64_t p0 = req_first_pos[r];
+    const uint16_t* keys = new_keys + (int64_t)req_tok_start[r] * QSA_D;
+    uint16_t* rr = ring + r * QSA_C * QSA_D;
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t p = p0 + i;
+      if (p % QSA_C != QSA_C - 1) continue;
+      int64_t b = p / QSA_C;
+      for (int c = 0; c < QSA_C; ++c) {
+        int64_t q = QSA_C * b + c;
+        const uint16_t* src = q >= p0 ? keys + (q - p0) * QSA_D : rr + c * QSA_D;
+        memcpy(blk + c * QSA_D, src, QSA_D * sizeof(uint16_t));
+      }
+      int64_t row = oracle_pool_row(page_table + r * ld_pt, b, page_size);
+      oracle_compress_block(blk, QSA_C * b, rope_base, pool + row * QSA_D);
+    }
+    for (int64_t i = 0; i < n; ++i)
+      memcpy(rr + ((p0 + i) % QSA_C) * QSA_D, keys + i * QSA_D, QSA_D * sizeof(uint16_t));
+  }
+}
+
 /* ---------- step 2: block scores ([QSA] score equation) ------------------ */
 
 /* s = (1/sqrt(128)) * sum_{h<4} ReLU(<q_h, kbar>), in FP64, rounded once to

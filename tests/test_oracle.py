@@ -557,3 +557,72 @@ def test_attn_slot_past_the_cache_is_flagged_and_skipped():
     out, lse, f = oracle.sparse_attn(q, k, v, np.array([[4, 1]], np.int32), 0.2)
     o1, _, _ = oracle.sparse_attn(q, k, v, np.array([[1]], np.int32), 0.2)
     assert f == 1 and np.array_equal(out, o1)
+
+
+# ------------------------------------------------------------ key path (ring)
+# Qwen3.8-Flash-Next write-up, "Qwen sparse attention (QSA)": the raw index
+# keys of a request's incomplete block wait in a 4-slot ring; a completed
+# block is compressed into the pool at full_slot/4.
+def _append_in_chunks(raw, chunks, P, pt, n_rows_pool, firsts=None):
+    """One request; raw [L][128] u16 appended chunk by chunk."""
+    ring = np.zeros((1, 4, D), np.uint16)
+    pool = np.zeros((n_rows_pool, D), np.uint16)
+    p = 0
+    for n in chunks:
+        oracle.append_keys(raw[p:p + n], np.array([0, n], np.int32), np.array([p], np.int32), ring, pt[None],
+                           P, 10000.0, pool)
+        p += n
+    return ring, pool
+
+
+@pytest.mark.parametrize("chunks", [[1] * 23, [6, 6, 6, 5], [3, 9, 4, 1, 2, 4], [23], [2, 2, 11, 8]])
+def test_append_keys_equals_direct_compression(chunks):
+    """Appending the tokens of a request in any chunking leaves in the pool
+    exactly the direct compression of its complete blocks, and in the ring
+    the keys of the last positions at slot p mod 4."""
+    L, P = sum(chunks), 8
+    rng = np.random.default_rng(len(chunks))
+    raw = normal_bf16(rng, (L, D))
+    pt = rng.permutation(8).astype(np.int32)
+    n_rows_pool = 8 * P // 4
+    ring, pool = _append_in_chunks(raw, chunks, P, pt, n_rows_pool)
+    nb = L // 4
+    want = np.zeros_like(pool)
+    oracle.compress(raw[:4 * nb], np.zeros(nb, np.int32), np.arange(nb, dtype=np.int32), pt[None], P, 10000.0,
+                    want)
+    assert np.array_equal(pool, want)
+    for p in range(max(0, L - 4), L):
+        assert np.array_equal(ring[0, p % 4], raw[p])
+
+
+def test_append_keys_several_requests_in_one_call():
+    """Requests with different first positions and token counts in one call
+    (a request completing two blocks, one completing none, one with no
+    tokens) match appending each request alone."""
+    P = 4
+    rng = np.random.default_rng(9)
+    firsts = np.array([5, 0, 7, 2], np.int32)
+    counts = np.array([7, 2, 0, 3], np.int32)
+    rts = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    raw_ctx = [normal_bf16(rng, (int(f + c), D)) for f, c in zip(firsts, counts)]
+    pt = rng.permutation(4 * 8).astype(np.int32).reshape(4, 8)
+    pool_rows = 32 * P // 4
+    ring = np.zeros((4, 4, D), np.uint16)
+    pool = np.zeros((pool_rows, D), np.uint16)
+    # the tokens before this call, one at a time
+    for r in range(4):
+        for p in range(int(firsts[r])):
+            oracle.append_keys(raw_ctx[r][p:p + 1], np.array([0] * r + [0, 1] + [1] * (3 - r), np.int32),
+                               np.where(np.arange(4) == r, p, 0).astype(np.int32), ring, pt, P, 10000.0, pool)
+    ring_a, pool_a = ring.copy(), pool.copy()
+    new = np.concatenate([raw_ctx[r][firsts[r]:] for r in range(4)])
+    oracle.append_keys(new, rts, firsts, ring_a, pt, P, 10000.0, pool_a)
+    for r in range(4):  # each request alone
+        rs = np.zeros(5, np.int32)
+        rs[r + 1:] = counts[r]
+        oracle.append_keys(raw_ctx[r][firsts[r]:], rs, firsts, ring, pt, P, 10000.0, pool)
+    assert np.array_equal(ring, ring_a) and np.array_equal(pool, pool_a)
+    # request 0 completed blocks 1 and 2 (positions 7 and 11)
+    for b in (1, 2):
+        want = oracle.compress_block(raw_ctx[0][4 * b:4 * b + 4], 4 * b)
+        assert np.array_equal(pool_a[oracle.pool_row(pt[0], b, P)], want)

@@ -53,6 +53,8 @@ MUTANTS = {
         "for (int64_t p = QSA_C * nb0; p < L; ++p) {", "for (int64_t p = cap_len; p < L; ++p) {"),
     "indexshare_no_causal_cut": ("      if (p >= L) continue;\n", ""),
     "indexshare_incomplete_block_kept": ("    if (b >= nb0) {\n      flags |= 2;\n      continue;\n    }\n", ""),
+    "append_first_new_key_from_ring": ("const uint16_t* src = q >= p0 ? keys", "const uint16_t* src = q > p0 ? keys"),
+    "append_ring_slot_by_call_index": ("memcpy(rr + ((p0 + i) % QSA_C) * QSA_D", "memcpy(rr + (i % QSA_C) * QSA_D"),
     "attn_kv_head_modulo": ("int64_t g = h / group;", "int64_t g = h % h_kv;"),
     "attn_no_max_subtraction": ("double w = exp(logit[j] - mx);", "double w = exp(logit[j]);"),
     "attn_mask_reads_slot_0": ("      if (s < 0) continue;\n      if (s >= n_slots) {",
