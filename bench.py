@@ -368,11 +368,63 @@ def e2e_decode(g: Gpu, st, iters, warmup):
     return times, h2d, d2h
 
 
+def setup_key_path(g, st):
+    """The decode key path of the step: every query row's own token is
+    appended (request r: positions row_len - 1 of its rows, consecutive)
+    through the 4-slot ring, which holds the earlier positions of the
+    block.  Raw keys come from the workload where it has them (complete
+    blocks), seeded N(0,1) BF16 otherwise."""
+    w = st["w"]
+    rng = np.random.default_rng(777)
+    raw_of = {}
+    for i in range(w.n_blocks):
+        raw_of[(int(w.block_req[i]), int(w.block_id[i]))] = i
+
+    def raw_key(r, p):
+        i = raw_of.get((r, p // 4))
+        if i is None:
+            return bf16_bits_of(rng.standard_normal(128).astype(np.float32))
+        return w.raw_keys[4 * i + p % 4]
+
+    keys, first, counts = [], [], []
+    ring = np.zeros((w.n_req, 4, 128), np.uint16)
+    for r in range(w.n_req):
+        pos = sorted(int(L) - 1 for L in w.row_len[w.req_row_start[r]:w.req_row_start[r + 1]])
+        p0 = pos[0]
+        first.append(p0)
+        counts.append(len(pos))
+        keys.extend(raw_key(r, p) for p in range(p0, p0 + len(pos)))
+        for p in range(4 * (p0 // 4), p0):
+            ring[r, p % 4] = raw_key(r, p)
+    st["kp_keys"] = g.bf16(np.stack(keys))
+    st["kp_rts"] = g.h2d(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+    st["kp_first"] = g.h2d(np.array(first, np.int32))
+    st["kp_ring"] = g.bf16(ring)
+
+
+def bf16_bits_of(x):
+    from workloads import bf16_bits
+    return bf16_bits(np.asarray(x, np.float32))
+
+
+def append_only(g, st):
+    """The key path alone (ring append + compression of the completed
+    blocks).  Replays repeat the same work; the ring then holds this
+    step's keys, so the values compressed from it differ after the first
+    replay (the timing does not depend on them)."""
+    w = st["w"]
+    g.qsa.append_keys(st["kp_keys"], st["kp_rts"], st["kp_first"], st["kp_ring"], st["pool"], st["pt"],
+                      w.page_size, w.rope_base)
+
+
 def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     st = setup_decode(g, w, new_blocks)
     t_step = g.timed(lambda: decode_step(g, st), iters, warmup)
     t_score = g.timed(lambda: scores_only(g, st), iters, warmup)
     t_select = g.timed(lambda: select_only(g, st), iters, warmup)
+    setup_key_path(g, st)
+    t_append = g.timed(lambda: append_only(g, st), iters, warmup)
+    t_compress = g.timed(lambda: compress_only(g, st), iters, warmup) if new_blocks > 0 else None
     by = decode_bytes(w)
     alg = by["keys"] + by["q"] + by["page_table"] + by["slots"]
     ms = statistics.mean(t_step)
@@ -381,6 +433,8 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
            "rows_per_s": w.n_rows / (ms * 1e-3), "alg_bytes": alg,
            "alg_GBps": alg / (ms * 1e-3) / 1e9, "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
            "score_kernel_us": 1e3 * ms_sc, "select_kernel_us": 1e3 * statistics.mean(t_select),
+           "key_path_append_us": 1e3 * statistics.mean(t_append),
+           "compress_kernel_us": 1e3 * statistics.mean(t_compress) if t_compress else None,
            "kernels": kernel_names(w),
            "score_alg_GBps": (by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"]) /
                              (ms_sc * 1e-3) / 1e9}

@@ -119,6 +119,32 @@ qsa_status qsa_compress_keys(const void* raw, const int32_t* block_req, const in
                              int64_t pool_rows, void* stream);
 
 /* ---------------------------------------------------------------------
+ * Decode key path through a per-request ring  ([QSA]: the raw index keys of
+ * the incomplete block wait in a 4-slot ring per request instead of being
+ * kept for the whole context; a completed block is compressed into the pool
+ * at full_slot/4).
+ *
+ *   new_keys      [n_tok][128] BF16 raw index keys appended by this call.
+ *   req_tok_start [n_req+1]: request r appends new_keys[req_tok_start[r] ..
+ *                 req_tok_start[r+1]-1] at consecutive positions
+ *                 req_first_pos[r], req_first_pos[r]+1, ...
+ *   ring          [n_req][4][128] BF16, updated in place: slot p mod 4 holds
+ *                 the raw key of position p of the request's incomplete
+ *                 block (written by earlier calls).
+ *   page_table, page_size, pool, pool_rows, rope_base: as qsa_compress_keys.
+ *
+ * Every block b that the appended positions complete (4b+3 among them) is
+ * compressed exactly as qsa_compress_keys does, from its 4 raw keys (this
+ * call's where present, the ring's for earlier positions), into pool row
+ * slot(4b)/4; then ring slot p mod 4 takes the key of each appended
+ * position p (the later ones win).  Device faults: a page id or pool row out
+ * of range (bits 0, 1), bad grouping (bit 3).
+ * ------------------------------------------------------------------- */
+qsa_status qsa_append_keys(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                           int32_t n_req, void* ring, const int32_t* page_table, int64_t ld_pt,
+                           int32_t page_size, double rope_base, void* pool, int64_t pool_rows, void* stream);
+
+/* ---------------------------------------------------------------------
  * Block scores  ([QSA] score equation:
  *   s[t][b] = (1/sqrt(128)) * sum_{h=1..4} ReLU(<q[t][h], kbar[b]>)
  * over the visible compressed blocks b < row_len[t]/4).

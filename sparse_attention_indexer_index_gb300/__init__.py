@@ -19,7 +19,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
-    "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn",
+    "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn", "append_keys",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -48,6 +48,7 @@ def lib():
             "qsa_version": (ctypes.c_int, []),
             "qsa_device_status": (ctypes.c_int, [p, ctypes.c_int, p]),
             "qsa_compress_keys": (ctypes.c_int, [p, p, p, i64, i32, p, i64, i32, d, p, i64, p]),
+            "qsa_append_keys": (ctypes.c_int, [p, p, p, i32, p, p, i64, i32, d, p, i64, p]),
             "qsa_index_scores": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
                                                 i64, i64, p]),
             "topk_select_workspace_size": (sz, [i32, i32, i32]),
@@ -139,6 +140,27 @@ def compress_keys(raw, block_id, pool, block_req=None, page_table=None, page_siz
         _ptr(raw), _ptr(block_req), _ptr(block_id), n_blocks, n_req, _ptr(page_table), ld_pt,
         int(page_size), float(rope_base), _ptr(pool), pool.shape[0], _stream(stream)))
     return pool
+
+
+def append_keys(new_keys, req_tok_start, req_first_pos, ring, pool, page_table, page_size, rope_base=10000.0,
+                stream=None):
+    """Decode key path: appends raw keys [n_tok][128] bf16 per request into
+    the 4-slot ring [n_req][4][128] and compresses the completed blocks into
+    the pool (both updated in place)."""
+    torch = _torch()
+    _dev(new_keys, torch.bfloat16, "new_keys", 2)
+    _dev(req_tok_start, torch.int32, "req_tok_start", 1)
+    _dev(req_first_pos, torch.int32, "req_first_pos", 1)
+    _dev(ring, torch.bfloat16, "ring", 3)
+    _dev(pool, torch.bfloat16, "pool", 2)
+    _dev(page_table, torch.int32, "page_table", 2)
+    n_req = req_first_pos.numel()
+    if req_tok_start.numel() != n_req + 1 or tuple(ring.shape) != (n_req, BLOCK, HEAD_DIM):
+        raise ValueError("req_tok_start must have n_req+1 entries and ring be [n_req][4][128]")
+    _check("qsa_append_keys", lib().qsa_append_keys(
+        _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), n_req, _ptr(ring), _ptr(page_table),
+        page_table.shape[1], int(page_size), float(rope_base), _ptr(pool), pool.shape[0], _stream(stream)))
+    return ring, pool
 
 
 def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len,

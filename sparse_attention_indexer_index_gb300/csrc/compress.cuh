@@ -64,6 +64,65 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// One block compressed by the 8 lanes of a group: lane8 holds dims
+// [8 lane8, +8) and [64 + 8 lane8, +8) of the 4 raw keys (vlo, vhi) and
+// writes the same dims of the compressed key at dst.  The 8 lanes of a
+// group always reach this together.
+__device__ __forceinline__ void compress_block_8(const uint4 (&vlo)[kBlock], const uint4 (&vhi)[kBlock],
+                                                 uint32_t pos, const uint64_t (&turn_frac)[8],
+                                                 __nv_bfloat16* dst, int lane8) {
+  // FP32 block mean, summed in token order: ((k0 + k1) + k2) + k3, * 0.25.
+  float lo[8], hi[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 fx = bf16x2_to_float2((&vlo[0].x)[e]), fy = bf16x2_to_float2((&vhi[0].x)[e]);
+    lo[2 * e] = fx.x; lo[2 * e + 1] = fx.y;
+    hi[2 * e] = fy.x; hi[2 * e + 1] = fy.y;
+  }
+#pragma unroll
+  for (int k = 1; k < kBlock; ++k) {
+    accumulate_bf16x8(lo, vlo[k]);
+    accumulate_bf16x8(hi, vhi[k]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    lo[e] *= 0.25f;
+    hi[e] *= 0.25f;
+    ss = fmaf(lo[e], lo[e], ss);
+    ss = fmaf(hi[e], hi[e], ss);
+  }
+  // The 8 lanes of a block always take the same path, so the shuffles name
+  // only their own group.
+  const unsigned group = 0xffu << (threadIdx.x & 24);
+  ss += __shfl_xor_sync(group, ss, 1);
+  ss += __shfl_xor_sync(group, ss, 2);
+  ss += __shfl_xor_sync(group, ss, 4);
+  const float inv_norm = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+
+  uint32_t out_lo[4], out_hi[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    float r_lo[2], r_hi[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t ph = (uint64_t)pos * turn_frac[e + h];  // turns mod 1, wraps
+      const int32_t top = (int32_t)(ph >> 32);               // signed: [-1/2, 1/2) turn
+      const float y = (float)top * 4.656612873077392578125e-10f;  // * 2^-31: units of pi
+      float s, c;
+      sincospif(y, &s, &c);
+      const float u = lo[e + h] * inv_norm, v = hi[e + h] * inv_norm;
+      r_lo[h] = u * c - v * s;
+      r_hi[h] = v * c + u * s;
+    }
+    out_lo[e / 2] = pack_bf16x2(r_lo[0], r_lo[1]);
+    out_hi[e / 2] = pack_bf16x2(r_hi[0], r_hi[1]);
+  }
+  *reinterpret_cast<uint4*>(dst + 8 * lane8) = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+  *reinterpret_cast<uint4*>(dst + 64 + 8 * lane8) =
+      make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+}
+
 __global__ void __launch_bounds__(kCompressThreads)
 compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
   // A dependent grid (launched with programmatic serialisation) may start
@@ -113,57 +172,90 @@ compress_keys_kernel(CompressArgs a, const __grid_constant__ RopeTurns turns) {
       continue;
     }
 
-    // FP32 block mean, summed in token order: ((k0 + k1) + k2) + k3, * 0.25.
-    float lo[8], hi[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 fx = bf16x2_to_float2((&vlo[0].x)[e]), fy = bf16x2_to_float2((&vhi[0].x)[e]);
-      lo[2 * e] = fx.x; lo[2 * e + 1] = fx.y;
-      hi[2 * e] = fy.x; hi[2 * e + 1] = fy.y;
-    }
-#pragma unroll
-    for (int k = 1; k < kBlock; ++k) {
-      accumulate_bf16x8(lo, vlo[k]);
-      accumulate_bf16x8(hi, vhi[k]);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      lo[e] *= 0.25f;
-      hi[e] *= 0.25f;
-      ss = fmaf(lo[e], lo[e], ss);
-      ss = fmaf(hi[e], hi[e], ss);
-    }
-    // The 8 lanes of a block always take the same path, so the shuffles name
-    // only their own group.
-    const unsigned group = 0xffu << (threadIdx.x & 24);
-    ss += __shfl_xor_sync(group, ss, 1);
-    ss += __shfl_xor_sync(group, ss, 2);
-    ss += __shfl_xor_sync(group, ss, 4);
-    const float inv_norm = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    compress_block_8(vlo, vhi, pos, turn_frac, a.pool + row * kDim, lane8);
+  }
+}
 
-    uint32_t out_lo[4], out_hi[4];
+// Key path of a decode step: request r appends raw keys at positions
+// first_pos[r] + i into its 4-slot ring (slot p mod 4) and compresses every
+// block those positions complete -- the raw keys of this call where
+// present, the ring's (earlier calls) otherwise -- into the pool at
+// slot(4b)/4.  Same source as compress_keys_kernel for the arithmetic.
+// One 64-thread CTA per request: 8 groups of 8 lanes compress the completed
+// blocks (reading the ring as it was), then, after a barrier, the ring takes
+// the last 4 appended keys.
+struct AppendArgs {
+  const __nv_bfloat16* keys;      // [n_tok][128]
+  const int32_t* req_tok_start;   // [n_req+1]
+  const int32_t* req_first_pos;   // [n_req]
+  int32_t n_req;
+  __nv_bfloat16* ring;            // [n_req][4][128]
+  const int32_t* page_table;      // [n_req][ld_pt]
+  int64_t ld_pt;
+  int32_t page_size;
+  __nv_bfloat16* pool;            // [pool_rows][128]
+  int64_t pool_rows;
+};
+
+constexpr int kAppendThreads = 64;
+
+__global__ void __launch_bounds__(kAppendThreads)
+append_keys_kernel(AppendArgs a, const __grid_constant__ RopeTurns turns) {
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  const int lane8 = threadIdx.x & (kCompressLanes - 1), grp = threadIdx.x / kCompressLanes;
+  const int start = __ldg(a.req_tok_start + r), end = __ldg(a.req_tok_start + r + 1);
+  const int p0 = __ldg(a.req_first_pos + r);
+  const int n = end - start;
+  if (n <= 0) return;
+  if (start < 0 || p0 < 0 || (int64_t)p0 + n > (int64_t)INT32_MAX) {
+    if (threadIdx.x == 0) raise_fault(kFaultGrouping);
+    return;
+  }
+  uint64_t turn_frac[8];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      float r_lo[2], r_hi[2];
+  for (int e = 0; e < 8; ++e) turn_frac[e] = turns.frac[kCompressLanes * lane8 + e];
+  __nv_bfloat16* ring = a.ring + (int64_t)r * kBlock * kDim;
+  const __nv_bfloat16* keys = a.keys + (int64_t)start * kDim;
+
+  // blocks b with 4b+3 in [p0, p0+n-1]
+  const int b_first = p0 / kBlock;
+  const int b_last = (p0 + n - kBlock) >= 0 ? (p0 + n - kBlock) / kBlock : -1;
+  for (int b = b_first + grp; b <= b_last; b += kAppendThreads / kCompressLanes) {
+    uint4 vlo[kBlock], vhi[kBlock];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint64_t ph = (uint64_t)pos * turn_frac[e + h];  // turns mod 1, wraps
-        const int32_t top = (int32_t)(ph >> 32);               // signed: [-1/2, 1/2) turn
-        const float y = (float)top * 4.656612873077392578125e-10f;  // * 2^-31: units of pi
-        float s, c;
-        sincospif(y, &s, &c);
-        const float u = lo[e + h] * inv_norm, v = hi[e + h] * inv_norm;
-        r_lo[h] = u * c - v * s;
-        r_hi[h] = v * c + u * s;
-      }
-      out_lo[e / 2] = pack_bf16x2(r_lo[0], r_lo[1]);
-      out_hi[e / 2] = pack_bf16x2(r_hi[0], r_hi[1]);
+    for (int c = 0; c < kBlock; ++c) {
+      const int q = kBlock * b + c;
+      const __nv_bfloat16* src = q >= p0 ? keys + (int64_t)(q - p0) * kDim : ring + c * kDim;
+      vlo[c] = *reinterpret_cast<const uint4*>(src + 8 * lane8);
+      vhi[c] = *reinterpret_cast<const uint4*>(src + 64 + 8 * lane8);
     }
-    __nv_bfloat16* dst = a.pool + row * kDim;
-    *reinterpret_cast<uint4*>(dst + 8 * lane8) = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-    *reinterpret_cast<uint4*>(dst + 64 + 8 * lane8) =
-        make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+    const uint32_t pos = (uint32_t)(kBlock * b);
+    const uint32_t ps = (uint32_t)a.page_size;
+    const uint32_t page_idx = pos / ps;
+    int64_t row = -1;
+    if ((int64_t)page_idx < a.ld_pt) {
+      const int64_t page = a.page_table[(int64_t)r * a.ld_pt + page_idx];
+      if (page >= 0) row = page * (int64_t)(ps / kBlock) + (int64_t)((pos - page_idx * ps) / kBlock);
+    }
+    if (row < 0) {
+      if (lane8 == 0) raise_fault(kFaultIndex);
+      continue;
+    }
+    if (row >= a.pool_rows) {
+      if (lane8 == 0) raise_fault(kFaultPool);
+      continue;
+    }
+    compress_block_8(vlo, vhi, pos, turn_frac, a.pool + row * kDim, lane8);
+  }
+  __syncthreads();  // every read of the ring is done
+  // the ring keeps the key of every appended position, the last 4 win
+  const int i0 = n > kBlock ? n - kBlock : 0;
+  for (int x = threadIdx.x; x < (n - i0) * (kDim / 8); x += kAppendThreads) {
+    const int i = i0 + x / (kDim / 8), part = x % (kDim / 8);
+    const int slot = (p0 + i) % kBlock;
+    *reinterpret_cast<uint4*>(ring + slot * kDim + 8 * part) =
+        *reinterpret_cast<const uint4*>(keys + (int64_t)i * kDim + 8 * part);
   }
 }
 

@@ -776,6 +776,25 @@ qsa_status qsa_compress_keys(const void* raw, const int32_t* block_req, const in
   return launch_status();
 }
 
+qsa_status qsa_append_keys(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                           int32_t n_req, void* ring, const int32_t* page_table, int64_t ld_pt,
+                           int32_t page_size, double rope_base, void* pool, int64_t pool_rows, void* stream) {
+  if (n_req < 0 || pool_rows < 0 || ld_pt < 0) return QSA_ERR_INVALID_ARG;
+  if (n_req == 0) return QSA_OK;
+  if (n_req > INT32_MAX / 2) return QSA_ERR_UNSUPPORTED;
+  if (!req_tok_start || !req_first_pos || !ring || !page_table || !pool || page_size <= 0 ||
+      !(rope_base > 0.0) || !std::isfinite(rope_base))
+    return QSA_ERR_INVALID_ARG;
+  if (page_size % kBlock != 0) return QSA_ERR_UNSUPPORTED;
+  if (!aligned16(ring) || !aligned16(pool) || (new_keys && !aligned16(new_keys))) return QSA_ERR_INVALID_ARG;
+  AppendArgs a{static_cast<const __nv_bfloat16*>(new_keys), req_tok_start, req_first_pos, n_req,
+               static_cast<__nv_bfloat16*>(ring), page_table, ld_pt, page_size,
+               static_cast<__nv_bfloat16*>(pool), pool_rows};
+  const RopeTurns turns = rope_turns(rope_base);
+  append_keys_kernel<<<(unsigned)n_req, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(a, turns);
+  return launch_status();
+}
+
 qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
                             const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
                             int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,

@@ -149,3 +149,15 @@ def test_sparse_attn_rejects_bad_arguments(L):
     assert f(FAKE, FAKE, FAKE, 100, 1, 8, 1, 128, FAKE, 2051, 2051, c, FAKE, None, None, 0, None) == -3
     # no rows: nothing to do
     assert f(None, None, None, 0, 0, 8, 1, 128, None, 0, 0, c, None, None, None, 0, None) == 0
+
+
+def test_append_keys_rejects_bad_arguments(L):
+    f = L.qsa_append_keys
+    # page size not a multiple of 4; no ring; bad RoPE base
+    assert f(FAKE, FAKE, FAKE, 2, FAKE, FAKE, 4, 6, 10000.0, FAKE, 64, None) == -2
+    assert f(FAKE, FAKE, FAKE, 2, None, FAKE, 4, 64, 10000.0, FAKE, 64, None) == -1
+    assert f(FAKE, FAKE, FAKE, 2, FAKE, FAKE, 4, 64, 0.0, FAKE, 64, None) == -1
+    # misaligned ring
+    assert f(FAKE, FAKE, FAKE, 2, ctypes.c_void_p(0x1008), FAKE, 4, 64, 10000.0, FAKE, 64, None) == -1
+    # no requests: nothing to do
+    assert f(None, None, None, 0, None, None, 0, 64, 10000.0, None, 0, None) == 0

@@ -609,3 +609,74 @@ def test_sparse_attn_after_the_fused_indexer(qsa):
     v = normal_bf16(rng, (n_slots, h_kv, d))
     assert (slots[1] == -1).sum() > 0  # the short context is padded
     _attn_check(qsa, qa, k, v, slots, d ** -0.5)
+
+
+# ----------------------------------------------------------------- key path (ring)
+def _ring_case(seed, firsts, counts, P):
+    """Requests with raw keys for positions 0 .. first+count-1, the ring and
+    pool state after the first `first` positions (built by the oracle), and
+    the tokens of one more call."""
+    rng = np.random.default_rng(seed)
+    n_req = len(firsts)
+    ctx = [int(f + c) for f, c in zip(firsts, counts)]
+    raw = [normal_bf16(rng, (max(L, 1), 128)) for L in ctx]
+    pages = max(1, (max(ctx) + P - 1) // P)
+    pt = rng.permutation(n_req * pages).astype(np.int32).reshape(n_req, pages)
+    pool = np.zeros((n_req * pages * P // 4, 128), np.uint16)
+    ring = np.zeros((n_req, 4, 128), np.uint16)
+    for r in range(n_req):  # the context before the call, in one chunk per request
+        if firsts[r] == 0:
+            continue
+        rts = np.zeros(n_req + 1, np.int32)
+        rts[r + 1:] = firsts[r]
+        oracle.append_keys(raw[r][:firsts[r]], rts, np.zeros(n_req, np.int32), ring, pt, P, 10000.0, pool)
+    new = np.concatenate([raw[r][firsts[r]:firsts[r] + counts[r]] for r in range(n_req)] + [np.zeros((0, 128), np.uint16)])
+    rts = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return new, rts, np.array(firsts, np.int32), ring, pool, pt
+
+
+@pytest.mark.parametrize("P", [4, 16, 64])
+def test_append_keys_parity(qsa, P):
+    """One decode/verify call over requests with every first-position phase,
+    calls completing 0, 1 or 2 blocks, a request with no tokens, and a long
+    call (13 tokens, 3 blocks): the ring bit-exact, the pool within the
+    compressed-key bound of the oracle."""
+    import torch
+    firsts = [0, 1, 2, 3, 5, 6, 7, 8, 12, 400, 4093]
+    counts = [1, 6, 6, 6, 2, 6, 13, 0, 3, 6, 7]
+    new, rts, fp, ring, pool, pt = _ring_case(30 + P, firsts, counts, P)
+    g_ring = bf16_dev(ring).view(torch.bfloat16).reshape(ring.shape).contiguous()
+    g_pool = bf16_dev(pool).view(torch.bfloat16).reshape(pool.shape).contiguous()
+    qsa.append_keys(bf16_dev(new).reshape(-1, 128), to_dev(rts), to_dev(fp), g_ring, g_pool, to_dev(pt), P)
+    oracle.append_keys(new, rts, fp, ring, pt, P, 10000.0, pool)
+    assert np.array_equal(bf16_host(g_ring).reshape(ring.shape), ring)
+    got = bf16_host(g_pool)
+    a, b = oracle.bf16_to_float(got), oracle.bf16_to_float(pool)
+    bad = np.abs(a - b) > key_tolerance(a, b)
+    assert not bad.any(), np.argwhere(bad)[:5]
+    assert (got == pool).mean() > 0.99
+
+
+def test_append_keys_sequence_matches_direct_compression(qsa):
+    """A request built by 40 calls of 1-9 tokens on the GPU holds the same
+    pool as the compression of all its complete blocks at once."""
+    import torch
+    P, L = 16, 203
+    rng = np.random.default_rng(44)
+    raw = normal_bf16(rng, (L, 128))
+    pt = rng.permutation(16).astype(np.int32)[None]
+    g_pool = torch.zeros((16 * P // 4, 128), dtype=torch.bfloat16, device="cuda")
+    g_ring = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    g_raw = bf16_dev(raw)
+    p = 0
+    while p < L:
+        n = int(min(L - p, rng.integers(1, 10)))
+        qsa.append_keys(g_raw[p:p + n], to_dev(np.array([0, n], np.int32)), to_dev(np.array([p], np.int32)),
+                        g_ring, g_pool, to_dev(pt), P)
+        p += n
+    direct = torch.zeros_like(g_pool)
+    nb = L // 4
+    qsa.compress_keys(g_raw[:4 * nb], to_dev(np.arange(nb, dtype=np.int32)), direct,
+                      block_req=to_dev(np.zeros(nb, np.int32)), page_table=to_dev(pt), page_size=P)
+    assert torch.equal(g_pool, direct)
+    assert torch.equal(g_ring[0, (L - 1) % 4], g_raw[L - 1])
