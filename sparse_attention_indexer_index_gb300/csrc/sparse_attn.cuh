@@ -80,6 +80,25 @@ __device__ __forceinline__ void sa_load_row(const uint16_t* p, float (&x)[E]) {
   }
 }
 
+// E consecutive BF16 at p as E/2 FP32 pairs.
+template <int E>
+__device__ __forceinline__ void sa_load_row2(const uint16_t* p, float2 (&x)[E / 2]) {
+  float f[E];
+  sa_load_row<E>(p, f);
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
+}
+
+// Two FP32 fused multiply-adds in one instruction (each rounded as fmaf).
+__device__ __forceinline__ float2 sa_fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+
 // Butterfly reduce-scatter of 32 per-lane partial sums: afterwards x[0] of
 // lane l is the warp-wide sum of value l.
 __device__ __forceinline__ float sa_reduce_scatter32(float (&x)[32]) {
@@ -108,7 +127,7 @@ struct SaSmem {
 };
 
 template <int G, int D>
-__global__ void __launch_bounds__(kSaThreads)
+__global__ void __launch_bounds__(kSaThreads, 4)
 sparse_attn_kernel(SaArgs a) {
   constexpr int E = D / 32;   // elements of a row per lane
   constexpr int P = 32 / G;   // slots per warp step
@@ -129,37 +148,37 @@ sparse_attn_kernel(SaArgs a) {
     }
     sm.slot[j] = s;
   }
-  __syncthreads();
-  // every K and V row of the chunk requested into L2 at once (the loads
-  // below then wait on L2, not on HBM one row at a time)
-  {
-    constexpr int kLines = D * 2 / 128;  // 128-byte lines per row
-    for (int x = tid; x < n * kLines * 2; x += kSaThreads) {
-      const int j = x / (2 * kLines), r = x % (2 * kLines);
-      const int s = sm.slot[j];
-      if (s < 0) continue;
-      const uint16_t* base = (r < kLines ? a.k : a.v) + ((int64_t)s * a.h_kv + g) * D + (r % kLines) * 64;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(base));
-    }
-  }
   // this lane's part of the G query rows
-  float qv[G][E];
+  float2 qv[G][E / 2];
 #pragma unroll
   for (int h = 0; h < G; ++h)
-    sa_load_row<E>(a.q + ((int64_t)t * a.h_q + (int64_t)g * G + h) * D + lane * E, qv[h]);
+    sa_load_row2<E>(a.q + ((int64_t)t * a.h_q + (int64_t)g * G + h) * D + lane * E, qv[h]);
   __syncthreads();
 
   // ---- 1. logits ----------------------------------------------------------------
+  constexpr int kLines = D * 2 / 128;  // 128-byte lines of a row
+  constexpr int kAhead = 4;            // warp steps of rows requested into L2 ahead
+  // the K rows of this warp's step `jj` into L2 (P rows x kLines lines)
+  auto prefetch_rows = [&](const uint16_t* base, int jj, int rows) {
+    if (lane < rows * kLines) {
+      const int s = jj + lane / kLines < n ? sm.slot[jj + lane / kLines] : -1;
+      if (s >= 0)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + ((int64_t)s * a.h_kv + g) * D + (lane % kLines) * 64));
+    }
+  };
+  for (int d = 0; d < kAhead; ++d) prefetch_rows(a.k, warp * P + d * kSaWarps * P, P);
+  for (int d = 0; d < kAhead; ++d) prefetch_rows(a.v, warp * 4 + d * kSaWarps * 4, 4);
   for (int j = warp * P; j < n; j += kSaWarps * P) {
-    float kv[P][E];
+    prefetch_rows(a.k, j + kAhead * kSaWarps * P, P);
+    float2 kv[P][E / 2];
 #pragma unroll
     for (int i = 0; i < P; ++i) {
       const int s = j + i < n ? sm.slot[j + i] : -1;
       if (s >= 0) {
-        sa_load_row<E>(a.k + ((int64_t)s * a.h_kv + g) * D + lane * E, kv[i]);
+        sa_load_row2<E>(a.k + ((int64_t)s * a.h_kv + g) * D + lane * E, kv[i]);
       } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) kv[i][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) kv[i][e] = make_float2(0.f, 0.f);
       }
     }
     float x[32];
@@ -167,10 +186,10 @@ sparse_attn_kernel(SaArgs a) {
     for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int i = 0; i < P; ++i) {
-        float acc = 0.f;
+        float2 acc = make_float2(0.f, 0.f);  // even and odd elements
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(qv[h][e], kv[i][e], acc);
-        x[h * P + i] = acc;
+        for (int e = 0; e < E / 2; ++e) acc = sa_fma2(qv[h][e], kv[i][e], acc);
+        x[h * P + i] = acc.x + acc.y;
       }
     const float dot = sa_reduce_scatter32(x);
     const int h = lane / P, i = lane % P;
@@ -201,22 +220,23 @@ sparse_attn_kernel(SaArgs a) {
   __syncthreads();
 
   // ---- 3. weighted value sums ---------------------------------------------------
-  float acc[G][E];
+  float2 acc[G][E / 2];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+    for (int e = 0; e < E / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
   constexpr int U = 4;  // value rows in flight per warp
   for (int j = warp * U; j < n; j += kSaWarps * U) {
-    float vv[U][E];
+    prefetch_rows(a.v, j + kAhead * kSaWarps * U, U);
+    float2 vv[U][E / 2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int s = j + u < n ? sm.slot[j + u] : -1;  // the same for the whole warp
       if (s >= 0) {
-        sa_load_row<E>(a.v + ((int64_t)s * a.h_kv + g) * D + lane * E, vv[u]);
+        sa_load_row2<E>(a.v + ((int64_t)s * a.h_kv + g) * D + lane * E, vv[u]);
       } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) vv[u][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) vv[u][e] = make_float2(0.f, 0.f);
       }
     }
 #pragma unroll
@@ -225,15 +245,17 @@ sparse_attn_kernel(SaArgs a) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float wgt = sm.w[j + u][h];
+        const float2 w2 = make_float2(wgt, wgt);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wgt, vv[u][e], acc[h][e]);
+        for (int e = 0; e < E / 2; ++e) acc[h][e] = sa_fma2(w2, vv[u][e], acc[h][e]);
       }
     }
   }
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int e = 0; e < E; ++e) sm.red[warp][h][lane * E + e] = acc[h][e];
+    for (int e = 0; e < E / 2; ++e)
+      *reinterpret_cast<float2*>(&sm.red[warp][h][lane * E + 2 * e]) = acc[h][e];
   __syncthreads();
 
   // ---- 4. the chunk's result ------------------------------------------------------
