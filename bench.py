@@ -190,23 +190,30 @@ class Gpu:
         torch.cuda.synchronize()
         return graph.replay
 
-    def timed(self, fn, iters, warmup, flush=True, graph=True):
+    def timed(self, fn, iters, warmup, flush=True, graph=True, pre=None):
         """Per-iteration CUDA-event times (ms) with an L2 flush before each.
         With graph=True the step is replayed from a CUDA graph, so the events
-        see device time rather than Python launch overhead."""
+        see device time rather than Python launch overhead.  pre(), if given,
+        runs before every iteration outside the timed region (state resets)."""
         torch = self.torch
         for _ in range(warmup):
+            if pre is not None:
+                pre()
             if flush:
                 self.flush()
             fn()
         torch.cuda.synchronize()
         run = self.capture(fn) if graph else fn
         for _ in range(2):
+            if pre is not None:
+                pre()
             run()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(iters)]
         for s, e in ev:
+            if pre is not None:
+                pre()
             if flush:
                 self.flush()
             s.record(self.stream)
@@ -400,6 +407,7 @@ def setup_key_path(g, st):
     st["kp_rts"] = g.h2d(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
     st["kp_first"] = g.h2d(np.array(first, np.int32))
     st["kp_ring"] = g.bf16(ring)
+    st["kp_ring0"] = st["kp_ring"].clone()  # the ring before the step (restored between replays)
 
 
 def bf16_bits_of(x):
@@ -409,12 +417,25 @@ def bf16_bits_of(x):
 
 def append_only(g, st):
     """The key path alone (ring append + compression of the completed
-    blocks).  Replays repeat the same work; the ring then holds this
-    step's keys, so the values compressed from it differ after the first
-    replay (the timing does not depend on them)."""
+    blocks); restore_ring() puts the ring back between replays."""
     w = st["w"]
     g.qsa.append_keys(st["kp_keys"], st["kp_rts"], st["kp_first"], st["kp_ring"], st["pool"], st["pt"],
                       w.page_size, w.rope_base)
+
+
+def restore_ring(st):
+    st["kp_ring"].copy_(st["kp_ring0"])
+
+
+def decode_step_ring(g, st):
+    """One decode step in one call (qsa_decode_step): the rows' own tokens
+    appended through the ring (completing their blocks), then the fused
+    indexer; scorer CTAs that read no new block do not wait for the key
+    path."""
+    w = st["w"]
+    g.qsa.decode_step(st["kp_keys"], st["kp_rts"], st["kp_first"], st["kp_ring"], st["q"], st["pool"], st["rrs"],
+                      st["row_len"], st["pt"], w.page_size, w.max_len, w.max_rows_per_req, k_blk=w.k_blk,
+                      rope_base=w.rope_base, workspace=st["ws"], out_slots=st["slots"])
 
 
 def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
@@ -423,7 +444,8 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     t_score = g.timed(lambda: scores_only(g, st), iters, warmup)
     t_select = g.timed(lambda: select_only(g, st), iters, warmup)
     setup_key_path(g, st)
-    t_append = g.timed(lambda: append_only(g, st), iters, warmup)
+    t_append = g.timed(lambda: append_only(g, st), iters, warmup, pre=lambda: restore_ring(st))
+    t_dstep = g.timed(lambda: decode_step_ring(g, st), iters, warmup, pre=lambda: restore_ring(st))
     t_compress = g.timed(lambda: compress_only(g, st), iters, warmup) if new_blocks > 0 else None
     by = decode_bytes(w)
     alg = by["keys"] + by["q"] + by["page_table"] + by["slots"]
@@ -434,6 +456,7 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
            "alg_GBps": alg / (ms * 1e-3) / 1e9, "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
            "score_kernel_us": 1e3 * ms_sc, "select_kernel_us": 1e3 * statistics.mean(t_select),
            "key_path_append_us": 1e3 * statistics.mean(t_append),
+           "decode_step_one_call_us": 1e3 * statistics.mean(t_dstep),
            "compress_kernel_us": 1e3 * statistics.mean(t_compress) if t_compress else None,
            "kernels": kernel_names(w),
            "score_alg_GBps": (by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"]) /

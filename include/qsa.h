@@ -205,6 +205,27 @@ qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_
                             int32_t* out_pos, int32_t* out_slots, void* stream);
 
 /* ---------------------------------------------------------------------
+ * One decode step in one call: the key path (qsa_append_keys: new raw index
+ * keys into the rings, completed blocks compressed into the pool) followed
+ * by the fused indexer (qsa_indexer_select) on the updated pool.
+ *
+ * Arguments as the two calls.  The positions this step appends must be the
+ * rows' own tokens or earlier, i.e. the compressed blocks the scorer reads
+ * may include the ones completed here.  The scorer reads no pool row the key
+ * path writes before that write is done; scorer CTAs whose key range ends
+ * before block req_first_pos[r]/4 do not wait for the key path at all (the
+ * launch is ordered with programmatic dependent launch).  Results equal the
+ * two calls made one after the other.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_decode_step(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                           void* ring, double rope_base, const void* q, void* pool, int64_t pool_rows,
+                           int32_t n_req, const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                           int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                           int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                           int32_t* out_pos, int32_t* out_slots, float* scores_out, int64_t ld_scores,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------
  * IndexShare reuse of a kept selection  ([QSA], section "IndexShare MTP:
  * reusing the QSA selection across draft steps": the QSA selection computed
  * at the draft-extend pass over the tokens the target just accepted is kept

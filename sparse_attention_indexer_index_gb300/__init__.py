@@ -19,7 +19,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
-    "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn", "append_keys",
+    "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn", "append_keys", "decode_step",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -49,6 +49,8 @@ def lib():
             "qsa_device_status": (ctypes.c_int, [p, ctypes.c_int, p]),
             "qsa_compress_keys": (ctypes.c_int, [p, p, p, i64, i32, p, i64, i32, d, p, i64, p]),
             "qsa_append_keys": (ctypes.c_int, [p, p, p, i32, p, p, i64, i32, d, p, i64, p]),
+            "qsa_decode_step": (ctypes.c_int, [p, p, p, p, d, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
+                                               i32, p, p, p, p, i64, p, sz, p]),
             "qsa_index_scores": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
                                                 i64, i64, p]),
             "topk_select_workspace_size": (sz, [i32, i32, i32]),
@@ -161,6 +163,50 @@ def append_keys(new_keys, req_tok_start, req_first_pos, ring, pool, page_table, 
         _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), n_req, _ptr(ring), _ptr(page_table),
         page_table.shape[1], int(page_size), float(rope_base), _ptr(pool), pool.shape[0], _stream(stream)))
     return ring, pool
+
+
+def decode_step(new_keys, req_tok_start, req_first_pos, ring, q, pool, req_row_start, row_len, page_table,
+                page_size, max_len, max_rows_per_req=None, k_blk=512, rope_base=10000.0, want_blocks=False,
+                want_pos=False, out_slots=None, scores_out=None, workspace=None, stream=None):
+    """Key path (append_keys) then the fused indexer (indexer_select) in one
+    call; returns dict(slots, blocks?, pos?) like indexer_select."""
+    torch = _torch()
+    for t, nm in [(new_keys, "new_keys"), (q, "q"), (pool, "pool"), (ring, "ring")]:
+        _dev(t, torch.bfloat16, nm)
+    for t, nm in [(req_tok_start, "req_tok_start"), (req_first_pos, "req_first_pos"),
+                  (req_row_start, "req_row_start"), (row_len, "row_len"), (page_table, "page_table")]:
+        _dev(t, torch.int32, nm)
+    n_req = req_row_start.numel() - 1
+    if req_first_pos.numel() != n_req or req_tok_start.numel() != n_req + 1:
+        raise ValueError("req_first_pos / req_tok_start must describe the same requests as req_row_start")
+    n_rows = row_len.numel()
+    if max_rows_per_req is None:
+        max_rows_per_req = n_rows
+    dev = q.device
+    w = out_width(k_blk)
+    if out_slots is None:
+        out_slots = torch.empty((n_rows, w), dtype=torch.int32, device=dev)
+    blocks = torch.empty((n_rows, k_blk), dtype=torch.int32, device=dev) if want_blocks else None
+    pos = torch.empty((n_rows, w), dtype=torch.int32, device=dev) if want_pos else None
+    ld = 0
+    if scores_out is not None:
+        _dev(scores_out, torch.float32, "scores_out", 2)
+        ld = scores_out.shape[1]
+    elif workspace is None:
+        nbytes = indexer_select_workspace_size(n_rows, max_len, k_blk)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    _check("qsa_decode_step", lib().qsa_decode_step(
+        _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), _ptr(ring), float(rope_base), _ptr(q),
+        _ptr(pool), pool.shape[0], n_req, _ptr(req_row_start), n_rows, _ptr(row_len), int(max_len),
+        int(max_rows_per_req), _ptr(page_table), page_table.shape[1], int(page_size), int(k_blk), _ptr(blocks),
+        _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
+    out = {"slots": out_slots}
+    if blocks is not None:
+        out["blocks"] = blocks
+    if pos is not None:
+        out["pos"] = pos
+    return out
 
 
 def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len,

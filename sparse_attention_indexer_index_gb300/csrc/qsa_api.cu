@@ -512,6 +512,7 @@ qsa_status launch_scores_balanced(const ScoreArgs& s, int max_rows_per_req, int 
   while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
   t.tmem_cols = cols;
   t.trigger_dependents = s.trigger_dependents;
+  t.new_pos = s.new_pos;
   t.box_rows = R;
   t.box4d = 1;
   t.row_tiles = 1;
@@ -585,6 +586,7 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
   t.tmem_cols = cols;
   t.trigger_dependents = s.trigger_dependents;
+  t.new_pos = s.new_pos;
   const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
   const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
   if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
@@ -980,13 +982,18 @@ size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_
   return (size_t)(n_rows * ld * (int64_t)sizeof(float)) + 256;
 }
 
-qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
-                              const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
-                              int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
-                              int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
-                              int32_t* out_pos, int32_t* out_slots, float* scores_out,
-                              int64_t ld_scores, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+}  // extern "C"
+
+namespace {
+// The fused indexer call; new_pos: see TcArgs::new_pos (nullptr: the scorer
+// waits for the previous grid in full).
+qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                               const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                               int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                               int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                               int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                               int64_t ld_scores, void* workspace, size_t workspace_bytes,
+                               void* stream, const int32_t* new_pos) {
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
@@ -1012,7 +1019,7 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1};
+              page_size, scores, ld, 0, 1, new_pos};
   if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
     return e;
 
@@ -1035,6 +1042,47 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
   a.ld_pt = ld_pt;
   a.page_size = page_size;
   return launch_select<kModeQsa>(a, nb_max > 0, st, d->sm_count);
+}
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
+                              const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                              int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                              int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                              int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                              int64_t ld_scores, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return indexer_select_impl(q, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
+                             max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos,
+                             out_slots, scores_out, ld_scores, workspace, workspace_bytes, stream, nullptr);
+}
+
+qsa_status qsa_decode_step(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                           void* ring, double rope_base, const void* q, void* pool, int64_t pool_rows,
+                           int32_t n_req, const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                           int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
+                           int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
+                           int32_t* out_pos, int32_t* out_slots, float* scores_out, int64_t ld_scores,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows > 0) {
+    if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+    if (!q || !pool || !out_slots || pool_rows < 0 || !aligned16(q) || !aligned16(pool))
+      return QSA_ERR_INVALID_ARG;
+    if (!scores_out && workspace_bytes < qsa_indexer_select_workspace_size(n_rows, max_len, k_blk))
+      return QSA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (qsa_status st = qsa_append_keys(new_keys, req_tok_start, req_first_pos, n_req, ring, page_table, ld_pt,
+                                      page_size, rope_base, pool, pool_rows, stream))
+    return st;
+  if (n_rows == 0) return QSA_OK;
+  return indexer_select_impl(q, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
+                             max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos,
+                             out_slots, scores_out, ld_scores, workspace, workspace_bytes, stream,
+                             req_first_pos);
 }
 
 }  // extern "C"

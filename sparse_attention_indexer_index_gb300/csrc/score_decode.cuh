@@ -47,6 +47,7 @@ struct ScoreArgs {
   int64_t ld_scores;
   int64_t n_fill;
   int32_t trigger_dependents;   // let a dependent grid launch early (PDL)
+  const int32_t* new_pos;       // see TcArgs::new_pos (TMA scorers only; others wait in full)
 };
 
 constexpr int kScoreThreads = 256;

@@ -61,6 +61,11 @@ struct TcArgs {
   int32_t box4d;                // TMA kernel: 4-D view, one box per run covers both K-halves
   int32_t row_tiles;            // balanced kernel: row tiles per request
   int32_t n_groups;             // balanced kernel: n_req * row_tiles (<= kTbMaxGroups)
+  // TMA kernels: nullptr, or per request the first position the previous
+  // grid (the key path of the same step) may have written: only CTAs whose
+  // blocks reach block new_pos[r]/4 wait for that grid (and CTA 0, so that
+  // this grid still completes after it); the rest read the pool at once.
+  const int32_t* new_pos;
 };
 
 // ---------------------------------------------------------------------------
@@ -464,9 +469,18 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Launched with programmatic serialisation: nothing is read before the
-  // previous grid on the stream has finished, and the dependent selection
-  // may only start once that holds here.
-  pdl_wait_primary();
+  // previous grid on the stream has finished (with new_pos: nothing that
+  // grid writes), and the dependent selection may only start once that
+  // holds here.
+  const bool relaxed = a.new_pos != nullptr;
+  // relaxed: CTA 0 waits before it leaves, so that this grid completes after
+  // the previous one; the producer waits before its first tile that reaches
+  // a block the previous grid may write
+  const bool cta0 = (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
+  auto leave = [&]() {
+    if (relaxed && cta0) pdl_wait_primary();
+  };
+  if (!relaxed) pdl_wait_primary();
   if (a.trigger_dependents) pdl_launch_dependents();
   if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pool_map)) : "memory");
 
@@ -474,6 +488,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
   if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
+    leave();
     return;
   }
   if (row1 - row0 > (int)gridDim.y * a.rows_per_tile) {  // more rows than max_rows_per_req promised
@@ -481,7 +496,10 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   }
   const int t0 = row0 + blockIdx.y * a.rows_per_tile;
   const int t1 = min(row1, t0 + a.rows_per_tile);
-  if (t0 >= t1) return;
+  if (t0 >= t1) {
+    leave();
+    return;
+  }
   const int nrows = t1 - t0;
   if (threadIdx.x < nrows) {
     int L = __ldg(a.row_len + t0 + threadIdx.x);
@@ -494,8 +512,12 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   const int n_kt = (nb_tile + kTcM - 1) / kTcM;
   const int kt0 = blockIdx.x * a.tiles_per_cta;
   const int kt1 = min(n_kt, kt0 + a.tiles_per_cta);
-  if (kt0 >= kt1) return;
+  if (kt0 >= kt1) {
+    leave();
+    return;
+  }
   const int n_local = kt1 - kt0;
+  const int first_new = relaxed ? max(0, __ldg(a.new_pos + r)) / kBlock : 0;
 
   // ---- page-table entries of this CTA's key range, staged once ------------
   const int kpp = a.page_size / kBlock;
@@ -550,12 +572,17 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
     // ---- producer: one lane per run of box_rows pool rows ------------------
     const int R = a.box_rows;
     const int runs = kTcM / R;
+    bool waited = !relaxed;
     int i = 0;
     for (; i < n_local; ++i) {
       const int st = i % S;
       if (i >= S) {
         const bool ok = lane == 0 ? tm_wait(&empty[st], (uint32_t)((i / S) - 1) & 1u, abort) : true;
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      }
+      if (!waited && (int64_t)(kt0 + i + 1) * kTcM > first_new) {  // this tile may hold new keys
+        pdl_wait_primary();
+        waited = true;
       }
       const int b = (kt0 + i) * kTcM + lane * R;  // first block of this lane's run
       bool valid = false;
@@ -683,6 +710,7 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) leave();
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
@@ -752,7 +780,14 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
   const int kpp = a.page_size / kBlock;
   const int G = a.n_groups;
 
-  pdl_wait_primary();
+  const bool relaxed = a.new_pos != nullptr;  // see TcArgs::new_pos
+  // relaxed: CTA 0 waits before it leaves, so that this grid completes after
+  // the previous one; the producer waits before its first tile that reaches
+  // a block the previous grid may write
+  auto leave = [&]() {
+    if (relaxed && blockIdx.x == 0) pdl_wait_primary();
+  };
+  if (!relaxed) pdl_wait_primary();
   if (a.trigger_dependents) pdl_launch_dependents();
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pool_map)) : "memory");
@@ -803,7 +838,10 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
   }
   const int64_t T = g_pre[G];
   const int w0 = (int)(T * blockIdx.x / gridDim.x), w1 = (int)(T * (blockIdx.x + 1) / gridDim.x);
-  if (w0 >= w1) return;
+  if (w0 >= w1) {
+    leave();
+    return;
+  }
   const int n_items = w1 - w0;
   auto group_of = [&](int w, int& g) {  // advance the cursor g to the group holding item w
     while (g_pre[g + 1] <= w) ++g;
@@ -817,6 +855,7 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
     }
     g_first = lo;
   }
+
 
   // ---- barriers and tensor memory -----------------------------------------
   if (warp == 1) {
@@ -880,6 +919,7 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
     };
     for (int i = 0; i < kTbPtAhead; ++i) prefetch(i);
     int g = g_first;
+    bool waited = !relaxed;
     int i = 0;
     for (; i < n_items; ++i) {
       prefetch(i + kTbPtAhead);
@@ -893,6 +933,10 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
       const int w = w0 + i;
       group_of(w, g);
       const int kt = w - g_pre[g];
+      if (!waited && (int64_t)(kt + 1) * kTcM > max(0, __ldg(a.new_pos + g / a.row_tiles)) / kBlock) {
+        pdl_wait_primary();  // this tile may hold keys the previous grid writes
+        waited = true;
+      }
       const int nb_tile = g_nb[g];
       const int b = kt * kTcM + lane * R;  // first block of this lane's run
       bool valid = false;
@@ -1036,6 +1080,7 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) leave();
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)

@@ -680,3 +680,62 @@ def test_append_keys_sequence_matches_direct_compression(qsa):
                       block_req=to_dev(np.zeros(nb, np.int32)), page_table=to_dev(pt), page_size=P)
     assert torch.equal(g_pool, direct)
     assert torch.equal(g_ring[0, (L - 1) % 4], g_raw[L - 1])
+
+
+# ----------------------------------------------------------------- decode step
+@pytest.mark.parametrize("case", ["verify_6rows", "batched_one_row", "multi_request_small_pages"])
+def test_decode_step_equals_append_then_indexer(qsa, case):
+    """qsa_decode_step (key path, then the fused indexer, the scorer CTAs
+    that read no new block not waiting for the key path) gives the same pool,
+    ring and slots as the two calls made one after the other."""
+    import torch
+    if case == "verify_6rows":
+        rows, P = [[20_000 - 5 + i for i in range(6)]], 64
+    elif case == "batched_one_row":
+        rows, P = [[5003], [12_000], [777], [30_001]], 64
+    else:
+        rows, P = [[4099, 4100, 4101], [9], [2051, 2052]], 16
+    rng = np.random.default_rng(81)
+    w = decode_workload(82, rows, page_size=P, k_blk=512)
+    n_req = w.n_req
+    firsts = np.array([min(r) - 1 for r in rows], np.int32)          # each row's own token is appended
+    counts = np.array([len(r) for r in rows], np.int32)
+    ctx = [int(f + c) for f, c in zip(firsts, counts)]
+    raw = [normal_bf16(rng, (L, 128)) for L in ctx]
+    # state before the step: blocks completed before first, ring with the rest
+    ring0 = np.zeros((n_req, 4, 128), np.uint16)
+    blocks_before, reqs_before, raws_before = [], [], []
+    for r in range(n_req):
+        nb0 = int(firsts[r]) // 4
+        blocks_before.append(np.arange(nb0, dtype=np.int32))
+        reqs_before.append(np.full(nb0, r, np.int32))
+        raws_before.append(raw[r][:4 * nb0])
+        for p in range(4 * nb0, int(firsts[r])):
+            ring0[r, p % 4] = raw[r][p]
+    pool0 = torch.zeros((w.pool_rows, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(bf16_dev(np.concatenate(raws_before)), to_dev(np.concatenate(blocks_before)), pool0,
+                      block_req=to_dev(np.concatenate(reqs_before)), page_table=to_dev(w.page_table), page_size=P)
+    new = np.concatenate([raw[r][firsts[r]:] for r in range(n_req)])
+    rts = to_dev(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+    fp, pt = to_dev(firsts), to_dev(w.page_table)
+    q, rrs, rl = bf16_dev(w.q), to_dev(w.req_row_start), to_dev(w.row_len)
+    # the two calls
+    ring_a, pool_a = bf16_dev(ring0), pool0.clone()
+    qsa.append_keys(bf16_dev(new), rts, fp, ring_a, pool_a, pt, P)
+    out_a = qsa.indexer_select(q, pool_a, rrs, rl, pt, P, w.max_len, w.max_rows_per_req, k_blk=512,
+                               want_blocks=True, want_pos=True)
+    # one call
+    ring_b, pool_b = bf16_dev(ring0), pool0.clone()
+    out_b = qsa.decode_step(bf16_dev(new), rts, fp, ring_b, q, pool_b, rrs, rl, pt, P, w.max_len,
+                            w.max_rows_per_req, k_blk=512, want_blocks=True, want_pos=True)
+    assert torch.equal(ring_a, ring_b) and torch.equal(pool_a, pool_b)
+    for key in ("slots", "blocks", "pos"):
+        assert torch.equal(out_a[key], out_b[key]), key
+    # and the step's selection is the oracle's on the GPU scores of the updated pool
+    pool_h = bf16_host(pool_b)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    qsa.indexer_select(q, pool_b, rrs, rl, pt, P, w.max_len, w.max_rows_per_req, k_blk=512, scores_out=scores)
+    sel_ref, _ = oracle.topk(scores.cpu().numpy(), 512, n_valid=w.row_len // 4)
+    assert np.array_equal(out_b["blocks"].cpu().numpy(), sel_ref)
+    assert pool_h.shape[0] == w.pool_rows
