@@ -293,7 +293,8 @@ def kernel_names(w, sm_count=152):
     TMA when a page holds a multiple of 8 compressed keys; one-row requests
     use the balanced tensor-core scorer on such pages; rows of up to
     32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
-    shared-memory-resident single-CTA selection otherwise; longer rows a
+    shared-memory-resident single-CTA selection up to two rows per SM and
+    small CTAs (three per SM) for more rows; longer rows a
     cluster of 2-16 CTAs per row when rows * 2 <= SMs, one streaming CTA per
     row otherwise)."""
     tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0
@@ -308,6 +309,8 @@ def kernel_names(w, sm_count=152):
         select = "select_long_kernel" if w.n_rows * 2 <= sm_count else "select_kernel"
     elif w.n_rows * 8 <= sm_count:
         select = "select_cluster_kernel"
+    elif w.n_rows > 2 * sm_count:
+        select = "select_rows_kernel"
     else:
         select = "select_resident_kernel"
     return {"compress": "compress_keys_kernel", "score": score, "select": select}
@@ -469,7 +472,9 @@ def topk_kernel_name(n_rows, n, sm_count=152):
     """The selection kernel topk_select runs for n_rows rows of n scores."""
     if n > 32768:
         return "select_long_kernel" if n_rows * 2 <= sm_count else "select_kernel"
-    return "select_cluster_kernel" if n_rows * 8 <= sm_count else "select_resident_kernel"
+    if n_rows * 8 <= sm_count:
+        return "select_cluster_kernel"
+    return "select_rows_kernel" if n_rows > 2 * sm_count else "select_resident_kernel"
 
 
 def bench_variant_topk(g, w, iters, warmup, peaks):
@@ -540,6 +545,8 @@ def bench_variant_prefill(g, w, iters, warmup, peaks):
                                              w.page_size, w.max_len, w.max_rows_per_req, k_blk=w.k_blk,
                                              workspace=st["ws"], out_slots=st["slots"]),
                 iters, warmup)
+    t_score = g.timed(lambda: scores_only(g, st), max(2, iters), warmup)
+    t_select = g.timed(lambda: select_only(g, st), max(2, iters), warmup)
     ms = statistics.mean(t)
     pairs = int(sum(int(L) // 4 for L in w.row_len))
     flop = 2 * 4 * 128 * pairs
@@ -547,7 +554,9 @@ def bench_variant_prefill(g, w, iters, warmup, peaks):
             "rows_per_s": w.n_rows / (ms * 1e-3), "flop": flop,
             "TFLOPs": flop / (ms * 1e-3) / 1e12,
             "frac_tensor": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
-            "path": "tensor-core scorer (tcgen05 MMA, TMA-fed key tiles) + resident-row selection"}
+            "score_kernel_us": 1e3 * statistics.mean(t_score), "select_kernel_us": 1e3 * statistics.mean(t_select),
+            "score_TFLOPs": flop / (statistics.mean(t_score) * 1e-3) / 1e12,
+            "path": "tensor-core scorer (tcgen05 MMA, TMA-fed key tiles) + small-CTA row selection"}
 
 
 def cpu_oracle_rate(w, budget_s=10.0):

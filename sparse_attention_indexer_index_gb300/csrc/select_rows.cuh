@@ -1,0 +1,422 @@
+// select_rows.cuh -- exact top-k of many rows of up to 32768 entries: one
+// small CTA per row, three per SM, so that launches with more rows than SMs
+// (a batch of verify steps, a prefill chunk of thousands of rows) run in few
+// waves and the rows stream at HBM rate instead of one row per SM.
+//
+// Same contract as select_kernel (SGLang GLM-5.2 blog, "Kernel Optimization /
+// TopK-V2": a selection, not a sort; exactly k entries, exact ties, runtime k
+// up to 2048; the page-table transform in the same kernel.  Qwen3.8-Flash-Next
+// write-up, "Qwen sparse attention (QSA)": blocks -> 4 positions each, then
+// the 0-3 pending tokens; -1 marks an empty entry).  Readings: ties go to the
+// lower index; -0 == +0; NaN ranks below -inf; ascending index order.
+//
+// Design (the single-CTA form of select_long_kernel's list path).  256
+// threads; warp w owns a contiguous segment of the row, walked 128 entries
+// at a time (4 consecutive per lane) with 16-byte loads, 4 in flight.  The
+// row's page-table entries are loaded at the start and kept in shared memory
+// for the outputs.
+//  1. Sampled bound: 1024 entries in 32 runs of 32 (one 16-byte load per
+//     thread); the edge of the top-12-bit bin below which the r-th largest
+//     sample lies, r about twice the expected number of samples above the
+//     k-th entry.
+//  2. One pass over the row: each warp lists its entries at or above the
+//     bound (key, index) in its own region of a shared-memory list, with
+//     ballot counts.  A warp whose region fills up makes the CTA walk the
+//     whole row in the steps below instead of the list.
+//  3. Radix levels of 12, 12 and 8 bits over the list (or the row) in a
+//     shared-memory histogram, until a bin is taken whole or the key is
+//     complete.  Fewer than k entries above the bound (the sample misled):
+//     level 0 again over every entry of the row.
+//  4. Two bitmaps of the row (entries above the k-th key's bin, entries in
+//     it) and prefix counts of their words give the first `need` entries of
+//     the bin and every winner's ascending output position; the outputs are
+//     written by all threads.
+// Every wait is a CTA barrier; no global scratch.
+#pragma once
+#include <type_traits>
+
+#include "select_long.cuh"
+
+namespace qsa {
+
+constexpr int kSrThreads = 256;
+constexpr int kSrWarps = kSrThreads / 32;
+constexpr int kSrMaxRow = 32768;
+constexpr int kSrBins = 4096;
+constexpr int kSrCandCap = 4096;                 // list entries per CTA (per warp: / kSrWarps)
+constexpr int kSrWords = kSrMaxRow / 32;         // bitmap words
+constexpr int kSrUnroll = 4;
+constexpr int kSrPt = 2048;                      // page-table entries staged for the outputs
+
+struct SrSmem {
+  uint32_t hist[kSrBins];
+  uint32_t cand_key[kSrCandCap];
+  uint32_t cand_idx[kSrCandCap];
+  uint32_t bm_eq[kSrWords];
+  uint32_t bm_win[kSrWords];
+  uint32_t pre_eq[kSrWords];
+  uint32_t pre_win[kSrWords];
+  int32_t pt[kSrPt];
+  uint32_t wsum[kSrWarps];
+  int info[4];
+  uint32_t n_eq;
+  int ovf;
+};
+
+__device__ __forceinline__ uint32_t sr_block_excl_scan(SrSmem& sm, uint32_t x, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = sl_warp_incl_scan(x);
+  if (lane == 31) sm.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0u, tot = 0u;
+#pragma unroll
+  for (int w = 0; w < kSrWarps; ++w) {
+    const uint32_t v = sm.wsum[w];
+    before += w < warp ? v : 0u;
+    tot += v;
+  }
+  total = tot;
+  __syncthreads();
+  return before + incl - x;
+}
+
+// (bin, entries in higher bins, entries in the bin, total) of the k_rem-th
+// largest entry of sm.hist; the first three are 0 when k_rem > total.
+__device__ __forceinline__ int4 sr_find_bin(SrSmem& sm, int k_rem) {
+  constexpr int kPer = kSrBins / kSrThreads;  // 16
+  const int top = kSrBins - 1 - kPer * (int)threadIdx.x;
+  uint32_t c[kPer];
+  uint32_t s = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    c[j] = sm.hist[top - j];
+    s += c[j];
+  }
+  if (threadIdx.x < 3) sm.info[threadIdx.x] = 0;
+  uint32_t tot;
+  uint32_t above = sr_block_excl_scan(sm, s, tot);
+  const uint32_t kr = (uint32_t)k_rem;
+  if (above < kr && kr <= above + s) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (above < kr && kr <= above + c[j]) {
+        sm.info[0] = top - j;
+        sm.info[1] = (int)above;
+        sm.info[2] = (int)c[j];
+      }
+      above += c[j];
+    }
+  }
+  __syncthreads();
+  const int4 r = make_int4(sm.info[0], sm.info[1], sm.info[2], (int)tot);
+  __syncthreads();
+  return r;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kSrThreads, 3)
+select_rows_kernel(SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char sr_smem_raw[];
+  SrSmem& sm = *reinterpret_cast<SrSmem*>(sr_smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x;
+
+  // ---- row metadata (not produced by the previous grid) ---------------------------
+  int n, L = 0;
+  const int32_t* pt_row = nullptr;
+  if (kMode == kModeTopk) {
+    n = a.n_valid ? __ldg(a.n_valid + t) : a.n_max;
+    if (a.out_slots != nullptr)
+      pt_row = a.page_table + (int64_t)(a.row_req ? __ldg(a.row_req + t) : t) * a.ld_pt;
+  } else {
+    const int req = row_request(a.req_row_start, a.n_req, t);
+    L = __ldg(a.row_len + t);
+    n = L / kBlock;
+    pt_row = a.page_table + (int64_t)req * a.ld_pt;
+  }
+  if (n < 0 || n > a.n_max || n > kSrMaxRow || L < 0) {  // bad length: emit an empty row
+    if (tid == 0) raise_fault(kFaultGrouping);
+    n = 0;
+    L = 0;
+  }
+  for (int i = tid; i < kSrBins; i += kSrThreads) sm.hist[i] = 0u;
+  if (tid == 0) sm.ovf = 0;
+  // the page-table entries of the row's positions, for the outputs (loads
+  // issued now, stored to shared memory once the first pass is done)
+  int pt_n = 0;
+  if (pt_row != nullptr) {
+    const int64_t last = kMode == kModeQsa ? (int64_t)L : (int64_t)n;  // positions < last
+    int64_t np = last > 0 ? (last - 1) / a.page_size + 1 : 0;
+    np = min(np, (int64_t)kSrPt);
+    np = min(np, a.ld_pt);
+    pt_n = (int)np;
+  }
+  int32_t ptv[kSrPt / kSrThreads];
+#pragma unroll
+  for (int u = 0; u < kSrPt / kSrThreads; ++u) {
+    const int i = tid + kSrThreads * u;
+    ptv[u] = i < pt_n ? __ldg(pt_row + i) : 0;
+  }
+  if (a.wait_primary) pdl_wait_primary();
+  const float* row = a.scores + (int64_t)t * a.ld;
+  const int k = a.k;
+  const int m_sel = n < k ? n : k;
+  const bool vec = a.vec_ok != 0;
+
+  auto slot = [&](uint32_t pos) -> int32_t {  // staged entries, else global
+    const uint32_t ps = (uint32_t)a.page_size;
+    const uint32_t page_idx = pos / ps;
+    if ((int)page_idx < pt_n) return sm.pt[page_idx] * a.page_size + (int32_t)(pos - page_idx * ps);
+    return sl_slot(a, pt_row, pos);
+  };
+  auto emit = [&](uint32_t idx, int pos) {
+    if (kMode == kModeTopk) {
+      a.out_idx[(int64_t)t * k + pos] = (int32_t)idx;
+      if (a.out_slots != nullptr) a.out_slots[(int64_t)t * k + pos] = slot(idx);
+    } else {
+      if (a.out_idx != nullptr) a.out_idx[(int64_t)t * k + pos] = (int32_t)idx;
+      const int64_t width = (int64_t)kBlock * k + (kBlock - 1);
+      const uint32_t p0 = kBlock * idx;  // 4 positions in one page
+      const int32_t base = slot(p0);
+      int32_t* xs = a.out_xslots + (int64_t)t * width + kBlock * pos;
+#pragma unroll
+      for (int c = 0; c < kBlock; ++c) xs[c] = base < 0 ? -1 : base + c;
+      if (a.out_pos != nullptr) {
+        int32_t* xp = a.out_pos + (int64_t)t * width + kBlock * pos;
+#pragma unroll
+        for (int c = 0; c < kBlock; ++c) xp[c] = (int32_t)p0 + c;
+      }
+    }
+  };
+
+#pragma unroll
+  for (int u = 0; u < kSrPt / kSrThreads; ++u) {
+    const int i = tid + kSrThreads * u;
+    if (i < pt_n) sm.pt[i] = ptv[u];
+  }
+  __syncthreads();
+  // ---- the tail after m_sel entries ----------------------------------------------
+  if (kMode == kModeTopk) {
+    for (int j = m_sel + tid; j < k; j += kSrThreads) {
+      a.out_idx[(int64_t)t * k + j] = -1;
+      if (a.out_slots != nullptr) a.out_slots[(int64_t)t * k + j] = -1;
+    }
+  } else {
+    if (a.out_idx != nullptr)
+      for (int j = m_sel + tid; j < k; j += kSrThreads) a.out_idx[(int64_t)t * k + j] = -1;
+    const int width = kBlock * k + (kBlock - 1);
+    const int pend = L - kBlock * n;
+    for (int j = kBlock * m_sel + tid; j < width; j += kSrThreads) {
+      const int i = j - kBlock * m_sel;
+      int32_t pos = -1, sl = -1;
+      if (i < pend) {
+        pos = kBlock * n + i;
+        sl = slot((uint32_t)pos);
+      }
+      a.out_xslots[(int64_t)t * width + j] = sl;
+      if (a.out_pos != nullptr) a.out_pos[(int64_t)t * width + j] = pos;
+    }
+  }
+  if (n <= k) {  // every entry is selected, in order
+    for (int j = tid; j < m_sel; j += kSrThreads) emit(j, j);
+    return;
+  }
+
+  // ---- warp segments and the row walk ---------------------------------------------
+  const int seg = (((n + kSrWarps - 1) / kSrWarps) + 127) & ~127;
+  const int w0 = min(n, warp * seg);
+  const int w1 = min(n, w0 + seg);
+  // f(i, v, full) on every 128-entry chunk of this warp's segment (lane:
+  // entries i..i+3; full: the chunk lies before w1, else f masks)
+  auto walk = [&](auto&& f) {
+    for (int c0 = w0; c0 < w1; c0 += 128 * kSrUnroll) {
+      float4 v[kSrUnroll];
+#pragma unroll
+      for (int u = 0; u < kSrUnroll; ++u) v[u] = sl_load4(row, c0 + 128 * u + 4 * lane, w1, vec);
+#pragma unroll
+      for (int u = 0; u < kSrUnroll; ++u) f(c0 + 128 * u + 4 * lane, v[u], std::false_type{});
+    }
+  };
+
+  // ---- 1. sampled bound -------------------------------------------------------------
+  uint64_t k_low = 0ull;
+  {
+    const int64_t r = 2 * (((int64_t)1024 * k + n - 1) / n) + 8;
+    if (r < 1024) {
+      const int run = tid >> 3;  // 32 runs of 32
+      const int p = (int)((((int64_t)run * n) / 32) & ~int64_t(3)) + 4 * (tid & 7);
+      const float4 v = sl_load4(row, p, n, vec);
+      const bool ok0 = p < n, ok1 = p + 1 < n, ok2 = p + 2 < n, ok3 = p + 3 < n;
+      __syncthreads();  // the histogram is cleared
+      if (ok0) atomicAdd(&sm.hist[order_key(v.x) >> 20], 1u);
+      if (ok1) atomicAdd(&sm.hist[order_key(v.y) >> 20], 1u);
+      if (ok2) atomicAdd(&sm.hist[order_key(v.z) >> 20], 1u);
+      if (ok3) atomicAdd(&sm.hist[order_key(v.w) >> 20], 1u);
+      __syncthreads();
+      const int4 f = sr_find_bin(sm, (int)r);
+      k_low = (uint64_t)f.x << 20;
+      for (int b = tid; b < kSrBins; b += kSrThreads) sm.hist[b] = 0u;
+    }
+  }
+  __syncthreads();
+  const SlBound low = sl_bound(k_low);
+
+  // ---- 2. one pass: each warp lists its entries at or above the bound ----------------
+  constexpr int kCw = kSrCandCap / kSrWarps;
+  uint32_t* ckey = sm.cand_key + warp * kCw;
+  uint32_t* cidx = sm.cand_idx + warp * kCw;
+  uint32_t wn = 0u;  // the same in every lane of the warp
+  walk([&](int i, float4 v, auto) {
+    const float xv[4] = {v.x, v.y, v.z, v.w};
+    bool c[4], any = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      c[e] = low.ge(xv[e]) & (i + e < w1);
+      any |= c[e];
+    }
+    if (__ballot_sync(0xffffffffu, any) == 0u) return;
+    uint32_t tot = 0u, before = 0u;
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = __ballot_sync(0xffffffffu, c[e]);
+      tot += __popc(m);
+      before += __popc(m & lt);
+    }
+    if (wn + tot > (uint32_t)kCw) {
+      wn = kCw + 1;  // overflowed (stays so)
+      return;
+    }
+    uint32_t o = wn + before;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (c[e]) {
+        ckey[o] = order_key(xv[e]);
+        cidx[o] = (uint32_t)(i + e);
+        ++o;
+      }
+    }
+    wn += tot;
+  });
+  if (lane == 0 && wn > (uint32_t)kCw) sm.ovf = 1;
+  __syncthreads();
+  bool use_list = sm.ovf == 0;
+
+  // ---- 3. radix levels ------------------------------------------------------------------
+  uint32_t prefix = 0u;  // the k-th key's bits above `shift`
+  int shift = 32, k_rem = k, lv = 0;
+  SlBound lo = low, hi = sl_bound(1ull << 32);
+  for (;;) {
+    const int nb = lv < 2 ? 12 : 8;
+    const int nshift = shift - nb;
+    const uint32_t mask = (1u << nb) - 1u;
+    if (use_list) {
+      for (int j = lane; j < (int)wn; j += 32) {
+        const uint32_t key = ckey[j];
+        if (lv == 0 || (key >> shift) == prefix) atomicAdd(&sm.hist[(key >> nshift) & mask], 1u);
+      }
+    } else {
+      walk([&](int i, float4 v, auto) {
+        if (!lo.all && !(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= lo.f)) return;
+        const float xv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool in = lo.ge(xv[e]) & !hi.ge(xv[e]) & (i + e < w1);
+          if (in) atomicAdd(&sm.hist[(order_key(xv[e]) >> nshift) & mask], 1u);
+        }
+      });
+    }
+    __syncthreads();
+    const int4 f = sr_find_bin(sm, k_rem);  // its barriers order the clear below
+    for (int b = tid; b < kSrBins; b += kSrThreads) sm.hist[b] = 0u;
+    if (lv == 0 && f.w < k_rem) {  // the sampled bound misled: every entry of the row
+      lo = sl_bound(0ull);
+      use_list = false;
+      __syncthreads();
+      continue;
+    }
+    prefix = shift == 32 ? (uint32_t)f.x : ((prefix << nb) | (uint32_t)f.x);
+    shift = nshift;
+    k_rem -= f.y;
+    __syncthreads();
+    if (f.z == k_rem || lv == 2) break;
+    ++lv;
+    lo = sl_bound((uint64_t)prefix << shift);
+    hi = sl_bound((uint64_t)(prefix + 1) << shift);
+  }
+  const uint32_t need = (uint32_t)k_rem;  // entries of the boundary bin to take, first by index
+  lo = sl_bound((uint64_t)prefix << shift);
+
+  // ---- 4. ranks from bitmaps of the row, outputs ----------------------------------------
+  for (int b = tid; b < kSrWords; b += kSrThreads) {
+    sm.bm_eq[b] = 0u;
+    sm.bm_win[b] = 0u;
+  }
+  __syncthreads();
+  auto mark = [&](uint32_t key, uint32_t idx) {
+    const uint32_t hb = key >> shift;
+    if (hb > prefix) atomicOr(&sm.bm_win[idx >> 5], 1u << (idx & 31));
+    else if (hb == prefix) atomicOr(&sm.bm_eq[idx >> 5], 1u << (idx & 31));
+  };
+  if (use_list) {
+    for (int j = lane; j < (int)wn; j += 32) mark(ckey[j], cidx[j]);
+  } else {
+    walk([&](int i, float4 v, auto) {
+      if (!lo.all && !(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= lo.f)) return;
+      const float xv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (lo.ge(xv[e]) & (i + e < w1)) mark(order_key(xv[e]), (uint32_t)(i + e));
+    });
+  }
+  __syncthreads();
+  // prefix counts of set bits per word (kSrWords / kSrThreads words per thread)
+  constexpr int kWpt = kSrWords / kSrThreads;
+  auto word_scan = [&](const uint32_t* bm, uint32_t* pre) {
+    uint32_t c[kWpt], sum = 0u;
+#pragma unroll
+    for (int u = 0; u < kWpt; ++u) {
+      c[u] = __popc(bm[kWpt * tid + u]);
+      sum += c[u];
+    }
+    uint32_t tot;
+    uint32_t x = sr_block_excl_scan(sm, sum, tot);
+#pragma unroll
+    for (int u = 0; u < kWpt; ++u) {
+      pre[kWpt * tid + u] = x;
+      x += c[u];
+    }
+  };
+  word_scan(sm.bm_eq, sm.pre_eq);
+  __syncthreads();
+  // the first `need` entries of the bin become winners
+#pragma unroll
+  for (int u = 0; u < kWpt; ++u) {
+    const int w = kWpt * tid + u;
+    uint32_t bits = sm.bm_eq[w];
+    uint32_t r = sm.pre_eq[w];
+    while (bits != 0u && r < need) {
+      const uint32_t b = bits & (0u - bits);
+      atomicOr(&sm.bm_win[w], b);
+      bits ^= b;
+      ++r;
+    }
+  }
+  __syncthreads();
+  word_scan(sm.bm_win, sm.pre_win);
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kWpt; ++u) {
+    const int w = kWpt * tid + u;
+    uint32_t bits = sm.bm_win[w];
+    uint32_t pos = sm.pre_win[w];
+    while (bits != 0u) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      emit((uint32_t)(32 * w + b), (int)pos);
+      ++pos;
+    }
+  }
+}
+
+}  // namespace qsa

@@ -91,3 +91,5 @@ def test_long_rows_take_the_cluster_selection():
     assert bench.topk_kernel_name(100, 80_000) == "select_kernel"
     assert bench.topk_kernel_name(6, 20_000) == "select_cluster_kernel"
     assert bench.topk_kernel_name(64, 20_000) == "select_resident_kernel"
+    assert bench.topk_kernel_name(200, 20_000) == "select_resident_kernel"
+    assert bench.topk_kernel_name(400, 20_000) == "select_rows_kernel"

@@ -134,7 +134,7 @@ def test_topk_parity_ragged(qsa, dist, k):
     run_topk(qsa, topk_workload(31, 9, 6000, k=k, dist=dist, ragged=True), k)
 
 
-@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (40, 20_000), (200, 3000),
+@pytest.mark.parametrize("n_rows,n", [(1, 100_000), (3, 50_000), (40, 33_000), (40, 20_000), (200, 3000), (400, 3000),
                                       (5, 32_768), (2, 32_772)])
 def test_topk_parity_row_lengths(qsa, n_rows, n):
     """Rows kept in shared memory (<= 32,768 scores) and rows streamed through
@@ -191,6 +191,41 @@ def test_topk_hard_rows_many_rows(qsa, n, copies):
     base[3, (np.arange(1024, dtype=np.int64) * n) // 1024] = 100.0
     s = np.concatenate([base] * copies + [rng.standard_normal((4, n)).astype(np.float32)])
     nv = np.full(s.shape[0], n, np.int32)
+    for k in [512, 2048]:
+        idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+        ref, _ = oracle.topk(s, k, n_valid=nv)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
+@pytest.mark.parametrize("n", [3000, 20_000, 32_768])
+def test_topk_many_rows_small_ctas(qsa, n):
+    """More than two rows per SM (one small CTA per row, three per SM): ordinary
+    rows, rows with every entry equal (the candidate lists overflow: whole-row
+    walks), three values, one top-bits bin, and rows whose sampled entries
+    (32 runs of 32) hold the largest values (too few entries above the
+    sampled bound: the level-0 histogram is redone over the row)."""
+    rng = np.random.default_rng(n + 3)
+    rows = []
+    for r in range(320):
+        kind = r % 5
+        if kind == 0:
+            x = np.full(n, 1.5, np.float32)
+        elif kind == 1:
+            x = rng.integers(0, 3, size=n).astype(np.float32)
+        elif kind == 2:
+            x = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)
+        elif kind == 3:
+            x = (rng.standard_normal(n) * 0.01).astype(np.float32)
+            for run in range(32):
+                p = ((run * n) // 32) & ~3
+                x[p:p + 32] = 100.0 + rng.standard_normal(min(32, n - p)).astype(np.float32)
+        else:
+            x = rng.standard_normal(n).astype(np.float32)
+        rows.append(x)
+    s = np.stack(rows)
+    nv = np.full(s.shape[0], n, np.int32)
+    nv[7] = 100      # fewer entries than k
+    nv[11] = n - 3   # ragged tail
     for k in [512, 2048]:
         idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
         ref, _ = oracle.topk(s, k, n_valid=nv)
