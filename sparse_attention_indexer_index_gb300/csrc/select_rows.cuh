@@ -59,7 +59,6 @@ struct SrSmem {
   int32_t pt[kSrPt];
   uint32_t wsum[kSrWarps];
   int info[4];
-  uint32_t n_eq;
   int ovf;
 };
 

@@ -24,8 +24,9 @@
 //     which lane l holds the logit of (head l / P, slot l % P).
 //  2. Per head: chunk maximum m and weights exp(logit - m), sum l.
 //  3. Values: each warp accumulates sum_j w_hj v_j for its slots (weights
-//     broadcast from shared memory), the 4 warps' sums are added in shared
-//     memory.  One chunk: the CTA normalises and writes out and lse;
+//     broadcast from shared memory; packed fma.rn.f32x2), the 4 warps' sums
+//     are added in shared memory.  Every warp requests the K (then V) rows
+//     of its next 4 steps into L2 ahead of its loads.  One chunk: the CTA normalises and writes out and lse;
 //     several: it writes (m, l, unnormalised sum) and a second kernel merges
 //     the chunks of every (row, head).
 #pragma once
@@ -54,9 +55,6 @@ struct SaArgs {
   float* lse;               // [rows][h_q] or nullptr
   float* part;              // n_split > 1: [rows][h_q][n_split][D + 2] (m, l, sum)
 };
-
-// BF16 bits -> FP32 (exact).
-__device__ __forceinline__ float sa_bf16(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // E consecutive BF16 (E = 4 or 8) at p (aligned to 2E bytes) -> FP32.
 template <int E>
