@@ -19,11 +19,11 @@
 //     chosen bin: all CTAs get the same 22-bit threshold t_s, which about
 //     1.5k entries of the row reach (no communication).
 //  2. Each CTA counts its candidates (key >= t_s, a float compare against the
-//     float image of t_s) and writes the count into the leader CTA's shared
-//     memory; after a cluster barrier every CTA knows its offset and writes
-//     its candidates (key, index) straight into the leader's list, in index
-//     order, with its largest candidate key; after a second cluster barrier
-//     the other CTAs are done.
+//     float image of t_s) and writes the count and its largest key into the
+//     leader CTA's shared memory; after a cluster barrier every CTA knows its
+//     offset and writes its candidates (key, index) straight into the
+//     leader's list, in index order; after a second cluster barrier the
+//     other CTAs are done.
 //  3. Leader: if the list holds at least k entries (it then holds all of the
 //     top k), radix passes over the candidates' offsets key - t_s (2048 bins
 //     sized by the largest candidate, then 11 bits at a time while the
@@ -33,8 +33,8 @@
 //     position.  If the sample misled (short list or overflow), the leader
 //     runs exact radix passes and an ordered emission over the whole row.
 //  4. The leader writes the outputs (indices and slots; for QSA the 4
-//     positions of every block, then the pending tokens, then -1) with
-//     consecutive threads on consecutive entries.
+//     positions of every block, one page lookup per block, then the pending
+//     tokens, then -1) with consecutive threads on consecutive entries.
 #pragma once
 #include "select.cuh"
 
@@ -210,6 +210,15 @@ select_cluster_kernel(SelectArgs a) {
   const int m_sel = n < k ? n : k;  // entries selected
 
   if (n > k) {
+    // The sample keys are needed first: their loads go out before the slice's.
+    uint32_t sk[4];
+    if (n >= kScSampleMin) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = (int)(((int64_t)(tid + kScThreads * u) * n) >> 10);
+        sk[u] = order_key(__ldg(row + p));
+      }
+    }
     // ---- this CTA's slice, thread t's contiguous run in registers --------
     const int S = (((n + (int)C - 1) / (int)C) + 3) & ~3;
     const int s0 = (int)rank * S;
@@ -237,13 +246,8 @@ select_cluster_kernel(SelectArgs a) {
     // ---- 1. threshold estimate (identical in every CTA) -----------------
     uint32_t t_s = 0u;
     if (n >= kScSampleMin) {
-      uint32_t sk[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int p = (int)(((int64_t)(tid + kScThreads * u) * n) >> 10);
-        sk[u] = order_key(__ldg(row + p));
-        atomicAdd(&fx.h1[sk[u] >> 21], 1u);
-      }
+      for (int u = 0; u < 4; ++u) atomicAdd(&fx.h1[sk[u] >> 21], 1u);
       __syncthreads();
       const int target = min(1024, (int)((3LL * k * 1024 + 2LL * n - 1) / (2LL * n)) + 8);
       const int3 f1 = sc_find_bin(fx, fx.h1, target);
@@ -265,19 +269,29 @@ select_cluster_kernel(SelectArgs a) {
     const int cmode = t_s == 0u ? 0 : (t_s <= 0x007fffffu ? 1 : 2);
     const float t_f = __uint_as_float(t_s >= 0x80000000u ? (t_s & 0x7fffffffu) : ~t_s);
     auto is_cand = [&](float x) { return cmode == 0 ? true : (cmode == 1 ? x == x : x >= t_f); };
+    // The largest key of the slice (padding is NaN, key 0) is the largest
+    // candidate key whenever the slice has a candidate; the leader takes the
+    // maximum over the CTAs, which some candidate reaches.
     uint32_t c = 0u;
+    float vmax = nan;
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
+      vmax = fmaxf(fmaxf(vmax, fmaxf(v[j].x, v[j].y)), fmaxf(v[j].z, v[j].w));  // NaN-ignoring
       if (j < J) {
         const int i = i0 + 4 * j;
         c += (i < s1 && is_cand(v[j].x)) + (i + 1 < s1 && is_cand(v[j].y)) + (i + 2 < s1 && is_cand(v[j].z)) +
              (i + 3 < s1 && is_cand(v[j].w));
       }
     }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(vmax));
+    if (lane == 0 && kmax > 0u) atomicMax(&fx.bmax, kmax);  // visible after the scan's barrier
     uint32_t ctot;
     uint32_t o = sc_block_excl_scan(c, fx.wsum, ctot);
     cluster_wait();  // every CTA has started
-    if (tid == 0) st_dsmem_u32(map_shared_rank(&fx.cnt[rank], 0), ctot);
+    if (tid == 0) {
+      st_dsmem_u32(map_shared_rank(&fx.cnt[rank], 0), ctot);
+      st_dsmem_u32(map_shared_rank(&fx.cmax[rank], 0), fx.bmax);
+    }
     cluster_sync();
     // every warp reads the C counts lane-parallel and scans them
     const uint32_t cr = (uint32_t)lane < C ? ld_dsmem_u32(map_shared_rank(&fx.cnt[lane], 0)) : 0u;
@@ -288,7 +302,6 @@ select_cluster_kernel(SelectArgs a) {
     const bool fast = m >= (uint32_t)k && m <= (uint32_t)cap;  // the same in every CTA
     if (fast) {
       const uint32_t lk0 = map_shared_rank(lkey, 0), li0 = map_shared_rank(lidx, 0);
-      uint32_t kmax = 0u;
       o += base;
       if (c > 0u) {
 #pragma unroll
@@ -302,17 +315,12 @@ select_cluster_kernel(SelectArgs a) {
                 const uint32_t key = order_key(xv[e]);
                 st_dsmem_u32(lk0 + 4u * o, key);
                 st_dsmem_u32(li0 + 4u * o, (uint32_t)(i + e));
-                kmax = kmax > key ? kmax : key;
                 ++o;
               }
             }
           }
         }
       }
-      kmax = __reduce_max_sync(0xffffffffu, kmax);
-      if (lane == 0 && kmax > 0u) atomicMax(&fx.bmax, kmax);
-      __syncthreads();
-      if (tid == 0) st_dsmem_u32(map_shared_rank(&fx.cmax[rank], 0), fx.bmax);
     }
     cluster_sync();  // the list is complete; the leader's shared memory is no longer touched remotely
     if (rank != 0) return;
@@ -415,7 +423,7 @@ select_cluster_kernel(SelectArgs a) {
     if (rank != 0) return;
   }
 
-  // ---- 4. outputs (leader), consecutive threads on consecutive entries --
+  // ---- 4. outputs (leader) ------------------------------------------------
   auto sel = [&](int j) { return n > k ? sel_s[j] : j; };
   if (kMode == kModeTopk) {
     int32_t* oi = a.out_idx + (int64_t)t * k;
@@ -426,21 +434,48 @@ select_cluster_kernel(SelectArgs a) {
       if (os != nullptr) os[j] = idx < 0 ? -1 : sc_slot(a, pt_s, pt_n, pt_row, idx);
     }
   } else {
-    if (a.out_idx != nullptr) {
-      int32_t* oi = a.out_idx + (int64_t)t * k;
-      for (int j = tid; j < k; j += kScThreads) oi[j] = j < m_sel ? sel(j) : -1;
-    }
+    int32_t* oi = a.out_idx != nullptr ? a.out_idx + (int64_t)t * k : nullptr;
     const int width = kBlock * k + (kBlock - 1);
     const int pend = L - kBlock * n;  // tokens of the incomplete block
     int32_t* xs = a.out_xslots + (int64_t)t * width;
     int32_t* xp = a.out_pos ? a.out_pos + (int64_t)t * width : nullptr;
-    for (int j = tid; j < width; j += kScThreads) {
-      int32_t p = -1;
-      if (j < kBlock * m_sel) p = kBlock * sel(j >> 2) + (j & (kBlock - 1));
-      else if (j - kBlock * m_sel < pend) p = kBlock * n + (j - kBlock * m_sel);
+    // Selected blocks: lane l of a warp owns block base + l and looks up its
+    // page once (a page holds whole blocks, so the block's 4 slots are
+    // consecutive); the warp then writes its 128 consecutive entries with
+    // consecutive lanes, each taking the block's slot from its owner lane.
+    for (int base = 32 * (tid >> 5); base < m_sel; base += kScThreads) {
+      const int b = base + lane;
+      int32_t blk = 0, s0 = 0;
+      bool ok = false;
+      if (b < m_sel) {
+        blk = sel(b);
+        s0 = sc_slot(a, pt_s, pt_n, pt_row, kBlock * blk);
+        ok = s0 != -1;  // -1 only for a page index past the table (fault raised)
+        if (oi != nullptr) oi[b] = blk;
+      }
+      const int nw = min(32, m_sel - base);
+#pragma unroll
+      for (int r = 0; r < kBlock; ++r) {
+        const int e = lane + 32 * r;  // entry of the warp's 4 x 32
+        const int src = e >> 2;
+        const int32_t sv = __shfl_sync(0xffffffffu, s0, src);
+        const int32_t bv = __shfl_sync(0xffffffffu, blk, src);
+        const bool okv = __shfl_sync(0xffffffffu, (int)ok, src) != 0;
+        if (src < nw) {
+          const int j = kBlock * base + e;
+          xs[j] = okv ? sv + (e & (kBlock - 1)) : -1;
+          if (xp != nullptr) xp[j] = kBlock * bv + (e & (kBlock - 1));
+        }
+      }
+    }
+    // then the pending tokens and the -1 padding
+    for (int j = kBlock * m_sel + tid; j < width; j += kScThreads) {
+      const int32_t p = j - kBlock * m_sel < pend ? kBlock * n + (j - kBlock * m_sel) : -1;
       xs[j] = p < 0 ? -1 : sc_slot(a, pt_s, pt_n, pt_row, p);
       if (xp != nullptr) xp[j] = p;
     }
+    if (oi != nullptr)
+      for (int j = m_sel + tid; j < k; j += kScThreads) oi[j] = -1;
   }
 }
 
