@@ -313,7 +313,8 @@ def kernel_names(w, sm_count=152):
         select = "select_rows_kernel"
     else:
         select = "select_resident_kernel"
-    return {"compress": "compress_keys_kernel", "score": score, "select": select}
+    return {"compress": "compress_keys_kernel", "append": "append_keys_kernel", "score": score,
+            "select": select}
 
 
 def kernel_bytes(w, new_blocks):
@@ -328,6 +329,23 @@ def kernel_bytes(w, new_blocks):
     return {"compress": n_new * (4 * 256 + 256 + 12),
             "score": by["keys"] + by["q"] + by["page_table"] + by["scores_fp32"],
             "select": by["scores_fp32"] + by["page_table"] + by["slots"]}
+
+
+def append_bytes(st):
+    """Algorithmic HBM bytes of one key-path launch (qsa_append_keys) as set
+    up by setup_key_path: per request, the appended raw keys read (256 B
+    each); per block they complete, its keys from earlier calls read from
+    the ring, the compressed key written (256 B) and its page-table entry
+    (4 B); the last 4 appended keys written to the ring; the request's
+    metadata (12 B)."""
+    total = 0
+    rts, first = st["kp_rts_h"], st["kp_first_h"]
+    for r in range(len(first)):
+        n, p0 = int(rts[r + 1] - rts[r]), int(first[r])
+        done = [p // 4 for p in range(p0, p0 + n) if p % 4 == 3]
+        from_ring = sum(max(0, p0 - 4 * b) for b in done)
+        total += 256 * n + 256 * from_ring + (256 + 4) * len(done) + 256 * min(n, 4) + 12
+    return total
 
 
 def decode_bytes(w):
@@ -347,15 +365,16 @@ def decode_bytes(w):
 
 def e2e_decode(g: Gpu, st, iters, warmup):
     """The same step through the public API with HOST buffers: pinned host
-    inputs (q, new raw keys and their ids, row metadata) copied in, the slots
-    copied back, inside the timed region."""
+    inputs (q, the appended raw keys, their positions and the row metadata)
+    copied in, one decode_step call, the slots copied back, inside the timed
+    region (the ring is put back before each step, outside it)."""
     torch = g.torch
     w = st["w"]
     host = {
         "q": torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory(),
-        "raw": torch.from_numpy(st["new_raw_h"].view(np.int16)).pin_memory(),
-        "id": torch.from_numpy(st["new_id_h"]).pin_memory(),
-        "req": torch.from_numpy(st["new_req_h"]).pin_memory(),
+        "keys": torch.from_numpy(np.ascontiguousarray(st["kp_keys_h"]).view(np.int16)).pin_memory(),
+        "rts": torch.from_numpy(st["kp_rts_h"]).pin_memory(),
+        "first": torch.from_numpy(st["kp_first_h"]).pin_memory(),
         "rrs": torch.from_numpy(w.req_row_start).pin_memory(),
         "rl": torch.from_numpy(w.row_len).pin_memory(),
     }
@@ -367,14 +386,13 @@ def e2e_decode(g: Gpu, st, iters, warmup):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        g.qsa.compress_keys(dev["raw"].view(torch.bfloat16), dev["id"], st["pool"], block_req=dev["req"],
-                            page_table=st["pt"], page_size=w.page_size, rope_base=w.rope_base)
-        g.qsa.indexer_select(dev["q"].view(torch.bfloat16), st["pool"], dev["rrs"], dev["rl"], st["pt"],
-                             w.page_size, w.max_len, w.max_rows_per_req, k_blk=w.k_blk,
-                             workspace=st["ws"], out_slots=st["slots"])
+        g.qsa.decode_step(dev["keys"].view(torch.bfloat16), dev["rts"], dev["first"], st["kp_ring"],
+                          dev["q"].view(torch.bfloat16), st["pool"], dev["rrs"], dev["rl"], st["pt"],
+                          w.page_size, w.max_len, w.max_rows_per_req, k_blk=w.k_blk, rope_base=w.rope_base,
+                          workspace=st["ws"], out_slots=st["slots"])
         out_h.copy_(st["slots"], non_blocking=True)
 
-    times = g.timed(step, iters, warmup, graph=False)
+    times = g.timed(step, iters, warmup, graph=False, pre=lambda: restore_ring(st))
     return times, h2d, d2h
 
 
@@ -406,9 +424,12 @@ def setup_key_path(g, st):
         keys.extend(raw_key(r, p) for p in range(p0, p0 + len(pos)))
         for p in range(4 * (p0 // 4), p0):
             ring[r, p % 4] = raw_key(r, p)
-    st["kp_keys"] = g.bf16(np.stack(keys))
-    st["kp_rts"] = g.h2d(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
-    st["kp_first"] = g.h2d(np.array(first, np.int32))
+    st["kp_keys_h"] = np.stack(keys)
+    st["kp_rts_h"] = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    st["kp_first_h"] = np.array(first, np.int32)
+    st["kp_keys"] = g.bf16(st["kp_keys_h"])
+    st["kp_rts"] = g.h2d(st["kp_rts_h"])
+    st["kp_first"] = g.h2d(st["kp_first_h"])
     st["kp_ring"] = g.bf16(ring)
     st["kp_ring0"] = st["kp_ring"].clone()  # the ring before the step (restored between replays)
 
@@ -721,19 +742,25 @@ def main():
     g = Gpu(device)
 
     # ---- primary: one decode step of the chosen workload ------------------
+    # (qsa_decode_step: the rows' own index keys appended through the ring,
+    # the blocks they complete compressed, then the fused indexer; the ring
+    # is put back before every step, outside the timed region)
     w, new_blocks = WORKLOADS[args.workload](rank)
     st = setup_decode(g, w, new_blocks=new_blocks)
+    setup_key_path(g, st)
     for _ in range(args.warmup):
+        restore_ring(st)
         g.flush()
-        decode_step(g, st)
+        decode_step_ring(g, st)
     torch.cuda.synchronize()
-    replay = g.capture(lambda: decode_step(g, st))
+    replay = g.capture(lambda: decode_step_ring(g, st))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
         t_end = time.perf_counter() + args.clock_window
         while time.perf_counter() < t_end:  # untimed: clocks settle, sampler starts
             for _ in range(20):
+                restore_ring(st)
                 g.flush()
                 replay()
             torch.cuda.synchronize()
@@ -741,6 +768,7 @@ def main():
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for s, e in ev:
+            restore_ring(st)
             g.flush()
             s.record(g.stream)
             replay()
@@ -757,9 +785,12 @@ def main():
     # object describes the one that takes longest -------------------------
     names = kernel_names(w, torch.cuda.get_device_properties(device).multi_processor_count)
     kbytes = kernel_bytes(w, new_blocks)
+    kbytes["append"] = append_bytes(st)
+    del kbytes["compress"]
     scores_only(g, st)  # the selection below reads these scores
     kms = {
-        "compress": statistics.mean(g.timed(lambda: compress_only(g, st), args.steps, args.warmup)),
+        "append": statistics.mean(g.timed(lambda: append_only(g, st), args.steps, args.warmup,
+                                          pre=lambda: restore_ring(st))),
         "score": statistics.mean(g.timed(lambda: scores_only(g, st), args.steps, args.warmup)),
         "select": statistics.mean(g.timed(lambda: select_only(g, st), args.steps, args.warmup)),
     }
@@ -782,8 +813,9 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "rows": w.n_rows, "requests": w.n_req,
                    "L": int(w.max_len), "k_blk": w.k_blk, "page_size": w.page_size,
-                   "step": f"compress {new_blocks} new block(s) per request + fused "
-                           "score/top-512/expand/slots, replayed from a CUDA graph",
+                   "step": f"one qsa_decode_step call: the rows' {int(st['kp_rts_h'][-1])} own index "
+                           "key(s) appended through the 4-slot ring (the blocks they complete "
+                           "compressed) + fused score/top-512/expand/slots, replayed from a CUDA graph",
                    "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": 1e3 * ms,

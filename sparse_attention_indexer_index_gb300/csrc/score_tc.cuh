@@ -485,6 +485,18 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pool_map)) : "memory");
 
   const int r = blockIdx.z;
+  // Page-table entries of this CTA's key range (at most tiles_per_cta tiles
+  // from kt0, a range fixed by the CTA index): their loads go out next to
+  // the row metadata's, one entry per thread, and land in shared memory
+  // once the metadata is known.
+  const int kpp = a.page_size / kBlock;
+  const int kt0 = blockIdx.x * a.tiles_per_cta;
+  const int pt0 = (kt0 * kTcM) / kpp;
+  int pt_n = min(((kt0 + a.tiles_per_cta) * kTcM - 1) / kpp + 1 - pt0, a.pt_cap);
+  if (pt_n > a.ld_pt - pt0) pt_n = (int)(a.ld_pt - pt0);
+  if (pt_n < 0) pt_n = 0;
+  const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
+  const int32_t pt_first = (int)threadIdx.x < pt_n ? __ldg(pt_row + pt0 + threadIdx.x) : 0;
   const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
   if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_fault(kFaultGrouping);
@@ -510,7 +522,6 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   int nb_tile = 0;
   for (int i = 0; i < nrows; ++i) nb_tile = max(nb_tile, s_nb[i]);
   const int n_kt = (nb_tile + kTcM - 1) / kTcM;
-  const int kt0 = blockIdx.x * a.tiles_per_cta;
   const int kt1 = min(n_kt, kt0 + a.tiles_per_cta);
   if (kt0 >= kt1) {
     leave();
@@ -520,13 +531,8 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   const int first_new = relaxed ? max(0, __ldg(a.new_pos + r)) / kBlock : 0;
 
   // ---- page-table entries of this CTA's key range, staged once ------------
-  const int kpp = a.page_size / kBlock;
-  const int pt0 = (kt0 * kTcM) / kpp;
-  int pt_n = min((kt1 * kTcM - 1) / kpp + 1 - pt0, a.pt_cap);
-  if (pt_n > a.ld_pt - pt0) pt_n = (int)(a.ld_pt - pt0);
-  if (pt_n < 0) pt_n = 0;
-  const int32_t* pt_row = a.page_table + (int64_t)r * a.ld_pt;
-  for (int i = threadIdx.x; i < pt_n; i += kThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
+  if ((int)threadIdx.x < pt_n) pt_s[threadIdx.x] = pt_first;
+  for (int i = threadIdx.x + kThreads; i < pt_n; i += kThreads) pt_s[i] = __ldg(pt_row + pt0 + i);
 
   // ---- query rows -> B (zero columns beyond 4 * nrows) ---------------------
   const int valid_cols = 4 * nrows;

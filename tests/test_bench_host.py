@@ -67,8 +67,8 @@ def test_kernel_names_follow_the_dispatch_rules():
     import bench
     from workloads import c2_verify, c3_batched
     n2 = bench.kernel_names(c2_verify(0))  # 6 rows per request, 64-token pages
-    assert n2 == {"compress": "compress_keys_kernel", "score": "score_tc_kernel",
-                  "select": "select_cluster_kernel"}
+    assert n2 == {"compress": "compress_keys_kernel", "append": "append_keys_kernel",
+                  "score": "score_tc_kernel", "select": "select_cluster_kernel"}
     n3 = bench.kernel_names(c3_batched(0))  # one row per request, 32 rows
     assert n3["score"] == "score_tcb_kernel" and n3["select"] == "select_resident_kernel"
 
@@ -82,6 +82,17 @@ def test_kernel_bytes_c2():
     assert kb["compress"] == 2 * (4 * 256 + 256 + 12)
     assert kb["select"] == 4 * sum(nb) + 4 * (80000 // 64) + 6 * 4 * (4 * 512 + 3)
     assert kb["score"] == 256 * max(nb) + 1024 * 6 + 4 * (80000 // 64) + 4 * sum(nb)
+
+
+def test_append_bytes_verify_step():
+    import bench
+    import numpy as np
+    # 6 tokens at 79994..79999: blocks 19998 (2 keys from the ring) and 19999 complete
+    st = {"kp_rts_h": np.array([0, 6], np.int32), "kp_first_h": np.array([79994], np.int32)}
+    assert bench.append_bytes(st) == 256 * 6 + 256 * 2 + 260 * 2 + 256 * 4 + 12
+    # one token that completes nothing: its key read, the ring written
+    st = {"kp_rts_h": np.array([0, 1], np.int32), "kp_first_h": np.array([8], np.int32)}
+    assert bench.append_bytes(st) == 256 + 256 + 12
 
 
 def test_long_rows_take_the_cluster_selection():
