@@ -294,7 +294,7 @@ def kernel_names(w, sm_count=152):
     use the balanced tensor-core scorer on such pages; rows of up to
     32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
     shared-memory-resident single-CTA selection up to two rows per SM and
-    small CTAs (three per SM) for more rows; longer rows a
+    small CTAs (four per SM) for more rows; longer rows a
     cluster of 2-16 CTAs per row when rows * 2 <= SMs, one streaming CTA per
     row otherwise)."""
     tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0

@@ -339,8 +339,8 @@ qsa_status launch_select_long(const SelectArgs& args, bool pdl, cudaStream_t str
 }
 
 // More than two rows per SM, rows of up to kSrMaxRow entries: one 256-thread
-// CTA per row, three per SM (select_rows_kernel).  Measured: a prefill chunk
-// of 4096 rows 396 -> 274 us; a batch of 192 verify rows still runs the step
+// CTA per row, four per SM (select_rows_kernel).  Measured: a prefill chunk
+// of 4096 rows 396 -> 274 us (three per SM) -> 244 us (four); a batch of 192 verify rows still runs the step
 // faster on the 1024-thread kernel (72.3 against 74.5 us).
 template <int kMode>
 qsa_status launch_select_rows(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count) {

@@ -1,5 +1,5 @@
 // select_rows.cuh -- exact top-k of many rows of up to 32768 entries: one
-// small CTA per row, three per SM, so that launches with more rows than SMs
+// small CTA per row, four per SM, so that launches with more rows than SMs
 // (a batch of verify steps, a prefill chunk of thousands of rows) run in few
 // waves and the rows stream at HBM rate instead of one row per SM.
 //
@@ -13,14 +13,15 @@
 // Design (the single-CTA form of select_long_kernel's list path).  256
 // threads; warp w owns a contiguous segment of the row, walked 128 entries
 // at a time (4 consecutive per lane) with 16-byte loads, 4 in flight.  The
-// row's page-table entries are loaded at the start and kept in shared memory
-// for the outputs.
+// outputs read the page table through L2 (shared memory is kept to 54 KB so
+// that four CTAs fit an SM: the rows are latency-bound, and a fourth CTA
+// per SM took a 4096-row prefill chunk from 274 to 244 us).
 //  1. Sampled bound: 1024 entries in 32 runs of 32 (one 16-byte load per
 //     thread); the edge of the top-12-bit bin below which the r-th largest
 //     sample lies, r about twice the expected number of samples above the
 //     k-th entry.
 //  2. One pass over the row: each warp lists its entries at or above the
-//     bound (key, index) in its own region of a shared-memory list, with
+//     bound (float bits, index) in its own region of a shared-memory list, with
 //     ballot counts.  A warp whose region fills up makes the CTA walk the
 //     whole row in the steps below instead of the list.
 //  3. Radix levels of 12, 12 and 8 bits over the list (or the row) in a
@@ -43,20 +44,16 @@ constexpr int kSrThreads = 256;
 constexpr int kSrWarps = kSrThreads / 32;
 constexpr int kSrMaxRow = 32768;
 constexpr int kSrBins = 4096;
-constexpr int kSrCandCap = 4096;                 // list entries per CTA (per warp: / kSrWarps)
+constexpr int kSrCandCap = 3840;                 // list entries per CTA (per warp: / kSrWarps)
 constexpr int kSrWords = kSrMaxRow / 32;         // bitmap words
 constexpr int kSrUnroll = 4;
-constexpr int kSrPt = 2048;                      // page-table entries staged for the outputs
 
 struct SrSmem {
   uint32_t hist[kSrBins];
-  uint32_t cand_key[kSrCandCap];
+  uint32_t cand_val[kSrCandCap];  // the candidates' float bits (keys are made when read)
   uint32_t cand_idx[kSrCandCap];
   uint32_t bm_eq[kSrWords];
   uint32_t bm_win[kSrWords];
-  uint32_t pre_eq[kSrWords];
-  uint32_t pre_win[kSrWords];
-  int32_t pt[kSrPt];
   uint32_t wsum[kSrWarps];
   int info[4];
   int ovf;
@@ -112,8 +109,12 @@ __device__ __forceinline__ int4 sr_find_bin(SrSmem& sm, int k_rem) {
   return r;
 }
 
+// four CTAs per SM: at most 56 KB of shared memory and 64 registers each
+static_assert(sizeof(SrSmem) + 1024 <= 228 * 1024 / 4, "four CTAs per SM");
+static_assert(2 * kSrWords <= kSrBins, "the word prefix counts reuse the histogram");
+
 template <int kMode>
-__global__ void __launch_bounds__(kSrThreads, 3)
+__global__ void __launch_bounds__(kSrThreads, 4)
 select_rows_kernel(SelectArgs a) {
   extern __shared__ __align__(16) unsigned char sr_smem_raw[];
   SrSmem& sm = *reinterpret_cast<SrSmem*>(sr_smem_raw);
@@ -140,34 +141,13 @@ select_rows_kernel(SelectArgs a) {
   }
   for (int i = tid; i < kSrBins; i += kSrThreads) sm.hist[i] = 0u;
   if (tid == 0) sm.ovf = 0;
-  // the page-table entries of the row's positions, for the outputs (loads
-  // issued now, stored to shared memory once the first pass is done)
-  int pt_n = 0;
-  if (pt_row != nullptr) {
-    const int64_t last = kMode == kModeQsa ? (int64_t)L : (int64_t)n;  // positions < last
-    int64_t np = last > 0 ? (last - 1) / a.page_size + 1 : 0;
-    np = min(np, (int64_t)kSrPt);
-    np = min(np, a.ld_pt);
-    pt_n = (int)np;
-  }
-  int32_t ptv[kSrPt / kSrThreads];
-#pragma unroll
-  for (int u = 0; u < kSrPt / kSrThreads; ++u) {
-    const int i = tid + kSrThreads * u;
-    ptv[u] = i < pt_n ? __ldg(pt_row + i) : 0;
-  }
   if (a.wait_primary) pdl_wait_primary();
   const float* row = a.scores + (int64_t)t * a.ld;
   const int k = a.k;
   const int m_sel = n < k ? n : k;
   const bool vec = a.vec_ok != 0;
 
-  auto slot = [&](uint32_t pos) -> int32_t {  // staged entries, else global
-    const uint32_t ps = (uint32_t)a.page_size;
-    const uint32_t page_idx = pos / ps;
-    if ((int)page_idx < pt_n) return sm.pt[page_idx] * a.page_size + (int32_t)(pos - page_idx * ps);
-    return sl_slot(a, pt_row, pos);
-  };
+  auto slot = [&](uint32_t pos) -> int32_t { return sl_slot(a, pt_row, pos); };
   auto emit = [&](uint32_t idx, int pos) {
     if (kMode == kModeTopk) {
       a.out_idx[(int64_t)t * k + pos] = (int32_t)idx;
@@ -188,11 +168,6 @@ select_rows_kernel(SelectArgs a) {
     }
   };
 
-#pragma unroll
-  for (int u = 0; u < kSrPt / kSrThreads; ++u) {
-    const int i = tid + kSrThreads * u;
-    if (i < pt_n) sm.pt[i] = ptv[u];
-  }
   __syncthreads();
   // ---- the tail after m_sel entries ----------------------------------------------
   if (kMode == kModeTopk) {
@@ -226,14 +201,23 @@ select_rows_kernel(SelectArgs a) {
   const int w0 = min(n, warp * seg);
   const int w1 = min(n, w0 + seg);
   // f(i, v, full) on every 128-entry chunk of this warp's segment (lane:
-  // entries i..i+3; full: the chunk lies before w1, else f masks)
+  // entries i..i+3; full: the chunk lies before w1, else f masks entries
+  // from w1 on, which read as NaN)
   auto walk = [&](auto&& f) {
     for (int c0 = w0; c0 < w1; c0 += 128 * kSrUnroll) {
       float4 v[kSrUnroll];
+      if (vec && c0 + 128 * kSrUnroll <= w1) {
 #pragma unroll
-      for (int u = 0; u < kSrUnroll; ++u) v[u] = sl_load4(row, c0 + 128 * u + 4 * lane, w1, vec);
+        for (int u = 0; u < kSrUnroll; ++u)
+          v[u] = __ldg(reinterpret_cast<const float4*>(row + c0 + 128 * u + 4 * lane));
 #pragma unroll
-      for (int u = 0; u < kSrUnroll; ++u) f(c0 + 128 * u + 4 * lane, v[u], std::false_type{});
+        for (int u = 0; u < kSrUnroll; ++u) f(c0 + 128 * u + 4 * lane, v[u], std::true_type{});
+      } else {
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; ++u) v[u] = sl_load4(row, c0 + 128 * u + 4 * lane, w1, vec);
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; ++u) f(c0 + 128 * u + 4 * lane, v[u], std::false_type{});
+      }
     }
   };
 
@@ -262,23 +246,26 @@ select_rows_kernel(SelectArgs a) {
 
   // ---- 2. one pass: each warp lists its entries at or above the bound ----------------
   constexpr int kCw = kSrCandCap / kSrWarps;
-  uint32_t* ckey = sm.cand_key + warp * kCw;
+  uint32_t* cval = sm.cand_val + warp * kCw;
   uint32_t* cidx = sm.cand_idx + warp * kCw;
   uint32_t wn = 0u;  // the same in every lane of the warp
-  walk([&](int i, float4 v, auto) {
+  // Candidates are a few per cent of the row: a lane's are written in a loop
+  // over its mask (mostly no iteration), placed by ballot counts.
+  walk([&](int i, float4 v, auto full) {
     const float xv[4] = {v.x, v.y, v.z, v.w};
-    bool c[4], any = false;
+    uint32_t cm = 0u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      c[e] = low.ge(xv[e]) & (i + e < w1);
-      any |= c[e];
+      bool ce = low.ge(xv[e]);
+      if (!decltype(full)::value) ce = ce & (i + e < w1);
+      cm |= (uint32_t)ce << e;
     }
-    if (__ballot_sync(0xffffffffu, any) == 0u) return;
+    if (__ballot_sync(0xffffffffu, cm != 0u) == 0u) return;
     uint32_t tot = 0u, before = 0u;
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t m = __ballot_sync(0xffffffffu, c[e]);
+      const uint32_t m = __ballot_sync(0xffffffffu, (cm >> e) & 1u);
       tot += __popc(m);
       before += __popc(m & lt);
     }
@@ -287,13 +274,13 @@ select_rows_kernel(SelectArgs a) {
       return;
     }
     uint32_t o = wn + before;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (c[e]) {
-        ckey[o] = order_key(xv[e]);
-        cidx[o] = (uint32_t)(i + e);
-        ++o;
-      }
+    while (cm != 0u) {
+      const int e = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      const float x = e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+      cval[o] = __float_as_uint(x);
+      cidx[o] = (uint32_t)(i + e);
+      ++o;
     }
     wn += tot;
   });
@@ -311,7 +298,7 @@ select_rows_kernel(SelectArgs a) {
     const uint32_t mask = (1u << nb) - 1u;
     if (use_list) {
       for (int j = lane; j < (int)wn; j += 32) {
-        const uint32_t key = ckey[j];
+        const uint32_t key = order_key(__uint_as_float(cval[j]));
         if (lv == 0 || (key >> shift) == prefix) atomicAdd(&sm.hist[(key >> nshift) & mask], 1u);
       }
     } else {
@@ -358,7 +345,7 @@ select_rows_kernel(SelectArgs a) {
     else if (hb == prefix) atomicOr(&sm.bm_eq[idx >> 5], 1u << (idx & 31));
   };
   if (use_list) {
-    for (int j = lane; j < (int)wn; j += 32) mark(ckey[j], cidx[j]);
+    for (int j = lane; j < (int)wn; j += 32) mark(order_key(__uint_as_float(cval[j])), cidx[j]);
   } else {
     walk([&](int i, float4 v, auto) {
       if (!lo.all && !(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) >= lo.f)) return;
@@ -386,14 +373,16 @@ select_rows_kernel(SelectArgs a) {
       x += c[u];
     }
   };
-  word_scan(sm.bm_eq, sm.pre_eq);
+  uint32_t* pre_eq = sm.hist;  // the histogram is free from here on
+  uint32_t* pre_win = sm.hist + kSrWords;
+  word_scan(sm.bm_eq, pre_eq);
   __syncthreads();
   // the first `need` entries of the bin become winners
 #pragma unroll
   for (int u = 0; u < kWpt; ++u) {
     const int w = kWpt * tid + u;
     uint32_t bits = sm.bm_eq[w];
-    uint32_t r = sm.pre_eq[w];
+    uint32_t r = pre_eq[w];
     while (bits != 0u && r < need) {
       const uint32_t b = bits & (0u - bits);
       atomicOr(&sm.bm_win[w], b);
@@ -402,13 +391,13 @@ select_rows_kernel(SelectArgs a) {
     }
   }
   __syncthreads();
-  word_scan(sm.bm_win, sm.pre_win);
+  word_scan(sm.bm_win, pre_win);
   __syncthreads();
 #pragma unroll
   for (int u = 0; u < kWpt; ++u) {
     const int w = kWpt * tid + u;
     uint32_t bits = sm.bm_win[w];
-    uint32_t pos = sm.pre_win[w];
+    uint32_t pos = pre_win[w];
     while (bits != 0u) {
       const int b = __ffs(bits) - 1;
       bits &= bits - 1u;
