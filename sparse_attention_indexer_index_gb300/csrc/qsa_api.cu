@@ -618,14 +618,32 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   t.page_size = s.page_size;
   t.scores = s.scores;
   t.ld_scores = s.ld_scores;
-  t.rows_per_tile = std::min(kTcMaxRowsPerTile, max_rows_per_req);
+  const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
+  int rpt = std::min(kTcMaxRowsPerTile, max_rows_per_req);
+  if (max_rows_per_req > kTcMaxRowsPerTile && sm_count > 0) {
+    // Many rows (a prefill chunk): the tile height whose CTAs (row tiles x
+    // key-range splits) fill one wave with the least work per CTA, i.e. key
+    // tiles x (MMA columns + a fixed share per tile).  4096 rows on 152
+    // SMs: 56-row tiles, 74 x 2 CTAs, instead of 64-row tiles on 128 SMs.
+    int64_t best = INT64_MAX;
+    for (int r = kTcMaxRowsPerTile; r >= 8; --r) {
+      const int64_t rt = (max_rows_per_req + r - 1) / r;
+      if (rt * s.n_req > sm_count) break;  // smaller r: more row tiles still
+      const int64_t x = std::min<int64_t>(n_kt, sm_count / (rt * s.n_req));
+      const int64_t cost = ((n_kt + x - 1) / x) * ((((int64_t)4 * r + 15) & ~15) + 32);
+      if (cost < best) {
+        best = cost;
+        rpt = r;
+      }
+    }
+  }
+  t.rows_per_tile = rpt;
   t.n_cols = ((4 * t.rows_per_tile) + 15) & ~15;
   int cols = 32;
   while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
   t.tmem_cols = cols;
   t.trigger_dependents = s.trigger_dependents;
   t.new_pos = s.new_pos;
-  const int64_t n_kt = (nb_max + kTcM - 1) / kTcM;
   const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
   if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
   qsa_status tma = launch_scores_tma(t, n_kt, row_tiles, s.n_req, sm_count, stream);

@@ -519,8 +519,11 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
     s_nb[threadIdx.x] = L / kBlock;
   }
   __syncthreads();
-  int nb_tile = 0;
-  for (int i = 0; i < nrows; ++i) nb_tile = max(nb_tile, s_nb[i]);
+  int nb_tile = 0, nb_min = INT_MAX;  // most and fewest visible blocks of the tile's rows
+  for (int i = 0; i < nrows; ++i) {
+    nb_tile = max(nb_tile, s_nb[i]);
+    nb_min = min(nb_min, s_nb[i]);
+  }
   const int n_kt = (nb_tile + kTcM - 1) / kTcM;
   const int kt1 = min(n_kt, kt0 + a.tiles_per_cta);
   if (kt0 >= kt1) {
@@ -665,6 +668,8 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
       if (!ok) break;
       tc_fence_after();
       const int b = (kt0 + i) * kTcM + quarter * 32 + lane;
+      // every row of the tile sees every key of this key tile: no per-row test
+      const bool all_vis = (kt0 + i + 1) * kTcM <= nb_min;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
       for (int c0 = 32 * cgroup; c0 < N; c0 += 32 * (kEpi / 4)) {
         uint32_t v[32];
@@ -678,15 +683,16 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
           for (int e = 0; e < 16; ++e) v[e] = w16[e];
           ncols = 16;
         }
+        float* dst = a.scores + (int64_t)(t0 + c0 / 4) * a.ld_scores + b;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int tr = c0 / 4 + j;  // row within the tile
-          if (4 * j < ncols && tr < nrows && b < s_nb[tr]) {
+          if (4 * j < ncols && tr < nrows && (all_vis || b < s_nb[tr])) {
             float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
             sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
             sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
             sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-            a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = sc * kScoreScale;
+            dst[(int64_t)j * a.ld_scores] = sc * kScoreScale;
           }
         }
       }
