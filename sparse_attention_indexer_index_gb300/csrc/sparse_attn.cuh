@@ -14,21 +14,26 @@
 // h / G, G = H_q / H_kv.  out [rows][H_q][D] FP32, lse [rows][H_q] FP32.
 //
 // Design (GB300).  The work is a gather: per (row, KV head) about 2K rows of
-// K and V (2 x D x 2 B each) against G query heads, 2 G D FMAs per 4 D bytes,
-// so HBM-bound at the FP32 CUDA-core rate; no tensor cores.  Flash-decoding
-// split: one 128-thread CTA per (row, KV head, chunk of the row's entries).
-//  1. Logits: a warp takes 32 / G slots at a time, each lane D / 32
-//     consecutive elements of every K row (one 8- or 16-byte load) and of
-//     the G query rows (registers); the G x (32 / G) partial dot products are
-//     summed by a butterfly reduce-scatter (31 shuffles for 32 sums), after
-//     which lane l holds the logit of (head l / P, slot l % P).
+// K and V (2 x D x 2 B each) against G query heads, 2 G D multiply-adds per
+// 4 D bytes, so HBM-bound once the arithmetic issues few instructions.
+// Flash-decoding split: one 128-thread CTA per (row, KV head, chunk of the
+// row's entries).
+//  1. Logits on the tensor cores (mma.sync m16n8k16, BF16 products exact,
+//     FP32 accumulation): a warp takes 16 slots at a time as the rows of A,
+//     loaded straight from global memory into the A fragments (the head
+//     dimension permuted alike for q and k so that every load is a 16-byte
+//     piece and the 4 lanes of a row read 64 contiguous bytes); the query
+//     heads are the 8 columns of B, held in registers.  The CUDA-core form
+//     (a butterfly reduce-scatter of per-lane partial dot products) issued
+//     about 80 instructions per slot here; this one issues a few.
 //  2. Per head: chunk maximum m and weights exp(logit - m), sum l.
 //  3. Values: each warp accumulates sum_j w_hj v_j for its slots (weights
 //     broadcast from shared memory; packed fma.rn.f32x2), the 4 warps' sums
-//     are added in shared memory.  Every warp requests the K (then V) rows
-//     of its next 4 steps into L2 ahead of its loads.  One chunk: the CTA normalises and writes out and lse;
-//     several: it writes (m, l, unnormalised sum) and a second kernel merges
-//     the chunks of every (row, head).
+//     are added in shared memory.
+// Every warp requests into L2 the K rows of its next 2 tiles and the V rows
+// of its next 4 value steps ahead of its loads.  One chunk: the CTA
+// normalises and writes out and lse; several: it writes (m, l, unnormalised
+// sum) and a second kernel merges the chunks of every (row, head).
 #pragma once
 #include "common.cuh"
 
@@ -114,6 +119,17 @@ __device__ __forceinline__ float sa_reduce_scatter32(float (&x)[32]) {
   return x[0];
 }
 
+// D += A B on the tensor cores: A 16 x 16 BF16 (row-major fragment a0..a3),
+// B 16 x 8 BF16 (column fragment b0, b1), D 16 x 8 FP32.
+__device__ __forceinline__ void sa_mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Shared memory of one CTA (D, G fixed by the template).
 template <int G, int D>
 struct SaSmem {
@@ -146,17 +162,52 @@ sparse_attn_kernel(SaArgs a) {
     }
     sm.slot[j] = s;
   }
-  // this lane's part of the G query rows
-  float2 qv[G][E / 2];
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-    sa_load_row2<E>(a.q + ((int64_t)t * a.h_q + (int64_t)g * G + h) * D + lane * E, qv[h]);
   __syncthreads();
 
-  // ---- 1. logits ----------------------------------------------------------------
-  constexpr int kLines = D * 2 / 128;  // 128-byte lines of a row
-  constexpr int kAhead = 4;            // warp steps of rows requested into L2 ahead
-  // the K rows of this warp's step `jj` into L2 (P rows x kLines lines)
+  // ---- 1. logits on the tensor cores ---------------------------------------------
+  // mma.sync m16n8k16 (BF16 in, FP32 accumulate): a warp takes 16 slots at a
+  // time (rows of A), the heads are the 8 columns of B (two n-tiles for 16).
+  // The head dimension is permuted the same way for q and k -- a dot
+  // product does not depend on the order of its terms -- so that the A words
+  // of lane (gq, tq) are 16-byte pieces of its two K rows and the 4 lanes of
+  // a row read 64 contiguous bytes per load: element d = 32 (s >> 1) + 8 tq
+  // + 4 (s & 1) + c plays column 2tq + (c & 1) + 8 (c >> 1) of k-step s.
+  constexpr int KS = D / 16;          // k-steps
+  constexpr int NT = (G + 7) / 8;     // n-tiles of 8 heads
+  constexpr int QW = D / 32;          // 16-byte words of a lane (one per 32 elements)
+  constexpr int kLines = D * 2 / 128; // 128-byte lines of a row
+  constexpr int kAhead = 2;           // tiles of K rows requested into L2 ahead
+  const int gq = lane >> 2, tq = lane & 3;
+  uint32_t bq[NT][KS][2];  // B fragments: head nt*8 + gq
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + gq;
+    uint4 u[QW];
+#pragma unroll
+    for (int i = 0; i < QW; ++i)
+      u[i] = h < G ? __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)t * a.h_q + (int64_t)g * G + h) * D) +
+                           tq + 4 * i)
+                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      bq[nt][s][0] = (s & 1) ? u[s >> 1].z : u[s >> 1].x;
+      bq[nt][s][1] = (s & 1) ? u[s >> 1].w : u[s >> 1].y;
+    }
+  }
+  // the K rows of the tile at jj into L2 (16 rows x kLines lines)
+  auto prefetch_tile = [&](int jj) {
+#pragma unroll
+    for (int u = 0; u < (16 * kLines + 31) / 32; ++u) {
+      const int idx = lane + 32 * u;
+      const int r = jj + idx / kLines;
+      if (idx < 16 * kLines && r < n) {
+        const int s = sm.slot[r];
+        if (s >= 0)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a.k + ((int64_t)s * a.h_kv + g) * D + (idx % kLines) * 64));
+      }
+    }
+  };
+  // the V rows of this warp's first value steps, and the first K tiles
   auto prefetch_rows = [&](const uint16_t* base, int jj, int rows) {
     if (lane < rows * kLines) {
       const int s = jj + lane / kLines < n ? sm.slot[jj + lane / kLines] : -1;
@@ -164,34 +215,44 @@ sparse_attn_kernel(SaArgs a) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(base + ((int64_t)s * a.h_kv + g) * D + (lane % kLines) * 64));
     }
   };
-  for (int d = 0; d < kAhead; ++d) prefetch_rows(a.k, warp * P + d * kSaWarps * P, P);
-  for (int d = 0; d < kAhead; ++d) prefetch_rows(a.v, warp * 4 + d * kSaWarps * 4, 4);
-  for (int j = warp * P; j < n; j += kSaWarps * P) {
-    prefetch_rows(a.k, j + kAhead * kSaWarps * P, P);
-    float2 kv[P][E / 2];
+  for (int d = 0; d < kAhead; ++d) prefetch_tile(warp * 16 + d * kSaWarps * 16);
+  for (int d = 0; d < 4; ++d) prefetch_rows(a.v, warp * 4 + d * kSaWarps * 4, 4);
+  const float ninf = -__int_as_float(0x7f800000);
+  for (int j = warp * 16; j < n; j += kSaWarps * 16) {
+    prefetch_tile(j + kAhead * kSaWarps * 16);
+    const int r0 = j + gq, r1 = j + gq + 8;
+    const int s0 = r0 < n ? sm.slot[r0] : -1, s1 = r1 < n ? sm.slot[r1] : -1;
+    uint4 ka[QW], kb[QW];
+    const uint4* pa = reinterpret_cast<const uint4*>(a.k + ((int64_t)max(s0, 0) * a.h_kv + g) * D) + tq;
+    const uint4* pb = reinterpret_cast<const uint4*>(a.k + ((int64_t)max(s1, 0) * a.h_kv + g) * D) + tq;
 #pragma unroll
-    for (int i = 0; i < P; ++i) {
-      const int s = j + i < n ? sm.slot[j + i] : -1;
-      if (s >= 0) {
-        sa_load_row2<E>(a.k + ((int64_t)s * a.h_kv + g) * D + lane * E, kv[i]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E / 2; ++e) kv[i][e] = make_float2(0.f, 0.f);
-      }
+    for (int i = 0; i < QW; ++i) {
+      ka[i] = s0 >= 0 ? __ldg(pa + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
+      kb[i] = s1 >= 0 ? __ldg(pb + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float x[32];
+    float acc[NT][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
-      for (int i = 0; i < P; ++i) {
-        float2 acc = make_float2(0.f, 0.f);  // even and odd elements
+    for (int s = 0; s < KS; ++s) {
+      const uint4& x = ka[s >> 1];
+      const uint4& y = kb[s >> 1];
+      const uint32_t a0 = (s & 1) ? x.z : x.x, a2 = (s & 1) ? x.w : x.y;
+      const uint32_t a1 = (s & 1) ? y.z : y.x, a3 = (s & 1) ? y.w : y.y;
 #pragma unroll
-        for (int e = 0; e < E / 2; ++e) acc = sa_fma2(qv[h][e], kv[i][e], acc);
-        x[h * P + i] = acc.x + acc.y;
+      for (int nt = 0; nt < NT; ++nt) sa_mma_bf16(acc[nt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+    }
+    // acc[nt]: (slot r0, heads 2tq, 2tq+1), then (slot r1, same heads)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = nt * 8 + 2 * tq + c;
+        if (h < G) {
+          if (r0 < n) sm.logit[h][r0] = s0 >= 0 ? a.scale * acc[nt][c] : ninf;
+          if (r1 < n) sm.logit[h][r1] = s1 >= 0 ? a.scale * acc[nt][2 + c] : ninf;
+        }
       }
-    const float dot = sa_reduce_scatter32(x);
-    const int h = lane / P, i = lane % P;
-    if (j + i < n) sm.logit[h][j + i] = sm.slot[j + i] >= 0 ? a.scale * dot : -__int_as_float(0x7f800000);
   }
   __syncthreads();
 
@@ -225,7 +286,7 @@ sparse_attn_kernel(SaArgs a) {
     for (int e = 0; e < E / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
   constexpr int U = 4;  // value rows in flight per warp
   for (int j = warp * U; j < n; j += kSaWarps * U) {
-    prefetch_rows(a.v, j + kAhead * kSaWarps * U, U);
+    prefetch_rows(a.v, j + 4 * kSaWarps * U, U);  // 4 value steps ahead
     float2 vv[U][E / 2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {

@@ -47,12 +47,14 @@ def pool_rows_of(page_table_row, nb, page_size):
 
 def attn_tolerance(q_bits, k_bits, v_bits, slots, scale, chunk=256):
     """Per-element bound of the sparse-attention comparison [rows][h_q][d].
-    A logit is an FP32 sum of exact BF16 products: each lane adds d/32 of
-    them in order, then a 5-level butterfly adds the lanes, so its error is
-    at most (d/32 + 5) 2^-24 scale sum|q k|; the weights carry twice that
-    relative error plus 2^-22 for exp; a warp adds at most chunk/4 weighted
-    rows in order.  Bound on |out - out_ref|: that relative error times
-    max_j |v_j| (over the valid entries), plus 1e-6."""
+    A logit is a tensor-core FP32 accumulation of exact BF16 products:
+    d/16 steps, each adding 16 products to the running sum; allowing each
+    step 2^-22 of sum|q k| (twice a rounding, for an adder that may
+    truncate), plus one step for the scale, its error is at most
+    (d/16 + 1) 2^-22 scale sum|q k|; the weights carry twice that relative
+    error plus 2^-22 for exp; a warp adds at most chunk/4 weighted rows in
+    order.  Bound on |out - out_ref|: that relative error times max_j |v_j|
+    (over the valid entries), plus 1e-6."""
     q = oracle.bf16_to_float(q_bits)   # [rows][h_q][d]
     k = oracle.bf16_to_float(k_bits)   # [n_slots][h_kv][d]
     v = oracle.bf16_to_float(v_bits)
@@ -60,7 +62,7 @@ def attn_tolerance(q_bits, k_bits, v_bits, slots, scale, chunk=256):
     h_kv = k.shape[1]
     g = h_q // h_kv
     tol = np.zeros(q.shape)
-    gam = (d / 32 + 5) * 2.0 ** -24
+    gam = (d / 16 + 1) * 2.0 ** -22
     for t in range(rows):
         sl = slots[t]
         sl = sl[(sl >= 0) & (sl < k.shape[0])]
