@@ -399,6 +399,14 @@ def test_fused_parity_prefill_chunk(qsa):
     check_fused(qsa, decode_workload(53, [[4000 + i for i in range(300)]], page_size=64, k_blk=512))
 
 
+def test_fused_parity_prefill_ragged_row_tiles(qsa):
+    """777 consecutive query rows: the prefill tile-height plan (more than 64
+    rows per request) takes 40-row tiles on 152 SMs, so the last row tile
+    holds 17 rows, and every key tile but the causal edge is fully visible to
+    its row tile (the epilogue's fast path)."""
+    check_fused(qsa, decode_workload(57, [[6001 + i for i in range(777)]], page_size=64, k_blk=512))
+
+
 def test_fused_parity_prefill_c5_sampled(qsa):
     """The full prefill chunk (4096 rows, L = 131,072): scores checked on 24
     sampled rows, selection and slots on 64."""
