@@ -469,14 +469,30 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
   int cols = 32;
   while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
   t.tmem_cols = cols;
-  // one CTA per SM (the key ring takes most of shared memory); key tiles per
-  // CTA: about one wave of CTAs in total
-  const int64_t x_ctas = std::max<int64_t>(1, std::min<int64_t>(n_kt, sm_count / (row_tiles * n_req)));
+  // One CTA per SM with the whole key ring, or two per SM with half of it
+  // each when that leaves fewer key tiles on the busiest SM: 32 verify
+  // requests split 4 ways fill only 128 SMs (40 tiles each), split 9 ways
+  // they fill all of them (at most 36 tiles per SM).  Key tiles per CTA:
+  // about one wave of CTAs in total.
+  const int64_t units = row_tiles * n_req;
+  int per_sm = 1;
+  int64_t x_ctas = std::max<int64_t>(1, std::min<int64_t>(n_kt, sm_count / units));
+  if (units <= sm_count) {
+    const int64_t t1 = (n_kt + x_ctas - 1) / x_ctas;
+    const int64_t x2 = std::max<int64_t>(1, std::min<int64_t>(n_kt, 2 * sm_count / units));
+    const int64_t t2 = (n_kt + x2 - 1) / x2;
+    const int64_t busy2 = units * ((n_kt + t2 - 1) / t2) > sm_count ? 2 * t2 : t2;
+    if (busy2 < t1) {
+      per_sm = 2;
+      x_ctas = x2;
+    }
+  }
   t.tiles_per_cta = (int32_t)((n_kt + x_ctas - 1) / x_ctas);
   t.pt_cap = (int32_t)std::min<int64_t>(kTcPtStage, (int64_t)t.tiles_per_cta * kTcM / kpp + 2);
   const size_t fixed = 1024 + 2 * (size_t)t.n_cols * 128 + (2 * kTcMaxStages + 4) * 8 + sizeof(TmCtl) +
                        4 * (size_t)t.rows_per_tile + 4 * (size_t)t.pt_cap;
-  t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / (2 * kTcHalf));
+  const size_t budget = per_sm == 1 ? (size_t)kTcMaxSmem : (size_t)kTcMaxSmem / 2 - 1024;
+  t.stages = (int)std::min<size_t>(kTcMaxStages, (budget - fixed) / (2 * kTcHalf));
   if (t.stages < 2) return QSA_ERR_UNSUPPORTED;
   const size_t smem = fixed + (size_t)t.stages * 2 * kTcHalf;
   // wide tiles (prefill) get 16 epilogue warps, narrow ones 8
