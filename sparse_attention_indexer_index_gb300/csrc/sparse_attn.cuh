@@ -30,7 +30,7 @@
 //  3. Values: each warp accumulates sum_j w_hj v_j for its slots (weights
 //     broadcast from shared memory; packed fma.rn.f32x2), the 4 warps' sums
 //     are added in shared memory.
-// Every warp requests into L2 the K rows of its next 2 tiles and the V rows
+// Every warp requests into L2 the K rows of its next tile and the V rows
 // of its next 4 value steps ahead of its loads.  One chunk: the CTA
 // normalises and writes out and lse; several: it writes (m, l, unnormalised
 // sum) and a second kernel merges the chunks of every (row, head).
@@ -176,7 +176,7 @@ sparse_attn_kernel(SaArgs a) {
   constexpr int NT = (G + 7) / 8;     // n-tiles of 8 heads
   constexpr int QW = D / 32;          // 16-byte words of a lane (one per 32 elements)
   constexpr int kLines = D * 2 / 128; // 128-byte lines of a row
-  constexpr int kAhead = 2;           // tiles of K rows requested into L2 ahead
+  constexpr int kAhead = 1;           // tiles of K rows requested into L2 ahead
   const int gq = lane >> 2, tq = lane & 3;
   uint32_t bq[NT][KS][2];  // B fragments: head nt*8 + gq
 #pragma unroll
