@@ -30,8 +30,9 @@
 //  3. Values: each warp accumulates sum_j w_hj v_j for its slots (weights
 //     broadcast from shared memory; packed fma.rn.f32x2), the 4 warps' sums
 //     are added in shared memory.
-// Every warp requests into L2 the K rows of its next tile and the V rows
-// of its next 4 value steps ahead of its loads.  One chunk: the CTA
+// Every warp requests into L2 the K rows of its next tile ahead of its
+// loads (further look-ahead, and any for the V rows, measured slower: the
+// loads in flight already cover the latency).  One chunk: the CTA
 // normalises and writes out and lse; several: it writes (m, l, unnormalised
 // sum) and a second kernel merges the chunks of every (row, head).
 #pragma once
@@ -207,16 +208,8 @@ sparse_attn_kernel(SaArgs a) {
       }
     }
   };
-  // the V rows of this warp's first value steps, and the first K tiles
-  auto prefetch_rows = [&](const uint16_t* base, int jj, int rows) {
-    if (lane < rows * kLines) {
-      const int s = jj + lane / kLines < n ? sm.slot[jj + lane / kLines] : -1;
-      if (s >= 0)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + ((int64_t)s * a.h_kv + g) * D + (lane % kLines) * 64));
-    }
-  };
+  // the first K tiles
   for (int d = 0; d < kAhead; ++d) prefetch_tile(warp * 16 + d * kSaWarps * 16);
-  for (int d = 0; d < 4; ++d) prefetch_rows(a.v, warp * 4 + d * kSaWarps * 4, 4);
   const float ninf = -__int_as_float(0x7f800000);
   for (int j = warp * 16; j < n; j += kSaWarps * 16) {
     prefetch_tile(j + kAhead * kSaWarps * 16);
@@ -286,7 +279,6 @@ sparse_attn_kernel(SaArgs a) {
     for (int e = 0; e < E / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
   constexpr int U = 4;  // value rows in flight per warp
   for (int j = warp * U; j < n; j += kSaWarps * U) {
-    prefetch_rows(a.v, j + 4 * kSaWarps * U, U);  // 4 value steps ahead
     float2 vv[U][E / 2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
