@@ -477,7 +477,7 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
   const int64_t units = row_tiles * n_req;
   int per_sm = 1;
   int64_t x_ctas = std::max<int64_t>(1, std::min<int64_t>(n_kt, sm_count / units));
-  if (units <= sm_count) {
+  if (units <= sm_count && 2 * t.tmem_cols <= 512) {  // two CTAs' accumulators fit the SM's TMEM
     const int64_t t1 = (n_kt + x_ctas - 1) / x_ctas;
     const int64_t x2 = std::max<int64_t>(1, std::min<int64_t>(n_kt, 2 * sm_count / units));
     const int64_t t2 = (n_kt + x2 - 1) / x2;
