@@ -1024,7 +1024,7 @@ score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
     // (reloaded only when the group changes)
     int len_t0 = -1, my_len = 0;
     for (int i = 0; i < n_items; ++i) {
-      const int st = i % S, acc = i & 1;
+      const int acc = i & 1;
       // the descriptor comes through desc_ready (a plain arrive by the MMA
       // thread, which read it after `full`); acc_full completes through the
       // tensor core
