@@ -6,8 +6,10 @@ all visible compressed blocks for the 6 query rows, keep the best 512 per
 row, expand to token positions plus pending tokens, translate to physical KV
 slots).  The reported value is query rows per second.
 
-Timing: the L2 cache (129 MB) is flushed before every timed step by writing a
-256 MB buffer, outside the timed region; each step is bracketed by CUDA
+Timing: the L2 cache (129 MB) is flushed before every timed step, outside the
+timed region: a 256 MB buffer is written, then another 256 MB buffer is read,
+so the step starts with none of its data in L2 and with no dirty lines of the
+flush left for the step to write back; each step is bracketed by CUDA
 events on the launching stream.  W untimed warm-up steps come first.  Under
 torchrun every rank runs an independent replica (the path shards by request
 with no exchange), and the time is the maximum over ranks.
@@ -168,10 +170,15 @@ class Gpu:
         import sparse_attention_indexer_index_gb300 as qsa
         self.torch, self.qsa, self.dev = torch, qsa, device
         self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_sum = torch.empty((), dtype=torch.float32, device=device)
         self.stream = torch.cuda.current_stream(device)
 
     def flush(self):
+        """Evict the step's data from L2: write 256 MB, then read 256 MB of
+        another buffer (the written lines are cleaned here, not in the step)."""
         self.flush_buf.fill_(1.0)
+        self.torch.sum(self.flush_read, 0, out=self.flush_sum)
 
     def h2d(self, a, dtype=None):
         t = self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
@@ -289,32 +296,23 @@ def select_only(g: Gpu, st):
 
 def kernel_names(w, sm_count=152):
     """Kernels the library dispatches to for this workload (the launch rules
-    of qsa_api.cu: requests with 2+ rows use the tensor-core scorer, fed by
-    TMA when a page holds a multiple of 8 compressed keys; one-row requests
-    use the balanced tensor-core scorer on such pages; rows of up to
-    32768 blocks take a cluster of 8 CTAs per row when rows * 8 <= SMs, the
-    shared-memory-resident single-CTA selection up to two rows per SM and
-    small CTAs (four per SM) for more rows; longer rows a
-    cluster of 2-16 CTAs per row when rows * 2 <= SMs, one streaming CTA per
-    row otherwise)."""
-    tma = (w.page_size // 4) % 8 == 0 and w.pool_rows % 8 == 0
-    balanced = tma and w.max_rows_per_req == 1
-    if balanced:
-        score = "score_tcb_kernel"
+    of qsa_api.cu: requests of up to 8 rows on pages holding a multiple of 8
+    compressed keys use the mma.sync decode scorer, requests with more rows
+    the tensor-core tile scorer (fed by TMA on such pages, by cp.async on
+    smaller ones), one-row requests on small pages the CUDA-core scorer; rows
+    of more than 32768 blocks take a cluster of 2-16 CTAs per row when
+    rows * 2 <= SMs (one streaming CTA per row otherwise), more than two rows
+    per SM take small CTAs (four per SM), other rows (k <= 1024) one
+    register-resident CTA per row)."""
+    kpp = w.page_size // 4
+    if kpp % 8 == 0 and w.max_rows_per_req <= 8:
+        score = "score_mma_kernel"
     elif w.max_rows_per_req >= 2:
-        score = "score_tc_kernel" if tma else "score_tc_cpasync_kernel"
+        score = "score_tc_kernel" if kpp % 8 == 0 and w.pool_rows % 8 == 0 else "score_tc_cpasync_kernel"
     else:
         score = "score_decode_kernel"
-    if w.max_len // 4 > 32768:
-        select = "select_long_kernel" if w.n_rows * 2 <= sm_count else "select_kernel"
-    elif w.n_rows * 8 <= sm_count:
-        select = "select_cluster_kernel"
-    elif w.n_rows > 2 * sm_count:
-        select = "select_rows_kernel"
-    else:
-        select = "select_resident_kernel"
     return {"compress": "compress_keys_kernel", "append": "append_keys_kernel", "score": score,
-            "select": select}
+            "select": topk_kernel_name(w.n_rows, w.max_len // 4, sm_count, w.k_blk)}
 
 
 def kernel_bytes(w, new_blocks):
@@ -504,13 +502,17 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     return res
 
 
-def topk_kernel_name(n_rows, n, sm_count=152):
-    """The selection kernel topk_select runs for n_rows rows of n scores."""
+def topk_kernel_name(n_rows, n, sm_count=152, k=2048):
+    """The selection kernel for n_rows rows of n scores and k winners."""
     if n > 32768:
         return "select_long_kernel" if n_rows * 2 <= sm_count else "select_kernel"
+    if n_rows > 2 * sm_count:
+        return "select_rows_kernel"
+    if k <= 1024:
+        return "select_fast_kernel"
     if n_rows * 8 <= sm_count:
         return "select_cluster_kernel"
-    return "select_rows_kernel" if n_rows > 2 * sm_count else "select_resident_kernel"
+    return "select_resident_kernel"
 
 
 def bench_variant_topk(g, w, iters, warmup, peaks):
@@ -529,7 +531,7 @@ def bench_variant_topk(g, w, iters, warmup, peaks):
             "rows_per_s": s.shape[0] / (ms * 1e-3), "alg_bytes": alg,
             "alg_GBps": alg / (ms * 1e-3) / 1e9, "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "dup_fraction": w.dup_fraction,
-            "kernel": topk_kernel_name(int(s.shape[0]), int(w.n_valid.max()))}
+            "kernel": topk_kernel_name(int(s.shape[0]), int(w.n_valid.max()), k=w.k)}
 
 
 def bench_variant_indexshare(g, w, iters, warmup, peaks):
@@ -831,7 +833,7 @@ def main():
                    "step": f"one qsa_decode_step call: the rows' {int(st['kp_rts_h'][-1])} own index "
                            "key(s) appended through the 4-slot ring (the blocks they complete "
                            "compressed) + fused score/top-512/expand/slots, replayed from a CUDA graph",
-                   "l2": "flushed (256 MB write) before every timed step",
+                   "l2": "flushed before every timed step (256 MB written, then 256 MB of another buffer read)",
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": 1e3 * ms,
         "us_per_step_median": 1e3 * statistics.median(step_ms),

@@ -13,12 +13,14 @@
 #include "compress.cuh"
 #include "expand.cuh"
 #include "score_decode.cuh"
+#include "score_mma.cuh"
 #include "score_tc.cuh"
 #include "select.cuh"
 #include "select_resident.cuh"
 #include "select_cluster.cuh"
 #include "select_long.cuh"
 #include "select_rows.cuh"
+#include "select_fast.cuh"
 #include "sparse_attn.cuh"
 
 using namespace qsa;
@@ -105,10 +107,6 @@ qsa_status device_info(DeviceInfo** out) {
                              kTcMaxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcMaxSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTcMaxSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(score_tcb_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -124,6 +122,20 @@ qsa_status device_info(DeviceInfo** out) {
         cudaGetLastError();
     }
     if (!set_attn_smem()) return QSA_ERR_CUDA;
+    if (cudaFuncSetAttribute(select_fast_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SfShared)) != cudaSuccess ||
+        cudaFuncSetAttribute(select_fast_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SfShared)) != cudaSuccess)
+      return QSA_ERR_CUDA;
+    if (cudaFuncSetAttribute(score_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_smem_bytes(kSmMaxReq, 1)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_smem_bytes(kSmMaxReq, 2)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_mma_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_smem_bytes(kSmMaxReq, 3)) != cudaSuccess ||
+        cudaFuncSetAttribute(score_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_smem_bytes(kSmMaxReq, 4)) != cudaSuccess)
+      return QSA_ERR_CUDA;
     if (cudaFuncSetAttribute(select_rows_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SrSmem)) != cudaSuccess ||
         cudaFuncSetAttribute(select_rows_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -366,6 +378,32 @@ qsa_status launch_select_rows(const SelectArgs& a, bool pdl, cudaStream_t stream
   return QSA_OK;
 }
 
+// Rows of up to kSfMaxRow entries with k <= kSfMaxK: one 1024-thread CTA per
+// row holding the row in registers (select_fast_kernel).
+template <int kMode>
+qsa_status launch_select_fast(const SelectArgs& a, bool pdl, cudaStream_t stream) {
+  if (a.n_max > kSfMaxRow || a.k > kSfMaxK) return QSA_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_rows, 1, 1);
+  cfg.blockDim = dim3(kSfThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(SfShared);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, select_fast_kernel<kMode>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
+}
+
 template <int kMode>
 qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count = 0) {
   if (a.n_rows == 0) return QSA_OK;
@@ -375,6 +413,10 @@ qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int
   }
   {
     const qsa_status st = launch_select_rows<kMode>(a, pdl, stream, sm_count);
+    if (st != QSA_ERR_UNSUPPORTED) return st;
+  }
+  {
+    const qsa_status st = launch_select_fast<kMode>(a, pdl, stream);
     if (st != QSA_ERR_UNSUPPORTED) return st;
   }
   if (sm_count > 0) {
@@ -512,101 +554,57 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
   return QSA_OK;
 }
 
-// The query rows as a 2-D tensor [n_rows * 4][128] BF16 for the balanced
-// scorer's B operand: boxes of 64 x n_cols with the 128-byte swizzle (one
-// K-half of the n_cols query heads starting at a row tile's first head).
-bool encode_q_map(CUtensorMap* m, const void* q, int32_t n_rows, int n_cols) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)n_rows * kHeads};
-  const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)n_cols};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Balanced tensor-core scorer for decode batches (one row per request,
-// TMA-compatible pages): the key tiles of all requests split evenly over one
-// CTA per SM.  QSA_ERR_UNSUPPORTED: take another path.
-qsa_status launch_scores_balanced(const ScoreArgs& s, int max_rows_per_req, int sm_count,
-                                  cudaStream_t stream) {
-  const int64_t nb_max = s.max_len / kBlock;
-  if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
-  // Measured: requests with several rows run faster on the per-request
-  // kernel (its tiles already spread over the grid, and it starts sooner).
-  if (max_rows_per_req != 1 || (int64_t)s.n_req > kTbMaxGroups) return QSA_ERR_UNSUPPORTED;
-  const int kpp = s.page_size / kBlock;
-  int R = 0;
-  for (int c = kTcM; c >= 8; c >>= 1)
-    if (kpp % c == 0) {
-      R = c;
-      break;
-    }
-  if (R == 0 || s.pool_rows <= 0 || s.pool_rows > INT32_MAX || s.pool_rows % 8 != 0) return QSA_ERR_UNSUPPORTED;
-  if ((int64_t)s.n_rows * kHeads > INT32_MAX) return QSA_ERR_UNSUPPORTED;
-  TcArgs t{};
-  t.q = s.q;
-  t.pool = s.pool;
-  t.pool_rows = s.pool_rows;
-  t.n_req = s.n_req;
-  t.req_row_start = s.req_row_start;
-  t.n_rows = s.n_rows;
-  t.row_len = s.row_len;
-  t.max_len = s.max_len;
-  t.page_table = s.page_table;
-  t.ld_pt = s.ld_pt;
-  t.page_size = s.page_size;
-  t.scores = s.scores;
-  t.ld_scores = s.ld_scores;
-  t.rows_per_tile = max_rows_per_req;
-  t.n_cols = ((4 * t.rows_per_tile) + 15) & ~15;
-  int cols = 32;
-  while (cols < 2 * t.n_cols) cols *= 2;  // two accumulators
-  t.tmem_cols = cols;
-  t.trigger_dependents = s.trigger_dependents;
-  t.new_pos = s.new_pos;
-  t.box_rows = R;
-  t.box4d = 1;
-  t.row_tiles = 1;
-  t.n_groups = s.n_req;
-  CUtensorMap pool_map, q_map;
-  if (!encode_pool_map(&pool_map, t.pool, t.pool_rows, R, true) || !encode_q_map(&q_map, t.q, s.n_rows, t.n_cols))
-    return QSA_ERR_UNSUPPORTED;
-  const size_t stage_bytes = ((size_t)2 * kTcHalf + 2 * (size_t)t.n_cols * 128 + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + (2 * kTcMaxStages + 6) * 8 + kTcMaxStages * sizeof(TbDesc) + sizeof(TbCtl) +
-                       4 * (4 * (size_t)t.n_groups + 1);
-  t.stages = (int)std::min<size_t>(kTcMaxStages, ((size_t)kTcMaxSmem - fixed) / stage_bytes);
-  if (t.stages < 3) return QSA_ERR_UNSUPPORTED;
-  const size_t smem = fixed + (size_t)t.stages * stage_bytes;
+// Decode scorer on mma.sync (score_mma_kernel): requests of up to kSmMaxRows
+// rows on pages holding a multiple of 8 compressed keys.  About one wave of
+// CTAs (three per SM), at least one 16-block tile per warp.
+template <int NT>
+qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream) {
+  const size_t smem = sm_smem_bytes(s.n_req, NT);
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_tcb_kernel, kTmThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_mma_kernel<NT>, kSmThreads, smem) != cudaSuccess)
     return QSA_ERR_CUDA;
-  if ((int64_t)occ * t.tmem_cols > 512) return QSA_ERR_UNSUPPORTED;
-  const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + kTcM - 1) / kTcM);
-  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(tiles_max, sm_count));
-  if (launch_pdl(score_tcb_kernel, dim3((unsigned)ctas), dim3(kTmThreads), smem, stream, t, pool_map, q_map) !=
-      cudaSuccess) {
+  const int64_t nb_max = s.max_len / kBlock;
+  const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + kSmTile - 1) / kSmTile);
+  const int64_t ctas =
+      std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(occ, 1) * sm_count, (tiles_max + kSmWarps - 1) / kSmWarps));
+  if (launch_pdl(score_mma_kernel<NT>, dim3((unsigned)ctas), dim3(kSmThreads), smem, stream, s) != cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
-  }
-  if (s.n_fill > 0) {
-    fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
-                                                              s.n_fill);
-    return launch_status();
   }
   return QSA_OK;
 }
 
-// Scorer dispatch: the balanced tensor-core kernel for decode batches, the
-// per-request tensor-core kernel for requests with several rows, the CUDA-
-// core streaming kernel otherwise.
+qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
+  const int64_t nb_max = s.max_len / kBlock;
+  if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
+  const int kpp = s.page_size / kBlock;
+  if (kpp % 8 != 0 || max_rows_per_req > kSmMaxRows || s.n_req > kSmMaxReq || s.pool_rows <= 0 ||
+      s.pool_rows > INT32_MAX || (int64_t)s.n_req * ((nb_max + kSmTile - 1) / kSmTile) > INT32_MAX)
+    return QSA_ERR_UNSUPPORTED;
+  qsa_status st;
+  switch ((max_rows_per_req + 1) / 2) {
+    case 1: st = launch_scores_mma_nt<1>(s, sm_count, stream); break;
+    case 2: st = launch_scores_mma_nt<2>(s, sm_count, stream); break;
+    case 3: st = launch_scores_mma_nt<3>(s, sm_count, stream); break;
+    default: st = launch_scores_mma_nt<4>(s, sm_count, stream); break;
+  }
+  if (st == QSA_OK && s.n_fill > 0) {
+    fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
+                                                              s.n_fill);
+    return launch_status();
+  }
+  return st;
+}
+
+// Scorer dispatch: the mma.sync decode kernel for requests of up to 8 rows
+// on pages of a multiple of 32 tokens, the per-request tensor-core kernel for
+// requests with more rows (or several rows on smaller pages), the CUDA-core
+// streaming kernel otherwise.
 qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream);
 qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream);
 qsa_status launch_scorer(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
-  const qsa_status b = launch_scores_balanced(s, max_rows_per_req, sm_count, stream);
-  if (b != QSA_ERR_UNSUPPORTED) return b;
+  const qsa_status m = launch_scores_mma(s, max_rows_per_req, sm_count, stream);
+  if (m != QSA_ERR_UNSUPPORTED) return m;
   return max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, sm_count, stream)
                                         : launch_scores(s, sm_count, stream);
 }

@@ -1,0 +1,292 @@
+// score_mma.cuh -- decode block scorer on the warp-level tensor-core path
+// (mma.sync m16n8k16, BF16 in, FP32 accumulate), keys streamed with plain
+// 16-byte loads.
+//
+// Qwen3.8-Flash-Next day-0 write-up (theainews.cc), section "Qwen sparse
+// attention (QSA)", score equation:
+//   s[t][b] = (1/sqrt(128)) * sum_{h<4} ReLU(<q[t][h], kbar[b]>)
+// for the visible compressed blocks b < row_len[t]/4 of each decode row; the
+// keys are found through the page table at full_slot/4.
+//
+// Why this shape: decode scoring is a stream of 256-byte keys with a few
+// query rows per request.  Measured on this GPU, 16-byte loads issued by
+// many warps stream scattered 4 KB pages at ~6.5 TB/s, while TMA and
+// bulk-copy rings stop near 5.5 TB/s; the arithmetic (4 heads x rows x 128
+// MACs per key) fits easily on mma.sync (~0.47 MMAs per clock per SM
+// measured, a decode row needs < 0.05), so no shared-memory staging of the
+// keys is needed at all:
+//  - A tile is 16 consecutive blocks of one request (one MMA M): one 4 KB run
+//    of pool rows when a page holds a multiple of 16 compressed keys, two
+//    2 KB runs when it holds 8 (32-token pages).
+//  - Lane (g, t) of a warp loads the 16-byte chunks 4c + t (c < 4) of key rows
+//    g and g + 8 straight into A fragments.  The MMA's K index is a
+//    permutation of the head dimension: step (c, h) pairs logical columns
+//    {2t, 2t+1} / {2t+8, 2t+9} with dims 8(4c+t) + 4h + {0,1} / {2,3}; the
+//    query columns (B) use the same permutation, so each B fragment is one
+//    16-byte chunk of a query head.  A warp instruction reads 8 rows x 64
+//    contiguous bytes.
+//  - N = 8 columns = 2 rows x 4 heads per n-tile; up to 4 n-tiles (8 rows).
+//    The B fragments of the current request sit in the warp's own slot of
+//    shared memory (re-staged only when the request changes).
+//  - Epilogue in registers: ReLU, the 4-head sum (one shuffle), the scale.
+//  - Every CTA builds the list of tiles of all requests (prefix over the
+//    requests' visible blocks); each warp takes a balanced contiguous range.
+//    One lane per tile issues a 4 KB bulk prefetch into L2 kSmAhead tiles
+//    ahead, so HBM sees many pages in flight without holding them in
+//    registers; the fragment loads then hit L2.
+//  - Page-table entries of the next 32 tiles are fetched one tile per lane.
+#pragma once
+
+#include "common.cuh"
+#include "score_decode.cuh"
+
+namespace qsa {
+
+constexpr int kSmWarps = 8;
+constexpr int kSmThreads = 32 * kSmWarps;
+constexpr int kSmTile = 16;        // keys per tile (MMA M)
+constexpr int kSmMaxRows = 8;      // rows per request: 4 n-tiles of 2 rows x 4 heads
+constexpr int kSmMaxReq = 4096;    // requests per launch (tile prefix in shared memory)
+constexpr int kSmAhead = 4;        // tiles requested into L2 ahead of their fragment loads
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Dynamic shared memory of one CTA: the tile prefix, then per warp a slot of
+// NT x 4 x 32 B fragments (16 bytes each).
+__host__ __device__ constexpr size_t sm_smem_bytes(int n_req, int nt) {
+  return (((size_t)(n_req + 1) * 4 + 15) & ~(size_t)15) + (size_t)kSmWarps * nt * 4 * 32 * 16;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kSmThreads, 3) score_mma_kernel(ScoreArgs a) {
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  int* g_pre = reinterpret_cast<int*>(sm_raw);  // [n_req + 1]: tiles before request r
+  uint4* bslot_all = reinterpret_cast<uint4*>(sm_raw + ((((size_t)a.n_req + 1) * 4 + 15) & ~(size_t)15));
+  __shared__ int s_wsum[kSmWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  uint4* bslot = bslot_all + (size_t)warp * NT * 4 * 32;  // [nt][c][lane]
+
+  // Without new_pos nothing is read before the previous grid completes.
+  // With it (the key path of the same step runs before): the metadata, the
+  // queries and keys the key path does not write are read at once; a warp
+  // waits before its first tile that reaches block new_pos[r] / 4.
+  const bool relaxed = a.new_pos != nullptr;
+  if (!relaxed) pdl_wait_primary();
+  if (a.trigger_dependents) pdl_launch_dependents();
+
+  // ---- tile list: ceil(nb_r / 16) tiles per request, prefix in shared memory
+  {
+    const int per = (a.n_req + kSmThreads - 1) / kSmThreads;
+    const int r_lo = min(a.n_req, (int)threadIdx.x * per), r_hi = min(a.n_req, r_lo + per);
+    int local = 0;
+    for (int r = r_lo; r < r_hi; ++r) {
+      local += (request_blocks(a, r) + kSmTile - 1) / kSmTile;
+      g_pre[r + 1] = local;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int before = incl - local;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    for (int r = r_lo; r < r_hi; ++r) g_pre[r + 1] += before;
+    if (threadIdx.x == 0) g_pre[0] = 0;
+    __syncthreads();
+  }
+  const int64_t T = g_pre[a.n_req];
+  const int64_t W = (int64_t)gridDim.x * kSmWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kSmWarps + warp;
+  const int i0 = (int)(T * gw / W), i1 = (int)(T * (gw + 1) / W);
+  // With new_pos, thread 0 of CTA 0 waits for the previous grid before it
+  // leaves, so that this grid still completes after it.
+  const bool anchor = relaxed && blockIdx.x == 0 && threadIdx.x == 0;
+  if (i0 >= i1) {
+    if (anchor) pdl_wait_primary();
+    return;
+  }
+
+  const int kpp = a.page_size / kBlock;  // compressed keys per page (a multiple of 8 here)
+  // Request of tile i: last r with g_pre[r] <= i (binary search).
+  auto request_of = [&](int i) {
+    int lo = 0, hi = a.n_req - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g_pre[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  // Pool rows of tile i's keys 0-7 and 8-15 (one run when a page holds a
+  // multiple of 16 keys, two pages of 8 otherwise); -1 if a page is out of
+  // range.
+  auto run_row = [&](int r, int b) -> int {
+    const int page_idx = b / kpp;
+    if (page_idx >= a.ld_pt) {
+      raise_fault(kFaultIndex);
+      return -1;
+    }
+    const int64_t page = __ldg(a.page_table + (int64_t)r * a.ld_pt + page_idx);
+    const int64_t row = page * kpp + (int64_t)(b - page_idx * kpp);
+    if (page < 0 || row >= a.pool_rows) {
+      raise_fault(kFaultPool);
+      return -1;
+    }
+    return (int)row;
+  };
+  auto tile_rows = [&](int i, int& ra, int& rb) {
+    ra = rb = -1;
+    if (i >= i1) return;
+    const int r = request_of(i);
+    const int b = (i - g_pre[r]) * kSmTile;
+    ra = run_row(r, b);
+    rb = kpp % kSmTile == 0 ? (ra >= 0 ? ra + 8 : -1) : run_row(r, b + 8);
+  };
+  int base = i0;
+  int pa_cur, pb_cur, pa_nxt, pb_nxt;
+  tile_rows(i0 + lane, pa_cur, pb_cur);
+  tile_rows(i0 + 32 + lane, pa_nxt, pb_nxt);
+  auto rows_of = [&](int i, int& ra, int& rb) {  // warp-uniform i in [base, base + 64)
+    const int d = i - base;
+    ra = __shfl_sync(0xffffffffu, d < 32 ? pa_cur : pa_nxt, d & 31);
+    rb = __shfl_sync(0xffffffffu, d < 32 ? pb_cur : pb_nxt, d & 31);
+  };
+  // The tile's pool rows (clipped to the pool) into L2: one 4 KB run, or two
+  // 2 KB runs.
+  auto prefetch_run = [&](int prow, int rows) {
+    if (prow >= 0)
+      prefetch_l2_bulk(a.pool + (int64_t)prow * kDim, (uint32_t)(rows < a.pool_rows - prow ? (int64_t)rows : a.pool_rows - prow) * kDim * 2);
+  };
+  auto prefetch_tile = [&](int ra, int rb) {
+    if (ra >= 0 && rb == ra + 8) {
+      prefetch_run(ra, kSmTile);
+    } else {
+      prefetch_run(ra, 8);
+      prefetch_run(rb, 8);
+    }
+  };
+  // L2 prefetch of the first kSmAhead tiles (one lane each; kSmAhead < 32).
+  if (lane < kSmAhead && i0 + lane < i1) prefetch_tile(pa_cur, pb_cur);
+
+  int r = -1, nb_req = 0, t0 = 0, nrows = 0, first_new = INT_MAX;
+  int nbr[NT];
+  bool waited = !relaxed;
+  for (int i = i0; i < i1; ++i) {
+    if (i - base >= 32) {  // next batch of pool rows
+      base += 32;
+      pa_cur = pa_nxt;
+      pb_cur = pb_nxt;
+      tile_rows(base + 32 + lane, pa_nxt, pb_nxt);
+    }
+    // L2 prefetch kSmAhead tiles ahead
+    if (i + kSmAhead < i1) {
+      int ra, rb;
+      rows_of(i + kSmAhead, ra, rb);
+      if (lane == 0) prefetch_tile(ra, rb);
+    }
+    // ---- request change: stage its query fragments, row lengths --------------
+    if (r < 0 || i >= g_pre[r + 1]) {
+      if (r < 0) r = request_of(i);
+      while (i >= g_pre[r + 1]) ++r;  // g_pre is non-decreasing: empty requests are skipped
+      t0 = __ldg(a.req_row_start + r);
+      nrows = min(__ldg(a.req_row_start + r + 1) - t0, 2 * NT);
+      if (__ldg(a.req_row_start + r + 1) - t0 > 2 * NT && lane == 0) raise_fault(kFaultGrouping);
+      first_new = relaxed ? max(0, __ldg(a.new_pos + r)) / kBlock : INT_MAX;
+      int mx = 0;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int rl = 2 * nt + (t >> 1);
+        int nb = 0;
+        if (rl < nrows) {
+          const int L = __ldg(a.row_len + t0 + rl);
+          nb = (L >= 0 && L <= a.max_len) ? L / kBlock : 0;
+        }
+        nbr[nt] = nb;
+        mx = max(mx, nb);
+      }
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      nb_req = mx;  // the longest row of the request (lanes t cover all rows)
+      __syncwarp();
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int rl = 2 * nt + (g >> 2), head = g & 3;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (rl < nrows)
+            v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(t0 + rl) * kHeads + head) * kDim + 8 * (4 * c + t)));
+          bslot[(nt * 4 + c) * 32 + lane] = v;
+        }
+      }
+      __syncwarp();
+    }
+    const int j = i - g_pre[r];
+    if (!waited && kSmTile * (j + 1) > first_new) {  // this tile may hold keys the key path writes
+      pdl_wait_primary();
+      waited = true;
+    }
+    const int vis = min(kSmTile, nb_req - j * kSmTile);
+    int pra, prb;
+    rows_of(i, pra, prb);
+    // ---- A fragments: chunks 4c + t of key rows g and g + 8 ------------------
+    uint4 ka[4], kb[4];
+    bool va = pra >= 0 && g < vis, vb = prb >= 0 && g + 8 < vis;
+    if ((va && pra + g >= a.pool_rows) || (vb && prb + g >= a.pool_rows)) {
+      raise_fault(kFaultPool);
+      va = va && pra + g < a.pool_rows;
+      vb = vb && prb + g < a.pool_rows;
+    }
+    const __nv_bfloat16* ra = a.pool + ((int64_t)max(pra, 0) + g) * kDim + 8 * t;
+    const __nv_bfloat16* rb = a.pool + ((int64_t)max(prb, 0) + g) * kDim + 8 * t;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      ka[c] = va ? ld_stream_16(ra + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
+      kb[c] = vb ? ld_stream_16(rb + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 bq = bslot[(nt * 4 + c) * 32 + lane];
+        mma_bf16_16816(acc[nt], ka[c].x, kb[c].x, ka[c].y, kb[c].y, bq.x, bq.y);
+        mma_bf16_16816(acc[nt], ka[c].z, kb[c].z, ka[c].w, kb[c].w, bq.z, bq.w);
+      }
+    }
+    // ---- epilogue: ReLU, head sum (lanes t and t^1 hold the two head pairs)
+    const int b = j * kSmTile + g;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float v0 = fmaxf(acc[nt][0], 0.f) + fmaxf(acc[nt][1], 0.f);
+      float v1 = fmaxf(acc[nt][2], 0.f) + fmaxf(acc[nt][3], 0.f);
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+      const int rl = 2 * nt + (t >> 1);
+      if ((t & 1) == 0 && rl < nrows) {
+        float* dst = a.scores + (int64_t)(t0 + rl) * a.ld_scores + b;
+        if (b < nbr[nt]) dst[0] = v0 * kScoreScale;
+        if (b + 8 < nbr[nt]) dst[8] = v1 * kScoreScale;
+      }
+    }
+  }
+  if (anchor && !waited) pdl_wait_primary();
+}
+
+}  // namespace qsa

@@ -11,15 +11,18 @@
 // with M = 128 keys per tile (TMEM lanes), N = 4 * rows per tile (rounded up
 // to a multiple of 16, zero-padded), K = 128 in 8 steps of 16 (BF16 inputs,
 // FP32 accumulation in TMEM).  Both operands are K-major in shared memory
-// with the 128-byte swizzle, filled by 16-byte cp.async pieces (keys come
-// from scattered pages, so every 256-byte key row is fetched on its own).
-// One thread issues the MMAs and commits them to an mbarrier; the epilogue
-// reads TMEM (each warp its 32 lanes = 32 keys), applies ReLU, sums the 4
-// head columns of each row, scales, and stores the FP32 scores (coalesced:
-// consecutive keys of one row).  A CTA keeps its query rows resident and
-// walks a group of key tiles through a ring of up to 8 key buffers (loads run
-// stages-2 tiles ahead), and the accumulator is double-buffered in TMEM, so
-// tile k's MMA overlaps tile k-1's epilogue.
+// with the 128-byte swizzle.  score_tc_kernel (pages of a multiple of 32
+// tokens) takes the keys as TMA boxes, one 4 KB box per run of pool rows
+// through a 4-D tensor map, so the engine writes them straight into the
+// swizzled layout; score_tc_cpasync_kernel (smaller pages, whose compressed
+// rows do not form whole 8-row atoms) fills the tile with 16-byte cp.async
+// pieces, every 256-byte key row fetched on its own.  One thread issues the
+// MMAs and commits them to an mbarrier; the epilogue reads TMEM (each warp
+// its 32 lanes = 32 keys), applies ReLU, sums the 4 head columns of each
+// row, scales, and stores the FP32 scores (coalesced: consecutive keys of one
+// row).  A CTA keeps its query rows resident and walks a group of key tiles
+// through a ring of up to 8 key buffers, and the accumulator is
+// double-buffered in TMEM, so tile k's MMA overlaps tile k-1's epilogue.
 //
 // Every wait is bounded (a timeout latches kFaultWait and the CTA frees its
 // tensor memory before leaving).
@@ -59,8 +62,6 @@ struct TcArgs {
   int32_t box_rows;             // TMA kernel: pool rows per tensor-map box (8..128, divides page_size/4)
   int32_t pt_cap;               // TMA kernel: page-table entries staged in shared memory
   int32_t box4d;                // TMA kernel: 4-D view, one box per run covers both K-halves
-  int32_t row_tiles;            // balanced kernel: row tiles per request
-  int32_t n_groups;             // balanced kernel: n_req * row_tiles (<= kTbMaxGroups)
   // TMA kernels: nullptr, or per request the first position the previous
   // grid (the key path of the same step) may have written: only CTAs whose
   // blocks reach block new_pos[r]/4 wait for that grid (and CTA 0, so that
@@ -707,376 +708,6 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
   if (threadIdx.x == 0 && *abort) {
     // Drain before the shared and tensor memory are released: copies issued
     // but never seen landing, and the last committed MMAs.
-    for (int j = ctl->consumed; j < ctl->issued; ++j) {
-      const uint64_t t_start = global_timer_ns();
-      while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1u) && global_timer_ns() - t_start < 20000000ull) {
-      }
-    }
-    for (int j = max(0, ctl->mma_done - 2); j < ctl->mma_done; ++j) {
-      const uint64_t t_start = global_timer_ns();
-      while (!mbar_try_wait(&acc_full[j & 1], (uint32_t)(j >> 1) & 1u) &&
-             global_timer_ns() - t_start < 20000000ull) {
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x == 0) leave();
-  if (warp == 1) {
-    __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
-                 : "memory");
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Balanced variant for decode batches (few rows per request, many ragged
-// requests): the key tiles of all (request, row tile) groups form one list
-// that the CTAs split evenly (one CTA per SM), so a CTA crosses requests.
-// Every ring stage carries its own query rows (B operand, via a second
-// tensor map over q, loaded only when the stage last held another group's
-// rows) and a small descriptor of its tile, so a change of request costs
-// nothing in the pipeline.  The page-table entries of a tile are fetched
-// kTbPtAhead tiles ahead (cp.async into a small ring): while HBM is
-// saturated a scattered 4-byte load takes microseconds.  A stage is released
-// when its MMAs complete; the MMA thread hands the tile's descriptor to the
-// epilogue through a per-accumulator slot and barrier.  Roles as in
-// score_tc_kernel.
-// ---------------------------------------------------------------------------
-constexpr int kTbMaxRowsPerTile = 16;  // N <= 64 columns: B of a stage <= 16 KB
-constexpr int kTbMaxGroups = 2048;
-constexpr int kTbPtAhead = 8;
-
-struct TbDesc {
-  int t0, nrows, kt, nb;  // first row, rows, key tile, visible blocks (max over the rows)
-};
-struct TbCtl {
-  int abort;
-  int issued;
-  int consumed;
-  int mma_done;
-  uint32_t tmem;
-  int wsum[kTmWarps];
-  int32_t pt_ring[kTbPtAhead + 1][16];  // page entries of upcoming tiles (<= 16 runs each)
-  int b_group[kTcMaxStages];            // group whose query rows a stage's B holds (-1: none)
-  TbDesc desc_acc[2];                   // descriptor of the tile in each accumulator
-};
-
-__global__ void __launch_bounds__(kTmThreads, 1)
-score_tcb_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map,
-                 const __grid_constant__ CUtensorMap q_map) {
-  extern __shared__ __align__(16) unsigned char tb_smem_raw[];
-  // [stages x (A 32 KB | B 2 x N x 128 B)][full][empty][acc_full][acc_empty][desc_ready][descs][control]
-  // [group prefix][group first row][group rows][group blocks]
-  unsigned char* base = tb_smem_raw + ((1024u - (smem_u32(tb_smem_raw) & 1023u)) & 1023u);
-  const int S = a.stages;
-  const int N = a.n_cols;
-  const size_t stage_bytes = ((size_t)2 * kTcHalf + 2 * (size_t)N * 128 + 1023) & ~(size_t)1023;
-  auto abuf = [&](int st) { return base + (size_t)st * stage_bytes; };
-  auto bbuf = [&](int st) { return base + (size_t)st * stage_bytes + 2 * kTcHalf; };
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * stage_bytes);  // [S]
-  uint64_t* empty = full + S;                                                    // [S]
-  uint64_t* acc_full = empty + S;                                                // [2]
-  uint64_t* acc_empty = acc_full + 2;                                            // [2]
-  uint64_t* desc_ready = acc_empty + 2;                                          // [2]
-  TbDesc* desc = reinterpret_cast<TbDesc*>(desc_ready + 2);                      // [S]
-  TbCtl* ctl = reinterpret_cast<TbCtl*>(desc + S);
-  int* g_pre = reinterpret_cast<int*>(ctl + 1);  // [G + 1] key tiles before group g
-  int* g_t0 = g_pre + a.n_groups + 1;            // [G] first row of group g
-  int* g_nr = g_t0 + a.n_groups;                 // [G] rows of group g
-  int* g_nb = g_nr + a.n_groups;                 // [G] visible blocks of group g (max over rows)
-  volatile int* abort = &ctl->abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int RT = a.rows_per_tile;
-  const int kpp = a.page_size / kBlock;
-  const int G = a.n_groups;
-
-  const bool relaxed = a.new_pos != nullptr;  // see TcArgs::new_pos
-  // relaxed: CTA 0 waits before it leaves, so that this grid completes after
-  // the previous one; the producer waits before its first tile that reaches
-  // a block the previous grid may write
-  auto leave = [&]() {
-    if (relaxed && blockIdx.x == 0) pdl_wait_primary();
-  };
-  if (!relaxed) pdl_wait_primary();
-  if (a.trigger_dependents) pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pool_map)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
-  }
-
-  // ---- work list: key tiles of every (request, row tile) group -----------
-  {
-    const int per = (G + kTmThreads - 1) / kTmThreads;
-    const int glo = min(G, (int)threadIdx.x * per), ghi = min(G, glo + per);
-    int local = 0;
-    for (int g = glo; g < ghi; ++g) {
-      const int r = g / a.row_tiles, y = g - r * a.row_tiles;
-      const int row0 = __ldg(a.req_row_start + r), row1 = __ldg(a.req_row_start + r + 1);
-      int nb = 0, t0 = 0, nr = 0;
-      if (row0 < 0 || row1 < row0 || row1 > a.n_rows) {
-        if (y == 0) raise_fault(kFaultGrouping);
-      } else {
-        if (y == 0 && row1 - row0 > a.row_tiles * RT) raise_fault(kFaultGrouping);  // more rows than promised
-        t0 = row0 + y * RT;
-        const int t1 = min(row1, t0 + RT);
-        nr = max(0, t1 - t0);
-        for (int t = t0; t < t1; ++t) {
-          const int L = __ldg(a.row_len + t);
-          if (L >= 0 && L <= a.max_len) nb = max(nb, L / kBlock);
-          else raise_fault(kFaultGrouping);
-        }
-      }
-      g_t0[g] = t0;
-      g_nr[g] = nr;
-      g_nb[g] = nb;
-      local += (nb + kTcM - 1) / kTcM;
-      g_pre[g + 1] = local;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) ctl->wsum[warp] = incl;
-    __syncthreads();
-    int before = incl - local;
-    for (int w = 0; w < warp; ++w) before += ctl->wsum[w];
-    for (int g = glo; g < ghi; ++g) g_pre[g + 1] += before;
-    if (threadIdx.x == 0) g_pre[0] = 0;
-    __syncthreads();
-  }
-  const int64_t T = g_pre[G];
-  const int w0 = (int)(T * blockIdx.x / gridDim.x), w1 = (int)(T * (blockIdx.x + 1) / gridDim.x);
-  if (w0 >= w1) {
-    leave();
-    return;
-  }
-  const int n_items = w1 - w0;
-  auto group_of = [&](int w, int& g) {  // advance the cursor g to the group holding item w
-    while (g_pre[g + 1] <= w) ++g;
-  };
-  int g_first = 0;
-  {
-    int lo = 0, hi = G - 1;  // last g with g_pre[g] <= w0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (g_pre[mid] <= w0) lo = mid; else hi = mid - 1;
-    }
-    g_first = lo;
-  }
-
-
-  // ---- barriers and tensor memory -----------------------------------------
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&ctl->tmem)),
-                 "r"(a.tmem_cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kTmEpiWarps);
-      mbar_init(&desc_ready[i], 1);
-    }
-    ctl->abort = 0;
-    ctl->issued = 0;
-    ctl->consumed = 0;
-    ctl->mma_done = 0;
-    for (int i = 0; i < kTcMaxStages; ++i) ctl->b_group[i] = -1;
-    fence_mbar_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem;
-
-  if (warp == 0) {
-    // ---- producer: key runs (one 4-D box per run), the group's query rows
-    // (two 2-D boxes, only when the stage's B holds another group's rows:
-    // the previous MMAs on the stage are complete once `empty` fired), the
-    // stage descriptor --------------------------------------------------------
-    const int R = a.box_rows;
-    const int runs = kTcM / R;  // <= 16
-    int g_ahead = g_first;
-    auto prefetch = [&](int i) {  // page entries of item w0 + i -> ring slot
-      if (i < n_items) {
-        const int w = w0 + i;
-        group_of(w, g_ahead);
-        const int kt = w - g_pre[g_ahead];
-        const int r = g_ahead / a.row_tiles;
-        const int b = kt * kTcM + lane * R;
-        if (lane < runs && b < g_nb[g_ahead]) {
-          const int page_idx = b / kpp;
-          int32_t* slot = &ctl->pt_ring[i % (kTbPtAhead + 1)][lane];
-          if (page_idx < a.ld_pt) {
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(slot)),
-                         "l"(a.page_table + (int64_t)r * a.ld_pt + page_idx)
-                         : "memory");
-          } else {
-            *slot = -1;
-            raise_fault(kFaultIndex);
-          }
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");  // one group per item, possibly empty
-    };
-    for (int i = 0; i < kTbPtAhead; ++i) prefetch(i);
-    int g = g_first;
-    bool waited = !relaxed;
-    int i = 0;
-    for (; i < n_items; ++i) {
-      prefetch(i + kTbPtAhead);
-      asm volatile("cp.async.wait_group %0;" ::"n"(kTbPtAhead) : "memory");
-      __syncwarp();
-      const int st = i % S;
-      if (i >= S) {
-        const bool ok = lane == 0 ? tm_wait(&empty[st], (uint32_t)((i / S) - 1) & 1u, abort) : true;
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      }
-      const int w = w0 + i;
-      group_of(w, g);
-      const int kt = w - g_pre[g];
-      if (!waited && (int64_t)(kt + 1) * kTcM > max(0, __ldg(a.new_pos + g / a.row_tiles)) / kBlock) {
-        pdl_wait_primary();  // this tile may hold keys the previous grid writes
-        waited = true;
-      }
-      const int nb_tile = g_nb[g];
-      const int b = kt * kTcM + lane * R;  // first block of this lane's run
-      bool valid = false;
-      int prow = 0;
-      if (lane < runs && b < nb_tile) {
-        const int page_idx = b / kpp;
-        const int64_t page = ctl->pt_ring[i % (kTbPtAhead + 1)][lane];
-        const int64_t pr = page * kpp + (b - page_idx * kpp);
-        if (page >= 0 && pr < a.pool_rows) {
-          valid = true;
-          prow = (int)pr;
-          if (pr + min(R, nb_tile - b) > a.pool_rows) raise_fault(kFaultPool);
-        } else if (page_idx < a.ld_pt) {
-          raise_fault(kFaultPool);
-        }
-      }
-      const unsigned vm = __ballot_sync(0xffffffffu, valid);
-      if (lane == 0) {
-        desc[st].t0 = g_t0[g];
-        desc[st].nrows = g_nr[g];
-        desc[st].kt = kt;
-        desc[st].nb = nb_tile;
-        const bool load_b = ctl->b_group[st] != g;
-        mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(vm) * 2u * (uint32_t)R * 128u +
-                                             (load_b ? 2u * (uint32_t)N * 128u : 0u));
-        if (load_b) {
-          ctl->b_group[st] = g;
-          unsigned char* bdst = bbuf(st);
-          tma_load_2d(bdst, &q_map, 0, g_t0[g] * kHeads, &full[st]);
-          tma_load_2d(bdst + N * 128, &q_map, 64, g_t0[g] * kHeads, &full[st]);
-        }
-      }
-      __syncwarp();
-      if (valid) tma_load_4d(abuf(st) + lane * R * 256, &pool_map, prow >> 3, &full[st]);
-      __syncwarp();  // the ring slot of item i is refilled by a later prefetch
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (lane == 0) ctl->issued = i;
-  } else if (warp == 1) {
-    // ---- MMA issuer ---------------------------------------------------------
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(kTcM, N);
-      for (int i = 0; i < n_items; ++i) {
-        const int st = i % S, acc = i & 1;
-        if (!tm_wait(&full[st], (uint32_t)(i / S) & 1u, abort)) break;
-        ctl->consumed = i + 1;
-        if (i >= 2 && !tm_wait(&acc_empty[acc], (uint32_t)((i >> 1) - 1) & 1u, abort)) break;
-        // hand the tile's descriptor to the epilogue (its previous reader of
-        // this accumulator is done: acc_empty above)
-        ctl->desc_acc[acc] = desc[st];
-        mbar_arrive(&desc_ready[acc]);
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(abuf(st)), b_base = smem_u32(bbuf(st));
-        const uint32_t d = tmem + (uint32_t)(acc * N);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t koff = (uint32_t)(k >> 2);
-          const uint32_t within = (uint32_t)((k & 3) * 32);
-          const uint64_t ad = umma_desc_sw128(a_base + koff * 1024u + within, 2048u);
-          const uint64_t bd = umma_desc_sw128(b_base + koff * (uint32_t)(N * 128) + within);
-          umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&empty[st]);
-        umma_commit(&acc_full[acc]);
-        ctl->mma_done = i + 1;
-      }
-    }
-  } else {
-    // ---- epilogue -------------------------------------------------------------
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    // row lengths of the current group's rows, lane j holding row t0 + j
-    // (reloaded only when the group changes)
-    int len_t0 = -1, my_len = 0;
-    for (int i = 0; i < n_items; ++i) {
-      const int acc = i & 1;
-      // the descriptor comes through desc_ready (a plain arrive by the MMA
-      // thread, which read it after `full`); acc_full completes through the
-      // tensor core
-      const bool ok = __all_sync(0xffffffffu, tm_wait(&desc_ready[acc], (uint32_t)(i >> 1) & 1u, abort) &&
-                                                  tm_wait(&acc_full[acc], (uint32_t)(i >> 1) & 1u, abort));
-      if (!ok) break;
-      tc_fence_after();
-      const TbDesc dd = ctl->desc_acc[acc];
-      if (dd.nrows > 1 && dd.t0 != len_t0) {
-        len_t0 = dd.t0;
-        my_len = lane < dd.nrows ? __ldg(a.row_len + dd.t0 + lane) : 0;
-      }
-      const int b = dd.kt * kTcM + quarter * 32 + lane;
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
-      for (int c0 = 32 * half; c0 < N; c0 += 64) {
-        uint32_t v[32];
-        int ncols = 32;
-        if (N - c0 >= 32) {
-          tmem_ld_32cols(taddr + (uint32_t)c0, v);
-        } else {
-          uint32_t w16[16];
-          tmem_ld_16cols(taddr + (uint32_t)c0, w16);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = w16[e];
-          ncols = 16;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int tr = c0 / 4 + j;  // row within the tile (warp-uniform)
-          // one row: its visible blocks are the group's; several: its own
-          const int Lr = dd.nrows == 1 ? kBlock * dd.nb : __shfl_sync(0xffffffffu, my_len, tr & 31);
-          if (4 * j < ncols && tr < dd.nrows && b < dd.nb) {
-            const int L = Lr;
-            if (L >= 0 && L <= a.max_len && b < L / kBlock) {
-              float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
-              sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
-              sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
-              sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-              a.scores[(int64_t)(dd.t0 + tr) * a.ld_scores + b] = sc * kScoreScale;
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x == 0 && *abort) {
     for (int j = ctl->consumed; j < ctl->issued; ++j) {
       const uint64_t t_start = global_timer_ns();
       while (!mbar_try_wait(&full[j % S], (uint32_t)(j / S) & 1u) && global_timer_ns() - t_start < 20000000ull) {

@@ -107,8 +107,9 @@ struct SelRow {
 };
 
 __device__ __forceinline__ int32_t slot_lookup(const SelectArgs& a, const SelRow& r, int64_t pos) {
-  const int64_t page_idx = pos / a.page_size;
-  const int32_t off = (int32_t)(pos - page_idx * a.page_size);
+  // positions are below a row length (int32): 32-bit division
+  const int32_t page_idx = (int32_t)pos / a.page_size;
+  const int32_t off = (int32_t)pos - page_idx * a.page_size;
   if (page_idx < r.pt_n) return r.pt_s[page_idx] * a.page_size + off;
   if (page_idx < a.ld_pt) return __ldg(r.pt_row + page_idx) * a.page_size + off;
   raise_fault(kFaultIndex);

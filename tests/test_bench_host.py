@@ -68,9 +68,12 @@ def test_kernel_names_follow_the_dispatch_rules():
     from workloads import c2_verify, c3_batched
     n2 = bench.kernel_names(c2_verify(0))  # 6 rows per request, 64-token pages
     assert n2 == {"compress": "compress_keys_kernel", "append": "append_keys_kernel",
-                  "score": "score_tc_kernel", "select": "select_cluster_kernel"}
+                  "score": "score_mma_kernel", "select": "select_fast_kernel"}
     n3 = bench.kernel_names(c3_batched(0))  # one row per request, 32 rows
-    assert n3["score"] == "score_tcb_kernel" and n3["select"] == "select_resident_kernel"
+    assert n3["score"] == "score_mma_kernel" and n3["select"] == "select_fast_kernel"
+    from workloads import c5_prefill
+    n5 = bench.kernel_names(c5_prefill(0))  # 4096 rows of one request
+    assert n5["score"] == "score_tc_kernel" and n5["select"] == "select_rows_kernel"
 
 
 def test_kernel_bytes_c2():
@@ -104,3 +107,7 @@ def test_long_rows_take_the_cluster_selection():
     assert bench.topk_kernel_name(64, 20_000) == "select_resident_kernel"
     assert bench.topk_kernel_name(200, 20_000) == "select_resident_kernel"
     assert bench.topk_kernel_name(400, 20_000) == "select_rows_kernel"
+    # k <= 1024: one register-resident CTA per row
+    assert bench.topk_kernel_name(6, 20_000, k=512) == "select_fast_kernel"
+    assert bench.topk_kernel_name(200, 32_768, k=1024) == "select_fast_kernel"
+    assert bench.topk_kernel_name(400, 20_000, k=512) == "select_rows_kernel"
