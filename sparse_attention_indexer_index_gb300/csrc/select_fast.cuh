@@ -285,30 +285,31 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
   uint32_t* lkey = sh.lkey + warp * kSfWarpCap;
   uint16_t* lidx = sh.lidx + warp * kSfWarpCap;
   {
-    int cnt = 0;
+    // bit 4j + c: entry (j, c) is a candidate (independent compares, no
+    // branches); set bits are then walked, each candidate's score read again
+    // from L2 (registers cannot be indexed by a runtime bit number)
+    uint32_t cm = 0u;
     if (!every) {
 #pragma unroll
       for (int j = 0; j < kSfRuns; ++j)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cnt += xs[j][c] >= vf;
+        for (int c = 0; c < 4; ++c) cm |= (xs[j][c] >= vf ? 1u : 0u) << (4 * j + c);
     }
+    const int cnt = __popc(cm);
     int off = (int)warp_incl_scan_u32((uint32_t)cnt) - cnt;
     const int wtot = __shfl_sync(0xffffffffu, off + cnt, 31);
     const bool fits = wtot <= kSfWarpCap;
-    if (!every) {
-#pragma unroll
-      for (int j = 0; j < kSfRuns; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (xs[j][c] >= vf) {
-            const uint32_t x = order_key(xs[j][c]) + 1u;
-            atomicAdd(&sh.hist[0][(x - v) >> sbin0], 1u);
-            if (fits) {
-              lkey[off] = x;
-              lidx[off] = (uint16_t)index_of(j, c);
-            }
-            ++off;
-          }
+    while (cm != 0u) {
+      const int b = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      const int i = index_of(b >> 2, b & 3);
+      const uint32_t x = order_key(__ldcg(row + i)) + 1u;
+      atomicAdd(&sh.hist[0][(x - v) >> sbin0], 1u);
+      if (fits) {
+        lkey[off] = x;
+        lidx[off] = (uint16_t)i;
+      }
+      ++off;
     }
     if (lane == 0) sh.wcnt[warp] = every ? 0xffffffffu : (uint32_t)wtot;
   }
@@ -434,8 +435,8 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
       for (int e = lane; e < my_cnt; e += 32) f(lkey[e], (int)lidx[e]);
     });
   } else {
-    // rare: the entries are read again from L2 on every pass (keeping them in
-    // registers for this path would cost the list path its registers)
+    // rare (a warp listed more than kSfWarpCap candidates: heavy ties): the
+    // entries are read again from L2 on every pass
     core([&](auto f) {
       for (int j = 0; j < (small ? 1 : kSfRuns); ++j)
         for (int c = 0; c < 4; ++c) {

@@ -24,6 +24,24 @@ def bf16_host(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+# Absolute term of the compressed-key bound.  The GPU rotates the normalised
+# mean in FP32: r = u c - v s with |u|, |v|, |c|, |s| <= 1 and u^2 + v^2 <= 1.
+# Errors proportional to |r| (the normalisation's scale, the subtraction's
+# rounding) are far below an ulp of r.  What is not proportional to |r| is
+# bounded by half an FP32 ulp for each of u and v, one for each product and
+# about one for sincospif on each of c and s: at most about 3 * 2^-24 in all,
+# so 2^-22.  It matters only where u c - v s nearly cancels and an ulp of the
+# BF16 result falls below it.
+KEY_ABS_TERM = 2.0 ** -22
+
+
+def key_tolerance(a, b):
+    """Compressed-key bound: one BF16 ulp of the larger magnitude (each side
+    rounds to BF16 once) plus KEY_ABS_TERM for the FP32 rotation."""
+    m = np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(m)) - 7) + KEY_ABS_TERM
+
+
 def score_tolerance(q_bits, pool_bits, req_row_start, row_len, page_table, page_size, ld):
     """Per-element bound of the score comparison:
     2e-5 * (1/sqrt(128)) * sum_{h,d} |q[t,h,d] * kbar[b,d]| + 1e-6

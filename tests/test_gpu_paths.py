@@ -1,0 +1,154 @@
+"""GPU parity on launch shapes that reach the less common kernels, and the
+headline decode step checked against the oracle end to end.
+
+- Many long rows: more than SMs/2 rows longer than 32,768 entries go to the
+  one-CTA streaming selection (select_kernel), in token mode (DSA top-2048
+  with slots) and in QSA mode (contexts past 131K tokens).
+- Ties at the boundary of the register-resident selection (k <= 1024): the
+  k-th key shared by many entries, so only the first `need` of them (lowest
+  indices) are taken.
+- The 6-row verify step at L = 80,000 as one qsa_decode_step call: the rows'
+  own keys (positions 79,994..79,999) complete blocks 19,998 and 19,999
+  through the 4-slot ring; the new pool rows against the oracle's key path,
+  the scores against the oracle on the same keys, the selection, positions
+  and slots bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import bf16_dev, bf16_host, key_tolerance, score_tolerance, to_dev
+from workloads import c2_verify, decode_workload, topk_workload, TOPK_DISTS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import sparse_attention_indexer_index_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _no_device_faults(qsa):
+    yield
+    assert qsa.device_status(clear=True) == 0, "a device-side bounds check fired"
+
+
+# ----------------------------------------------------------------- many long rows
+@pytest.mark.parametrize("dist", TOPK_DISTS)
+def test_topk_many_long_rows_streaming_selection(qsa, dist):
+    """128 DSA rows of 80,000 scores, k = 2048, slots through per-row page
+    tables: 128 rows x 2 CTAs exceed the SMs, so every row takes one
+    streaming CTA (select_kernel)."""
+    w = topk_workload(61, 128, 80_000, k=2048, dist=dist)
+    idx, slots = qsa.topk_select(to_dev(w.scores), 2048, n_valid=to_dev(w.n_valid), n_max=80_000,
+                                 page_table=to_dev(w.page_table), page_size=w.page_size)
+    ref_idx, ref_slots = oracle.topk(w.scores, 2048, n_valid=w.n_valid, page_table=w.page_table,
+                                     page_size=w.page_size)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+
+
+def test_select_blocks_many_long_qsa_rows(qsa):
+    """96 QSA rows of contexts between 131,073 and 200,000 tokens (more than
+    32,768 blocks each) through qsa_select_blocks: the streaming CTA in QSA
+    mode (top-512 blocks, expansion with 0-3 pending tokens, slots)."""
+    rng = np.random.default_rng(62)
+    lens = [int(x) for x in rng.integers(131_073, 200_001, size=96)]
+    w = decode_workload(63, [[L] for L in lens], page_size=64, k_blk=512, with_keys=False)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    s = rng.standard_normal((w.n_rows, ld)).astype(np.float32)
+    out = qsa.select_blocks(to_dev(s), to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table),
+                            w.page_size, w.max_len, k_blk=512, want_blocks=True, want_pos=True)
+    sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+# ----------------------------------------------------------------- boundary ties
+@pytest.mark.parametrize("n", [3000, 20_000, 32_768])
+@pytest.mark.parametrize("k", [512, 1000])
+def test_topk_boundary_ties_take_lowest_indices(qsa, n, k):
+    """Rows whose k-th largest value is shared by many entries on both sides
+    of the cut (some taken, some not): the taken ones are the lowest indices.
+    Row 0: k - 40 distinct large values, then 300 copies of one value spread
+    over the row.  Row 1: the same with the copies at the front.  Row 2: a
+    row of 5 distinct values (massive ties everywhere)."""
+    rng = np.random.default_rng(n + k)
+    s = (rng.standard_normal((3, n)) * 0.1).astype(np.float32)
+    big = rng.permutation(n)[: k - 40]
+    s[0, big] = 10.0 + rng.standard_normal(k - 40).astype(np.float32)
+    rest = np.setdiff1d(np.arange(n), big)
+    s[0, rng.choice(rest, 300, replace=False)] = 5.0
+    s[1] = s[0]
+    s[1, np.flatnonzero(s[0] == 5.0)] = 0.0
+    s[1, rest[:300]] = 5.0
+    s[2] = rng.integers(0, 5, n).astype(np.float32)
+    nv = np.full(3, n, np.int32)
+    idx, _ = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n)
+    ref, _ = oracle.topk(s, k, n_valid=nv)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+# ----------------------------------------------------------------- the headline step
+def test_decode_step_c2_verify_against_the_oracle(qsa):
+    """The 6-row verify step at L = 80,000 (rows at positions
+    79,994..79,999), as one qsa_decode_step call on a pool holding blocks
+    0..19,997 and a ring holding tokens 79,992..79,993."""
+    import torch
+    w = c2_verify(0)
+    assert w.n_req == 1 and list(w.row_len) == [79_995 + i for i in range(6)]
+    first, count = 79_994, 6
+    nb0 = first // 4  # 19,998 blocks complete before the step
+    ids = w.block_id
+    order = np.argsort(ids)
+    raw_tok = w.raw_keys.reshape(-1, 4, 128)[order].reshape(-1, 128)  # token order 0..79,999
+    # the state before the step: blocks 0..19,997 compressed (oracle), ring slots 0, 1
+    pool0 = np.zeros((w.pool_rows, 128), np.uint16)
+    oracle.compress(raw_tok[: 4 * nb0], np.zeros(nb0, np.int32), np.arange(nb0, dtype=np.int32), w.page_table,
+                    w.page_size, w.rope_base, pool0)
+    ring0 = np.zeros((1, 4, 128), np.uint16)
+    for p in range(4 * nb0, first):
+        ring0[0, p % 4] = raw_tok[p]
+    new = np.ascontiguousarray(raw_tok[first:first + count])
+    rts = np.array([0, count], np.int32)
+    fp = np.array([first], np.int32)
+    # oracle key path
+    ring_o, pool_o = oracle.append_keys(new, rts, fp, ring0.copy(), w.page_table, w.page_size, w.rope_base,
+                                        pool0.copy())
+    # one GPU call
+    g_pool, g_ring = bf16_dev(pool0), bf16_dev(ring0)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.decode_step(bf16_dev(new), to_dev(rts), to_dev(fp), g_ring, bf16_dev(w.q), g_pool,
+                          to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table), w.page_size,
+                          w.max_len, w.max_rows_per_req, k_blk=512, rope_base=w.rope_base, want_blocks=True,
+                          want_pos=True, scores_out=scores)
+    pool_g, ring_g = bf16_host(g_pool), bf16_host(g_ring)
+    # ring: the last 4 appended tokens (bit copies)
+    assert np.array_equal(ring_g, ring_o)
+    # pool: blocks 19,998 and 19,999 written within the key bound, nothing else touched
+    new_rows = [oracle.pool_row(w.page_table[0], b, w.page_size) for b in (nb0, nb0 + 1)]
+    a_, b_ = oracle.bf16_to_float(pool_g[new_rows]), oracle.bf16_to_float(pool_o[new_rows])
+    assert (np.abs(a_ - b_) <= key_tolerance(a_, b_)).all()
+    others = np.setdiff1d(np.arange(w.pool_rows), new_rows)
+    assert np.array_equal(pool_g[others], pool0[others])
+    # scores against the oracle on the GPU's keys (the rule: fed identically)
+    s = scores.cpu().numpy()
+    want = oracle.index_scores(w.q, pool_g, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    tol = score_tolerance(w.q, pool_g, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        err = np.abs(s[t, :nb].astype(np.float64) - want[t, :nb])
+        assert (err <= tol[t, :nb]).all(), (t, float(err.max()))
+    # selection, positions and slots bit-exact on the GPU's scores
+    sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)

@@ -90,11 +90,12 @@ class DecodeWorkload:
 
 def decode_workload(seed: int, rows_per_req: list[list[int]], page_size: int = 64,
                     k_blk: int = 512, rope_base: float = 10000.0, name: str = "",
-                    pad_pages: int = 0) -> DecodeWorkload:
+                    pad_pages: int = 0, with_keys: bool = True) -> DecodeWorkload:
     """rows_per_req[r] lists the row lengths (visible tokens) of request r's
     query rows.  A request's context is its longest row; its page table covers
     that context (plus ``pad_pages`` spare pages), drawn as a seeded random
-    permutation of the whole pool."""
+    permutation of the whole pool.  with_keys=False leaves out the raw keys
+    (for selection-only cases whose scores are drawn directly)."""
     rng = np.random.default_rng(seed)
     row_len = np.array([L for rows in rows_per_req for L in rows], np.int32)
     counts = np.array([len(rows) for rows in rows_per_req], np.int32)
@@ -110,7 +111,7 @@ def decode_workload(seed: int, rows_per_req: list[list[int]], page_size: int = 6
         page_table[r, :n] = perm[off:off + n]
         off += n
     q = normal_bf16(rng, (row_len.size, H, D))
-    nb = ctx // C
+    nb = ctx // C if with_keys else np.zeros_like(ctx)
     block_req = np.repeat(np.arange(len(rows_per_req), dtype=np.int32), nb)
     block_id = np.concatenate([np.arange(n, dtype=np.int32) for n in nb]) if nb.size else \
         np.zeros(0, np.int32)
