@@ -22,6 +22,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qsa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libqsa_oracle.so")
+_OMP_PATH = os.path.join(_HERE, "libqsa_oracle_omp.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -37,6 +38,37 @@ def build(force: bool = False) -> str:
         subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def build_omp(force: bool = False) -> str:
+    """The same source built with OpenMP: rows and blocks of the whole-path
+    call split over the host cores.  Used only to time the oracle on all
+    cores (the tests use the plain build)."""
+    if force or not os.path.exists(_OMP_PATH) or os.path.getmtime(_OMP_PATH) < os.path.getmtime(_SRC):
+        tmp = _OMP_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", *_CFLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _OMP_PATH)
+    return _OMP_PATH
+
+
+_omp_lib = None
+
+
+def indexer_select_threads(q, pool, req_row_start, row_len, page_table, page_size, k_blk=512, threads=1):
+    """indexer_select on `threads` host cores (the OpenMP build); returns
+    the same dict.  For timing only."""
+    global _omp_lib
+    with _lock:
+        if _omp_lib is None:
+            L = ctypes.CDLL(build_omp())
+            p, i64 = ctypes.c_void_p, ctypes.c_int64
+            L.oracle_indexer_select.restype = None
+            L.oracle_indexer_select.argtypes = [p, p, i64, p, p, p, i64, i64, i64, p, i64, p, p, p]
+            L.oracle_set_threads.restype = ctypes.c_int
+            L.oracle_set_threads.argtypes = [ctypes.c_int]
+            _omp_lib = L
+    _omp_lib.oracle_set_threads(int(threads))
+    return _indexer_select_with(_omp_lib, q, pool, req_row_start, row_len, page_table, page_size, k_blk)
 
 
 def _load():
@@ -223,6 +255,10 @@ def expand(sel, req_row_start, row_len, page_table, page_size):
 # ---------------------------------------------------------------- whole path
 def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, k_blk=512):
     """Returns dict(scores, blocks, pos, slots)."""
+    return _indexer_select_with(_load(), q, pool, req_row_start, row_len, page_table, page_size, k_blk)
+
+
+def _indexer_select_with(L, q, pool, req_row_start, row_len, page_table, page_size, k_blk):
     q = _c(q, np.uint16)
     rrs = _c(req_row_start, np.int32)
     rl = _c(row_len, np.int32)
@@ -234,9 +270,9 @@ def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, k_blk
     w = out_width(k_blk)
     pos = np.empty((n_rows, w), np.int32)
     slots = np.empty((n_rows, w), np.int32)
-    _load().oracle_indexer_select(_ptr(q), _ptr(pool), rrs.size - 1, _ptr(rrs), _ptr(rl),
-                                  _ptr(pt), pt.shape[-1], int(page_size), int(k_blk),
-                                  _ptr(scores), ld, _ptr(blocks), _ptr(pos), _ptr(slots))
+    L.oracle_indexer_select(_ptr(q), _ptr(pool), rrs.size - 1, _ptr(rrs), _ptr(rl),
+                            _ptr(pt), pt.shape[-1], int(page_size), int(k_blk),
+                            _ptr(scores), ld, _ptr(blocks), _ptr(pos), _ptr(slots))
     return {"scores": scores, "blocks": blocks, "pos": pos, "slots": slots}
 
 

@@ -214,6 +214,9 @@ void oracle_index_scores(const uint16_t* q, const uint16_t* pool, int64_t n_req,
     const int32_t* pt_row = page_table + r * ld_pt;
     for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t) {
       int64_t nb = row_len[t] / QSA_C;
+      /* independent blocks: the timing build (-fopenmp) splits them over the
+       * host cores; the plain build ignores the pragma */
+#pragma omp parallel for schedule(static)
       for (int64_t b = 0; b < nb; ++b) {
         const uint16_t* key = pool + oracle_pool_row(pt_row, b, page_size) * QSA_D;
         scores[t * ld_scores + b] = oracle_score_one(q + t * QSA_H * QSA_D, key);
@@ -459,6 +462,21 @@ int oracle_sparse_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 
 /* ---------- the whole decode path: score -> top-k blocks -> slots ------- */
 
+/* Host threads of the timing build (built with -fopenmp); the plain build
+ * runs single-threaded and returns 1. */
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_set_threads(int n) {
+  omp_set_num_threads(n);
+  return n;
+}
+#else
+int oracle_set_threads(int n) {
+  (void)n;
+  return 1;
+}
+#endif
+
 /* scores must hold n_rows * ld_scores floats (ld_scores >= max nb).  The
  * selection runs on these FP32 scores, blocks b < row_len/4 only. */
 void oracle_indexer_select(const uint16_t* q, const uint16_t* pool, int64_t n_req,
@@ -468,9 +486,11 @@ void oracle_indexer_select(const uint16_t* q, const uint16_t* pool, int64_t n_re
                            int32_t* out_pos, int32_t* out_slots) {
   oracle_index_scores(q, pool, n_req, req_row_start, row_len, page_table, ld_pt, page_size,
                       scores, ld_scores);
-  for (int64_t r = 0; r < n_req; ++r)
-    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t)
-      oracle_topk_row(scores + t * ld_scores, row_len[t] / QSA_C, k_blk, out_blocks + t * k_blk);
+  const int64_t n_rows = req_row_start[n_req];
+  /* independent rows (the timing build runs them on the host cores) */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < n_rows; ++t)
+    oracle_topk_row(scores + t * ld_scores, row_len[t] / QSA_C, k_blk, out_blocks + t * k_blk);
   oracle_expand(out_blocks, k_blk, n_req, req_row_start, row_len, page_table, ld_pt, page_size,
                 out_pos, out_slots);
 }
