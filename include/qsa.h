@@ -340,10 +340,11 @@ qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows
  * (Library addition with no counterpart in the source pages.)
  *
  * Who needs it: code that must not call cudaMalloc at the point where the
- * indexer runs -- for example a serving step being recorded into a CUDA
- * graph, an engine whose memory planner hands out every byte up front, or a
- * plugin living inside another framework that gives it no allocator.  Such
- * callers cannot size and pass the workspace of qsa_indexer_select, so this
+ * indexer runs -- for example an engine whose memory planner hands out every
+ * byte up front, a plugin living inside another framework that gives it no
+ * allocator, or a latency-critical loop that cannot afford the device-wide
+ * synchronisation an allocation may cause.  Such callers cannot size and
+ * pass the workspace of qsa_indexer_select, so this
  * call keeps the FP32 scores in a fixed scratch array that is part of the
  * library itself: QSA_NOALLOC_SCRATCH_BYTES bytes of device memory, held on
  * every GPU that loads the library until the process exits.

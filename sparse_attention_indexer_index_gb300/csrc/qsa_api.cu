@@ -1160,8 +1160,8 @@ qsa_status qsa_decode_step(const void* new_keys, const int32_t* req_tok_start, c
 // ---------------------------------------------------------------------------
 // qsa_indexer_select_noalloc: the fused path with its score scratch in a
 // library-owned device array instead of a caller workspace, for callers that
-// may not allocate device memory (graph capture, pre-planned memory, plugins
-// without an allocator).  See include/qsa.h for the contract.
+// may not allocate device memory (pre-planned memory, plugins without an
+// allocator).  See include/qsa.h for the contract.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -1208,35 +1208,10 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
   const int64_t ld = (nb_max + 3) & ~3;
   if ((uint64_t)n_rows * (uint64_t)ld * sizeof(float) > (uint64_t)QSA_NOALLOC_SCRATCH_BYTES)
     return QSA_ERR_UNSUPPORTED;  // the scores do not fit in the fixed scratch array
-  DeviceInfo* d = nullptr;
-  if (qsa_status st = device_info(&d)) return st;
   float* scores = nullptr;
   if (qsa_status st = noalloc_scratch(&scores)) return st;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
-              pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1};
-  if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
-    return e;
-
-  SelectArgs a{};
-  a.scores = scores;
-  a.ld = ld;
-  a.n_rows = n_rows;
-  a.k = k_blk;
-  a.n_max = nb_max;
-  plan_select(a);
-  a.vec_ok = 1;  // the array is 256-byte aligned and ld is a multiple of 4
-  a.wait_primary = 1;
-  a.n_req = n_req;
-  a.req_row_start = req_row_start;
-  a.row_len = row_len;
-  a.out_idx = out_blocks;
-  a.out_pos = out_pos;
-  a.out_xslots = out_slots;
-  a.page_table = page_table;
-  a.ld_pt = ld_pt;
-  a.page_size = page_size;
-  return launch_select<kModeQsa>(a, nb_max > 0, st, d->sm_count);
+  // the fused path with the scratch array as its score buffer
+  return indexer_select_impl(q, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
+                             max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos,
+                             out_slots, scores, ld, nullptr, 0, stream, nullptr);
 }
