@@ -540,6 +540,56 @@ def bench_variant_topk(g, w, iters, warmup, peaks):
             "kernel": topk_kernel_name(int(s.shape[0]), int(w.n_valid.max()), k=w.k)}
 
 
+def bench_variant_topk_mixed(g, iters, warmup, peaks, seed=0, k=2048, page_size=64):
+    """DSA top-2048 with slots on a mixed batch in one call: one row of
+    1,000,000 scores, four of 80,000 and 100 of 3,000-30,000 (seeded, in
+    shuffled order; N(0,1) scores drawn on the device).  The library plans the
+    rows on the device (long rows on clusters, short ones one CTA each);
+    beside it the same rows as two calls, the long ones and the short ones."""
+    torch, qsa = g.torch, g.qsa
+    rng = np.random.default_rng(seed + 77)
+    lens = np.array([1_000_000] + [80_000] * 4 + list(rng.integers(3000, 30_000, size=100)), np.int32)
+    nv_h = rng.permutation(lens).astype(np.int32)
+    ld = int(nv_h.max())
+    gen = torch.Generator(device=g.dev)
+    gen.manual_seed(seed + 78)
+    s = torch.randn((nv_h.size, ld), generator=gen, device=g.dev)
+    pt_h = np.stack([rng.permutation((ld + page_size - 1) // page_size) for _ in range(nv_h.size)]).astype(np.int32)
+    nv, pt = g.h2d(nv_h), g.h2d(pt_h)
+    long_i = np.flatnonzero(nv_h > 32768)
+    short_i = np.flatnonzero(nv_h <= 32768)
+    s_long, s_short = s[g.h2d(long_i)].contiguous(), s[g.h2d(short_i)][:, :32768].contiguous()
+    nv_long, nv_short = g.h2d(nv_h[long_i]), g.h2d(nv_h[short_i])
+    pt_long, pt_short = g.h2d(pt_h[long_i]), g.h2d(pt_h[short_i])
+    n_short_max = int(nv_h[short_i].max())
+    outs = {}
+    for name, rows in (("mixed", nv_h.size), ("long", long_i.size), ("short", short_i.size)):
+        outs[name] = (torch.empty((rows, k), dtype=torch.int32, device=g.dev),
+                      torch.empty((rows, k), dtype=torch.int32, device=g.dev))
+    fn_mixed = lambda: qsa.topk_select(s, k, n_valid=nv, n_max=ld, page_table=pt, page_size=page_size,
+                                       out_idx=outs["mixed"][0], out_slots=outs["mixed"][1])
+    fn_long = lambda: qsa.topk_select(s_long, k, n_valid=nv_long, n_max=ld, page_table=pt_long,
+                                      page_size=page_size, out_idx=outs["long"][0], out_slots=outs["long"][1])
+    fn_short = lambda: qsa.topk_select(s_short, k, n_valid=nv_short, n_max=n_short_max, page_table=pt_short,
+                                       page_size=page_size, out_idx=outs["short"][0], out_slots=outs["short"][1])
+    no_ws = torch.empty(0, dtype=torch.uint8, device=g.dev)
+    fn_noplan = lambda: qsa.topk_select(s, k, n_valid=nv, n_max=ld, page_table=pt, page_size=page_size,
+                                        out_idx=outs["mixed"][0], out_slots=outs["mixed"][1], workspace=no_ws)
+    t_noplan = 1e3 * statistics.mean(g.timed(fn_noplan, iters, warmup))
+    t_mixed = 1e3 * statistics.mean(g.timed(fn_mixed, iters, warmup))
+    t_long = 1e3 * statistics.mean(g.timed(fn_long, iters, warmup))
+    t_short = 1e3 * statistics.mean(g.timed(fn_short, iters, warmup))
+    alg = int(nv_h.sum()) * 4 + 2 * nv_h.size * k * 4 + int(sum((n + page_size - 1) // page_size for n in nv_h)) * 4
+    ms = t_mixed * 1e-3
+    return {"workload": "dsa_topk_mixed_1x1M_4x80K_100short", "rows": int(nv_h.size), "us_per_call": t_mixed,
+            "rows_per_s": nv_h.size / (ms * 1e-3), "alg_bytes": alg, "alg_GBps": alg / (ms * 1e-3) / 1e9,
+            "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "classes_apart_us": {"long_5_rows": t_long, "short_100_rows": t_short, "sum": t_long + t_short},
+            "without_plan_us": t_noplan,
+            "without_plan": "no workspace for the plan: the host rule from the longest row and the row count "
+                            "(every row on one streaming CTA)"}
+
+
 def bench_variant_indexshare(g, w, iters, warmup, peaks):
     """One draft step of an MTP iteration with IndexShare: each request's
     draft row reads the selection kept at its draft-extend row
@@ -742,6 +792,7 @@ def variant_table(g, it, warmup, peaks):
                                                               peaks),
         "dsa_topk_verify_6x1M": lambda: bench_variant_topk(g, c4_dsa_topk(0, "normal", n_rows=6, n=1_000_000), it,
                                                            warmup, peaks),
+        "dsa_topk_mixed_1M_4x80K_100short": lambda: bench_variant_topk_mixed(g, it, warmup, peaks),
         "c5_prefill_4096rows": lambda: bench_variant_prefill(g, c5_prefill(0), 3, 3, peaks),
         "indexshare_32req_draft": lambda: bench_variant_indexshare(g, indexshare_mtp(0), it, warmup, peaks),
         "sparse_attn_32req": lambda: bench_variant_attn(g, c3_batched(0), it, warmup, peaks),

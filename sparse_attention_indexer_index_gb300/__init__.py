@@ -234,9 +234,11 @@ def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len
 
 
 def topk_select(scores, k, n_valid=None, n_max=None, page_table=None, row_req=None, page_size=0,
-                out_idx=None, out_slots=None, want_slots=None, stream=None):
+                out_idx=None, out_slots=None, want_slots=None, workspace=None, stream=None):
     """Exact top-k per row, ascending indices, -1 padded; optionally slots.
-    Returns (idx, slots or None)."""
+    workspace: None (allocated from the size query: room for the device row
+    plan), or a uint8 tensor (an empty one: no plan).  Returns (idx, slots or
+    None)."""
     torch = _torch()
     _dev(scores, torch.float32, "scores", 2)
     n_rows, ld = scores.shape
@@ -254,8 +256,12 @@ def topk_select(scores, k, n_valid=None, n_max=None, page_table=None, row_req=No
         out_idx = torch.empty((n_rows, k), dtype=torch.int32, device=scores.device)
     if want_slots and out_slots is None:
         out_slots = torch.empty((n_rows, k), dtype=torch.int32, device=scores.device)
-    ws_bytes = lib().topk_select_workspace_size(n_rows, int(n_max), int(k))
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    if workspace is None:
+        ws_bytes = lib().topk_select_workspace_size(n_rows, int(n_max), int(k))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    else:
+        ws_bytes = workspace.numel() * workspace.element_size()
+        ws = workspace if ws_bytes else None
     _check("topk_select", lib().topk_select(
         _ptr(scores), ld, _ptr(n_valid), n_rows, int(n_max), int(k), _ptr(page_table),
         0 if page_table is None else page_table.shape[1], _ptr(row_req), int(page_size),
@@ -406,6 +412,8 @@ def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, max_l
     if scores_out is not None:
         _dev(scores_out, torch.float32, "scores_out", 2)
         ld = scores_out.shape[1]
+        if workspace is not None:  # may still hold the device row plan
+            ws_bytes = workspace.numel() * workspace.element_size()
     else:
         ws_bytes = indexer_select_workspace_size(n_rows, max_len, k_blk)
         if workspace is None and ws_bytes:

@@ -308,24 +308,15 @@ qsa_status launch_select_cluster(const SelectArgs& args, bool pdl, int sm_count,
   return QSA_OK;
 }
 
-// Long rows: a cluster of C CTAs per row, C the largest of 16, 8, 4, 2 with
-// rows * C <= SMs (and such clusters schedulable).  QSA_ERR_UNSUPPORTED: one
-// CTA per row (select_kernel) instead.
+// Long rows on clusters of C CTAs (one cluster per row, `clusters` of them).
 template <int kMode>
-qsa_status launch_select_long(const SelectArgs& args, bool pdl, cudaStream_t stream) {
-  if (args.n_max <= kRsMaxRow) return QSA_ERR_UNSUPPORTED;
-  DeviceInfo* d = nullptr;
-  if (qsa_status st = device_info(&d)) return st;
-  int e = 4;
-  while (e >= 1 && ((int64_t)args.n_rows << e > d->sm_count || d->sl_clusters[e] < 1)) --e;
-  if (e < 1) return QSA_ERR_UNSUPPORTED;
-  const int C = 1 << e;
+qsa_status launch_select_long_c(const SelectArgs& args, int C, int64_t clusters, bool pdl, cudaStream_t stream) {
   SelectArgs a = args;
   const int64_t S = (((int64_t)a.n_max + C - 1) / C + 3) & ~int64_t(3);
   const int64_t cap = ((kSlSmem - kSlFixedBytes) / 4) & ~3;
   a.list_cap = (int32_t)std::min(S, cap);  // slice entries kept in shared memory
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.n_rows * C), 1, 1);
+  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
   cfg.blockDim = dim3(kSlThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)kSlFixedBytes + (size_t)a.list_cap * 4;
   cfg.stream = stream;
@@ -348,6 +339,20 @@ qsa_status launch_select_long(const SelectArgs& args, bool pdl, cudaStream_t str
     return QSA_ERR_CUDA;
   }
   return QSA_OK;
+}
+
+// Long rows: a cluster of C CTAs per row, C the largest of 16, 8, 4, 2 with
+// rows * C <= SMs (and such clusters schedulable).  QSA_ERR_UNSUPPORTED: one
+// CTA per row (select_kernel) instead.
+template <int kMode>
+qsa_status launch_select_long(const SelectArgs& args, bool pdl, cudaStream_t stream) {
+  if (args.n_max <= kRsMaxRow) return QSA_ERR_UNSUPPORTED;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  int e = 4;
+  while (e >= 1 && ((int64_t)args.n_rows << e > d->sm_count || d->sl_clusters[e] < 1)) --e;
+  if (e < 1) return QSA_ERR_UNSUPPORTED;
+  return launch_select_long_c<kMode>(args, 1 << e, args.n_rows, pdl, stream);
 }
 
 // More than two rows per SM, rows of up to kSrMaxRow entries: one 256-thread
@@ -404,8 +409,104 @@ qsa_status launch_select_fast(const SelectArgs& a, bool pdl, cudaStream_t stream
   return QSA_OK;
 }
 
+// Bytes of the device row plan for n_rows rows (plan_rows_kernel).
+size_t plan_bytes(int32_t n_rows) { return (((size_t)4 + 2 * (size_t)n_rows) * 4 + 255) & ~(size_t)255; }
+
+// Whether a launch of these rows takes the device plan: some rows may be long
+// (more than kRsMaxRow candidates) and there are too many rows to give each a
+// cluster, so the host bound alone would send every row, short or long, to
+// one streaming CTA.
+bool wants_plan(int32_t n_rows, int32_t n_max, int sm_count) {
+  return n_max > kRsMaxRow && (int64_t)n_rows * 2 > sm_count;
+}
+
 template <int kMode>
-qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count = 0) {
+qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count = 0);
+
+// Rows split by length class on the device (plan_rows_kernel, one CTA): the
+// long rows (more than kRsMaxRow candidates) on clusters sized from their
+// count, the short ones one CTA each.  The cluster size is a launch
+// attribute, so the long class is launched once per size the plan can pick
+// (16 or 2 CTAs per row, and the one-CTA streaming kernel); the launches the
+// plan did not pick wait for it and exit.  Every launch after
+// the plan waits for its predecessor, so the chain completes after the plan
+// and the plan after the previous grid (the scorer in the fused call).
+template <int kMode>
+qsa_status launch_select_planned(const SelectArgs& args, int32_t* plan, bool pdl, cudaStream_t stream,
+                                 DeviceInfo* d) {
+  const int sm = d->sm_count;
+  PlanArgs p{};
+  p.n_valid = kMode == kModeTopk ? args.n_valid : nullptr;
+  p.row_len = kMode == kModeQsa ? args.row_len : nullptr;
+  p.n_rows = args.n_rows;
+  p.n_max = args.n_max;
+  p.cut = kRsMaxRow;
+  // Sizes the plan may pick: 16 (a few long rows, e.g. one of 1M) and 2
+  // (many); every size is one more launch, and each launch the plan does not
+  // pick still costs a dependent-launch hop, so the sizes are few.
+  for (int e : {1, 4})
+    if (d->sl_clusters[e] >= 1) p.c_mask |= 1 << e;
+  p.sm_count = sm;
+  p.plan = plan;
+  if (pdl) {
+    if (launch_pdl(plan_rows_kernel, dim3(1), dim3(1024), 0, stream, p) != cudaSuccess) {
+      cudaGetLastError();
+      return QSA_ERR_CUDA;
+    }
+  } else {
+    plan_rows_kernel<<<1, 1024, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
+  }
+  // long class: the sizes the plan can pick for 1 <= n_long <= n_rows
+  SelectArgs L = args;
+  L.plan = plan;
+  L.row_list = plan + 4;
+  L.count_at = 0;
+  L.wait_primary = 1;
+  int64_t prev_hi = 0;  // rows a larger schedulable size takes
+  for (int e = 4; e >= 1; --e) {
+    if (!(p.c_mask >> e & 1)) continue;
+    const int c = 1 << e;
+    const int64_t hi = sm / c;  // the plan picks c for prev_hi < n_long <= hi
+    if (prev_hi < args.n_rows && prev_hi < hi) {
+      L.plan_c = c;
+      if (qsa_status st = launch_select_long_c<kMode>(L, c, std::min<int64_t>(args.n_rows, hi), true, stream))
+        return st;
+    }
+    prev_hi = std::max(prev_hi, hi);
+  }
+  if (prev_hi < args.n_rows) {  // one streaming CTA per long row
+    L.plan_c = 1;
+    plan_select(L);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)args.n_rows, 1, 1);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = select_smem_bytes(L);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, select_kernel<kMode>, L) != cudaSuccess) {
+      cudaGetLastError();
+      return QSA_ERR_CUDA;
+    }
+  }
+  // short class: rows of at most kRsMaxRow candidates, one CTA each
+  SelectArgs S = args;
+  S.plan = plan;
+  S.row_list = plan + 4 + args.n_rows;
+  S.count_at = 2;
+  S.plan_c = 0;
+  S.wait_primary = 1;
+  S.n_max = kRsMaxRow;
+  plan_select(S);
+  return launch_select<kMode>(S, true, stream, sm);
+}
+
+template <int kMode>
+qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int sm_count) {
   if (a.n_rows == 0) return QSA_OK;
   {
     const qsa_status st = launch_select_long<kMode>(a, pdl, stream);
@@ -887,15 +988,15 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
 }
 
 size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k) {
-  (void)n_rows; (void)n_max; (void)k;
-  return 0;  // the selection keeps everything on chip
+  (void)k;
+  // the device row plan when rows may exceed the single-CTA length
+  return (n_rows > 0 && n_max > kRsMaxRow) ? plan_bytes(n_rows) : 0;
 }
 
 qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int32_t n_rows,
                        int32_t n_max, int32_t k, const int32_t* page_table, int64_t ld_pt,
                        const int32_t* row_req, int32_t page_size, int32_t* out_idx,
                        int32_t* out_slots, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)workspace; (void)workspace_bytes;
   if (n_rows < 0 || n_max < 0 || ld < 0) return QSA_ERR_INVALID_ARG;
   if (k < 1 || k > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (n_rows == 0) return QSA_OK;
@@ -920,9 +1021,11 @@ qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, 
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size > 0 ? page_size : 1;
-  if (qsa_status st = launch_select<kModeTopk>(a, false, static_cast<cudaStream_t>(stream), d->sm_count))
-    return st;
-  return QSA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (workspace && aligned4(workspace) && workspace_bytes >= plan_bytes(n_rows) &&
+      wants_plan(n_rows, n_max, d->sm_count))
+    return launch_select_planned<kModeTopk>(a, static_cast<int32_t*>(workspace), false, st, d);
+  return launch_select<kModeTopk>(a, false, st, d->sm_count);
 }
 
 qsa_status qsa_expand_slots(const int32_t* sel_blocks, int32_t k_blk, int32_t n_req,
@@ -1049,7 +1152,9 @@ size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_
   (void)k_blk;
   if (n_rows <= 0 || max_len <= 0) return 0;
   const int64_t ld = ((int64_t)(max_len / kBlock) + 3) & ~int64_t(3);
-  return (size_t)(n_rows * ld * (int64_t)sizeof(float)) + 256;
+  // scores (256-byte aligned), then the device row plan when rows may be long
+  const size_t scores = ((size_t)(n_rows * ld * (int64_t)sizeof(float)) + 255) & ~(size_t)255;
+  return scores + 256 + (max_len / kBlock > kRsMaxRow ? plan_bytes(n_rows) : 0);
 }
 
 }  // extern "C"
@@ -1073,15 +1178,21 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
   const int32_t nb_max = max_len / kBlock;
   float* scores = scores_out;
   int64_t ld = ld_scores;
+  int32_t* plan = nullptr;  // the device row plan, when the workspace holds one
+  const uintptr_t ws_lo = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
+  const uintptr_t ws_hi = reinterpret_cast<uintptr_t>(workspace) + workspace_bytes;
   if (scores_out) {
     if (ld_scores < nb_max || !aligned4(scores_out)) return QSA_ERR_INVALID_ARG;
+    if (workspace && ws_lo + plan_bytes(n_rows) <= ws_hi) plan = reinterpret_cast<int32_t*>(ws_lo);
   } else {
     const size_t need = qsa_indexer_select_workspace_size(n_rows, max_len, k_blk);
     if (need > 0) {
       if (!workspace || workspace_bytes < need) return QSA_ERR_WORKSPACE_TOO_SMALL;
-      scores = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
+      scores = reinterpret_cast<float*>(ws_lo);
     }
     ld = (nb_max + 3) & ~3;
+    const uintptr_t plan_at = (ws_lo + (uintptr_t)n_rows * (uintptr_t)ld * 4 + 255) & ~uintptr_t(255);
+    if (workspace && plan_at + plan_bytes(n_rows) <= ws_hi) plan = reinterpret_cast<int32_t*>(plan_at);
   }
   DeviceInfo* d = nullptr;
   if (qsa_status st = device_info(&d)) return st;
@@ -1111,6 +1222,8 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
   a.page_table = page_table;
   a.ld_pt = ld_pt;
   a.page_size = page_size;
+  if (plan && wants_plan(n_rows, nb_max, d->sm_count))
+    return launch_select_planned<kModeQsa>(a, plan, nb_max > 0, st, d);
   return launch_select<kModeQsa>(a, nb_max > 0, st, d->sm_count);
 }
 }  // namespace

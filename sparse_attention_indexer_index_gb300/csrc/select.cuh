@@ -86,7 +86,95 @@ struct SelectArgs {
   const int32_t* page_table;    // [.][ld_pt] or nullptr
   int64_t ld_pt;
   int32_t page_size;
+  // Row plan (rows split by length class on the device by plan_rows_kernel):
+  // nullptr, or plan[0] = long rows, plan[1] = CTAs per long row, plan[2] =
+  // short rows, then the long and the short row lists.  Unit u of a planned
+  // launch (a CTA, or a cluster) serves row_list[u] for u < plan[count_at];
+  // a launch standing for one cluster size (plan_c != 0) works only when the
+  // plan chose that size.
+  const int32_t* plan;
+  const int32_t* row_list;
+  int32_t count_at;
+  int32_t plan_c;
 };
+
+// The row served by unit u (CTA or cluster) of this launch; false: none.
+// A planned launch first waits for the planning grid (the previous one on the
+// stream), then reads the plan.
+__device__ __forceinline__ bool sel_unit_row(const SelectArgs& a, int u, int& t) {
+  if (a.plan == nullptr) {
+    t = u;
+    return true;
+  }
+  pdl_wait_primary();
+  if (a.plan_c != 0 && __ldcg(a.plan + 1) != a.plan_c) return false;
+  if (u >= __ldcg(a.plan + a.count_at)) return false;
+  t = __ldcg(a.row_list + u);
+  return t >= 0 && t < a.n_rows;
+}
+
+// ---------------------------------------------------------------------------
+// Row plan (SGLang GLM-5.2 blog, "Kernel Optimization / TopK-V2": a planning
+// kernel reads the batch's sequence lengths and builds the work lists, so
+// that long rows get a cluster of CTAs and short ones a single CTA).  One
+// 1024-thread CTA: rows with more than `cut` candidates go to the long list,
+// the others to the short list, both in row order; the long list's CTAs per
+// row is the largest C allowed by c_mask (schedulable sizes among 16 and 2)
+// with n_long * C <= SMs, else 1.
+// ---------------------------------------------------------------------------
+struct PlanArgs {
+  const int32_t* n_valid;  // token mode: candidates per row (nullptr: n_max)
+  const int32_t* row_len;  // QSA mode: visible tokens per row (candidates row_len / 4)
+  int32_t n_rows;
+  int32_t n_max;
+  int32_t cut;
+  int32_t c_mask;          // bit e set: the plan may pick clusters of 2^e CTAs (e = 1..4)
+  int32_t sm_count;
+  int32_t* plan;           // [4 + 2 * n_rows]
+};
+
+__global__ void __launch_bounds__(1024) plan_rows_kernel(PlanArgs p) {
+  __shared__ int s_cnt[2][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the plan may still be read by the previous call's selection
+  pdl_wait_primary();
+  int n_long = 0, n_short = 0;
+  for (int base = 0; base < p.n_rows; base += 1024) {
+    const int t = base + tid;
+    int n = 0;
+    if (t < p.n_rows) n = p.row_len ? __ldg(p.row_len + t) / kBlock : (p.n_valid ? __ldg(p.n_valid + t) : p.n_max);
+    const bool is_long = t < p.n_rows && n > p.cut, is_short = t < p.n_rows && !is_long;
+    const unsigned bl = __ballot_sync(0xffffffffu, is_long), bs = __ballot_sync(0xffffffffu, is_short);
+    if (lane == 0) {
+      s_cnt[0][warp] = __popc(bl);
+      s_cnt[1][warp] = __popc(bs);
+    }
+    __syncthreads();
+    int ol = 0, os = 0, tl = 0, ts = 0;
+    for (int w = 0; w < 32; ++w) {
+      if (w < warp) {
+        ol += s_cnt[0][w];
+        os += s_cnt[1][w];
+      }
+      tl += s_cnt[0][w];
+      ts += s_cnt[1][w];
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    if (is_long) p.plan[4 + n_long + ol + __popc(bl & lt)] = t;
+    if (is_short) p.plan[4 + p.n_rows + n_short + os + __popc(bs & lt)] = t;
+    n_long += tl;
+    n_short += ts;
+    __syncthreads();  // s_cnt is rewritten by the next chunk
+  }
+  if (tid == 0) {
+    int c = 16;
+    while (c > 1 && !((int64_t)n_long * c <= p.sm_count && (p.c_mask >> (31 - __clz(c)) & 1))) c >>= 1;
+    p.plan[0] = n_long;
+    p.plan[1] = c;
+    p.plan[2] = n_short;
+    p.plan[3] = 0;
+  }
+}
 
 struct SelFixed {
   uint32_t hist[kHistCopies][kHistBins];
@@ -320,7 +408,7 @@ select_kernel(SelectArgs a) {
   const unsigned lt_mask = (1u << lane) - 1u;
 
   SelRow r;
-  r.t = blockIdx.x;
+  if (!sel_unit_row(a, blockIdx.x, r.t)) return;
   r.L = 0;
   r.pt_row = nullptr;
   r.pt_s = pt_s;

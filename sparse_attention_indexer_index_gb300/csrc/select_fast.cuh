@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   SelRow r;
-  r.t = blockIdx.x;
+  if (!sel_unit_row(a, blockIdx.x, r.t)) return;
   r.L = 0;
   r.pt_row = nullptr;
   r.pt_s = sh.pt;

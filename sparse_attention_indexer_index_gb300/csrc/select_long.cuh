@@ -202,6 +202,10 @@ select_long_kernel(SelectArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const uint32_t C = cluster_nctarank();
+  // the row of this cluster (every CTA of a cluster gets the same answer, so
+  // a cluster without a row leaves before its first cluster barrier)
+  int t;
+  if (!sel_unit_row(a, (int)(blockIdx.x / C), t)) return;
 
   for (int i = tid; i < kSlBins; i += kSlThreads) fx.hloc[i] = 0u;
   if (rank == 0)
@@ -220,7 +224,6 @@ select_long_kernel(SelectArgs a) {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // ---- row metadata --------------------------------------------------------
-  const int t = (int)(blockIdx.x / C);
   int n, L = 0;
   const int32_t* pt_row = nullptr;
   if (kMode == kModeTopk) {

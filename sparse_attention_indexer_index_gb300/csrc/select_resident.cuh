@@ -148,7 +148,8 @@ select_resident_kernel(SelectArgs a) {
 
   // ---- row metadata and page-table entries: not produced by the previous
   // grid, so read before waiting on it -----------------------------------
-  const int t = blockIdx.x;
+  int t;
+  if (!sel_unit_row(a, blockIdx.x, t)) return;
   int n, L = 0;
   const int32_t* pt_row = nullptr;
   if (kMode == kModeTopk) {

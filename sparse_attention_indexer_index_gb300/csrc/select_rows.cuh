@@ -119,7 +119,8 @@ select_rows_kernel(SelectArgs a) {
   extern __shared__ __align__(16) unsigned char sr_smem_raw[];
   SrSmem& sm = *reinterpret_cast<SrSmem*>(sr_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = blockIdx.x;
+  int t;
+  if (!sel_unit_row(a, blockIdx.x, t)) return;
 
   // ---- row metadata (not produced by the previous grid) ---------------------------
   int n, L = 0;

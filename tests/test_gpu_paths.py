@@ -152,3 +152,54 @@ def test_decode_step_c2_verify_against_the_oracle(qsa):
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
     assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
     assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+# ----------------------------------------------------------------- per-row plan
+def _mixed_rows(rng, n_short, lengths_long, short_lo=3000, short_hi=30_000):
+    lens = np.concatenate([lengths_long, rng.integers(short_lo, short_hi, size=n_short)]).astype(np.int32)
+    return rng.permutation(lens).astype(np.int32)
+
+
+@pytest.mark.parametrize("k,with_slots", [(2048, True), (512, False)])
+def test_topk_mixed_lengths_take_the_row_plan(qsa, k, with_slots):
+    """One call with a 1M-entry row, four 80,000-entry rows and 100 short
+    rows (3,000-30,000), in random order: the device plan sends the five long
+    rows to clusters sized from their count and the short ones to one CTA
+    each.  Bit-exact against the oracle, slots included."""
+    rng = np.random.default_rng(k)
+    nv = _mixed_rows(rng, 100, [1_000_000, 80_000, 80_000, 80_000, 80_000])
+    ld = int(nv.max())
+    s = rng.standard_normal((nv.size, ld), dtype=np.float32)
+    P = 64
+    pt = np.stack([rng.permutation((ld + P - 1) // P) for _ in range(nv.size)]).astype(np.int32)
+    idx, slots = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=ld,
+                                 page_table=to_dev(pt) if with_slots else None, page_size=P)
+    ref_idx, ref_slots = oracle.topk(s, k, n_valid=nv, page_table=pt if with_slots else None, page_size=P)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    if with_slots:
+        assert np.array_equal(slots.cpu().numpy(), ref_slots)
+
+
+def test_indexer_mixed_contexts_take_the_row_plan(qsa):
+    """The fused indexer on 80 one-row requests, two of them with contexts
+    past 131K tokens (more than 32,768 blocks) among short ones, with a
+    workspace (so the device plan runs): the selection, positions and slots
+    bit-exact against the oracle on the GPU's scores."""
+    import torch
+    rng = np.random.default_rng(71)
+    lens = _mixed_rows(rng, 78, [150_001, 199_998], 4096, 40_000)
+    w = decode_workload(72, [[int(L)] for L in lens], page_size=64, k_blk=512, with_keys=False)
+    pool = torch.randn((w.pool_rows, 128), device="cuda").to(torch.bfloat16)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    ws = torch.empty(qsa.indexer_select_workspace_size(w.n_rows, w.max_len, 512), dtype=torch.uint8,
+                     device="cuda")
+    out = qsa.indexer_select(bf16_dev(w.q), pool, to_dev(w.req_row_start), to_dev(w.row_len),
+                             to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, k_blk=512,
+                             want_blocks=True, want_pos=True, scores_out=scores, workspace=ws)
+    s = scores.cpu().numpy()
+    sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
