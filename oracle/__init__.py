@@ -102,6 +102,13 @@ def _load():
                 "oracle_append_keys": (None, [p, p, p, i64, p, p, i64, i64, d, p]),
                 "oracle_sparse_attn_row": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, p, i64, d, p, p]),
                 "oracle_sparse_attn": (ctypes.c_int, [p, p, p, i64, i64, i64, i64, i64, p, i64, i64, d, p, p]),
+                "oracle_rope_queries": (None, [p, p, i64, d, p]),
+                "oracle_e4m3_to_double": (d, [ctypes.c_uint8]),
+                "oracle_e4m3_round": (ctypes.c_uint8, [ctypes.c_float]),
+                "oracle_quantize_keys_fp8": (None, [p, i64, p, p]),
+                "oracle_f16_round": (d, [d]),
+                "oracle_score_one_fp8": (ctypes.c_float, [p, p, ctypes.c_float]),
+                "oracle_index_scores_fp8": (None, [p, p, p, i64, p, p, p, i64, i64, p, i64]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -345,3 +352,59 @@ def append_keys(new_keys, req_tok_start, req_first_pos, ring, page_table, page_s
     _load().oracle_append_keys(_ptr(nk), _ptr(rts), _ptr(rfp), rts.size - 1, _ptr(ring), _ptr(pt),
                                pt.shape[-1], int(page_size), float(rope_base), _ptr(pool))
     return ring, pool
+
+
+# ---------------------------------------------------------------- prologue tails
+def rope_queries(q, pos, rope_base=10000.0):
+    """q [n_rows][4][128] u16 (BF16 bits), pos [n_rows] -> the rotated query."""
+    q = _c(q, np.uint16)
+    pos = _c(pos, np.int32)
+    out = np.empty_like(q)
+    _load().oracle_rope_queries(_ptr(q), _ptr(pos), pos.size, float(rope_base), _ptr(out))
+    return out
+
+
+def e4m3_to_float(code: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(code)))
+
+
+def e4m3_round(x: float) -> int:
+    return int(_load().oracle_e4m3_round(float(x)))
+
+
+def f16_round(x: float) -> float:
+    return float(_load().oracle_f16_round(float(x)))
+
+
+def quantize_keys_fp8(keys):
+    """keys [n][128] u16 (BF16 bits) -> (codes [n][128] u8, scales [n] f32)."""
+    keys = _c(keys, np.uint16)
+    n = keys.shape[0]
+    codes = np.empty((n, 128), np.uint8)
+    scales = np.empty(n, np.float32)
+    _load().oracle_quantize_keys_fp8(_ptr(keys), n, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def score_one_fp8(q_row, codes, scale) -> float:
+    q_row = _c(q_row, np.uint16)
+    codes = _c(codes, np.uint8)
+    return float(_load().oracle_score_one_fp8(_ptr(q_row), _ptr(codes), float(scale)))
+
+
+def index_scores_fp8(q, codes, scales, req_row_start, row_len, page_table, page_size, ld_scores=None):
+    """index_scores with FP8 keys (codes [pool_rows][128] u8, scales [pool_rows]);
+    entries b >= row_len/4 are NaN."""
+    q = _c(q, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    rrs = _c(req_row_start, np.int32)
+    rl = _c(row_len, np.int32)
+    pt = _c(page_table, np.int32)
+    n_rows = rl.size
+    if ld_scores is None:
+        ld_scores = max(1, int(rl.max()) // C) if n_rows else 1
+    out = np.full((n_rows, ld_scores), np.nan, np.float32)
+    _load().oracle_index_scores_fp8(_ptr(q), _ptr(codes), _ptr(scales), rrs.size - 1, _ptr(rrs), _ptr(rl),
+                                    _ptr(pt), pt.shape[-1], int(page_size), _ptr(out), ld_scores)
+    return out

@@ -494,3 +494,139 @@ void oracle_indexer_select(const uint16_t* q, const uint16_t* pool, int64_t n_re
   oracle_expand(out_blocks, k_blk, n_req, req_row_start, row_len, page_table, ld_pt, page_size,
                 out_pos, out_slots);
 }
+
+/* ---------- prologue tails: query RoPE and FP8 index keys ----------------
+ * SGLang GLM-5.2 blog, section "Indexer Prologue Fusion": the query path is
+ * RoPE + FP8 quantisation (+ head gates, which QSA's score does not have),
+ * the key path LayerNorm + RoPE + FP8 quantisation + the paged index-cache
+ * store.  For QSA's compressed keys the pages give no FP8 layout; the
+ * reading taken: e4m3 codes with one FP32 scale per compressed key. */
+
+/* Query RoPE: the 4 heads of row t rotated at the row's own position
+ * pos[t] (the newest token it sees), rotate-half pairs (i, i+64), angle
+ * pos * rope_base^(-2i/128), in FP64, one round to BF16. */
+void oracle_rope_queries(const uint16_t* q, const int32_t* pos, int64_t n_rows, double rope_base,
+                         uint16_t* out) {
+  const int half = QSA_D / 2;
+  for (int64_t t = 0; t < n_rows; ++t)
+    for (int h = 0; h < QSA_H; ++h) {
+      const uint16_t* x = q + (t * QSA_H + h) * QSA_D;
+      uint16_t* y = out + (t * QSA_H + h) * QSA_D;
+      for (int i = 0; i < half; ++i) {
+        double inv_freq = pow(rope_base, -(2.0 * (double)i) / (double)QSA_D);
+        double theta = (double)pos[t] * inv_freq;
+        double c = cos(theta), s = sin(theta);
+        double u = oracle_bf16_to_double(x[i]), v = oracle_bf16_to_double(x[i + half]);
+        y[i] = oracle_bf16_round(u * c - v * s);
+        y[i + half] = oracle_bf16_round(v * c + u * s);
+      }
+    }
+}
+
+/* FP8 e4m3 (the "fn" variant): 1 sign bit, 4 exponent bits biased by 7,
+ * 3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9; the
+ * largest finite value is 448 (0x7E); 0x7F and 0xFF are NaN; there is no
+ * infinity. */
+double oracle_e4m3_to_double(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+  return s ? -v : v;
+}
+
+/* Nearest e4m3 value of a float, ties to even, saturating at +-448 (finite
+ * results only); NaN gives 0x7F. */
+uint8_t oracle_e4m3_round(float xf) {
+  double x = (double)xf;
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  int e;
+  frexp(a, &e);                    /* a = f * 2^e, f in [0.5, 1) */
+  int qexp = e - 4;                /* quantum of a 4-significant-bit value */
+  if (qexp < -9) qexp = -9;        /* subnormal quantum */
+  double r = a == 0.0 ? 0.0 : nearbyint(a / ldexp(1.0, qexp)) * ldexp(1.0, qexp);
+  if (r > 448.0) r = 448.0;        /* saturate */
+  if (r == 0.0) return sign;
+  int re;
+  frexp(r, &re);                   /* r = g * 2^re, g in [0.5, 1) */
+  int ue = re - 1;                 /* r in [2^ue, 2^(ue+1)) */
+  uint8_t code;
+  if (ue < -6) {                   /* subnormal: r = m * 2^-9 */
+    code = (uint8_t)(r / ldexp(1.0, -9));
+  } else {
+    int m = (int)(r / ldexp(1.0, ue - 3)) - 8;   /* r = (8 + m) * 2^(ue-3) */
+    code = (uint8_t)(((ue + 7) << 3) | m);
+  }
+  return (uint8_t)(sign | code);
+}
+
+/* FP8 compressed keys: per key, scale = fp32(max_d |k_d|) / 448 (FP32
+ * division) and code_d = e4m3(k_d / scale) (FP32 division, then the nearest
+ * e4m3 value, ties to even, saturating); a zero key gets scale 0 and zero
+ * codes.  Every step that decides a code is FP32, so both sides of a parity
+ * check take the same decisions. */
+void oracle_quantize_keys_fp8(const uint16_t* keys, int64_t n, uint8_t* codes, float* scales) {
+  for (int64_t r = 0; r < n; ++r) {
+    float mx = 0.0f;
+    for (int d = 0; d < QSA_D; ++d) {
+      float v = fabsf((float)oracle_bf16_to_double(keys[r * QSA_D + d]));
+      if (v > mx) mx = v;
+    }
+    const float scale = mx / 448.0f;
+    scales[r] = scale;
+    for (int d = 0; d < QSA_D; ++d) {
+      float v = (float)oracle_bf16_to_double(keys[r * QSA_D + d]);
+      codes[r * QSA_D + d] = scale > 0.0f ? oracle_e4m3_round(v / scale) : 0;
+    }
+  }
+}
+
+/* Nearest IEEE binary16 value (1 sign, 5 exponent bits biased by 15, 10
+ * mantissa bits; subnormal quantum 2^-24; largest finite 65504), ties to
+ * even, as a double.  Beyond 65520 the nearest value is infinity. */
+double oracle_f16_round(double x) {
+  if (x == 0.0 || isnan(x)) return x;
+  double a = fabs(x);
+  int e;
+  frexp(a, &e);
+  int qexp = e - 11;               /* quantum of an 11-significant-bit value */
+  if (qexp < -24) qexp = -24;
+  double r = nearbyint(a / ldexp(1.0, qexp)) * ldexp(1.0, qexp);
+  if (r > 65504.0) r = INFINITY;
+  return signbit(x) ? -r : r;
+}
+
+/* Score of one query row against one FP8 key: the FP8 scorer holds the query
+ * in FP16 (each BF16 element rounded to the nearest binary16 value), the key
+ * is code * scale:
+ *   s = (1/sqrt(128)) * sum_h ReLU( sum_d f16(q_hd) * e4m3(c_d) * scale ),
+ * in FP64, rounded once to FP32. */
+float oracle_score_one_fp8(const uint16_t* q, const uint8_t* codes, float scale) {
+  double total = 0.0;
+  for (int h = 0; h < QSA_H; ++h) {
+    const uint16_t* qh = q + h * QSA_D;   /* head h */
+    double hdot = 0.0;
+    for (int d = 0; d < QSA_D; ++d)
+      hdot += oracle_f16_round(oracle_bf16_to_double(qh[d])) * oracle_e4m3_to_double(codes[d]) * (double)scale;
+    total += hdot > 0.0 ? hdot : 0.0;
+  }
+  return (float)(total / sqrt((double)QSA_D));
+}
+
+/* oracle_index_scores with FP8 keys: codes [pool_rows][128], scales
+ * [pool_rows], the same pool-row addressing (full_slot/4). */
+void oracle_index_scores_fp8(const uint16_t* q, const uint8_t* codes, const float* scales, int64_t n_req,
+                             const int32_t* req_row_start, const int32_t* row_len, const int32_t* page_table,
+                             int64_t ld_pt, int64_t page_size, float* scores, int64_t ld_scores) {
+  for (int64_t r = 0; r < n_req; ++r) {
+    const int32_t* pt_row = page_table + r * ld_pt;
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t) {
+      const int64_t n_blocks = row_len[t] / QSA_C;   /* complete blocks only */
+      for (int64_t b = 0; b < n_blocks; ++b) {
+        const int64_t row = oracle_pool_row(pt_row, b, page_size);
+        scores[t * ld_scores + b] = oracle_score_one_fp8(q + t * QSA_H * QSA_D, codes + row * QSA_D, scales[row]);
+      }
+    }
+  }
+}

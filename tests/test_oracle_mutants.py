@@ -62,6 +62,18 @@ MUTANTS = {
     "attn_nan_when_all_masked": ("out[h * d + e] = sum > 0.0 ? (float)(acc[e] / sum) : 0.0f;",
                                  "out[h * d + e] = (float)(acc[e] / sum);"),
     "attn_no_scale": ("      logit[j] = scale * dot;", "      logit[j] = dot;"),
+    "rope_queries_wrong_sign": ("y[i + half] = oracle_bf16_round(v * c + u * s);",
+                                "y[i + half] = oracle_bf16_round(v * c - u * s);"),
+    "rope_queries_position_off_by_one": ("double theta = (double)pos[t] * inv_freq;",
+                                         "double theta = (double)(pos[t] + 1) * inv_freq;"),
+    "e4m3_truncates": ("double r = a == 0.0 ? 0.0 : nearbyint(a / ldexp(1.0, qexp)) * ldexp(1.0, qexp);",
+                       "double r = a == 0.0 ? 0.0 : floor(a / ldexp(1.0, qexp)) * ldexp(1.0, qexp);"),
+    "e4m3_no_saturation": ("  if (r > 448.0) r = 448.0;        /* saturate */\n", ""),
+    "fp8_scale_wrong_range": ("const float scale = mx / 448.0f;", "const float scale = mx / 256.0f;"),
+    "fp8_score_no_relu": ("total += hdot > 0.0 ? hdot : 0.0;", "total += hdot;"),
+    "fp8_query_not_binary16": ("hdot += oracle_f16_round(oracle_bf16_to_double(qh[d]))",
+                               "hdot += oracle_bf16_to_double(qh[d])"),
+    "f16_no_subnormal_quantum": ("  if (qexp < -24) qexp = -24;\n", ""),
     "indexshare_no_drafted_columns": (
         "int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;\n  int64_t nb0",
         "int64_t width = QSA_C * k_blk + (QSA_C - 1);\n  int64_t nb0"),
@@ -81,7 +93,8 @@ def _run_mutant(name, tmpdir):
                            "-o", lib, csrc, "-lm"])
     env = dict(os.environ, QSA_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                        os.path.join(ROOT, "tests", "test_oracle.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_prologue.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode
 
