@@ -508,6 +508,51 @@ def bench_variant_decode(g, w, new_blocks, iters, warmup, peaks):
     return res
 
 
+def bench_variant_decode_fp8(g, w, iters, warmup, peaks):
+    """The fused indexer call on FP8 index keys (e4m3 codes + one FP32 scale
+    per compressed key: 132 B a key instead of 256 B) beside the same call
+    on BF16 keys, L2 flushed before every call; plus the scorer alone on
+    each, and how many of the BF16 call's selected blocks the FP8 call also
+    selects (the quality cost of the smaller keys)."""
+    torch, qsa = g.torch, g.qsa
+    st = setup_decode(g, w, 0)
+    codes, scales = qsa.quantize_keys_fp8(st["pool"])
+    args = (st["rrs"], st["row_len"], st["pt"], w.page_size, w.max_len, w.max_rows_per_req)
+
+    def bf16_call():
+        qsa.indexer_select(st["q"], st["pool"], *args, k_blk=w.k_blk, workspace=st["ws"], out_slots=st["slots"])
+
+    def fp8_call():
+        qsa.indexer_select_fp8(st["q"], codes, scales, *args, k_blk=w.k_blk, workspace=st["ws"],
+                               out_slots=st["slots"])
+
+    t_bf16 = g.timed(bf16_call, iters, warmup)
+    t_fp8 = g.timed(fp8_call, iters, warmup)
+    t_sc_bf16 = g.timed(lambda: qsa.index_scores(st["q"], st["pool"], *args, scores=st["scores"]), iters, warmup)
+    t_sc_fp8 = g.timed(lambda: qsa.index_scores_fp8(st["q"], codes, scales, *args, scores=st["scores"]),
+                       iters, warmup)
+    sel = {}
+    for name, fn in (("bf16", qsa.indexer_select), ("fp8", qsa.indexer_select_fp8)):
+        keys = (st["pool"],) if name == "bf16" else (codes, scales)
+        sel[name] = fn(st["q"], *keys, *args, k_blk=w.k_blk, want_blocks=True)["blocks"].cpu().numpy()
+    overlap = [len(np.intersect1d(a[a >= 0], b[b >= 0])) / max(1, int((a >= 0).sum()))
+               for a, b in zip(sel["bf16"], sel["fp8"])]
+    by = decode_bytes(w)
+    keys8 = by["keys"] // 256 * (128 + 4)
+    alg = keys8 + by["q"] + by["page_table"] + by["slots"]
+    ms, ms16 = statistics.mean(t_fp8), statistics.mean(t_bf16)
+    res = {"workload": w.name + "_fp8_keys", "rows": w.n_rows, "us_per_call": 1e3 * ms,
+           "bf16_keys_us_per_call": 1e3 * ms16, "speedup_vs_bf16_keys": ms16 / ms,
+           "alg_bytes": alg, "alg_GBps": alg / (ms * 1e-3) / 1e9,
+           "frac_hbm": alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "score_kernel_us": 1e3 * statistics.mean(t_sc_fp8),
+           "score_kernel_bf16_keys_us": 1e3 * statistics.mean(t_sc_bf16),
+           "selection_overlap_with_bf16_keys": float(np.mean(overlap))}
+    del st
+    torch.cuda.synchronize()
+    return res
+
+
 def topk_kernel_name(n_rows, n, sm_count=152, k=2048):
     """The selection kernel for n_rows rows of n scores and k winners."""
     if n > 32768:
@@ -784,6 +829,7 @@ def variant_table(g, it, warmup, peaks):
         "c1_decode_L8192": lambda: bench_variant_decode(g, c1_decode(0), 1, it, warmup, peaks),
         "c2_b32_verify_x32": lambda: bench_variant_decode(g, c2_batched(0), 2, it, warmup, peaks),
         "c3_batched_32req": lambda: bench_variant_decode(g, c3_batched(0), 1, it, warmup, peaks),
+        "c3_batched_32req_fp8_keys": lambda: bench_variant_decode_fp8(g, c3_batched(0), it, warmup, peaks),
         "c4_dsa_topk_normal": lambda: bench_variant_topk(g, c4_dsa_topk(0, "normal"), it, warmup, peaks),
         "c4_dsa_topk_relu4": lambda: bench_variant_topk(g, c4_dsa_topk(0, "relu4"), it, warmup, peaks),
         "c4_dsa_topk_fp16dup": lambda: bench_variant_topk(g, c4_dsa_topk(0, "fp16dup"), it, warmup, peaks),

@@ -181,6 +181,12 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
  *   out_slots  [n_rows][k] or NULL: slot(out_idx), -1 stays -1.
  * Order: larger value first; equal values by ascending index; -0 == +0; NaN
  * below every number.  The result is unique, so it is bit-exact.
+ * Workspace: topk_select_workspace_size(...) bytes (4-byte aligned) hold a
+ * row plan made on the device ([TOPK]: a planning kernel reads the batch's
+ * lengths so that long rows get a cluster of CTAs and short rows one CTA);
+ * it is used when n_max exceeds 32768 and there are more rows than half the
+ * SMs.  With a smaller or no workspace every row takes the kernel chosen
+ * from n_max and n_rows alone.  The size query may return 0.
  * ------------------------------------------------------------------- */
 size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k);
 qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int32_t n_rows,
@@ -324,7 +330,10 @@ qsa_status qsa_select_blocks(const float* scores, int64_t ld_scores, int32_t n_r
  *              workspace.
  * Workspace: when scores_out is NULL the scores live in the workspace, which
  * must hold qsa_indexer_select_workspace_size(n_rows, max_len, k_blk) bytes;
- * when scores_out is given the workspace may be NULL with 0 bytes.
+ * when scores_out is given the workspace may be NULL with 0 bytes.  Past the
+ * scores (or from its start, with scores_out) a workspace of that size also
+ * holds the selection's row plan for contexts of more than 131,072 tokens
+ * (see topk_select); without room for it the plan is made on the host.
  * ------------------------------------------------------------------- */
 size_t qsa_indexer_select_workspace_size(int32_t n_rows, int32_t max_len, int32_t k_blk);
 qsa_status qsa_indexer_select(const void* q, const void* pool, int64_t pool_rows, int32_t n_req,
@@ -374,6 +383,53 @@ qsa_status qsa_indexer_select_noalloc(const void* q, const void* pool, int64_t p
                                       int64_t ld_pt, int32_t page_size, int32_t k_blk,
                                       int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots,
                                       void* stream);
+
+/* ---------------------------------------------------------------------
+ * Prologue tails  (SGLang GLM-5.2 blog, section "Indexer Prologue Fusion":
+ * the query path applies RoPE and FP8 quantisation, the key path FP8
+ * quantisation before the paged index-cache store; QSA's score has no head
+ * gates, so none are applied).
+ *
+ * qsa_rope_queries: the 4 index heads of row t rotated at position pos[t]
+ * (the newest token the row sees, row_len - 1), rotate-half pairs (i, i+64),
+ * angle pos * rope_base^(-2i/128), the angle reduced exactly as in
+ * qsa_compress_keys; FP32 arithmetic, one rounding to BF16 (nearest even).
+ *   q, q_out   [n_rows][4][128] BF16, 16-byte aligned (q_out may equal q).
+ *   pos        [n_rows] positions >= 0 (a negative one latches the grouping
+ *              fault bit and leaves that row's output unwritten).
+ *
+ * qsa_quantize_keys_fp8: compressed keys to FP8.  The pages give no layout
+ * for FP8 index keys; the one used here: e4m3 codes (1 sign, 4 exponent bits
+ * biased by 7, 3 mantissa bits, largest finite 448) with one FP32 scale per
+ * key, scale = max_d |k_d| / 448 (FP32 division) and code_d = e4m3(k_d /
+ * scale) (FP32 division, nearest value, ties to even, saturating); a zero key
+ * gets scale 0 and zero codes.
+ *   keys   [n_keys][128] BF16 (16-byte aligned), e.g. a whole pool.
+ *   codes  [n_keys][128] bytes (16-byte aligned); scales [n_keys] FP32.
+ *
+ * qsa_index_scores_fp8 / qsa_indexer_select_fp8: qsa_index_scores and
+ * qsa_indexer_select on FP8 keys (codes and scales in place of the BF16
+ * pool, same pool-row addressing).  The query is held in FP16 (each BF16
+ * element rounded to the nearest binary16 value, exact for magnitudes in
+ * [2^-14, 65504)); a key contributes code * scale:
+ *   s[t][b] = (1/sqrt(128)) sum_h ReLU( scale_b sum_d f16(q[t][h][d]) code_b[d] ).
+ * Up to 4096 requests of up to 8 rows each, on pages holding a multiple of
+ * 8 compressed keys (page_size a multiple of 32); other shapes return
+ * QSA_ERR_UNSUPPORTED.  Workspace, outputs and errors as for the BF16 calls.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_rope_queries(const void* q, const int32_t* pos, int32_t n_rows, double rope_base, void* q_out,
+                            void* stream);
+qsa_status qsa_quantize_keys_fp8(const void* keys, int64_t n_keys, uint8_t* codes, float* scales, void* stream);
+qsa_status qsa_index_scores_fp8(const void* q, const uint8_t* codes, const float* scales, int64_t pool_rows,
+                                int32_t n_req, const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                                int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table, int64_t ld_pt,
+                                int32_t page_size, float* scores, int64_t ld_scores, int64_t n_fill, void* stream);
+qsa_status qsa_indexer_select_fp8(const void* q, const uint8_t* codes, const float* scales, int64_t pool_rows,
+                                  int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                  const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                  const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                  int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                  int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,7 @@ __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
     "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn", "append_keys", "decode_step",
+    "rope_queries", "quantize_keys_fp8", "index_scores_fp8", "indexer_select_fp8",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -66,6 +67,12 @@ def lib():
             "qsa_indexer_select_workspace_size": (sz, [i32, i32, i32]),
             "qsa_indexer_select": (ctypes.c_int, [p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                   i32, p, p, p, p, i64, p, sz, p]),
+            "qsa_rope_queries": (ctypes.c_int, [p, p, i32, d, p, p]),
+            "qsa_quantize_keys_fp8": (ctypes.c_int, [p, i64, p, p, p]),
+            "qsa_index_scores_fp8": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
+                                                    i64, i64, p]),
+            "qsa_indexer_select_fp8": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
+                                                      i32, p, p, p, p, i64, p, sz, p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -214,8 +221,29 @@ def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len
     """Block scores [n_rows][ld] float32 (entries b < row_len/4 written,
     [row_len/4, n_fill) set to -inf)."""
     torch = _torch()
-    _dev(q, torch.bfloat16, "q", 3)
     _dev(pool, torch.bfloat16, "pool", 2)
+    return _index_scores_call("qsa_index_scores", (_ptr(pool),), pool.shape[0], q, req_row_start, row_len,
+                              page_table, page_size, max_len, max_rows_per_req, scores, n_fill, stream)
+
+
+def index_scores_fp8(q, codes, scales, req_row_start, row_len, page_table, page_size, max_len,
+                     max_rows_per_req=None, scores=None, n_fill=0, stream=None):
+    """index_scores on FP8 keys: codes [pool_rows][128] uint8 (e4m3) and
+    scales [pool_rows] float32 from quantize_keys_fp8."""
+    torch = _torch()
+    _dev(codes, torch.uint8, "codes", 2)
+    _dev(scales, torch.float32, "scales", 1)
+    if scales.numel() != codes.shape[0]:
+        raise ValueError("scales must have one entry per key")
+    return _index_scores_call("qsa_index_scores_fp8", (_ptr(codes), _ptr(scales)), codes.shape[0], q,
+                              req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req,
+                              scores, n_fill, stream)
+
+
+def _index_scores_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, page_table, page_size, max_len,
+                       max_rows_per_req, scores, n_fill, stream):
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
     _dev(req_row_start, torch.int32, "req_row_start", 1)
     _dev(row_len, torch.int32, "row_len", 1)
     _dev(page_table, torch.int32, "page_table", 2)
@@ -226,11 +254,44 @@ def index_scores(q, pool, req_row_start, row_len, page_table, page_size, max_len
         ld = max(1, (max(int(max_len) // BLOCK, int(n_fill)) + 3) // 4 * 4)
         scores = torch.empty((n_rows, ld), dtype=torch.float32, device=q.device)
     _dev(scores, torch.float32, "scores", 2)
-    _check("qsa_index_scores", lib().qsa_index_scores(
-        _ptr(q), _ptr(pool), pool.shape[0], req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+    _check(fn, getattr(lib(), fn)(
+        _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
         _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
         int(page_size), _ptr(scores), scores.shape[1], int(n_fill), _stream(stream)))
     return scores
+
+
+def rope_queries(q, pos, out=None, rope_base=10000.0, stream=None):
+    """Index-query RoPE: q [n_rows][4][128] bf16 rotated (rotate-half) at
+    pos [n_rows] int32; out may be q itself.  Returns out."""
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
+    _dev(pos, torch.int32, "pos", 1)
+    if pos.numel() != q.shape[0]:
+        raise ValueError("pos must have one entry per row")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, torch.bfloat16, "out", 3)
+    _check("qsa_rope_queries", lib().qsa_rope_queries(
+        _ptr(q), _ptr(pos), q.shape[0], float(rope_base), _ptr(out), _stream(stream)))
+    return out
+
+
+def quantize_keys_fp8(keys, codes=None, scales=None, stream=None):
+    """Compressed keys [n][128] bf16 -> (codes [n][128] uint8 e4m3,
+    scales [n] float32), scale = max|k| / 448 per key."""
+    torch = _torch()
+    _dev(keys, torch.bfloat16, "keys", 2)
+    n = keys.shape[0]
+    if codes is None:
+        codes = torch.empty((n, keys.shape[1]), dtype=torch.uint8, device=keys.device)
+    if scales is None:
+        scales = torch.empty(n, dtype=torch.float32, device=keys.device)
+    _dev(codes, torch.uint8, "codes", 2)
+    _dev(scales, torch.float32, "scales", 1)
+    _check("qsa_quantize_keys_fp8", lib().qsa_quantize_keys_fp8(
+        _ptr(keys), n, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
 
 
 def topk_select(scores, k, n_valid=None, n_max=None, page_table=None, row_req=None, page_size=0,
@@ -393,8 +454,31 @@ def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, max_l
     """Fused decode path: score -> top-k_blk blocks -> expand -> slots.
     Returns dict(slots, blocks?, pos?, scores?)."""
     torch = _torch()
-    _dev(q, torch.bfloat16, "q", 3)
     _dev(pool, torch.bfloat16, "pool", 2)
+    return _indexer_select_call("qsa_indexer_select", (_ptr(pool),), pool.shape[0], q, req_row_start,
+                                row_len, page_table, page_size, max_len, max_rows_per_req, k_blk,
+                                want_blocks, want_pos, scores_out, workspace, out_slots, stream)
+
+
+def indexer_select_fp8(q, codes, scales, req_row_start, row_len, page_table, page_size, max_len,
+                       max_rows_per_req=None, k_blk=512, want_blocks=False, want_pos=False,
+                       scores_out=None, workspace=None, out_slots=None, stream=None):
+    """indexer_select on FP8 keys (codes, scales from quantize_keys_fp8)."""
+    torch = _torch()
+    _dev(codes, torch.uint8, "codes", 2)
+    _dev(scales, torch.float32, "scales", 1)
+    if scales.numel() != codes.shape[0]:
+        raise ValueError("scales must have one entry per key")
+    return _indexer_select_call("qsa_indexer_select_fp8", (_ptr(codes), _ptr(scales)), codes.shape[0], q,
+                                req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req,
+                                k_blk, want_blocks, want_pos, scores_out, workspace, out_slots, stream)
+
+
+def _indexer_select_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, page_table, page_size,
+                         max_len, max_rows_per_req, k_blk, want_blocks, want_pos, scores_out, workspace,
+                         out_slots, stream):
+    torch = _torch()
+    _dev(q, torch.bfloat16, "q", 3)
     _dev(req_row_start, torch.int32, "req_row_start", 1)
     _dev(row_len, torch.int32, "row_len", 1)
     _dev(page_table, torch.int32, "page_table", 2)
@@ -420,8 +504,8 @@ def indexer_select(q, pool, req_row_start, row_len, page_table, page_size, max_l
             workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         elif workspace is not None:
             ws_bytes = workspace.numel() * workspace.element_size()
-    _check("qsa_indexer_select", lib().qsa_indexer_select(
-        _ptr(q), _ptr(pool), pool.shape[0], req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+    _check(fn, getattr(lib(), fn)(
+        _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
         _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
         int(page_size), int(k_blk), _ptr(blocks), _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld,
         _ptr(workspace), ws_bytes, _stream(stream)))

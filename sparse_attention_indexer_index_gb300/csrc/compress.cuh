@@ -23,6 +23,8 @@
 // as a kernel parameter (FP64 arithmetic is slow on this GPU: one pow per
 // thread cost ~8 us of latency).
 #pragma once
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace qsa {
@@ -62,6 +64,16 @@ __device__ __forceinline__ void accumulate_bf16x8(float (&acc)[8], uint4 v) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// sin and cos of the RoPE angle pos * t, with t a 64-bit fraction of a turn:
+// pos * t mod 1 as a wrapping integer product, its top 32 bits (signed, half a
+// turn either way) as the angle in units of pi.
+__device__ __forceinline__ void rope_sincos(uint32_t pos, uint64_t turn_frac, float& s, float& c) {
+  const uint64_t ph = (uint64_t)pos * turn_frac;               // turns mod 1, wraps
+  const int32_t top = (int32_t)(ph >> 32);                     // signed: [-1/2, 1/2) turn
+  const float y = (float)top * 4.656612873077392578125e-10f;   // * 2^-31: units of pi
+  sincospif(y, &s, &c);
 }
 
 // One block compressed by the 8 lanes of a group: lane8 holds dims
@@ -106,11 +118,8 @@ __device__ __forceinline__ void compress_block_8(const uint4 (&vlo)[kBlock], con
     float r_lo[2], r_hi[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint64_t ph = (uint64_t)pos * turn_frac[e + h];  // turns mod 1, wraps
-      const int32_t top = (int32_t)(ph >> 32);               // signed: [-1/2, 1/2) turn
-      const float y = (float)top * 4.656612873077392578125e-10f;  // * 2^-31: units of pi
       float s, c;
-      sincospif(y, &s, &c);
+      rope_sincos(pos, turn_frac[e + h], s, c);
       const float u = lo[e + h] * inv_norm, v = hi[e + h] * inv_norm;
       r_lo[h] = u * c - v * s;
       r_hi[h] = v * c + u * s;
@@ -257,6 +266,110 @@ append_keys_kernel(AppendArgs a, const __grid_constant__ RopeTurns turns) {
     *reinterpret_cast<uint4*>(ring + slot * kDim + 8 * part) =
         *reinterpret_cast<const uint4*>(keys + (int64_t)i * kDim + 8 * part);
   }
+}
+
+}  // namespace qsa
+
+namespace qsa {
+
+// ---------------------------------------------------------------------------
+// Prologue tails (SGLang GLM-5.2 blog, section "Indexer Prologue Fusion": the
+// query path applies RoPE and FP8 quantisation, the key path FP8 quantisation
+// before the paged index-cache store).
+// ---------------------------------------------------------------------------
+
+// Query RoPE: the 4 heads of row t rotated at position pos[t] (the newest
+// token the row sees), rotate-half pairs (i, i+64), the angle reduced exactly
+// as in the key path; one BF16 rounding.  8 lanes per (row, head): lane j owns
+// dims [8j, 8j+8) and their partners [64+8j, ...).
+struct RopeQArgs {
+  const __nv_bfloat16* q;   // [n_rows][4][128]
+  const int32_t* pos;       // [n_rows]
+  int32_t n_rows;
+  __nv_bfloat16* out;       // [n_rows][4][128] (may be q)
+};
+constexpr int kRopeQThreads = 256;
+
+__global__ void __launch_bounds__(kRopeQThreads)
+rope_queries_kernel(RopeQArgs a, const __grid_constant__ RopeTurns turns) {
+  pdl_launch_dependents();  // the scorer may start its set-up; it waits for the queries
+  const int lane8 = threadIdx.x & (kCompressLanes - 1);
+  const int64_t unit = (int64_t)blockIdx.x * (kRopeQThreads / kCompressLanes) + threadIdx.x / kCompressLanes;
+  if (unit >= (int64_t)a.n_rows * kHeads) return;
+  const int p = __ldg(a.pos + unit / kHeads);
+  if (p < 0) {
+    if (lane8 == 0) raise_fault(kFaultGrouping);
+    return;
+  }
+  const __nv_bfloat16* src = a.q + unit * kDim;
+  const uint4 lo4 = ld_stream_16(src + 8 * lane8), hi4 = ld_stream_16(src + 64 + 8 * lane8);
+  const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+  uint32_t out_lo[4], out_hi[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 u = bf16x2_to_float2(lo[e]), v = bf16x2_to_float2(hi[e]);
+    float s0, c0, s1, c1;
+    rope_sincos((uint32_t)p, turns.frac[8 * lane8 + 2 * e], s0, c0);
+    rope_sincos((uint32_t)p, turns.frac[8 * lane8 + 2 * e + 1], s1, c1);
+    out_lo[e] = pack_bf16x2(u.x * c0 - v.x * s0, u.y * c1 - v.y * s1);
+    out_hi[e] = pack_bf16x2(v.x * c0 + u.x * s0, v.y * c1 + u.y * s1);
+  }
+  __nv_bfloat16* dst = a.out + unit * kDim;
+  *reinterpret_cast<uint4*>(dst + 8 * lane8) = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+  *reinterpret_cast<uint4*>(dst + 64 + 8 * lane8) = make_uint4(out_hi[0], out_hi[1], out_hi[2], out_hi[3]);
+}
+
+// FP8 compressed keys: per key, scale = max_d |k_d| / 448 (FP32 division)
+// and code_d = e4m3(k_d / scale) (FP32 division, nearest e4m3 value, ties to
+// even, saturating); a zero key gets scale 0 and zero codes.  8 lanes per key,
+// 16 dims each.
+struct QuantArgs {
+  const __nv_bfloat16* keys;  // [n][128]
+  int64_t n;
+  uint8_t* codes;             // [n][128]
+  float* scales;              // [n]
+};
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_keys_fp8_kernel(QuantArgs a) {
+  pdl_launch_dependents();
+  const int lane8 = threadIdx.x & (kCompressLanes - 1);
+  const int64_t key = (int64_t)blockIdx.x * (kQuantThreads / kCompressLanes) + threadIdx.x / kCompressLanes;
+  const bool live = key < a.n;
+  const __nv_bfloat16* src = a.keys + (live ? key : 0) * kDim + 16 * lane8;
+  const uint4 w0 = live ? ld_stream_16(src) : make_uint4(0u, 0u, 0u, 0u);
+  const uint4 w1 = live ? ld_stream_16(src + 8) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float x[16];
+  float mx = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float2 f = bf16x2_to_float2(w[e]);
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  // the 8 lanes of a key always reach this together
+  const unsigned group = 0xffu << (threadIdx.x & 24);
+  mx = fmaxf(mx, __shfl_xor_sync(group, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(group, mx, 2));
+  mx = fmaxf(mx, __shfl_xor_sync(group, mx, 4));
+  if (!live) return;
+  const float scale = mx / 448.0f;
+  uint32_t out[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint32_t word = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t code =
+          scale > 0.f ? (uint32_t)__nv_cvt_float_to_fp8(x[4 * e + b] / scale, __NV_SATFINITE, __NV_E4M3) : 0u;
+      word |= (code & 0xffu) << (8 * b);
+    }
+    out[e] = word;
+  }
+  *reinterpret_cast<uint4*>(a.codes + key * kDim + 16 * lane8) = make_uint4(out[0], out[1], out[2], out[3]);
+  if (lane8 == 0) a.scales[key] = scale;
 }
 
 }  // namespace qsa

@@ -66,6 +66,18 @@ bool set_attn_smem() {
          set_attn_smem_one<2, 256>() && set_attn_smem_one<4, 256>() && set_attn_smem_one<8, 256>();
 }
 
+template <bool kFp8>
+bool set_mma_smem() {
+  return cudaFuncSetAttribute(score_mma_kernel<1, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sm_smem_bytes(kSmMaxReq, 1)) == cudaSuccess &&
+         cudaFuncSetAttribute(score_mma_kernel<2, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sm_smem_bytes(kSmMaxReq, 2)) == cudaSuccess &&
+         cudaFuncSetAttribute(score_mma_kernel<3, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sm_smem_bytes(kSmMaxReq, 3)) == cudaSuccess &&
+         cudaFuncSetAttribute(score_mma_kernel<4, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sm_smem_bytes(kSmMaxReq, 4)) == cudaSuccess;
+}
+
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
@@ -127,15 +139,7 @@ qsa_status device_info(DeviceInfo** out) {
         cudaFuncSetAttribute(select_fast_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SfShared)) != cudaSuccess)
       return QSA_ERR_CUDA;
-    if (cudaFuncSetAttribute(score_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm_smem_bytes(kSmMaxReq, 1)) != cudaSuccess ||
-        cudaFuncSetAttribute(score_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm_smem_bytes(kSmMaxReq, 2)) != cudaSuccess ||
-        cudaFuncSetAttribute(score_mma_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm_smem_bytes(kSmMaxReq, 3)) != cudaSuccess ||
-        cudaFuncSetAttribute(score_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm_smem_bytes(kSmMaxReq, 4)) != cudaSuccess)
-      return QSA_ERR_CUDA;
+    if (!set_mma_smem<false>() || !set_mma_smem<true>()) return QSA_ERR_CUDA;
     if (cudaFuncSetAttribute(select_rows_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SrSmem)) != cudaSuccess ||
         cudaFuncSetAttribute(select_rows_kernel<kModeQsa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -658,17 +662,19 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
 // Decode scorer on mma.sync (score_mma_kernel): requests of up to kSmMaxRows
 // rows on pages holding a multiple of 8 compressed keys.  About one wave of
 // CTAs (three per SM), at least one 16-block tile per warp.
-template <int NT>
+template <int NT, bool kFp8>
 qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream) {
   const size_t smem = sm_smem_bytes(s.n_req, NT);
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_mma_kernel<NT>, kSmThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_mma_kernel<NT, kFp8>, kSmThreads, smem) !=
+      cudaSuccess)
     return QSA_ERR_CUDA;
   const int64_t nb_max = s.max_len / kBlock;
   const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + kSmTile - 1) / kSmTile);
   const int64_t ctas =
       std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(occ, 1) * sm_count, (tiles_max + kSmWarps - 1) / kSmWarps));
-  if (launch_pdl(score_mma_kernel<NT>, dim3((unsigned)ctas), dim3(kSmThreads), smem, stream, s) != cudaSuccess) {
+  if (launch_pdl(score_mma_kernel<NT, kFp8>, dim3((unsigned)ctas), dim3(kSmThreads), smem, stream, s) !=
+      cudaSuccess) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
   }
@@ -683,11 +689,12 @@ qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_co
       s.pool_rows > INT32_MAX || (int64_t)s.n_req * ((nb_max + kSmTile - 1) / kSmTile) > INT32_MAX)
     return QSA_ERR_UNSUPPORTED;
   qsa_status st;
+  const bool fp8 = s.pool8 != nullptr;
   switch ((max_rows_per_req + 1) / 2) {
-    case 1: st = launch_scores_mma_nt<1>(s, sm_count, stream); break;
-    case 2: st = launch_scores_mma_nt<2>(s, sm_count, stream); break;
-    case 3: st = launch_scores_mma_nt<3>(s, sm_count, stream); break;
-    default: st = launch_scores_mma_nt<4>(s, sm_count, stream); break;
+    case 1: st = fp8 ? launch_scores_mma_nt<1, true>(s, sm_count, stream) : launch_scores_mma_nt<1, false>(s, sm_count, stream); break;
+    case 2: st = fp8 ? launch_scores_mma_nt<2, true>(s, sm_count, stream) : launch_scores_mma_nt<2, false>(s, sm_count, stream); break;
+    case 3: st = fp8 ? launch_scores_mma_nt<3, true>(s, sm_count, stream) : launch_scores_mma_nt<3, false>(s, sm_count, stream); break;
+    default: st = fp8 ? launch_scores_mma_nt<4, true>(s, sm_count, stream) : launch_scores_mma_nt<4, false>(s, sm_count, stream); break;
   }
   if (st == QSA_OK && s.n_fill > 0) {
     fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
@@ -705,7 +712,7 @@ qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream);
 qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream);
 qsa_status launch_scorer(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
   const qsa_status m = launch_scores_mma(s, max_rows_per_req, sm_count, stream);
-  if (m != QSA_ERR_UNSUPPORTED) return m;
+  if (m != QSA_ERR_UNSUPPORTED || s.pool8 != nullptr) return m;  // FP8 keys: the mma.sync scorer only
   return max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, sm_count, stream)
                                         : launch_scores(s, sm_count, stream);
 }
@@ -1168,13 +1175,15 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
                                int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
                                int32_t* out_pos, int32_t* out_slots, float* scores_out,
                                int64_t ld_scores, void* workspace, size_t workspace_bytes,
-                               void* stream, const int32_t* new_pos) {
+                               void* stream, const int32_t* new_pos, const uint8_t* pool8 = nullptr,
+                               const float* key_scales = nullptr) {
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
   if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
-  if (!q || !pool || !out_slots || pool_rows < 0) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(pool)) return QSA_ERR_INVALID_ARG;
+  if (!q || !(pool || pool8) || !out_slots || pool_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || (pool && !aligned16(pool)) || (pool8 && (!aligned16(pool8) || !key_scales)))
+    return QSA_ERR_INVALID_ARG;
   const int32_t nb_max = max_len / kBlock;
   float* scores = scores_out;
   int64_t ld = ld_scores;
@@ -1200,7 +1209,7 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1, new_pos};
+              page_size, scores, ld, 0, 1, new_pos, pool8, key_scales};
   if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
     return e;
 
@@ -1328,3 +1337,66 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
                              max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos,
                              out_slots, scores, ld, nullptr, 0, stream, nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// Prologue tails: query RoPE, FP8 index keys and the indexer on them.
+// ---------------------------------------------------------------------------
+extern "C" {
+
+qsa_status qsa_rope_queries(const void* q, const int32_t* pos, int32_t n_rows, double rope_base, void* q_out,
+                            void* stream) {
+  if (n_rows < 0) return QSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return QSA_OK;
+  if (!q || !pos || !q_out || !aligned16(q) || !aligned16(q_out) || !(rope_base > 0.0) || !std::isfinite(rope_base))
+    return QSA_ERR_INVALID_ARG;
+  RopeQArgs a{static_cast<const __nv_bfloat16*>(q), pos, n_rows, static_cast<__nv_bfloat16*>(q_out)};
+  const int64_t units = (int64_t)n_rows * kHeads;
+  const int64_t per_cta = kRopeQThreads / kCompressLanes;
+  rope_queries_kernel<<<(unsigned)((units + per_cta - 1) / per_cta), kRopeQThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(a, rope_turns(rope_base));
+  return launch_status();
+}
+
+qsa_status qsa_quantize_keys_fp8(const void* keys, int64_t n_keys, uint8_t* codes, float* scales, void* stream) {
+  if (n_keys < 0) return QSA_ERR_INVALID_ARG;
+  if (n_keys == 0) return QSA_OK;
+  if (!keys || !codes || !scales || !aligned16(keys) || !aligned16(codes) || !aligned4(scales))
+    return QSA_ERR_INVALID_ARG;
+  const int64_t per_cta = kQuantThreads / kCompressLanes;
+  if ((n_keys + per_cta - 1) / per_cta > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  QuantArgs a{static_cast<const __nv_bfloat16*>(keys), n_keys, codes, scales};
+  quantize_keys_fp8_kernel<<<(unsigned)((n_keys + per_cta - 1) / per_cta), kQuantThreads, 0,
+                             static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
+qsa_status qsa_index_scores_fp8(const void* q, const uint8_t* codes, const float* scales, int64_t pool_rows,
+                                int32_t n_req, const int32_t* req_row_start, int32_t n_rows, const int32_t* row_len,
+                                int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table, int64_t ld_pt,
+                                int32_t page_size, float* scores, int64_t ld_scores, int64_t n_fill, void* stream) {
+  if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
+  if (n_rows == 0) return QSA_OK;
+  if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
+  if (!q || !codes || !scales || !scores || pool_rows < 0 || n_fill < 0) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(codes) || !aligned4(scales) || !aligned4(scores)) return QSA_ERR_INVALID_ARG;
+  if (ld_scores < std::max<int64_t>(max_len / kBlock, n_fill)) return QSA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (qsa_status st = device_info(&d)) return st;
+  ScoreArgs s{static_cast<const __nv_bfloat16*>(q), nullptr, pool_rows, n_req, req_row_start, n_rows, row_len,
+              max_len, page_table, ld_pt, page_size, scores, ld_scores, n_fill, 0, nullptr, codes, scales};
+  return launch_scorer(s, max_rows_per_req, d->sm_count, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_indexer_select_fp8(const void* q, const uint8_t* codes, const float* scales, int64_t pool_rows,
+                                  int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                  const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                  const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                  int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                  int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!codes || !scales) return QSA_ERR_INVALID_ARG;
+  return indexer_select_impl(q, nullptr, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
+                             max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos, out_slots,
+                             scores_out, ld_scores, workspace, workspace_bytes, stream, nullptr, codes, scales);
+}
+
+}  // extern "C"

@@ -48,6 +48,10 @@ struct ScoreArgs {
   int64_t n_fill;
   int32_t trigger_dependents;   // let a dependent grid launch early (PDL)
   const int32_t* new_pos;       // see TcArgs::new_pos (TMA scorers only; others wait in full)
+  // FP8 keys (mma.sync scorer only): nullptr, or the e4m3 codes [pool_rows][128]
+  // and one FP32 scale per pool row; `pool` is then unused
+  const uint8_t* pool8;
+  const float* key_scales;
 };
 
 constexpr int kScoreThreads = 256;

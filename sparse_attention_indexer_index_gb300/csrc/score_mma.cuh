@@ -35,7 +35,18 @@
 //    4 KB bulk prefetch into L2 a few tiles ahead made the 32-request batch
 //    slower, 35.5 against 31.5 us.)
 //  - Page-table entries of the next 32 tiles are fetched one tile per lane.
+//
+// FP8 keys (kFp8): the pool holds e4m3 codes (128 bytes per key) and one
+// FP32 scale per key.  Lane (g, t) loads the 16-byte chunks 4c + t (c < 2)
+// of rows g and g + 8 (16 dims each); the codes become FP16 in registers
+// (exact) and the MMA runs on FP16 with the query held in FP16: step (c, j)
+// pairs logical columns {2t, 2t+1} / {2t+8, 2t+9} with dims
+// 16(4c+t) + 4j + {0,1} / {2,3}.  The accumulator times the key's scale is
+// the dot product with the dequantised key.
 #pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "score_decode.cuh"
@@ -59,13 +70,36 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low byte first) -> two FP16 values packed low first.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// A tile's key fragments of one lane: BF16 keys use a[0..3] / b[0..3]
+// (chunks of rows g / g + 8), FP8 keys a[0..1] / b[0..1] and the two rows'
+// scales.
+struct SmFrag {
+  uint4 a[4], b[4];
+  float sa, sb;
+};
+
 // Dynamic shared memory of one CTA: the tile prefix, then per warp a slot of
 // NT x 4 x 32 B fragments (16 bytes each).
 __host__ __device__ constexpr size_t sm_smem_bytes(int n_req, int nt) {
   return (((size_t)(n_req + 1) * 4 + 15) & ~(size_t)15) + (size_t)kSmWarps * nt * 4 * 32 * 16;
 }
 
-template <int NT>
+template <int NT, bool kFp8>
 __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(ScoreArgs a) {
   extern __shared__ __align__(16) unsigned char sm_raw[];
   int* g_pre = reinterpret_cast<int*>(sm_raw);  // [n_req + 1]: tiles before request r
@@ -165,7 +199,7 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   // ---- load side: the tile's request, its longest row, the PDL wait -------
   int r_ld = -1, nb_ld = 0, fn_ld = INT_MAX;
   bool waited = !relaxed;
-  auto load_tile = [&](int i, uint4 (&ka)[4], uint4 (&kb)[4]) {
+  auto load_tile = [&](int i, SmFrag& f) {
     if (i - base >= 32) {  // next batch of pool rows
       base += 32;
       pa_cur = pa_nxt;
@@ -197,19 +231,31 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
       va = va && pra + g < a.pool_rows;
       vb = vb && prb + g < a.pool_rows;
     }
-    const __nv_bfloat16* ra = a.pool + ((int64_t)max(pra, 0) + g) * kDim + 8 * t;
-    const __nv_bfloat16* rb = a.pool + ((int64_t)max(prb, 0) + g) * kDim + 8 * t;
+    if (kFp8) {
+      const uint8_t* ra = a.pool8 + ((int64_t)max(pra, 0) + g) * kDim + 16 * t;
+      const uint8_t* rb = a.pool8 + ((int64_t)max(prb, 0) + g) * kDim + 16 * t;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      ka[c] = va ? ld_stream_16(ra + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
-      kb[c] = vb ? ld_stream_16(rb + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < 2; ++c) {
+        f.a[c] = va ? ld_stream_16(ra + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
+        f.b[c] = vb ? ld_stream_16(rb + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      f.sa = va ? __ldg(a.key_scales + max(pra, 0) + g) : 0.f;
+      f.sb = vb ? __ldg(a.key_scales + max(prb, 0) + g) : 0.f;
+    } else {
+      const __nv_bfloat16* ra = a.pool + ((int64_t)max(pra, 0) + g) * kDim + 8 * t;
+      const __nv_bfloat16* rb = a.pool + ((int64_t)max(prb, 0) + g) * kDim + 8 * t;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        f.a[c] = va ? ld_stream_16(ra + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
+        f.b[c] = vb ? ld_stream_16(rb + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   };
 
   // ---- compute side: query fragments of the tile's request, row lengths ---
   int r = -1, t0 = 0, nrows = 0;
   int nbr[NT];
-  auto compute_tile = [&](int i, const uint4 (&ka)[4], const uint4 (&kb)[4]) {
+  auto compute_tile = [&](int i, const SmFrag& f) {
     if (r < 0 || i >= g_pre[r + 1]) {
       if (r < 0) r = request_of(i);
       while (i >= g_pre[r + 1]) ++r;
@@ -232,9 +278,22 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
         const int rl = 2 * nt + (g >> 2), head = g & 3;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          // BF16: chunk 4c + t of the head (8 dims); FP8 path: dims
+          // 16(4(c/2) + t) + 8(c%2) .. +7 as FP16
+          const int d0 = kFp8 ? 16 * (4 * (c >> 1) + t) + 8 * (c & 1) : 8 * (4 * c + t);
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (rl < nrows)
-            v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(t0 + rl) * kHeads + head) * kDim + 8 * (4 * c + t)));
+            v = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)(t0 + rl) * kHeads + head) * kDim + d0));
+          if (kFp8) {  // BF16 -> FP16, nearest (exact for |q| in [2^-14, 65504) and BF16's 8 bits)
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 p = bf16x2_to_float2(w[e]);
+              const __half2 h = __floats2half2_rn(p.x, p.y);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          }
           bslot[(nt * 4 + c) * 32 + lane] = v;
         }
       }
@@ -244,13 +303,39 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    if (kFp8) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t wa[4] = {f.a[c].x, f.a[c].y, f.a[c].z, f.a[c].w};
+        const uint32_t wb[4] = {f.b[c].x, f.b[c].y, f.b[c].z, f.b[c].w};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 bq = bslot[(nt * 4 + c) * 32 + lane];
-        mma_bf16_16816(acc[nt], ka[c].x, kb[c].x, ka[c].y, kb[c].y, bq.x, bq.y);
-        mma_bf16_16816(acc[nt], ka[c].z, kb[c].z, ka[c].w, kb[c].w, bq.z, bq.w);
+        for (int j = 0; j < 4; ++j) {  // dims 16(4c+t) + 4j + {0,1} / {2,3}
+          const uint32_t a0 = e4m3x2_to_f16x2(wa[j]), a2 = e4m3x2_to_f16x2(wa[j] >> 16);
+          const uint32_t a1 = e4m3x2_to_f16x2(wb[j]), a3 = e4m3x2_to_f16x2(wb[j] >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint4 bq = bslot[(nt * 4 + 2 * c + (j >> 1)) * 32 + lane];
+            if (j & 1) mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.z, bq.w);
+            else mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.x, bq.y);
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {  // dequantise: row g by its scale, row g + 8 by its own
+        acc[nt][0] *= f.sa;
+        acc[nt][1] *= f.sa;
+        acc[nt][2] *= f.sb;
+        acc[nt][3] *= f.sb;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 bq = bslot[(nt * 4 + c) * 32 + lane];
+          mma_bf16_16816(acc[nt], f.a[c].x, f.b[c].x, f.a[c].y, f.b[c].y, bq.x, bq.y);
+          mma_bf16_16816(acc[nt], f.a[c].z, f.b[c].z, f.a[c].w, f.b[c].w, bq.z, bq.w);
+        }
       }
     }
     // epilogue: ReLU, head sum (lanes t and t^1 hold the two head pairs)
@@ -272,21 +357,17 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
 
   // ---- the warp's tiles: the next tile's fragments load while this one is
   // computed (kSmDepth 2), or one tile at a time (1) --------------------------
-  uint4 ka[4], kb[4];
-  load_tile(i0, ka, kb);
+  SmFrag cur;
+  load_tile(i0, cur);
   for (int i = i0; i < i1; ++i) {
     if (kSmDepth == 2) {
-      uint4 na[4], nb4[4];
-      if (i + 1 < i1) load_tile(i + 1, na, nb4);
-      compute_tile(i, ka, kb);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        ka[c] = na[c];
-        kb[c] = nb4[c];
-      }
+      SmFrag nxt;
+      if (i + 1 < i1) load_tile(i + 1, nxt);
+      compute_tile(i, cur);
+      cur = nxt;
     } else {
-      compute_tile(i, ka, kb);
-      if (i + 1 < i1) load_tile(i + 1, ka, kb);
+      compute_tile(i, cur);
+      if (i + 1 < i1) load_tile(i + 1, cur);
     }
   }
   if (anchor && !waited) pdl_wait_primary();

@@ -1,0 +1,217 @@
+"""GPU parity of the prologue tails against the oracle (SGLang GLM-5.2 blog,
+"Indexer Prologue Fusion"): the index-query RoPE, the FP8 key quantiser,
+the FP8-key scorer and the fused selection on FP8 keys.
+
+- RoPE: within one BF16 ulp plus the FP32 rotation's absolute term
+  2^-22 (|u| + |v|) per pair (both sides round once to BF16; the GPU's sine
+  and cosine and its products are FP32); in place equals out of place to the
+  bit; a negative position latches the grouping fault and leaves the row.
+- Quantiser: codes and scales bit-exact (both take the same FP32 divisions
+  and one round-to-nearest-even to e4m3).
+- Scores: within 2e-5 * (1/sqrt(128)) * sum |f16(q) * code * scale| + 1e-6
+  of the oracle's FP64 score on the same codes (the GPU multiplies exact
+  FP16 x e4m3 products and accumulates in FP32).
+- Selection, positions and slots: bit-exact against the oracle on the GPU's
+  scores, at small ragged shapes and at the full 32-request batch
+  (contexts 4,096..131,072).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import SCALE, bf16_dev, bf16_host, key_tolerance, pool_rows_of, to_dev
+from workloads import c3_batched, decode_workload, normal_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import sparse_attention_indexer_index_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _no_device_faults(qsa):
+    yield
+    assert qsa.device_status(clear=True) == 0, "a device-side bounds check fired"
+
+
+def _deq(codes, scales):
+    table = np.array([oracle.e4m3_to_float(c) for c in range(256)])
+    return table[codes] * scales[:, None].astype(np.float64)
+
+
+def fp8_score_tolerance(q_bits, codes, scales, req_row_start, row_len, page_table, page_size, ld):
+    qa = np.abs(oracle.bf16_to_float(q_bits)).astype(np.float64).sum(axis=1)  # [n_rows][128]
+    tol = np.full((row_len.size, ld), np.inf)
+    for r in range(req_row_start.size - 1):
+        rows = np.arange(req_row_start[r], req_row_start[r + 1])
+        if rows.size == 0:
+            continue
+        nb = int(row_len[rows].max()) // 4
+        prow = pool_rows_of(page_table[r], nb, page_size)
+        ka = np.abs(_deq(codes[prow], scales[prow]))
+        tol[rows, :nb] = 2e-5 * SCALE * (qa[rows] @ ka.T) + 1e-6
+    return tol
+
+
+# ----------------------------------------------------------------- query RoPE
+def test_rope_queries_parity(qsa):
+    """37 rows (148 (row, head) units: 5 CTAs, the last ragged) at positions
+    from 0 to 2^20, against the oracle's FP64 rotation."""
+    rng = np.random.default_rng(81)
+    n = 37
+    q = normal_bf16(rng, (n, 4, 128))
+    q[3] *= 0  # a zero row stays zero
+    pos = rng.integers(0, 1 << 20, size=n).astype(np.int32)
+    pos[:5] = [0, 1, 79_999, 131_071, (1 << 20) - 1]
+    got = bf16_host(qsa.rope_queries(bf16_dev(q), to_dev(pos)))
+    want = oracle.rope_queries(q, pos)
+    a, b = oracle.bf16_to_float(got).astype(np.float64), oracle.bf16_to_float(want).astype(np.float64)
+    u = np.abs(oracle.bf16_to_float(q)).astype(np.float64)
+    pair = u[..., :64] + u[..., 64:]
+    tol = key_tolerance(a, b) - 2.0 ** -22 + 2.0 ** -22 * np.concatenate([pair, pair], axis=-1)
+    assert (np.abs(a - b) <= tol).all(), float(np.abs(a - b).max())
+    assert np.array_equal(got[0], q[0])          # position 0: identity, to the bit
+    assert (a[3] == 0).all()                     # (either sign of zero)
+
+
+def test_rope_queries_in_place_and_negative_position(qsa):
+    import torch
+    rng = np.random.default_rng(82)
+    q = normal_bf16(rng, (9, 4, 128))
+    pos = rng.integers(0, 200_000, size=9).astype(np.int32)
+    ref = bf16_host(qsa.rope_queries(bf16_dev(q), to_dev(pos)))
+    g = bf16_dev(q)
+    qsa.rope_queries(g, to_dev(pos), out=g)
+    assert np.array_equal(bf16_host(g), ref)
+    # a negative position: the fault bit, that row untouched, the others rotated
+    pos_bad = pos.copy()
+    pos_bad[4] = -1
+    out = torch.zeros((9, 4, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.rope_queries(bf16_dev(q), to_dev(pos_bad), out=out)
+    assert qsa.device_status(clear=True) != 0
+    got = bf16_host(out)
+    assert (got[4] == 0).all()
+    keep = np.arange(9) != 4
+    assert np.array_equal(got[keep], ref[keep])
+
+
+# ----------------------------------------------------------------- quantiser
+@pytest.mark.parametrize("n", [1, 31, 1003])
+def test_quantize_keys_fp8_bit_exact(qsa, n):
+    rng = np.random.default_rng(83 + n)
+    keys = normal_bf16(rng, (n, 128))
+    if n > 8:
+        keys[1] = 0                                                    # zero key: scale 0
+        keys[2] = oracle.bf16_round_array(rng.standard_normal(128) * 1e-38)  # subnormal scale
+        keys[3] = oracle.bf16_round_array(rng.standard_normal(128) * 1e30)
+        keys[4] = oracle.bf16_round_array(np.full(128, -0.5))             # every element at the max
+    codes, scales = qsa.quantize_keys_fp8(bf16_dev(keys))
+    ref_c, ref_s = oracle.quantize_keys_fp8(keys)
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+# ----------------------------------------------------------------- scores
+def _fp8_case(qsa, seed, rows_per_req, page_size):
+    w = decode_workload(seed, rows_per_req, page_size=page_size, with_keys=False)
+    rng = np.random.default_rng(seed + 1)
+    pool = normal_bf16(rng, (w.pool_rows, 128))
+    codes, scales = qsa.quantize_keys_fp8(bf16_dev(pool))
+    return w, codes, scales
+
+
+@pytest.mark.parametrize("page_size", [32, 64])
+def test_index_scores_fp8_parity(qsa, page_size):
+    """Requests of 1..8 rows, contexts with ragged tails (several 16-block
+    tiles plus a partial one), n_fill past the longest row."""
+    import torch
+    rows = [[1000], [37, 40, 41], [4096 + 4 * i for i in range(8)], [9001, 9002], [12], [2051] * 5]
+    w, codes, scales = _fp8_case(qsa, 84, rows, page_size)
+    ld = (w.max_len // 4 + 3) // 4 * 4 + 8
+    s = qsa.index_scores_fp8(bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len),
+                             to_dev(w.page_table), page_size, w.max_len, w.max_rows_per_req,
+                             scores=torch.full((w.n_rows, ld), float("nan"), device="cuda"),
+                             n_fill=ld - 3).cpu().numpy()
+    c, sc = codes.cpu().numpy(), scales.cpu().numpy()
+    want = oracle.index_scores_fp8(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, page_size, ld)
+    tol = fp8_score_tolerance(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        err = np.abs(s[t, :nb].astype(np.float64) - want[t, :nb])
+        assert (err <= tol[t, :nb]).all(), (t, float(err.max()))
+        assert (s[t, nb:ld - 3] == -np.inf).all()
+        assert np.isnan(s[t, ld - 3:]).all()
+
+
+def test_index_scores_fp8_rejects_unsupported_shapes(qsa):
+    w, codes, scales = _fp8_case(qsa, 85, [[256]], 64)
+    args = (bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table))
+    with pytest.raises(qsa.QSAError):
+        qsa.index_scores_fp8(*args, 16, w.max_len)            # 4 keys per page
+    w9, c9, s9 = _fp8_case(qsa, 86, [[256] * 9], 64)
+    with pytest.raises(qsa.QSAError):                          # 9 rows in one request
+        qsa.index_scores_fp8(bf16_dev(w9.q), c9, s9, to_dev(w9.req_row_start), to_dev(w9.row_len),
+                             to_dev(w9.page_table), 64, w9.max_len)
+
+
+# ----------------------------------------------------------------- fused selection
+def _check_selection(out, s, w, k_blk):
+    sel_ref, _ = oracle.topk(s, k_blk, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+def test_indexer_select_fp8_small(qsa):
+    import torch
+    rows = [[3000 + i for i in range(6)], [513], [2047, 2048, 2049], [40_003]]
+    w, codes, scales = _fp8_case(qsa, 87, rows, 64)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.indexer_select_fp8(bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len),
+                                 to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, k_blk=512,
+                                 want_blocks=True, want_pos=True, scores_out=scores)
+    s = scores.cpu().numpy()
+    c, sc = codes.cpu().numpy(), scales.cpu().numpy()
+    want = oracle.index_scores_fp8(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    tol = fp8_score_tolerance(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        assert (np.abs(s[t, :nb].astype(np.float64) - want[t, :nb]) <= tol[t, :nb]).all(), t
+    _check_selection(out, s, w, 512)
+    # without scores_out (the workspace holds them): the same selection
+    out2 = qsa.indexer_select_fp8(bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len),
+                                  to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, k_blk=512,
+                                  want_blocks=True, want_pos=True)
+    assert np.array_equal(out2["slots"].cpu().numpy(), out["slots"].cpu().numpy())
+
+
+def test_indexer_select_fp8_full_batch(qsa):
+    """The 32-request batch (one row each, contexts 4,096..131,072 tokens):
+    scores against the oracle on the GPU's codes, selection bit-exact."""
+    import torch
+    w = c3_batched(0, with_keys=False)
+    rng = np.random.default_rng(88)
+    pool = normal_bf16(rng, (w.pool_rows, 128))
+    codes, scales = qsa.quantize_keys_fp8(bf16_dev(pool))
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.indexer_select_fp8(bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len),
+                                 to_dev(w.page_table), w.page_size, w.max_len, 1, k_blk=512,
+                                 want_blocks=True, want_pos=True, scores_out=scores)
+    s = scores.cpu().numpy()
+    c, sc = codes.cpu().numpy(), scales.cpu().numpy()
+    ref_c, ref_s = oracle.quantize_keys_fp8(pool)
+    assert np.array_equal(c, ref_c) and np.array_equal(sc.view(np.uint32), ref_s.view(np.uint32))
+    want = oracle.index_scores_fp8(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    tol = fp8_score_tolerance(w.q, c, sc, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        assert (np.abs(s[t, :nb].astype(np.float64) - want[t, :nb]) <= tol[t, :nb]).all(), t
+    _check_selection(out, s, w, 512)

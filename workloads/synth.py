@@ -144,11 +144,13 @@ def c2_batched(seed: int = 0, n_req: int = 32, L: int = 80_000, n_rows: int = 6)
                            name=f"verify_L{L}_{n_rows}rows_x{n_req}")
 
 
-def c3_batched(seed: int = 0, n_req: int = 32, lo: int = 4096, hi: int = 131_072) -> DecodeWorkload:
+def c3_batched(seed: int = 0, n_req: int = 32, lo: int = 4096, hi: int = 131_072,
+               with_keys: bool = True) -> DecodeWorkload:
     """Batched decode: n_req requests, one row each, L uniform in [lo, hi]."""
     rng = np.random.default_rng(seed + 1_000_003)
     lens = rng.integers(lo, hi, size=n_req, endpoint=True)
-    return decode_workload(seed, [[int(L)] for L in lens], name=f"decode_batched_{n_req}req")
+    return decode_workload(seed, [[int(L)] for L in lens], name=f"decode_batched_{n_req}req",
+                           with_keys=with_keys)
 
 
 def indexshare_mtp(seed: int = 0, n_req: int = 32, lo: int = 4096, hi: int = 131_072, n_draft: int = 3,
