@@ -58,7 +58,6 @@ constexpr int kSmThreads = 32 * kSmWarps;
 constexpr int kSmTile = 16;        // keys per tile (MMA M)
 constexpr int kSmMaxRows = 8;      // rows per request: 4 n-tiles of 2 rows x 4 heads
 constexpr int kSmMaxReq = 4096;    // requests per launch (tile prefix in shared memory)
-constexpr int kSmDepth = 2;        // tiles of fragments in flight per warp (measured: 2 at 2 CTAs/SM beats 1 at 3)
 constexpr int kSmMinCtas = 2;      // CTAs per SM the register budget is sized for
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -356,19 +355,15 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   };
 
   // ---- the warp's tiles: the next tile's fragments load while this one is
-  // computed (kSmDepth 2), or one tile at a time (1) --------------------------
+  // computed (2 tiles in flight per warp; measured: 2 at 2 CTAs per SM beats
+  // 1 at 3, and 3 FP8 tiles in flight gained nothing) ------------------------
   SmFrag cur;
   load_tile(i0, cur);
   for (int i = i0; i < i1; ++i) {
-    if (kSmDepth == 2) {
-      SmFrag nxt;
-      if (i + 1 < i1) load_tile(i + 1, nxt);
-      compute_tile(i, cur);
-      cur = nxt;
-    } else {
-      compute_tile(i, cur);
-      if (i + 1 < i1) load_tile(i + 1, cur);
-    }
+    SmFrag nxt;
+    if (i + 1 < i1) load_tile(i + 1, nxt);
+    compute_tile(i, cur);
+    cur = nxt;
   }
   if (anchor && !waited) pdl_wait_primary();
 }

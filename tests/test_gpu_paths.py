@@ -12,6 +12,10 @@ headline decode step checked against the oracle end to end.
   through the 4-slot ring; the new pool rows against the oracle's key path,
   the scores against the oracle on the same keys, the selection, positions
   and slots bit-exact.
+- Mixed row lengths in one call (the device row plan).
+- More than two rows per SM with k <= 512 (small CTAs, four per SM): hard
+  rows, rows whose evenly spaced 16-byte groups hold the largest values,
+  special values, ragged lengths, token and QSA modes.
 """
 import numpy as np
 import pytest
@@ -198,6 +202,79 @@ def test_indexer_mixed_contexts_take_the_row_plan(qsa):
                              to_dev(w.page_table), w.page_size, w.max_len, w.max_rows_per_req, k_blk=512,
                              want_blocks=True, want_pos=True, scores_out=scores, workspace=ws)
     s = scores.cpu().numpy()
+    sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+# ----------------------------------------------------------------- many rows, k <= 512
+def _group_sample_positions(n):
+    """256 evenly spaced groups of 4 entries: groups floor(j * (n // 4) / 256)
+    (a sampled bound read there would sit far above the k-th entry)."""
+    g = (np.arange(256, dtype=np.int64) * (n // 4)) // 256
+    return (4 * g[:, None] + np.arange(4)).ravel()
+
+
+@pytest.mark.parametrize("n", [1000, 1537, 3001, 20_000, 32_768])
+def test_topk_many_rows_k_up_to_512(qsa, n):
+    """More than two rows per SM with k <= 512 (small CTAs).  Ordinary rows,
+    rows of one value, three values, one top-bits bin, rows whose evenly
+    spaced groups hold the largest values, rows with NaN, +-inf and -0,
+    ragged lengths (n not a multiple of 4, fewer entries than k); token mode
+    with slots."""
+    rng = np.random.default_rng(n + 11)
+    rows = []
+    for r in range(336):
+        kind = r % 6
+        if kind == 0:
+            x = np.full(n, 1.5, np.float32)
+        elif kind == 1:
+            x = rng.integers(0, 3, size=n).astype(np.float32)
+        elif kind == 2:
+            x = (rng.integers(0, 64, size=n) / 64.0 + 1.0).astype(np.float32)
+        elif kind == 3:
+            x = (rng.standard_normal(n) * 0.01).astype(np.float32)
+            x[_group_sample_positions(n)] = 100.0 + rng.standard_normal(1024).astype(np.float32)
+        elif kind == 4:
+            x = rng.standard_normal(n).astype(np.float32)
+            x[rng.choice(n, 40, replace=False)] = np.nan
+            x[rng.choice(n, 3, replace=False)] = np.inf
+            x[rng.choice(n, 3, replace=False)] = -np.inf
+            x[rng.choice(n, 50, replace=False)] = -0.0
+            x[rng.choice(n, 50, replace=False)] = 0.0
+        else:
+            x = rng.standard_normal(n).astype(np.float32)
+        rows.append(x)
+    s = np.stack(rows)
+    nv = np.full(s.shape[0], n, np.int32)
+    nv[5] = 100                # fewer entries than k
+    nv[11] = n - 3             # ragged tail
+    nv[17] = n - 1
+    nv[23] = 0
+    P = 64
+    pt = np.stack([rng.permutation((n + P - 1) // P) for _ in range(s.shape[0])]).astype(np.int32)
+    for k in [1, 100, 512]:
+        idx, slots = qsa.topk_select(to_dev(s), k, n_valid=to_dev(nv), n_max=n, page_table=to_dev(pt),
+                                     page_size=P)
+        ref, ref_slots = oracle.topk(s, k, n_valid=nv, page_table=pt, page_size=P)
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+        assert np.array_equal(slots.cpu().numpy(), ref_slots), k
+
+
+def test_select_blocks_many_qsa_rows(qsa):
+    """400 one-row requests, contexts 1..131,072 tokens (every pending count,
+    rows with fewer blocks than k), top-512 blocks expanded to positions and
+    slots through the requests' page tables: bit-exact."""
+    rng = np.random.default_rng(91)
+    lens = rng.integers(1, 131_073, size=400)
+    lens[:8] = [1, 3, 4, 2047, 2048, 2051, 6147, 131_072]
+    w = decode_workload(92, [[int(L)] for L in lens], page_size=64, k_blk=512, with_keys=False)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    s = rng.standard_normal((w.n_rows, ld)).astype(np.float32)
+    out = qsa.select_blocks(to_dev(s), to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table),
+                            w.page_size, w.max_len, k_blk=512, want_blocks=True, want_pos=True)
     sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
     pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
