@@ -661,7 +661,7 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
 
 // Decode scorer on mma.sync (score_mma_kernel): requests of up to kSmMaxRows
 // rows on pages holding a multiple of 8 compressed keys.  About one wave of
-// CTAs (three per SM), at least one 16-block tile per warp.
+// CTAs (two per SM), at least one tile (16 BF16 or 32 FP8 keys) per warp.
 template <int NT, bool kFp8>
 qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream) {
   const size_t smem = sm_smem_bytes(s.n_req, NT);
@@ -670,7 +670,7 @@ qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t s
       cudaSuccess)
     return QSA_ERR_CUDA;
   const int64_t nb_max = s.max_len / kBlock;
-  const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + kSmTile - 1) / kSmTile);
+  const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + sm_tile<NT, kFp8>() - 1) / sm_tile<NT, kFp8>());
   const int64_t ctas =
       std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(occ, 1) * sm_count, (tiles_max + kSmWarps - 1) / kSmWarps));
   if (launch_pdl(score_mma_kernel<NT, kFp8>, dim3((unsigned)ctas), dim3(kSmThreads), smem, stream, s) !=

@@ -42,7 +42,10 @@
 // (exact) and the MMA runs on FP16 with the query held in FP16: step (c, j)
 // pairs logical columns {2t, 2t+1} / {2t+8, 2t+9} with dims
 // 16(4c+t) + 4j + {0,1} / {2,3}.  The accumulator times the key's scale is
-// the dot product with the dequantised key.
+// the dot product with the dequantised key.  For one-row requests a tile
+// holds 32 FP8 keys (rows g, g + 8, g + 16, g + 24: 4 KB, as a BF16 tile),
+// so the per-tile work (page rows, request lookup, epilogue set-up) is spread
+// over as many bytes as with BF16 keys.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -55,7 +58,11 @@ namespace qsa {
 
 constexpr int kSmWarps = 8;
 constexpr int kSmThreads = 32 * kSmWarps;
-constexpr int kSmTile = 16;        // keys per tile (MMA M)
+constexpr int kSmTile = 16;        // keys per tile (MMA M); FP8 tiles of one-row requests hold 32 (two MMA M)
+// Keys per tile: 4 KB of BF16 keys; FP8 keys of one-row requests take 32
+// (4 KB of codes; with more rows the second accumulator set would spill).
+template <int NT, bool kFp8>
+__host__ __device__ constexpr int sm_tile() { return kFp8 && NT == 1 ? 32 : 16; }
 constexpr int kSmMaxRows = 8;      // rows per request: 4 n-tiles of 2 rows x 4 heads
 constexpr int kSmMaxReq = 4096;    // requests per launch (tile prefix in shared memory)
 constexpr int kSmMinCtas = 2;      // CTAs per SM the register budget is sized for
@@ -89,7 +96,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 // scales.
 struct SmFrag {
   uint4 a[4], b[4];
-  float sa, sb;
+  float sa, sb, sc, sd;
 };
 
 // Dynamic shared memory of one CTA: the tile prefix, then per warp a slot of
@@ -107,6 +114,8 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   uint4* bslot = bslot_all + (size_t)warp * NT * 4 * 32;  // [nt][c][lane]
+  constexpr int kTile = sm_tile<NT, kFp8>();
+  constexpr int kRuns = kTile / 8;        // 8-key runs of pool rows per tile
 
   // Without new_pos nothing is read before the previous grid completes.
   // With it (the key path of the same step runs before): the metadata, the
@@ -122,7 +131,7 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     const int r_lo = min(a.n_req, (int)threadIdx.x * per), r_hi = min(a.n_req, r_lo + per);
     int local = 0;
     for (int r = r_lo; r < r_hi; ++r) {
-      local += (request_blocks(a, r) + kSmTile - 1) / kSmTile;
+      local += (request_blocks(a, r) + kTile - 1) / kTile;
       g_pre[r + 1] = local;
     }
     int incl = local;
@@ -161,9 +170,10 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     }
     return lo;
   };
-  // Pool rows of tile i's keys 0-7 and 8-15 (one run when a page holds a
-  // multiple of 16 keys, two pages of 8 otherwise); -1 if a page is out of
-  // range.
+  // Pool rows of tile i's 8-key runs (a run never straddles a page: pages
+  // hold a multiple of 8 keys); -1 if a page is out of range or the run lies
+  // past the request's blocks (its last tile only: no page-table entry is
+  // read there).
   auto run_row = [&](int r, int b) -> int {
     const int page_idx = b / kpp;
     if (page_idx >= a.ld_pt) {
@@ -178,22 +188,28 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     }
     return (int)row;
   };
-  auto tile_rows = [&](int i, int& ra, int& rb) {
-    ra = rb = -1;
+  auto tile_rows = [&](int i, int (&rr)[kRuns]) {
+#pragma unroll
+    for (int q = 0; q < kRuns; ++q) rr[q] = -1;
     if (i >= i1) return;
     const int r = request_of(i);
-    const int b = (i - g_pre[r]) * kSmTile;
-    ra = run_row(r, b);
-    rb = kpp % kSmTile == 0 ? (ra >= 0 ? ra + 8 : -1) : run_row(r, b + 8);
+    const int b = (i - g_pre[r]) * kTile;
+    const int nbv = i == g_pre[r + 1] - 1 ? request_blocks(a, r) : INT_MAX;
+#pragma unroll
+    for (int q = 0; q < kRuns; ++q) {
+      const int bq = b + 8 * q;
+      if (bq >= nbv) break;
+      rr[q] = (q > 0 && bq % kpp != 0) ? (rr[q - 1] >= 0 ? rr[q - 1] + 8 : -1) : run_row(r, bq);
+    }
   };
   int base = i0;
-  int pa_cur, pb_cur, pa_nxt, pb_nxt;
-  tile_rows(i0 + lane, pa_cur, pb_cur);
-  tile_rows(i0 + 32 + lane, pa_nxt, pb_nxt);
-  auto rows_of = [&](int i, int& ra, int& rb) {  // warp-uniform i in [base, base + 64)
+  int pr_cur[kRuns], pr_nxt[kRuns];
+  tile_rows(i0 + lane, pr_cur);
+  tile_rows(i0 + 32 + lane, pr_nxt);
+  auto rows_of = [&](int i, int (&rr)[kRuns]) {  // warp-uniform i in [base, base + 64)
     const int d = i - base;
-    ra = __shfl_sync(0xffffffffu, d < 32 ? pa_cur : pa_nxt, d & 31);
-    rb = __shfl_sync(0xffffffffu, d < 32 ? pb_cur : pb_nxt, d & 31);
+#pragma unroll
+    for (int q = 0; q < kRuns; ++q) rr[q] = __shfl_sync(0xffffffffu, d < 32 ? pr_cur[q] : pr_nxt[q], d & 31);
   };
   // ---- load side: the tile's request, its longest row, the PDL wait -------
   int r_ld = -1, nb_ld = 0, fn_ld = INT_MAX;
@@ -201,9 +217,9 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   auto load_tile = [&](int i, SmFrag& f) {
     if (i - base >= 32) {  // next batch of pool rows
       base += 32;
-      pa_cur = pa_nxt;
-      pb_cur = pb_nxt;
-      tile_rows(base + 32 + lane, pa_nxt, pb_nxt);
+#pragma unroll
+      for (int q = 0; q < kRuns; ++q) pr_cur[q] = pr_nxt[q];
+      tile_rows(base + 32 + lane, pr_nxt);
     }
     if (r_ld < 0 || i >= g_pre[r_ld + 1]) {
       if (r_ld < 0) r_ld = request_of(i);
@@ -216,30 +232,47 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
       fn_ld = relaxed ? max(0, __ldg(a.new_pos + r_ld)) / kBlock : INT_MAX;
     }
     const int j = i - g_pre[r_ld];
-    if (!waited && kSmTile * (j + 1) > fn_ld) {  // this tile may hold keys the key path writes
+    if (!waited && kTile * (j + 1) > fn_ld) {  // this tile may hold keys the key path writes
       pdl_wait_primary();
       waited = true;
     }
-    const int vis = min(kSmTile, nb_ld - j * kSmTile);
-    int pra, prb;
-    rows_of(i, pra, prb);
-    // chunks 4c + t of key rows g and g + 8 (rows past the request's blocks: zero)
-    bool va = pra >= 0 && g < vis, vb = prb >= 0 && g + 8 < vis;
-    if ((va && pra + g >= a.pool_rows) || (vb && prb + g >= a.pool_rows)) {
-      raise_fault(kFaultPool);
-      va = va && pra + g < a.pool_rows;
-      vb = vb && prb + g < a.pool_rows;
-    }
-    if (kFp8) {
-      const uint8_t* ra = a.pool8 + ((int64_t)max(pra, 0) + g) * kDim + 16 * t;
-      const uint8_t* rb = a.pool8 + ((int64_t)max(prb, 0) + g) * kDim + 16 * t;
+    const int vis = min(kTile, nb_ld - j * kTile);
+    int pr[kRuns];
+    rows_of(i, pr);
+    // key row g of each run (rows past the request's blocks: zero)
+    bool v[kRuns];
+    bool bad = false;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        f.a[c] = va ? ld_stream_16(ra + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
-        f.b[c] = vb ? ld_stream_16(rb + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
+    for (int q = 0; q < kRuns; ++q) {
+      v[q] = pr[q] >= 0 && g + 8 * q < vis;
+      if (v[q] && pr[q] + g >= a.pool_rows) {
+        bad = true;
+        v[q] = false;
       }
-      f.sa = va ? __ldg(a.key_scales + max(pra, 0) + g) : 0.f;
-      f.sb = vb ? __ldg(a.key_scales + max(prb, 0) + g) : 0.f;
+    }
+    if (bad) raise_fault(kFaultPool);
+    const int pra = pr[0], prb = pr[1];
+    const bool va = v[0], vb = v[1];
+    if (kFp8) {
+      // runs 0/1 (rows g, g + 8) in a/b[0..1], runs 2/3 (rows g + 16, g + 24)
+      // in a/b[2..3]: chunks 4c + t (c < 2) of each row, 16 dims each
+#pragma unroll
+      for (int h = 0; h < kRuns / 2; ++h) {
+        const int q0 = 2 * h, q1 = 2 * h + 1;
+        const uint8_t* ra = a.pool8 + ((int64_t)max(pr[q0], 0) + g) * kDim + 16 * t;
+        const uint8_t* rb = a.pool8 + ((int64_t)max(pr[q1], 0) + g) * kDim + 16 * t;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          f.a[2 * h + c] = v[q0] ? ld_stream_16(ra + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
+          f.b[2 * h + c] = v[q1] ? ld_stream_16(rb + 64 * c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      f.sa = v[0] ? __ldg(a.key_scales + max(pr[0], 0) + g) : 0.f;
+      f.sb = v[1] ? __ldg(a.key_scales + max(pr[1], 0) + g) : 0.f;
+      if constexpr (kRuns == 4) {
+        f.sc = v[2] ? __ldg(a.key_scales + max(pr[2], 0) + g) : 0.f;
+        f.sd = v[3] ? __ldg(a.key_scales + max(pr[3], 0) + g) : 0.f;
+      }
     } else {
       const __nv_bfloat16* ra = a.pool + ((int64_t)max(pra, 0) + g) * kDim + 8 * t;
       const __nv_bfloat16* rb = a.pool + ((int64_t)max(prb, 0) + g) * kDim + 8 * t;
@@ -299,57 +332,65 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
       __syncwarp();
     }
     const int j = i - g_pre[r];
-    float acc[NT][4];
+    // One MMA M block of 16 keys at a time (FP8 tiles hold two: keys g, g + 8
+    // of fragments a/b[0..1], then g + 16, g + 24 of a/b[2..3]), each
+    // followed by its epilogue: ReLU, head sum (lanes t and t^1 hold the two
+    // head pairs), scale.
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    if (kFp8) {
+    for (int h = 0; h < kRuns / 2; ++h) {
+      float acc[NT][4];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t wa[4] = {f.a[c].x, f.a[c].y, f.a[c].z, f.a[c].w};
-        const uint32_t wb[4] = {f.b[c].x, f.b[c].y, f.b[c].z, f.b[c].w};
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      if (kFp8) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // dims 16(4c+t) + 4j + {0,1} / {2,3}
-          const uint32_t a0 = e4m3x2_to_f16x2(wa[j]), a2 = e4m3x2_to_f16x2(wa[j] >> 16);
-          const uint32_t a1 = e4m3x2_to_f16x2(wb[j]), a3 = e4m3x2_to_f16x2(wb[j] >> 16);
+        for (int c = 0; c < 2; ++c) {
+          const uint4 fa = f.a[2 * h + c], fb = f.b[2 * h + c];
+          const uint32_t wa[4] = {fa.x, fa.y, fa.z, fa.w};
+          const uint32_t wb[4] = {fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {  // dims 16(4c+t) + 4jj + {0,1} / {2,3}
+            const uint32_t a0 = e4m3x2_to_f16x2(wa[jj]), a2 = e4m3x2_to_f16x2(wa[jj] >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(wb[jj]), a3 = e4m3x2_to_f16x2(wb[jj] >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 bq = bslot[(nt * 4 + 2 * c + (jj >> 1)) * 32 + lane];
+              if (jj & 1) mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.z, bq.w);
+              else mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.x, bq.y);
+            }
+          }
+        }
+        const float s_lo = h == 0 ? f.sa : f.sc, s_hi = h == 0 ? f.sb : f.sd;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {  // dequantise: each key row by its own scale
+          acc[nt][0] *= s_lo;
+          acc[nt][1] *= s_lo;
+          acc[nt][2] *= s_hi;
+          acc[nt][3] *= s_hi;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint4 bq = bslot[(nt * 4 + 2 * c + (j >> 1)) * 32 + lane];
-            if (j & 1) mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.z, bq.w);
-            else mma_f16_16816(acc[nt], a0, a1, a2, a3, bq.x, bq.y);
+            const uint4 bq = bslot[(nt * 4 + c) * 32 + lane];
+            mma_bf16_16816(acc[nt], f.a[c].x, f.b[c].x, f.a[c].y, f.b[c].y, bq.x, bq.y);
+            mma_bf16_16816(acc[nt], f.a[c].z, f.b[c].z, f.a[c].w, f.b[c].w, bq.z, bq.w);
           }
         }
       }
+      const int b = j * kTile + 16 * h + g;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {  // dequantise: row g by its scale, row g + 8 by its own
-        acc[nt][0] *= f.sa;
-        acc[nt][1] *= f.sa;
-        acc[nt][2] *= f.sb;
-        acc[nt][3] *= f.sb;
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint4 bq = bslot[(nt * 4 + c) * 32 + lane];
-          mma_bf16_16816(acc[nt], f.a[c].x, f.b[c].x, f.a[c].y, f.b[c].y, bq.x, bq.y);
-          mma_bf16_16816(acc[nt], f.a[c].z, f.b[c].z, f.a[c].w, f.b[c].w, bq.z, bq.w);
+      for (int nt = 0; nt < NT; ++nt) {
+        float v0 = fmaxf(acc[nt][0], 0.f) + fmaxf(acc[nt][1], 0.f);
+        float v1 = fmaxf(acc[nt][2], 0.f) + fmaxf(acc[nt][3], 0.f);
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        const int rl = 2 * nt + (t >> 1);
+        if ((t & 1) == 0 && rl < nrows) {
+          float* dst = a.scores + (int64_t)(t0 + rl) * a.ld_scores + b;
+          if (b < nbr[nt]) dst[0] = v0 * kScoreScale;
+          if (b + 8 < nbr[nt]) dst[8] = v1 * kScoreScale;
         }
-      }
-    }
-    // epilogue: ReLU, head sum (lanes t and t^1 hold the two head pairs)
-    const int b = j * kSmTile + g;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float v0 = fmaxf(acc[nt][0], 0.f) + fmaxf(acc[nt][1], 0.f);
-      float v1 = fmaxf(acc[nt][2], 0.f) + fmaxf(acc[nt][3], 0.f);
-      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-      const int rl = 2 * nt + (t >> 1);
-      if ((t & 1) == 0 && rl < nrows) {
-        float* dst = a.scores + (int64_t)(t0 + rl) * a.ld_scores + b;
-        if (b < nbr[nt]) dst[0] = v0 * kScoreScale;
-        if (b + 8 < nbr[nt]) dst[8] = v1 * kScoreScale;
       }
     }
   };

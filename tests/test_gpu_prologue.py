@@ -125,12 +125,18 @@ def _fp8_case(qsa, seed, rows_per_req, page_size):
     return w, codes, scales
 
 
+@pytest.mark.parametrize("layout", ["mixed_rows", "one_row"])
 @pytest.mark.parametrize("page_size", [32, 64])
-def test_index_scores_fp8_parity(qsa, page_size):
-    """Requests of 1..8 rows, contexts with ragged tails (several 16-block
-    tiles plus a partial one), n_fill past the longest row."""
+def test_index_scores_fp8_parity(qsa, page_size, layout):
+    """Requests of 1..8 rows (16-key tiles), or of one row each (32-key
+    tiles: two or four pages per tile), contexts with ragged tails (several
+    tiles plus a partial one, contexts shorter than one tile), n_fill past
+    the longest row."""
     import torch
-    rows = [[1000], [37, 40, 41], [4096 + 4 * i for i in range(8)], [9001, 9002], [12], [2051] * 5]
+    if layout == "mixed_rows":
+        rows = [[1000], [37, 40, 41], [4096 + 4 * i for i in range(8)], [9001, 9002], [12], [2051] * 5]
+    else:
+        rows = [[L] for L in [12, 37, 128, 129, 1000, 2051, 4096, 4100, 9001, 40_003]]
     w, codes, scales = _fp8_case(qsa, 84, rows, page_size)
     ld = (w.max_len // 4 + 3) // 4 * 4 + 8
     s = qsa.index_scores_fp8(bf16_dev(w.q), codes, scales, to_dev(w.req_row_start), to_dev(w.row_len),
