@@ -299,17 +299,31 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
     int off = (int)warp_incl_scan_u32((uint32_t)cnt) - cnt;
     const int wtot = __shfl_sync(0xffffffffu, off + cnt, 31);
     const bool fits = wtot <= kSfWarpCap;
+    // two candidates per step, their loads issued together
     while (cm != 0u) {
-      const int b = __ffs(cm) - 1;
+      const int b0 = __ffs(cm) - 1;
       cm &= cm - 1u;
-      const int i = index_of(b >> 2, b & 3);
-      const uint32_t x = order_key(__ldcg(row + i)) + 1u;
-      atomicAdd(&sh.hist[0][(x - v) >> sbin0], 1u);
+      const bool two = cm != 0u;
+      const int b1 = two ? __ffs(cm) - 1 : b0;
+      cm &= cm - 1u;
+      const int i0 = index_of(b0 >> 2, b0 & 3), i1 = index_of(b1 >> 2, b1 & 3);
+      const float f0 = __ldcg(row + i0), f1 = __ldcg(row + i1);
+      const uint32_t x0 = order_key(f0) + 1u;
+      atomicAdd(&sh.hist[0][(x0 - v) >> sbin0], 1u);
       if (fits) {
-        lkey[off] = x;
-        lidx[off] = (uint16_t)i;
+        lkey[off] = x0;
+        lidx[off] = (uint16_t)i0;
       }
       ++off;
+      if (two) {
+        const uint32_t x1 = order_key(f1) + 1u;
+        atomicAdd(&sh.hist[0][(x1 - v) >> sbin0], 1u);
+        if (fits) {
+          lkey[off] = x1;
+          lidx[off] = (uint16_t)i1;
+        }
+        ++off;
+      }
     }
     if (lane == 0) sh.wcnt[warp] = every ? 0xffffffffu : (uint32_t)wtot;
   }
@@ -355,6 +369,12 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
       const int cnt = sh.info[2];
       lo += (uint32_t)bin << sbin;
       span = sbin;
+      if (cnt == k_rem) {  // the whole bin is taken: the winners are the keys >= lo
+        T = lo;
+        need = k_rem;
+        all_ties = true;
+        break;
+      }
       if (span == 0) {  // the bin is one key
         T = lo;
         need = k_rem;
