@@ -186,7 +186,10 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
  * lengths so that long rows get a cluster of CTAs and short rows one CTA);
  * it is used when n_max exceeds 32768 and there are more rows than half the
  * SMs.  With a smaller or no workspace every row takes the kernel chosen
- * from n_max and n_rows alone.  The size query may return 0.
+ * from n_max and n_rows alone.  The size query may return 0.  With the plan,
+ * the short rows run on a library-owned side stream beside the long ones
+ * (forked from and joined back to `stream` with events, so the call's work
+ * stays ordered on `stream`, stream capture included).
  * ------------------------------------------------------------------- */
 size_t topk_select_workspace_size(int32_t n_rows, int32_t n_max, int32_t k);
 qsa_status topk_select(const float* scores, int64_t ld, const int32_t* n_valid, int32_t n_rows,

@@ -82,6 +82,7 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   int sl_clusters[5] = {0, 0, 0, 0, 0};  // co-resident clusters of 1, 2, 4, 8, 16 long-row CTAs
+  cudaStream_t side = nullptr;           // the planned selection's short class runs here, beside the long one
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -95,6 +96,8 @@ qsa_status device_info(DeviceInfo** out) {
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QSA_ERR_CUDA;
+    if (d.side == nullptr && cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess)
       return QSA_ERR_CUDA;
     const int smem = kSelMaxSmem;
     if (cudaFuncSetAttribute(select_kernel<kModeTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -432,9 +435,11 @@ qsa_status launch_select(const SelectArgs& a, bool pdl, cudaStream_t stream, int
 // count, the short ones one CTA each.  The cluster size is a launch
 // attribute, so the long class is launched once per size the plan can pick
 // (16 or 2 CTAs per row, and the one-CTA streaming kernel); the launches the
-// plan did not pick wait for it and exit.  Every launch after
-// the plan waits for its predecessor, so the chain completes after the plan
-// and the plan after the previous grid (the scorer in the fused call).
+// plan did not pick wait for it and exit.  The long launches follow the plan
+// on the caller's stream (each waits for its predecessor, the plan for the
+// previous grid: the scorer in the fused call); the short class runs on a
+// side stream from the plan's completion, beside them, and the caller's
+// stream waits for it before the call returns.
 template <int kMode>
 qsa_status launch_select_planned(const SelectArgs& args, int32_t* plan, bool pdl, cudaStream_t stream,
                                  DeviceInfo* d) {
@@ -460,6 +465,40 @@ qsa_status launch_select_planned(const SelectArgs& args, int32_t* plan, bool pdl
   } else {
     plan_rows_kernel<<<1, 1024, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
+  }
+  // short class: rows of at most kRsMaxRow candidates, one CTA each, on the
+  // side stream once the plan is complete, so that it runs beside the long
+  // class instead of after it; the caller's stream waits for both at the end
+  cudaEvent_t planned = nullptr, short_done = nullptr;
+  if (cudaEventCreateWithFlags(&planned, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&short_done, cudaEventDisableTiming) != cudaSuccess) {
+    if (planned) cudaEventDestroy(planned);
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  struct EventGuard {  // destruction is deferred by CUDA until the events complete
+    cudaEvent_t a, b;
+    ~EventGuard() {
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+    }
+  } guard{planned, short_done};
+  SelectArgs S = args;
+  S.plan = plan;
+  S.row_list = plan + 4 + args.n_rows;
+  S.count_at = 2;
+  S.plan_c = 0;
+  S.wait_primary = 0;  // stream order: the plan (and what it waited for) is complete
+  S.n_max = kRsMaxRow;
+  plan_select(S);
+  if (cudaEventRecord(planned, stream) != cudaSuccess || cudaStreamWaitEvent(d->side, planned, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  if (qsa_status st = launch_select<kMode>(S, false, d->side, sm)) return st;
+  if (cudaEventRecord(short_done, d->side) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
   }
   // long class: the sizes the plan can pick for 1 <= n_long <= n_rows
   SelectArgs L = args;
@@ -497,16 +536,11 @@ qsa_status launch_select_planned(const SelectArgs& args, int32_t* plan, bool pdl
       return QSA_ERR_CUDA;
     }
   }
-  // short class: rows of at most kRsMaxRow candidates, one CTA each
-  SelectArgs S = args;
-  S.plan = plan;
-  S.row_list = plan + 4 + args.n_rows;
-  S.count_at = 2;
-  S.plan_c = 0;
-  S.wait_primary = 1;
-  S.n_max = kRsMaxRow;
-  plan_select(S);
-  return launch_select<kMode>(S, true, stream, sm);
+  if (cudaStreamWaitEvent(stream, short_done, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  return QSA_OK;
 }
 
 template <int kMode>
