@@ -222,10 +222,37 @@ select_rows_kernel(SelectArgs a) {
     }
   };
 
+  // f2(i, va, vb, full) on every pair of 128-entry chunks (lane: entries
+  // i..i+3 and i+128..i+131; the list pass takes 8 entries per lane per
+  // round of ballots)
+  auto walk2 = [&](auto&& f2) {
+    static_assert(kSrUnroll % 2 == 0, "chunks go in pairs");
+    for (int c0 = w0; c0 < w1; c0 += 128 * kSrUnroll) {
+      float4 v[kSrUnroll];
+      if (vec && c0 + 128 * kSrUnroll <= w1) {
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; ++u)
+          v[u] = __ldg(reinterpret_cast<const float4*>(row + c0 + 128 * u + 4 * lane));
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; u += 2) f2(c0 + 128 * u + 4 * lane, v[u], v[u + 1], std::true_type{});
+      } else {
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; ++u) v[u] = sl_load4(row, c0 + 128 * u + 4 * lane, w1, vec);
+#pragma unroll
+        for (int u = 0; u < kSrUnroll; u += 2) f2(c0 + 128 * u + 4 * lane, v[u], v[u + 1], std::false_type{});
+      }
+    }
+  };
+
   // ---- 1. sampled bound -------------------------------------------------------------
+  // The r-th largest of 1024 sampled keys, r = mu + 3.5 sqrt(mu) + 2 with mu
+  // = 1024 k / n the expected number of samples among the row's k largest:
+  // below the k-th largest entry unless the sample is off by 3.5 standard
+  // deviations (then the exact passes run over the row).
   uint64_t k_low = 0ull;
   {
-    const int64_t r = 2 * (((int64_t)1024 * k + n - 1) / n) + 8;
+    const float mu = 1024.0f * (float)k / (float)n;
+    const int64_t r = (int64_t)ceilf(mu + 3.5f * sqrtf(mu) + 2.0f);
     if (r < 1024) {
       const int run = tid >> 3;  // 32 runs of 32
       const int p = (int)((((int64_t)run * n) / 32) & ~int64_t(3)) + 4 * (tid & 7);
@@ -250,37 +277,37 @@ select_rows_kernel(SelectArgs a) {
   uint32_t* cval = sm.cand_val + warp * kCw;
   uint32_t* cidx = sm.cand_idx + warp * kCw;
   uint32_t wn = 0u;  // the same in every lane of the warp
-  // Candidates are a few per cent of the row: a lane's are written in a loop
-  // over its mask (mostly no iteration), placed by ballot counts.
-  walk([&](int i, float4 v, auto full) {
-    const float xv[4] = {v.x, v.y, v.z, v.w};
+  // Candidates are a few per cent of the row: a lane's (up to 8 per round)
+  // are written in a loop over its mask (mostly no iteration), placed by
+  // four ballots of the lanes' counts.
+  const uint32_t lt = (1u << lane) - 1u;
+  walk2([&](int i, float4 va, float4 vb, auto full) {
+    const float xv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
     uint32_t cm = 0u;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 8; ++e) {
       bool ce = low.ge(xv[e]);
-      if (!decltype(full)::value) ce = ce & (i + e < w1);
+      if (!decltype(full)::value) ce = ce & ((e < 4 ? i + e : i + 124 + e) < w1);
       cm |= (uint32_t)ce << e;
     }
     if (__ballot_sync(0xffffffffu, cm != 0u) == 0u) return;
-    uint32_t tot = 0u, before = 0u;
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t m = __ballot_sync(0xffffffffu, (cm >> e) & 1u);
-      tot += __popc(m);
-      before += __popc(m & lt);
-    }
+    const uint32_t c = __popc(cm);
+    const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u),
+                   b2 = __ballot_sync(0xffffffffu, c & 4u), b3 = __ballot_sync(0xffffffffu, c & 8u);
+    const uint32_t tot = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2) + 8u * __popc(b3);
     if (wn + tot > (uint32_t)kCw) {
       wn = kCw + 1;  // overflowed (stays so)
       return;
     }
-    uint32_t o = wn + before;
+    uint32_t o = wn + __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt) + 8u * __popc(b3 & lt);
     while (cm != 0u) {
       const int e = __ffs(cm) - 1;
       cm &= cm - 1u;
-      const float x = e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+      const float4& h = e < 4 ? va : vb;
+      const int q = e & 3;
+      const float x = q == 0 ? h.x : (q == 1 ? h.y : (q == 2 ? h.z : h.w));
       cval[o] = __float_as_uint(x);
-      cidx[o] = (uint32_t)(i + e);
+      cidx[o] = (uint32_t)(e < 4 ? i + e : i + 124 + e);
       ++o;
     }
     wn += tot;
