@@ -12,7 +12,9 @@ headline decode step checked against the oracle end to end.
   through the 4-slot ring; the new pool rows against the oracle's key path,
   the scores against the oracle on the same keys, the selection, positions
   and slots bit-exact.
-- Mixed row lengths in one call (the device row plan).
+- Mixed row lengths in one call (the device row plan), also recorded in a
+  CUDA graph (the short rows run on a side stream forked and joined inside
+  the call).
 - More than two rows per SM with k <= 512 (small CTAs, four per SM): hard
   rows, rows whose evenly spaced 16-byte groups hold the largest values,
   special values, ragged lengths, token and QSA modes.
@@ -280,3 +282,42 @@ def test_select_blocks_many_qsa_rows(qsa):
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
     assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
     assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+def test_planned_selection_in_a_cuda_graph(qsa):
+    """The planned selection forks its short rows onto a side stream and
+    joins them back: recorded in a CUDA graph (after one eager call) and
+    replayed on new scores, it matches the oracle every time."""
+    import torch
+    rng = np.random.default_rng(95)
+    nv = _mixed_rows(rng, 80, [100_000, 40_000, 40_000, 40_000], 3000, 8000)
+    ld = int(nv.max())
+    P = 64
+    pt = np.stack([rng.permutation((ld + P - 1) // P) for _ in range(nv.size)]).astype(np.int32)
+    k = 2048
+    s_dev = torch.empty((nv.size, ld), dtype=torch.float32, device="cuda")
+    nv_dev, pt_dev = to_dev(nv), to_dev(pt)
+    ws = torch.empty(qsa.lib().topk_select_workspace_size(nv.size, ld, k), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    idx = torch.empty((nv.size, k), dtype=torch.int32, device="cuda")
+    slots = torch.empty((nv.size, k), dtype=torch.int32, device="cuda")
+
+    def call():
+        qsa.topk_select(s_dev, k, n_valid=nv_dev, n_max=ld, page_table=pt_dev, page_size=P, out_idx=idx,
+                        out_slots=slots, workspace=ws)
+
+    s_dev.copy_(torch.from_numpy(rng.standard_normal((nv.size, ld), dtype=np.float32)))
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    torch.cuda.synchronize()
+    for rep in range(2):
+        s = rng.standard_normal((nv.size, ld), dtype=np.float32)
+        s_dev.copy_(torch.from_numpy(s))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_idx, ref_slots = oracle.topk(s, k, n_valid=nv, page_table=pt, page_size=P)
+        assert np.array_equal(idx.cpu().numpy(), ref_idx), rep
+        assert np.array_equal(slots.cpu().numpy(), ref_slots), rep
