@@ -109,6 +109,8 @@ def _load():
                 "oracle_f16_round": (d, [d]),
                 "oracle_score_one_fp8": (ctypes.c_float, [p, p, ctypes.c_float]),
                 "oracle_index_scores_fp8": (None, [p, p, p, i64, p, p, p, i64, i64, p, i64]),
+                "oracle_score_one_gated": (ctypes.c_float, [p, p, p]),
+                "oracle_index_scores_gated": (None, [p, p, p, i64, p, p, p, i64, i64, p, i64]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -407,4 +409,31 @@ def index_scores_fp8(q, codes, scales, req_row_start, row_len, page_table, page_
     out = np.full((n_rows, ld_scores), np.nan, np.float32)
     _load().oracle_index_scores_fp8(_ptr(q), _ptr(codes), _ptr(scales), rrs.size - 1, _ptr(rrs), _ptr(rl),
                                     _ptr(pt), pt.shape[-1], int(page_size), _ptr(out), ld_scores)
+    return out
+
+
+def score_one_gated(q_row, gates, key) -> float:
+    """(1/sqrt(128)) sum_h gates[h] ReLU(<q_h, key>): q_row [4][128] and key
+    [128] u16 (BF16 bits), gates [4] float32."""
+    q_row = _c(q_row, np.uint16)
+    gates = _c(gates, np.float32)
+    key = _c(key, np.uint16)
+    return float(_load().oracle_score_one_gated(_ptr(q_row), _ptr(gates), _ptr(key)))
+
+
+def index_scores_gated(q, gates, pool, req_row_start, row_len, page_table, page_size, ld_scores=None):
+    """index_scores with a gate per row and head (gates [n_rows][4] float32);
+    entries b >= row_len/4 are NaN."""
+    q = _c(q, np.uint16)
+    gates = _c(gates, np.float32)
+    pool = _c(pool, np.uint16)
+    rrs = _c(req_row_start, np.int32)
+    rl = _c(row_len, np.int32)
+    pt = _c(page_table, np.int32)
+    n_rows = rl.size
+    if ld_scores is None:
+        ld_scores = max(1, int(rl.max()) // C) if n_rows else 1
+    out = np.full((n_rows, ld_scores), np.nan, np.float32)
+    _load().oracle_index_scores_gated(_ptr(q), _ptr(gates), _ptr(pool), rrs.size - 1, _ptr(rrs), _ptr(rl),
+                                      _ptr(pt), pt.shape[-1], int(page_size), _ptr(out), ld_scores)
     return out

@@ -630,3 +630,35 @@ void oracle_index_scores_fp8(const uint16_t* q, const uint8_t* codes, const floa
     }
   }
 }
+
+/* ---------- head-gated score ([TOPK], "Indexer Prologue Fusion": the query
+ * path scales each index head by a gate) ----------------------------------
+ * s = (1/sqrt(128)) sum_h g[h] * ReLU(<q_h, kbar>): the gate multiplies the
+ * head's rectified dot product; g = 1 for every head is the plain score.
+ * FP64, one rounding to FP32. */
+float oracle_score_one_gated(const uint16_t* q, const float* g, const uint16_t* key) {
+  double sum_w = 0.0;
+  for (int hg = 0; hg < QSA_H; ++hg) {
+    double hd = 0.0;
+    for (int d = 0; d < QSA_D; ++d)
+      hd += oracle_bf16_to_double(q[hg * QSA_D + d]) * oracle_bf16_to_double(key[d]);
+    const double rect = hd > 0.0 ? hd : 0.0;
+    sum_w += (double)g[hg] * rect;
+  }
+  return (float)(sum_w / sqrt((double)QSA_D));
+}
+
+/* Gated block scores: gates [n_rows][4] FP32, one per row and head. */
+void oracle_index_scores_gated(const uint16_t* q, const float* gates, const uint16_t* pool, int64_t n_req,
+                               const int32_t* req_row_start, const int32_t* row_len, const int32_t* page_table,
+                               int64_t ld_pt, int64_t page_size, float* scores, int64_t ld_scores) {
+  for (int64_t r = 0; r < n_req; ++r) {
+    const int32_t* ptr_r = page_table + r * ld_pt;
+    for (int64_t t = req_row_start[r]; t < req_row_start[r + 1]; ++t) {
+      const int64_t n_blk = row_len[t] / QSA_C;
+      for (int64_t b = 0; b < n_blk; ++b)
+        scores[t * ld_scores + b] = oracle_score_one_gated(q + t * QSA_H * QSA_D, gates + t * QSA_H,
+                                                           pool + oracle_pool_row(ptr_r, b, page_size) * QSA_D);
+    }
+  }
+}

@@ -74,6 +74,10 @@ MUTANTS = {
     "fp8_query_not_binary16": ("hdot += oracle_f16_round(oracle_bf16_to_double(qh[d]))",
                                "hdot += oracle_bf16_to_double(qh[d])"),
     "f16_no_subnormal_quantum": ("  if (qexp < -24) qexp = -24;\n", ""),
+    "gate_before_relu": ("const double rect = hd > 0.0 ? hd : 0.0;\n    sum_w += (double)g[hg] * rect;",
+                         "const double gd = (double)g[hg] * hd;\n    sum_w += gd > 0.0 ? gd : 0.0;"),
+    "gate_of_the_next_head": ("sum_w += (double)g[hg] * rect;", "sum_w += (double)g[(hg + 1) % QSA_H] * rect;"),
+    "gated_rows_share_row_0_gates": ("gates + t * QSA_H,", "gates,"),
     "indexshare_no_drafted_columns": (
         "int64_t width = QSA_C * k_blk + (QSA_C - 1) + n_extra;\n  int64_t nb0",
         "int64_t width = QSA_C * k_blk + (QSA_C - 1);\n  int64_t nb0"),

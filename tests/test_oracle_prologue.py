@@ -169,3 +169,62 @@ def test_rope_queries_position_zero_is_identity_and_matches_the_key_rotation():
         qq = np.zeros((1, 4, 128), np.uint16)
         qq[0, 1] = bf16_bits(u)
         assert np.array_equal(oracle.rope_queries(qq, np.array([p], np.int32))[0, 1], key)
+
+
+# ----------------------------------------------------------------- head gate
+def test_gated_score_with_unit_gates_is_the_plain_score():
+    rng = np.random.default_rng(9)
+    ones = np.ones(4, np.float32)
+    for _ in range(30):
+        q = normal_bf16(rng, (4, 128))
+        key = normal_bf16(rng, (128,))
+        assert oracle.score_one_gated(q, ones, key) == oracle.score_one(q, key)
+
+
+def test_gated_score_closed_form_one_head_at_a_time():
+    """A basis key e_d and a gate on head h alone: the score is
+    g * ReLU(q[h][d]) / sqrt(128)."""
+    q = np.zeros((4, 128), np.float32)
+    q[:, 5] = [1.5, -2.0, 0.75, 3.0]
+    qb = bf16_bits(q)
+    key = np.zeros(128, np.float32)
+    key[5] = 1.0
+    kb = bf16_bits(key)
+    for h in range(4):
+        g = np.zeros(4, np.float32)
+        g[h] = 0.5
+        want = np.float32(0.5 * max(float(q[h, 5]), 0.0) * SCALE)
+        assert oracle.score_one_gated(qb, g, kb) == want, h
+
+
+def test_gated_score_odd_in_the_gates_and_scales_with_them():
+    """The gate multiplies the rectified dot product: negating every gate
+    negates the score and doubling them doubles it, to the bit (a gate
+    applied before the ReLU breaks both)."""
+    rng = np.random.default_rng(10)
+    for _ in range(30):
+        q = normal_bf16(rng, (4, 128))
+        key = normal_bf16(rng, (128,))
+        g = rng.uniform(-2, 2, 4).astype(np.float32)
+        s = oracle.score_one_gated(q, g, key)
+        assert oracle.score_one_gated(q, -g, key) == -s
+        assert oracle.score_one_gated(q, 2 * g, key) == np.float32(2 * s)
+
+
+def test_gated_block_scores_follow_the_rows_gates():
+    """index_scores_gated on a paged pool equals score_one_gated of each
+    row's own gates against each visible block's key."""
+    rng = np.random.default_rng(11)
+    P = 16
+    row_len = np.array([13, 40, 9], np.int32)
+    rrs = np.array([0, 2, 3], np.int32)
+    pt = np.array([[3, 0, 2], [1, 4, 5]], np.int32)
+    pool = normal_bf16(rng, (6 * P // 4, 128))
+    q = normal_bf16(rng, (3, 4, 128))
+    gates = rng.uniform(-1, 2, (3, 4)).astype(np.float32)
+    s = oracle.index_scores_gated(q, gates, pool, rrs, row_len, pt, P, ld_scores=12)
+    for t, r in [(0, 0), (1, 0), (2, 1)]:
+        for b in range(row_len[t] // 4):
+            key = pool[oracle.pool_row(pt[r], b, P)]
+            assert s[t, b] == np.float32(oracle.score_one_gated(q[t], gates[t], key))
+        assert np.isnan(s[t, row_len[t] // 4:]).all()
