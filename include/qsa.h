@@ -434,6 +434,29 @@ qsa_status qsa_indexer_select_fp8(const void* q, const uint8_t* codes, const flo
                                   int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
                                   int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------
+ * Head gates  (SGLang GLM-5.2 blog, section "Indexer Prologue Fusion": the
+ * query path scales the index heads by a gate).  QSA's own score has no
+ * head weights; with gates g [n_rows][4] (FP32, row-major, 16-byte aligned)
+ * every head's rectified dot product is multiplied by its row's gate before
+ * the head sum:
+ *   s[t][b] = (1/sqrt(128)) sum_h g[t][h] * ReLU(<q[t][h], kbar[b]>).
+ * head_gates = NULL is the plain score (qsa_index_scores and
+ * qsa_indexer_select are these calls without gates).  Every other argument,
+ * the workspace, outputs and errors as for the ungated calls.
+ * ------------------------------------------------------------------- */
+qsa_status qsa_index_scores_gated(const void* q, const float* head_gates, const void* pool, int64_t pool_rows,
+                                  int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                  const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                  const int32_t* page_table, int64_t ld_pt, int32_t page_size, float* scores,
+                                  int64_t ld_scores, int64_t n_fill, void* stream);
+qsa_status qsa_indexer_select_gated(const void* q, const float* head_gates, const void* pool, int64_t pool_rows,
+                                    int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                    const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                    const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                    int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                    int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

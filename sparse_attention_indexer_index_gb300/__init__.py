@@ -20,7 +20,8 @@ __all__ = [
     "build", "lib", "QSAError", "compress_keys", "index_scores", "topk_select", "expand_slots",
     "indexer_select", "indexer_select_workspace_size", "device_status", "out_width",
     "select_blocks", "indexshare_slots", "indexshare_width", "sparse_attn", "append_keys", "decode_step",
-    "rope_queries", "quantize_keys_fp8", "index_scores_fp8", "indexer_select_fp8",
+    "rope_queries", "quantize_keys_fp8", "index_scores_fp8", "indexer_select_fp8", "index_scores_gated",
+    "indexer_select_gated",
     "HEAD_DIM", "HEADS", "BLOCK", "MAX_K",
 ]
 
@@ -73,6 +74,10 @@ def lib():
                                                     i64, i64, p]),
             "qsa_indexer_select_fp8": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                       i32, p, p, p, p, i64, p, sz, p]),
+            "qsa_index_scores_gated": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
+                                                      i64, i64, p]),
+            "qsa_indexer_select_gated": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
+                                                        i32, p, p, p, p, i64, p, sz, p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -238,6 +243,25 @@ def index_scores_fp8(q, codes, scales, req_row_start, row_len, page_table, page_
     return _index_scores_call("qsa_index_scores_fp8", (_ptr(codes), _ptr(scales)), codes.shape[0], q,
                               req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req,
                               scores, n_fill, stream)
+
+
+def index_scores_gated(q, head_gates, pool, req_row_start, row_len, page_table, page_size, max_len,
+                       max_rows_per_req=None, scores=None, n_fill=0, stream=None):
+    """index_scores with a gate per row and head: head_gates [n_rows][4]
+    float32 multiplies each head's rectified dot product before the sum."""
+    torch = _torch()
+    _dev(pool, torch.bfloat16, "pool", 2)
+    _gates(head_gates, row_len)
+    return _index_scores_call("qsa_index_scores_gated", (_ptr(head_gates), _ptr(pool)), pool.shape[0], q,
+                              req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req, scores,
+                              n_fill, stream)
+
+
+def _gates(head_gates, row_len):
+    torch = _torch()
+    _dev(head_gates, torch.float32, "head_gates", 2)
+    if head_gates.shape[1] != HEADS or head_gates.shape[0] != row_len.numel():
+        raise ValueError("head_gates must be [n_rows][4]")
 
 
 def _index_scores_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, page_table, page_size, max_len,
@@ -472,6 +496,19 @@ def indexer_select_fp8(q, codes, scales, req_row_start, row_len, page_table, pag
     return _indexer_select_call("qsa_indexer_select_fp8", (_ptr(codes), _ptr(scales)), codes.shape[0], q,
                                 req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req,
                                 k_blk, want_blocks, want_pos, scores_out, workspace, out_slots, stream)
+
+
+def indexer_select_gated(q, head_gates, pool, req_row_start, row_len, page_table, page_size, max_len,
+                         max_rows_per_req=None, k_blk=512, want_blocks=False, want_pos=False,
+                         scores_out=None, workspace=None, out_slots=None, stream=None):
+    """indexer_select with a gate per row and head (head_gates [n_rows][4]
+    float32)."""
+    torch = _torch()
+    _dev(pool, torch.bfloat16, "pool", 2)
+    _gates(head_gates, row_len)
+    return _indexer_select_call("qsa_indexer_select_gated", (_ptr(head_gates), _ptr(pool)), pool.shape[0], q,
+                                req_row_start, row_len, page_table, page_size, max_len, max_rows_per_req, k_blk,
+                                want_blocks, want_pos, scores_out, workspace, out_slots, stream)
 
 
 def _indexer_select_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, page_table, page_size,

@@ -800,6 +800,7 @@ qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_cou
   t.tmem_cols = cols;
   t.trigger_dependents = s.trigger_dependents;
   t.new_pos = s.new_pos;
+  t.head_gates = s.head_gates;
   const int64_t row_tiles = (max_rows_per_req + t.rows_per_tile - 1) / t.rows_per_tile;
   if (row_tiles > 65535) return QSA_ERR_UNSUPPORTED;
   qsa_status tma = launch_scores_tma(t, n_kt, row_tiles, s.n_req, sm_count, stream);
@@ -1014,17 +1015,28 @@ qsa_status qsa_index_scores(const void* q, const void* pool, int64_t pool_rows, 
                             int32_t max_len, int32_t max_rows_per_req, const int32_t* page_table,
                             int64_t ld_pt, int32_t page_size, float* scores, int64_t ld_scores,
                             int64_t n_fill, void* stream) {
+  return qsa_index_scores_gated(q, nullptr, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
+                                max_rows_per_req, page_table, ld_pt, page_size, scores, ld_scores, n_fill, stream);
+}
+
+qsa_status qsa_index_scores_gated(const void* q, const float* head_gates, const void* pool, int64_t pool_rows,
+                                  int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                  const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                  const int32_t* page_table, int64_t ld_pt, int32_t page_size, float* scores,
+                                  int64_t ld_scores, int64_t n_fill, void* stream) {
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
   if (qsa_status st = check_paging(page_table, ld_pt, page_size, max_len)) return st;
   if (!q || !pool || !scores || pool_rows < 0 || n_fill < 0) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(pool) || !aligned4(scores)) return QSA_ERR_INVALID_ARG;
+  if (head_gates && !aligned16(head_gates)) return QSA_ERR_INVALID_ARG;
   if (ld_scores < std::max<int64_t>(max_len / kBlock, n_fill)) return QSA_ERR_INVALID_ARG;
   DeviceInfo* d = nullptr;
   if (qsa_status st = device_info(&d)) return st;
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld_scores, n_fill, 0};
+  s.head_gates = head_gates;
   return launch_scorer(s, max_rows_per_req, d->sm_count, static_cast<cudaStream_t>(stream));
 }
 
@@ -1210,7 +1222,7 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
                                int32_t* out_pos, int32_t* out_slots, float* scores_out,
                                int64_t ld_scores, void* workspace, size_t workspace_bytes,
                                void* stream, const int32_t* new_pos, const uint8_t* pool8 = nullptr,
-                               const float* key_scales = nullptr) {
+                               const float* key_scales = nullptr, const float* head_gates = nullptr) {
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows == 0) return QSA_OK;
@@ -1218,6 +1230,7 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
   if (!q || !(pool || pool8) || !out_slots || pool_rows < 0) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q) || (pool && !aligned16(pool)) || (pool8 && (!aligned16(pool8) || !key_scales)))
     return QSA_ERR_INVALID_ARG;
+  if (head_gates && !aligned16(head_gates)) return QSA_ERR_INVALID_ARG;
   const int32_t nb_max = max_len / kBlock;
   float* scores = scores_out;
   int64_t ld = ld_scores;
@@ -1243,7 +1256,7 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
 
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
-              page_size, scores, ld, 0, 1, new_pos, pool8, key_scales};
+              page_size, scores, ld, 0, 1, new_pos, pool8, key_scales, head_gates};
   if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
     return e;
 
@@ -1376,6 +1389,18 @@ extern "C" qsa_status qsa_indexer_select_noalloc(
 // Prologue tails: query RoPE, FP8 index keys and the indexer on them.
 // ---------------------------------------------------------------------------
 extern "C" {
+
+qsa_status qsa_indexer_select_gated(const void* q, const float* head_gates, const void* pool, int64_t pool_rows,
+                                    int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                    const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                    const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                    int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                    int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!pool) return QSA_ERR_INVALID_ARG;
+  return indexer_select_impl(q, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len, max_rows_per_req,
+                             page_table, ld_pt, page_size, k_blk, out_blocks, out_pos, out_slots, scores_out,
+                             ld_scores, workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, head_gates);
+}
 
 qsa_status qsa_rope_queries(const void* q, const int32_t* pos, int32_t n_rows, double rope_base, void* q_out,
                             void* stream) {

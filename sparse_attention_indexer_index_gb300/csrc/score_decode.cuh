@@ -52,7 +52,15 @@ struct ScoreArgs {
   // and one FP32 scale per pool row; `pool` is then unused
   const uint8_t* pool8;
   const float* key_scales;
+  // nullptr, or a gate per row and head [n_rows][4] (FP32) multiplying the
+  // head's rectified dot product before the head sum (DSA-style head gates)
+  const float* head_gates;
 };
+
+// Gate of (row, head): 1 without gates (then the products below are exact).
+__device__ __forceinline__ float head_gate(const float* gates, int64_t row, int head) {
+  return gates != nullptr ? __ldg(gates + row * kHeads + head) : 1.f;
+}
 
 constexpr int kScoreThreads = 256;
 constexpr int kScoreHalfWarps = kScoreThreads / 16;            // 16
@@ -273,7 +281,7 @@ score_decode_kernel(ScoreArgs a) {
             }
             // lane quad l>>2 holds the full dot product of head l>>2
             float sc = reduce_scatter4_x16(d[0], d[1], d[2], d[3], lane16);
-            sc = fmaxf(sc, 0.f);
+            sc = fmaxf(sc, 0.f) * head_gate(a.head_gates, t, lane16 >> 2);
             sc += __shfl_xor_sync(0xffffffffu, sc, 4);
             sc += __shfl_xor_sync(0xffffffffu, sc, 8);
             if (lane16 == 0 && b < nb_t) srow[b] = sc * kScoreScale;

@@ -28,7 +28,8 @@
 //  - N = 8 columns = 2 rows x 4 heads per n-tile; up to 4 n-tiles (8 rows).
 //    The B fragments of the current request sit in the warp's own slot of
 //    shared memory (re-staged only when the request changes).
-//  - Epilogue in registers: ReLU, the 4-head sum (one shuffle), the scale.
+//  - Epilogue in registers: ReLU, the optional head gates, the 4-head sum
+//    (one shuffle), the scale.
 //  - Every CTA builds the list of tiles of all requests (prefix over the
 //    requests' visible blocks); each warp takes a balanced contiguous range.
 //    The loads are plain 16-byte loads from 24 warps per SM.  (Measured: a
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   // ---- compute side: query fragments of the tile's request, row lengths ---
   int r = -1, t0 = 0, nrows = 0;
   int nbr[NT];
+  float gate_a[NT], gate_b[NT];  // gates of this lane's two heads (columns 2t, 2t+1) of row 2nt + t/2
   auto compute_tile = [&](int i, const SmFrag& f) {
     if (r < 0 || i >= g_pre[r + 1]) {
       if (r < 0) r = request_of(i);
@@ -298,9 +300,12 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
       for (int nt = 0; nt < NT; ++nt) {
         const int rl = 2 * nt + (t >> 1);
         int nb = 0;
+        gate_a[nt] = gate_b[nt] = 1.f;
         if (rl < nrows) {
           const int L = __ldg(a.row_len + t0 + rl);
           nb = (L >= 0 && L <= a.max_len) ? L / kBlock : 0;
+          gate_a[nt] = head_gate(a.head_gates, t0 + rl, 2 * (t & 1));
+          gate_b[nt] = head_gate(a.head_gates, t0 + rl, 2 * (t & 1) + 1);
         }
         nbr[nt] = nb;
       }
@@ -381,8 +386,9 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
       const int b = j * kTile + 16 * h + g;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float v0 = fmaxf(acc[nt][0], 0.f) + fmaxf(acc[nt][1], 0.f);
-        float v1 = fmaxf(acc[nt][2], 0.f) + fmaxf(acc[nt][3], 0.f);
+        // gated heads (gates 1 without head gates: then exactly the plain sums)
+        float v0 = fmaf(gate_b[nt], fmaxf(acc[nt][1], 0.f), gate_a[nt] * fmaxf(acc[nt][0], 0.f));
+        float v1 = fmaf(gate_b[nt], fmaxf(acc[nt][3], 0.f), gate_a[nt] * fmaxf(acc[nt][2], 0.f));
         v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
         v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
         const int rl = 2 * nt + (t >> 1);

@@ -67,7 +67,26 @@ struct TcArgs {
   // blocks reach block new_pos[r]/4 wait for that grid (and CTA 0, so that
   // this grid still completes after it); the rest read the pool at once.
   const int32_t* new_pos;
+  const float* head_gates;      // nullptr, or [n_rows][4] gates (see ScoreArgs)
 };
+
+// Score of one (row, key) from its 4 head accumulators: the rectified dot
+// products summed and scaled; gated: each multiplied by its head's gate
+// first (with unit gates the same sums: 1 * x and fma(1, x, y) round like x
+// and x + y).
+__device__ __forceinline__ float tc_head_sum(const uint32_t* v) {
+  float sc = fmaxf(__uint_as_float(v[0]), 0.f);
+  sc += fmaxf(__uint_as_float(v[1]), 0.f);
+  sc += fmaxf(__uint_as_float(v[2]), 0.f);
+  sc += fmaxf(__uint_as_float(v[3]), 0.f);
+  return sc * kScoreScale;
+}
+__device__ __forceinline__ float tc_head_sum_gated(const uint32_t* v, const float* gates, int64_t row) {
+  const float4 g = __ldg(reinterpret_cast<const float4*>(gates) + row);
+  const float r0 = fmaxf(__uint_as_float(v[0]), 0.f), r1 = fmaxf(__uint_as_float(v[1]), 0.f);
+  const float r2 = fmaxf(__uint_as_float(v[2]), 0.f), r3 = fmaxf(__uint_as_float(v[3]), 0.f);
+  return fmaf(g.w, r3, fmaf(g.z, r2, fmaf(g.y, r1, g.x * r0))) * kScoreScale;
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers (tcgen05, cp.async).
@@ -308,15 +327,18 @@ score_tc_cpasync_kernel(TcArgs a) {
     for (int c0 = 32 * (warp >> 2); c0 < a.n_cols; c0 += 32 * (kTcThreads / 128)) {
       uint32_t v[32];
       tmem_ld_32cols(tmem + ((uint32_t)(quarter * 32) << 16) + acc_col + (uint32_t)c0, v);
+      if (a.head_gates == nullptr) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int tr = c0 / 4 + j;  // row within the tile
-        if (tr < t1 - t0 && b < s_nb[tr]) {
-          float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
-          sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
-          sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
-          sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-          a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = sc * kScoreScale;
+        for (int j = 0; j < 8; ++j) {
+          const int tr = c0 / 4 + j;  // row within the tile
+          if (tr < t1 - t0 && b < s_nb[tr]) a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = tc_head_sum(v + 4 * j);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int tr = c0 / 4 + j;
+          if (tr < t1 - t0 && b < s_nb[tr])
+            a.scores[(int64_t)(t0 + tr) * a.ld_scores + b] = tc_head_sum_gated(v + 4 * j, a.head_gates, t0 + tr);
         }
       }
     }
@@ -685,15 +707,19 @@ score_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap pool_map) {
           ncols = 16;
         }
         float* dst = a.scores + (int64_t)(t0 + c0 / 4) * a.ld_scores + b;
+        if (a.head_gates == nullptr) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int tr = c0 / 4 + j;  // row within the tile
-          if (4 * j < ncols && tr < nrows && (all_vis || b < s_nb[tr])) {
-            float sc = fmaxf(__uint_as_float(v[4 * j]), 0.f);
-            sc += fmaxf(__uint_as_float(v[4 * j + 1]), 0.f);
-            sc += fmaxf(__uint_as_float(v[4 * j + 2]), 0.f);
-            sc += fmaxf(__uint_as_float(v[4 * j + 3]), 0.f);
-            dst[(int64_t)j * a.ld_scores] = sc * kScoreScale;
+          for (int j = 0; j < 8; ++j) {
+            const int tr = c0 / 4 + j;  // row within the tile
+            if (4 * j < ncols && tr < nrows && (all_vis || b < s_nb[tr]))
+              dst[(int64_t)j * a.ld_scores] = tc_head_sum(v + 4 * j);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int tr = c0 / 4 + j;
+            if (4 * j < ncols && tr < nrows && (all_vis || b < s_nb[tr]))
+              dst[(int64_t)j * a.ld_scores] = tc_head_sum_gated(v + 4 * j, a.head_gates, t0 + tr);
           }
         }
       }

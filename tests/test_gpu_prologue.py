@@ -1,6 +1,7 @@
 """GPU parity of the prologue tails against the oracle (SGLang GLM-5.2 blog,
 "Indexer Prologue Fusion"): the index-query RoPE, the FP8 key quantiser,
-the FP8-key scorer and the fused selection on FP8 keys.
+the FP8-key scorer and the fused selection on FP8 keys, and the head-gated
+score on every scorer.
 
 - RoPE: within one BF16 ulp plus the FP32 rotation's absolute term
   2^-22 (|u| + |v|) per pair (both sides round once to BF16; the GPU's sine
@@ -221,3 +222,72 @@ def test_indexer_select_fp8_full_batch(qsa):
         nb = int(w.row_len[t]) // 4
         assert (np.abs(s[t, :nb].astype(np.float64) - want[t, :nb]) <= tol[t, :nb]).all(), t
     _check_selection(out, s, w, 512)
+
+
+# ----------------------------------------------------------------- head gates
+def gated_score_tolerance(q_bits, gates, pool_bits, req_row_start, row_len, page_table, page_size, ld):
+    """2e-5 * (1/sqrt(128)) * sum_{h,d} |g_h q_hd kbar_d| + 1e-6: the score
+    bound with each head's terms weighted by |gate|."""
+    qa = np.abs(oracle.bf16_to_float(q_bits)).astype(np.float64)  # [rows][4][128]
+    qa = (qa * np.abs(gates)[:, :, None]).sum(axis=1)             # [rows][128]
+    tol = np.full((row_len.size, ld), np.inf)
+    for r in range(req_row_start.size - 1):
+        rows = np.arange(req_row_start[r], req_row_start[r + 1])
+        if rows.size == 0:
+            continue
+        nb = int(row_len[rows].max()) // 4
+        prow = pool_rows_of(page_table[r], nb, page_size)
+        ka = np.abs(oracle.bf16_to_float(pool_bits[prow])).astype(np.float64)
+        tol[rows, :nb] = 2e-5 * SCALE * (qa[rows] @ ka.T) + 1e-6
+    return tol
+
+
+@pytest.mark.parametrize("layout,page_size", [("decode_rows", 64), ("prefill_rows", 64), ("one_row_small_pages", 16)])
+def test_gated_scores_and_selection(qsa, layout, page_size):
+    """Gated scores on each scorer (requests of up to 8 rows: the mma.sync
+    decode scorer; a request of 100 rows: the tcgen05 scorer; one-row
+    requests on 16-token pages: the CUDA-core scorer) against the oracle,
+    gates drawn in [-1, 2] (some negative); the fused gated call's selection
+    bit-exact on its own scores; unit gates give the ungated scores to the
+    bit."""
+    import torch
+    if layout == "decode_rows":
+        rows = [[3001 + i for i in range(6)], [513], [2047, 2048, 2049], [20_003]]
+    elif layout == "prefill_rows":
+        rows = [[5000 + i for i in range(100)]]
+    else:
+        rows = [[L] for L in [37, 1000, 4099, 12_001]]
+    w = decode_workload(96, rows, page_size=page_size, with_keys=False)
+    rng = np.random.default_rng(97)
+    pool_h = normal_bf16(rng, (w.pool_rows, 128))
+    gates = rng.uniform(-1, 2, (w.n_rows, 4)).astype(np.float32)
+    pool = bf16_dev(pool_h)
+    args = (to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table), w.page_size, w.max_len,
+            w.max_rows_per_req)
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    s = qsa.index_scores_gated(bf16_dev(w.q), to_dev(gates), pool, *args,
+                               scores=torch.full((w.n_rows, ld), float("nan"), device="cuda")).cpu().numpy()
+    want = oracle.index_scores_gated(w.q, gates, pool_h, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    tol = gated_score_tolerance(w.q, gates, pool_h, w.req_row_start, w.row_len, w.page_table, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        err = np.abs(s[t, :nb].astype(np.float64) - want[t, :nb])
+        assert (err <= tol[t, :nb]).all(), (t, float(err.max()))
+    # fused call: selection bit-exact on its scores
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.indexer_select_gated(bf16_dev(w.q), to_dev(gates), pool, *args, k_blk=512, want_blocks=True,
+                                   want_pos=True, scores_out=scores)
+    sg = scores.cpu().numpy()
+    sel_ref, _ = oracle.topk(sg, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+    # unit gates: the ungated scores, to the bit
+    s1 = qsa.index_scores_gated(bf16_dev(w.q), torch.ones((w.n_rows, 4), device="cuda"), pool, *args,
+                                scores=torch.full((w.n_rows, ld), float("nan"), device="cuda")).cpu().numpy()
+    s0 = qsa.index_scores(bf16_dev(w.q), pool, *args,
+                          scores=torch.full((w.n_rows, ld), float("nan"), device="cuda")).cpu().numpy()
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        assert np.array_equal(s1[t, :nb].view(np.uint32), s0[t, :nb].view(np.uint32)), t
