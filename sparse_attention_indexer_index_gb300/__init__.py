@@ -94,13 +94,25 @@ def _torch():
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None):
+_raw_stream = None
+
+
+def _stream(stream=None, device=None):
+    """The CUDA stream handle: `stream`'s, else the current stream of
+    `device` (a tensor's device; the current device if None)."""
+    global _raw_stream
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is None:  # the raw query avoids building a Stream object per call
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _raw_stream:
+        idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(_raw_stream(idx))
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
 def _dev(t, dtype, name, ndim=None):
@@ -212,7 +224,7 @@ def decode_step(new_keys, req_tok_start, req_first_pos, ring, q, pool, req_row_s
         _ptr(pool), pool.shape[0], n_req, _ptr(req_row_start), n_rows, _ptr(row_len), int(max_len),
         int(max_rows_per_req), _ptr(page_table), page_table.shape[1], int(page_size), int(k_blk), _ptr(blocks),
         _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld, _ptr(workspace),
-        0 if workspace is None else workspace.numel(), _stream(stream)))
+        0 if workspace is None else workspace.numel(), _stream(stream, q.device)))
     out = {"slots": out_slots}
     if blocks is not None:
         out["blocks"] = blocks
@@ -545,7 +557,7 @@ def _indexer_select_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, pag
         _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
         _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
         int(page_size), int(k_blk), _ptr(blocks), _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld,
-        _ptr(workspace), ws_bytes, _stream(stream)))
+        _ptr(workspace), ws_bytes, _stream(stream, q.device)))
     out = {"slots": out_slots}
     if blocks is not None:
         out["blocks"] = blocks

@@ -699,10 +699,21 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
 template <int NT, bool kFp8>
 qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream) {
   const size_t smem = sm_smem_bytes(s.n_req, NT);
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, score_mma_kernel<NT, kFp8>, kSmThreads, smem) !=
-      cudaSuccess)
-    return QSA_ERR_CUDA;
+  // CTAs per SM, queried once (the query costs microseconds of host time on
+  // every call otherwise): at the largest shared memory a launch can ask
+  // for, so never more than fit for any request count (the register budget
+  // caps it at kSmMinCtas anyway)
+  static const int occ_max = [] {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, score_mma_kernel<NT, kFp8>, kSmThreads,
+                                                      sm_smem_bytes(kSmMaxReq, NT)) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return o;
+  }();
+  if (occ_max <= 0) return QSA_ERR_CUDA;
+  const int occ = occ_max;
   const int64_t nb_max = s.max_len / kBlock;
   const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + sm_tile<NT, kFp8>() - 1) / sm_tile<NT, kFp8>());
   const int64_t ctas =
