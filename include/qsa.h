@@ -456,6 +456,15 @@ qsa_status qsa_indexer_select_gated(const void* q, const float* head_gates, cons
                                     const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
                                     int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
                                     int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream);
+/* qsa_decode_step with head gates for the step's query rows (between q and
+ * pool; NULL: qsa_decode_step). */
+qsa_status qsa_decode_step_gated(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                                 void* ring, double rope_base, const void* q, const float* head_gates, void* pool,
+                                 int64_t pool_rows, int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                 const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                 const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                 int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                 int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

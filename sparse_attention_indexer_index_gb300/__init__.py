@@ -76,6 +76,8 @@ def lib():
                                                       i32, p, p, p, p, i64, p, sz, p]),
             "qsa_index_scores_gated": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32, p,
                                                       i64, i64, p]),
+            "qsa_decode_step_gated": (ctypes.c_int, [p, p, p, p, d, p, p, p, i64, i32, p, i32, p, i32, i32, p,
+                                                     i64, i32, i32, p, p, p, p, i64, p, sz, p]),
             "qsa_indexer_select_gated": (ctypes.c_int, [p, p, p, i64, i32, p, i32, p, i32, i32, p, i64, i32,
                                                         i32, p, p, p, p, i64, p, sz, p]),
         }
@@ -191,10 +193,13 @@ def append_keys(new_keys, req_tok_start, req_first_pos, ring, pool, page_table, 
 
 def decode_step(new_keys, req_tok_start, req_first_pos, ring, q, pool, req_row_start, row_len, page_table,
                 page_size, max_len, max_rows_per_req=None, k_blk=512, rope_base=10000.0, want_blocks=False,
-                want_pos=False, out_slots=None, scores_out=None, workspace=None, stream=None):
+                want_pos=False, out_slots=None, scores_out=None, workspace=None, stream=None, head_gates=None):
     """Key path (append_keys) then the fused indexer (indexer_select) in one
-    call; returns dict(slots, blocks?, pos?) like indexer_select."""
+    call; returns dict(slots, blocks?, pos?) like indexer_select.  head_gates
+    [n_rows][4] float32: gated scores (qsa_decode_step_gated)."""
     torch = _torch()
+    if head_gates is not None:
+        _gates(head_gates, row_len)
     for t, nm in [(new_keys, "new_keys"), (q, "q"), (pool, "pool"), (ring, "ring")]:
         _dev(t, torch.bfloat16, nm)
     for t, nm in [(req_tok_start, "req_tok_start"), (req_first_pos, "req_first_pos"),
@@ -219,9 +224,11 @@ def decode_step(new_keys, req_tok_start, req_first_pos, ring, q, pool, req_row_s
     elif workspace is None:
         nbytes = indexer_select_workspace_size(n_rows, max_len, k_blk)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
-    _check("qsa_decode_step", lib().qsa_decode_step(
+    fn = "qsa_decode_step" if head_gates is None else "qsa_decode_step_gated"
+    gate_args = () if head_gates is None else (_ptr(head_gates),)
+    _check(fn, getattr(lib(), fn)(
         _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), _ptr(ring), float(rope_base), _ptr(q),
-        _ptr(pool), pool.shape[0], n_req, _ptr(req_row_start), n_rows, _ptr(row_len), int(max_len),
+        *gate_args, _ptr(pool), pool.shape[0], n_req, _ptr(req_row_start), n_rows, _ptr(row_len), int(max_len),
         int(max_rows_per_req), _ptr(page_table), page_table.shape[1], int(page_size), int(k_blk), _ptr(blocks),
         _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream, q.device)))

@@ -1316,6 +1316,19 @@ qsa_status qsa_decode_step(const void* new_keys, const int32_t* req_tok_start, c
                            int64_t ld_pt, int32_t page_size, int32_t k_blk, int32_t* out_blocks,
                            int32_t* out_pos, int32_t* out_slots, float* scores_out, int64_t ld_scores,
                            void* workspace, size_t workspace_bytes, void* stream) {
+  return qsa_decode_step_gated(new_keys, req_tok_start, req_first_pos, ring, rope_base, q, nullptr, pool, pool_rows,
+                               n_req, req_row_start, n_rows, row_len, max_len, max_rows_per_req, page_table, ld_pt,
+                               page_size, k_blk, out_blocks, out_pos, out_slots, scores_out, ld_scores, workspace,
+                               workspace_bytes, stream);
+}
+
+qsa_status qsa_decode_step_gated(const void* new_keys, const int32_t* req_tok_start, const int32_t* req_first_pos,
+                                 void* ring, double rope_base, const void* q, const float* head_gates, void* pool,
+                                 int64_t pool_rows, int32_t n_req, const int32_t* req_row_start, int32_t n_rows,
+                                 const int32_t* row_len, int32_t max_len, int32_t max_rows_per_req,
+                                 const int32_t* page_table, int64_t ld_pt, int32_t page_size, int32_t k_blk,
+                                 int32_t* out_blocks, int32_t* out_pos, int32_t* out_slots, float* scores_out,
+                                 int64_t ld_scores, void* workspace, size_t workspace_bytes, void* stream) {
   if (k_blk < 1 || k_blk > kMaxK) return QSA_ERR_UNSUPPORTED;
   if (qsa_status st = check_rows(n_req, req_row_start, n_rows, row_len, max_len)) return st;
   if (n_rows > 0) {
@@ -1332,7 +1345,7 @@ qsa_status qsa_decode_step(const void* new_keys, const int32_t* req_tok_start, c
   return indexer_select_impl(q, pool, pool_rows, n_req, req_row_start, n_rows, row_len, max_len,
                              max_rows_per_req, page_table, ld_pt, page_size, k_blk, out_blocks, out_pos,
                              out_slots, scores_out, ld_scores, workspace, workspace_bytes, stream,
-                             req_first_pos);
+                             req_first_pos, nullptr, nullptr, head_gates);
 }
 
 }  // extern "C"

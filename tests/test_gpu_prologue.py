@@ -291,3 +291,53 @@ def test_gated_scores_and_selection(qsa, layout, page_size):
     for t in range(w.n_rows):
         nb = int(w.row_len[t]) // 4
         assert np.array_equal(s1[t, :nb].view(np.uint32), s0[t, :nb].view(np.uint32)), t
+
+
+def test_gated_decode_step_equals_append_then_gated_indexer(qsa):
+    """qsa_decode_step_gated (key path, then the gated fused indexer) gives
+    the same pool, ring, scores and slots as qsa_append_keys followed by
+    qsa_indexer_select_gated."""
+    import torch
+    rows, P = [[20_000 - 5 + i for i in range(6)], [5003], [777]], 64
+    rng = np.random.default_rng(98)
+    w = decode_workload(99, rows, page_size=P, k_blk=512)
+    n_req = w.n_req
+    firsts = np.array([min(r) - 1 for r in rows], np.int32)
+    counts = np.array([len(r) for r in rows], np.int32)
+    raw = [normal_bf16(rng, (int(f + c), 128)) for f, c in zip(firsts, counts)]
+    ring0 = np.zeros((n_req, 4, 128), np.uint16)
+    blocks, reqs, raws = [], [], []
+    for r in range(n_req):
+        nb0 = int(firsts[r]) // 4
+        blocks.append(np.arange(nb0, dtype=np.int32))
+        reqs.append(np.full(nb0, r, np.int32))
+        raws.append(raw[r][:4 * nb0])
+        for p in range(4 * nb0, int(firsts[r])):
+            ring0[r, p % 4] = raw[r][p]
+    pool0 = torch.zeros((w.pool_rows, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(bf16_dev(np.concatenate(raws)), to_dev(np.concatenate(blocks)), pool0,
+                      block_req=to_dev(np.concatenate(reqs)), page_table=to_dev(w.page_table), page_size=P)
+    new = np.concatenate([raw[r][firsts[r]:] for r in range(n_req)])
+    rts = to_dev(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+    fp, pt = to_dev(firsts), to_dev(w.page_table)
+    q, rrs, rl = bf16_dev(w.q), to_dev(w.req_row_start), to_dev(w.row_len)
+    gates = to_dev(rng.uniform(-1, 2, (w.n_rows, 4)).astype(np.float32))
+    ld = (w.max_len // 4 + 3) // 4 * 4
+    ring_a, pool_a = bf16_dev(ring0), pool0.clone()
+    sa = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    qsa.append_keys(bf16_dev(new), rts, fp, ring_a, pool_a, pt, P)
+    out_a = qsa.indexer_select_gated(q, gates, pool_a, rrs, rl, pt, P, w.max_len, w.max_rows_per_req, k_blk=512,
+                                     want_blocks=True, want_pos=True, scores_out=sa)
+    ring_b, pool_b = bf16_dev(ring0), pool0.clone()
+    sb = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out_b = qsa.decode_step(bf16_dev(new), rts, fp, ring_b, q, pool_b, rrs, rl, pt, P, w.max_len,
+                            w.max_rows_per_req, k_blk=512, want_blocks=True, want_pos=True, scores_out=sb,
+                            head_gates=gates)
+    assert torch.equal(ring_a, ring_b) and torch.equal(pool_a, pool_b)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        assert torch.equal(sa[t, :nb].view(torch.int32), sb[t, :nb].view(torch.int32)), t
+    for key in ("slots", "blocks", "pos"):
+        assert torch.equal(out_a[key], out_b[key]), key
+    sel_ref, _ = oracle.topk(sb.cpu().numpy(), 512, n_valid=w.row_len // 4)
+    assert np.array_equal(out_b["blocks"].cpu().numpy(), sel_ref)
