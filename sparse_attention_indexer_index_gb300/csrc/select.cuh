@@ -195,9 +195,17 @@ struct SelRow {
 };
 
 __device__ __forceinline__ int32_t slot_lookup(const SelectArgs& a, const SelRow& r, int64_t pos) {
-  // positions are below a row length (int32): 32-bit division
-  const int32_t page_idx = (int32_t)pos / a.page_size;
-  const int32_t off = (int32_t)pos - page_idx * a.page_size;
+  // positions are below a row length (int32): 32-bit division, a shift and a
+  // mask for page sizes that are powers of two (the usual case)
+  const int32_t ps = a.page_size;
+  int32_t page_idx, off;
+  if ((ps & (ps - 1)) == 0) {
+    page_idx = (int32_t)pos >> (31 - __clz(ps));
+    off = (int32_t)pos & (ps - 1);
+  } else {
+    page_idx = (int32_t)pos / ps;
+    off = (int32_t)pos - page_idx * ps;
+  }
   if (page_idx < r.pt_n) return r.pt_s[page_idx] * a.page_size + off;
   if (page_idx < a.ld_pt) return __ldg(r.pt_row + page_idx) * a.page_size + off;
   raise_fault(kFaultIndex);

@@ -290,10 +290,15 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
     // from L2 (registers cannot be indexed by a runtime bit number)
     uint32_t cm = 0u;
     if (!every) {
+      // one compare per run of 4 (its maximum; NaN never passes), the 4
+      // compares only for the few runs that hold a candidate
 #pragma unroll
-      for (int j = 0; j < kSfRuns; ++j)
+      for (int j = 0; j < kSfRuns; ++j) {
+        if (fmaxf(fmaxf(xs[j][0], xs[j][1]), fmaxf(xs[j][2], xs[j][3])) >= vf) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cm |= (xs[j][c] >= vf ? 1u : 0u) << (4 * j + c);
+          for (int c = 0; c < 4; ++c) cm |= (xs[j][c] >= vf ? 1u : 0u) << (4 * j + c);
+        }
+      }
     }
     const int cnt = __popc(cm);
     int off = (int)warp_incl_scan_u32((uint32_t)cnt) - cnt;

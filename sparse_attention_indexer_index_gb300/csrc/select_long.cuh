@@ -185,7 +185,8 @@ __device__ __forceinline__ float4 sl_load4(const float* __restrict__ row, int i,
 // Positions are below 2^31 (row lengths are int32), so 32-bit arithmetic.
 __device__ __forceinline__ int32_t sl_slot(const SelectArgs& a, const int32_t* pt_row, uint32_t pos) {
   const uint32_t ps = (uint32_t)a.page_size;
-  const uint32_t page_idx = pos / ps;
+  // a shift for page sizes that are powers of two (the usual case)
+  const uint32_t page_idx = (ps & (ps - 1u)) == 0u ? pos >> (31 - __clz((int)ps)) : pos / ps;
   if ((int64_t)page_idx >= a.ld_pt) {
     raise_fault(kFaultIndex);
     return -1;
