@@ -56,7 +56,11 @@ constexpr int kSlMaxCluster = 16;
 constexpr int kSlBins = 4096;   // 12-bit digits; the last level uses 256 of them
 constexpr int kSlUnroll = 4;    // 128-entry chunks per warp in flight from global memory
 constexpr int kSlSamples = 2048;  // evenly spaced entries behind the first histogram's bound
-constexpr int kSlCandCap = 4096;  // candidate entries per CTA (kSlCandCap / kSlWarps per warp)
+// Candidate entries per CTA (kSlCandCap / kSlWarps per warp).  Rows of 80,000
+// on clusters of 2 leave about 170 entries per warp above the sampled bound,
+// up to 300 in the tail of ReLU-sum rows (2 % of rows passed 256, the
+// previous capacity, and took the whole-slice path).
+constexpr int kSlCandCap = 6144;
 constexpr int kSlBitmapWords = kSlBins / 2;  // slices of up to 65536 entries for the list path
 
 struct SlFixed {
