@@ -35,8 +35,10 @@
 //     to T too when all of them are taken, otherwise they go to a second
 //     bitmap whose first `need` set bits (a block scan of its words'
 //     popcounts) are added.  A block scan of the words' popcounts then gives
-//     each thread the output position of its first set bit, and it emits its
-//     set bits in ascending order.
+//     each thread the output position of its first set bit; it places the
+//     indices of its set bits in that order in shared memory, and the
+//     outputs (indices, or the 4 positions and slots of each block) are
+//     written from there, every thread taking every 1024-th output.
 // With 32 warps on the SM every per-entry instruction costs 8 issue slots per
 // scheduler, so each step is a short loop body over the 32 entries held in
 // registers, and the emission code is a single loop (not one copy per
@@ -129,6 +131,46 @@ __device__ __forceinline__ void sf_find_bin(SfShared& sh, const uint32_t* h, int
     sh.info[2] = (int)c_lo;
   }
   __syncthreads();
+}
+
+// Outputs of a row from its winners' indices in output order (sel[0, m)):
+// the same values as emit_one for each of them followed by emit_tail(m), each
+// thread writing every kSfThreads-th output (coalesced stores).
+template <int kMode>
+__device__ __forceinline__ void sf_emit_sorted(const SelectArgs& a, const SelRow& r, const uint32_t* sel, int m) {
+  const int t = r.t, k = a.k;
+  if (kMode == kModeTopk) {
+    for (int j = threadIdx.x; j < k; j += kSfThreads) {
+      const int idx = j < m ? (int)sel[j] : -1;
+      a.out_idx[(int64_t)t * k + j] = idx;
+      if (a.out_slots != nullptr) a.out_slots[(int64_t)t * k + j] = idx < 0 ? -1 : slot_lookup(a, r, idx);
+    }
+  } else {
+    if (a.out_idx != nullptr)
+      for (int j = threadIdx.x; j < k; j += kSfThreads) a.out_idx[(int64_t)t * k + j] = j < m ? (int32_t)sel[j] : -1;
+    const int width = kBlock * k + (kBlock - 1);
+    const int nb = r.L / kBlock, pend = r.L - kBlock * nb;
+    int32_t* xs = a.out_xslots + (int64_t)t * width;
+    int32_t* xp = a.out_pos != nullptr ? a.out_pos + (int64_t)t * width : nullptr;
+    for (int j = threadIdx.x; j < width; j += kSfThreads) {
+      int32_t pos = -1, slot = -1;
+      if (j < kBlock * m) {  // token c of the winner j / 4 (its block's 4 tokens share a page)
+        const int c = j & (kBlock - 1);
+        const int32_t p0 = kBlock * (int32_t)sel[j / kBlock];
+        const int32_t base = slot_lookup(a, r, p0);
+        slot = base < 0 ? -1 : base + c;
+        pos = p0 + c;
+      } else {
+        const int i = j - kBlock * m;
+        if (i < pend) {
+          pos = kBlock * nb + i;
+          slot = slot_lookup(a, r, pos);
+        }
+      }
+      xs[j] = slot;
+      if (xp != nullptr) xp[j] = pos;
+    }
+  }
 }
 
 template <int kMode>
@@ -473,20 +515,26 @@ __global__ void __launch_bounds__(kSfThreads, 1) select_fast_kernel(SelectArgs a
         }
     });
   }
-  // ---- 5. ordered emission: a scan of the bitmap words' popcounts -----------
+  // ---- 5. ordered emission: a scan of the bitmap words' popcounts gives each
+  // winner its output position; the winners' indices go to shared memory in
+  // output order (the lists are no longer read), then every thread writes an
+  // even, contiguous share of the outputs (a word holds 0 to about 6 winners,
+  // so writing them from the word's thread left most threads idle)
   {
     uint32_t w = sh.bm[threadIdx.x];
     uint32_t total;
     int pos = (int)sf_block_excl_scan(sh, (uint32_t)__popc(w), total);
     if (total != (uint32_t)a.k && threadIdx.x == 0) raise_fault(kFaultGrouping);  // cannot happen
+    uint32_t* sel = sh.lkey;
     while (w != 0u) {
       const int b = __ffs(w) - 1;
       w &= w - 1u;
-      if (pos < a.k) emit_one<kMode>(a, r, 32 * (int)threadIdx.x + b, pos);
+      if (pos < a.k) sel[pos] = 32u * threadIdx.x + (uint32_t)b;
       ++pos;
     }
+    __syncthreads();
+    sf_emit_sorted<kMode>(a, r, sel, min((int)total, a.k));
   }
-  emit_tail<kMode>(a, r, a.k);
 }
 
 }  // namespace qsa

@@ -35,8 +35,10 @@
 //     in two bitmaps of its slice; the CTAs exchange their counts (one
 //     cluster barrier); prefix counts of the bitmap words give the entries of
 //     P's bin that are taken (the first `need` of the row) and every
-//     winner's ascending output position, written with the slot translation
-//     or the QSA expansion by every CTA at once.
+//     winner's ascending output position.  Each CTA places its winners'
+//     indices in that order in shared memory and writes their outputs (with
+//     the slot translation or the QSA expansion) from there, every thread
+//     taking every 512-th output; all CTAs at once.
 // Fallbacks, all exact: a CTA whose warp lists overflow counts and marks by
 // walking its whole slice; a sampled bound with fewer than k entries above
 // it (retry flag from the leader), or slices longer than the bitmaps, take
@@ -578,6 +580,7 @@ select_long_kernel(SelectArgs a) {
         pre[4 * tid + u] = x;
         x += c4[u];
       }
+      return tot;
     };
     static_assert(kSlBitmapWords == 4 * kSlThreads, "four bitmap words per thread");
     word_scan(bm_eq, pre_eq);
@@ -603,18 +606,47 @@ select_long_kernel(SelectArgs a) {
       }
     }
     __syncthreads();
-    word_scan(bm_win, pre_win);
+    const uint32_t n_win = min(word_scan(bm_win, pre_win), (uint32_t)kSlCandCap);  // this CTA's winners
     __syncthreads();
+    // The CTA's winners in output order into shared memory (the lists are no
+    // longer read), then their outputs G.. from there, each thread taking
+    // every kSlThreads-th one: coalesced stores, and the page-table loads of a
+    // thread's outputs independent of one another.
+    uint32_t* sel = fx.cand_idx;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int w = 4 * tid + u;
       uint32_t bits = bm_win[w];
-      uint32_t pos = G + pre_win[w];
+      uint32_t pos = pre_win[w];
       while (bits != 0u) {
         const int b = __ffs(bits) - 1;
         bits &= bits - 1u;
-        emit((uint32_t)(s0 + 32 * w + b), (int)pos);
+        if (pos < n_win) sel[pos] = (uint32_t)(s0 + 32 * w + b);
         ++pos;
+      }
+    }
+    __syncthreads();
+    const uint32_t n_out = min(n_win, (uint32_t)k - min(G, (uint32_t)k));  // never past k (cannot happen)
+    if (kMode == kModeTopk) {
+#pragma unroll 4
+      for (uint32_t j = tid; j < n_out; j += kSlThreads) {
+        const uint32_t idx = sel[j];
+        a.out_idx[(int64_t)t * k + G + j] = (int32_t)idx;
+        if (a.out_slots != nullptr) a.out_slots[(int64_t)t * k + G + j] = sl_slot(a, pt_row, idx);
+      }
+    } else {
+      if (a.out_idx != nullptr)
+        for (uint32_t j = tid; j < n_out; j += kSlThreads) a.out_idx[(int64_t)t * k + G + j] = (int32_t)sel[j];
+      const int64_t width = (int64_t)kBlock * k + (kBlock - 1);
+      int32_t* xs = a.out_xslots + (int64_t)t * width + (int64_t)kBlock * G;
+      int32_t* xp = a.out_pos != nullptr ? a.out_pos + (int64_t)t * width + (int64_t)kBlock * G : nullptr;
+#pragma unroll 4
+      for (uint32_t j = tid; j < kBlock * n_out; j += kSlThreads) {  // token j % 4 of winner j / 4 (one page)
+        const uint32_t p0 = kBlock * sel[j / kBlock];
+        const int32_t base = sl_slot(a, pt_row, p0);
+        const int c = (int)(j & (kBlock - 1));
+        xs[j] = base < 0 ? -1 : base + c;
+        if (xp != nullptr) xp[j] = (int32_t)p0 + c;
       }
     }
     return;

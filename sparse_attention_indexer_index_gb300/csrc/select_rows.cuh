@@ -30,8 +30,9 @@
 //     level 0 again over every entry of the row.
 //  4. Two bitmaps of the row (entries above the k-th key's bin, entries in
 //     it) and prefix counts of their words give the first `need` entries of
-//     the bin and every winner's ascending output position; the outputs are
-//     written by all threads.
+//     the bin and every winner's ascending output position; the winners'
+//     indices are placed in that order in shared memory and the outputs are
+//     written from there by all threads, each taking every 256-th output.
 // Every wait is a CTA barrier; no global scratch.
 #pragma once
 #include <type_traits>
@@ -421,6 +422,12 @@ select_rows_kernel(SelectArgs a) {
   __syncthreads();
   word_scan(sm.bm_win, pre_win);
   __syncthreads();
+  // the winners' indices in output order into shared memory (the lists are
+  // no longer read), then the outputs from there, each thread taking every
+  // kSrThreads-th one: coalesced stores, and the page-table loads of a
+  // thread's outputs independent of one another (writing a word's winners
+  // from its thread chained one L2 load per winner)
+  uint32_t* sel = sm.cand_idx;
 #pragma unroll
   for (int u = 0; u < kWpt; ++u) {
     const int w = kWpt * tid + u;
@@ -429,8 +436,31 @@ select_rows_kernel(SelectArgs a) {
     while (bits != 0u) {
       const int b = __ffs(bits) - 1;
       bits &= bits - 1u;
-      emit((uint32_t)(32 * w + b), (int)pos);
+      if (pos < (uint32_t)k) sel[pos] = (uint32_t)(32 * w + b);
       ++pos;
+    }
+  }
+  __syncthreads();
+  if (kMode == kModeTopk) {
+#pragma unroll 4
+    for (int j = tid; j < k; j += kSrThreads) {
+      const uint32_t idx = sel[j];
+      a.out_idx[(int64_t)t * k + j] = (int32_t)idx;
+      if (a.out_slots != nullptr) a.out_slots[(int64_t)t * k + j] = slot(idx);
+    }
+  } else {
+    if (a.out_idx != nullptr)
+      for (int j = tid; j < k; j += kSrThreads) a.out_idx[(int64_t)t * k + j] = (int32_t)sel[j];
+    const int64_t width = (int64_t)kBlock * k + (kBlock - 1);
+    int32_t* xs = a.out_xslots + (int64_t)t * width;
+    int32_t* xp = a.out_pos != nullptr ? a.out_pos + (int64_t)t * width : nullptr;
+#pragma unroll 4
+    for (int j = tid; j < kBlock * k; j += kSrThreads) {  // token j % 4 of winner j / 4 (one page)
+      const uint32_t p0 = kBlock * sel[j / kBlock];
+      const int32_t base = slot(p0);
+      const int c = j & (kBlock - 1);
+      xs[j] = base < 0 ? -1 : base + c;
+      if (xp != nullptr) xp[j] = (int32_t)p0 + c;
     }
   }
 }
