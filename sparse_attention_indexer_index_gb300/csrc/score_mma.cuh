@@ -126,8 +126,29 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   if (!relaxed) pdl_wait_primary();
   if (a.trigger_dependents) pdl_launch_dependents();
 
+  // One request (a verify step, a lone decode row): the tile list follows
+  // from max_len alone and the request's metadata is loaded here, beside the
+  // page-table entries below, so that the keys are one memory round trip
+  // away instead of four (metadata, row lengths, page table, new_pos).
+  // Tiles past the request's blocks load nothing.  A row list that does not
+  // start at row 0 reads its lengths again after the start is known.
+  const bool single = a.n_req == 1;
+  int pf_rs0 = 0, pf_rs1 = 0, pf_np = 0, pf_len = 0;
+  if (single) {
+    pf_rs0 = __ldg(a.req_row_start);
+    pf_rs1 = __ldg(a.req_row_start + 1);
+    if (relaxed) pf_np = __ldg(a.new_pos);
+    if (lane < min(a.n_rows, 2 * NT)) pf_len = __ldg(a.row_len + lane);
+  }
+
   // ---- tile list: ceil(nb_r / 16) tiles per request, prefix in shared memory
-  {
+  if (single) {
+    if (threadIdx.x == 0) {
+      g_pre[0] = 0;
+      g_pre[1] = (a.max_len / kBlock + kTile - 1) / kTile;
+    }
+    __syncthreads();
+  } else {
     const int per = (a.n_req + kSmThreads - 1) / kSmThreads;
     const int r_lo = min(a.n_req, (int)threadIdx.x * per), r_hi = min(a.n_req, r_lo + per);
     int local = 0;
@@ -174,16 +195,21 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
   // Pool rows of tile i's 8-key runs (a run never straddles a page: pages
   // hold a multiple of 8 keys); -1 if a page is out of range or the run lies
   // past the request's blocks (its last tile only: no page-table entry is
-  // read there).
+  // read there).  One request: the tile list may reach past the request's
+  // blocks, so an out-of-range entry gives kRunBadIndex / kRunBadPool and
+  // faults at the load only if the run's first block is below the length.
+  constexpr int kRunBadIndex = -2, kRunBadPool = -3;
   auto run_row = [&](int r, int b) -> int {
     const int page_idx = b / kpp;
     if (page_idx >= a.ld_pt) {
+      if (single) return kRunBadIndex;
       raise_fault(kFaultIndex);
       return -1;
     }
     const int64_t page = __ldg(a.page_table + (int64_t)r * a.ld_pt + page_idx);
     const int64_t row = page * kpp + (int64_t)(b - page_idx * kpp);
     if (page < 0 || row >= a.pool_rows) {
+      if (single) return kRunBadPool;
       raise_fault(kFaultPool);
       return -1;
     }
@@ -195,7 +221,7 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     if (i >= i1) return;
     const int r = request_of(i);
     const int b = (i - g_pre[r]) * kTile;
-    const int nbv = i == g_pre[r + 1] - 1 ? request_blocks(a, r) : INT_MAX;
+    const int nbv = !single && i == g_pre[r + 1] - 1 ? request_blocks(a, r) : INT_MAX;
 #pragma unroll
     for (int q = 0; q < kRuns; ++q) {
       const int bq = b + 8 * q;
@@ -225,21 +251,33 @@ __global__ void __launch_bounds__(kSmThreads, kSmMinCtas) score_mma_kernel(Score
     if (r_ld < 0 || i >= g_pre[r_ld + 1]) {
       if (r_ld < 0) r_ld = request_of(i);
       while (i >= g_pre[r_ld + 1]) ++r_ld;  // g_pre is non-decreasing: empty requests are skipped
-      const int t0l = __ldg(a.req_row_start + r_ld);
-      const int nrl = min(__ldg(a.req_row_start + r_ld + 1) - t0l, 2 * NT);
-      int L = lane < nrl ? __ldg(a.row_len + t0l + lane) : 0;
+      int L;
+      if (single) {  // the loads issued at the start
+        const int nrl = min(pf_rs1 - pf_rs0, 2 * NT);
+        L = lane < nrl ? (pf_rs0 == 0 ? pf_len : __ldg(a.row_len + pf_rs0 + lane)) : 0;
+        fn_ld = relaxed ? max(0, pf_np) / kBlock : INT_MAX;
+      } else {
+        const int t0l = __ldg(a.req_row_start + r_ld);
+        const int nrl = min(__ldg(a.req_row_start + r_ld + 1) - t0l, 2 * NT);
+        L = lane < nrl ? __ldg(a.row_len + t0l + lane) : 0;
+        fn_ld = relaxed ? max(0, __ldg(a.new_pos + r_ld)) / kBlock : INT_MAX;
+      }
       if (L < 0 || L > a.max_len) L = 0;
       nb_ld = __reduce_max_sync(0xffffffffu, (unsigned)(L / kBlock));
-      fn_ld = relaxed ? max(0, __ldg(a.new_pos + r_ld)) / kBlock : INT_MAX;
     }
     const int j = i - g_pre[r_ld];
-    if (!waited && kTile * (j + 1) > fn_ld) {  // this tile may hold keys the key path writes
+    const int vis = min(kTile, nb_ld - j * kTile);
+    if (!waited && vis > 0 && kTile * (j + 1) > fn_ld) {  // this tile may hold keys the key path writes
       pdl_wait_primary();
       waited = true;
     }
-    const int vis = min(kTile, nb_ld - j * kTile);
     int pr[kRuns];
     rows_of(i, pr);
+    if (single) {  // deferred page faults: only runs below the request's length
+#pragma unroll
+      for (int q = 0; q < kRuns; ++q)
+        if (pr[q] <= kRunBadIndex && 8 * q < vis && lane == 0) raise_fault(pr[q] == kRunBadIndex ? kFaultIndex : kFaultPool);
+    }
     // key row g of each run (rows past the request's blocks: zero)
     bool v[kRuns];
     bool bad = false;

@@ -11,7 +11,10 @@ headline decode step checked against the oracle end to end.
   own keys (positions 79,994..79,999) complete blocks 19,998 and 19,999
   through the 4-slot ring; the new pool rows against the oracle's key path,
   the scores against the oracle on the same keys, the selection, positions
-  and slots bit-exact.
+  and slots bit-exact; also with max_len past the rows.
+- One request with max_len far past its rows: the one-request scorer's
+  tiles reach page-table entries past the rows (unmapped, past the pool,
+  other data's pages) without a fault or a stray score.
 - Mixed row lengths in one call (the device row plan), also recorded in a
   CUDA graph (the short rows run on a side stream forked and joined inside
   the call).
@@ -102,12 +105,22 @@ def test_topk_boundary_ties_take_lowest_indices(qsa, n, k):
 
 
 # ----------------------------------------------------------------- the headline step
-def test_decode_step_c2_verify_against_the_oracle(qsa):
+@pytest.mark.parametrize("max_len", [None, 131_072])
+def test_decode_step_c2_verify_against_the_oracle(qsa, max_len):
     """The 6-row verify step at L = 80,000 (rows at positions
     79,994..79,999), as one qsa_decode_step call on a pool holding blocks
-    0..19,997 and a ring holding tokens 79,992..79,993."""
+    0..19,997 and a ring holding tokens 79,992..79,993.  Also with max_len
+    past the rows (a capacity bound, as a captured graph would pass) and the
+    table's pages past the rows unmapped: the one-request scorer then builds
+    tiles past the rows, which must not fault."""
     import torch
     w = c2_verify(0)
+    page_table = w.page_table
+    if max_len is None:
+        max_len = w.max_len
+    else:  # the table covers max_len (the call's contract); pages past the rows unmapped
+        page_table = np.full((1, (max_len + w.page_size - 1) // w.page_size), -1, np.int32)
+        page_table[0, :w.page_table.shape[1]] = w.page_table[0]
     assert w.n_req == 1 and list(w.row_len) == [79_995 + i for i in range(6)]
     first, count = 79_994, 6
     nb0 = first // 4  # 19,998 blocks complete before the step
@@ -129,11 +142,11 @@ def test_decode_step_c2_verify_against_the_oracle(qsa):
                                         pool0.copy())
     # one GPU call
     g_pool, g_ring = bf16_dev(pool0), bf16_dev(ring0)
-    ld = (w.max_len // 4 + 3) // 4 * 4
+    ld = (max_len // 4 + 3) // 4 * 4
     scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
     out = qsa.decode_step(bf16_dev(new), to_dev(rts), to_dev(fp), g_ring, bf16_dev(w.q), g_pool,
-                          to_dev(w.req_row_start), to_dev(w.row_len), to_dev(w.page_table), w.page_size,
-                          w.max_len, w.max_rows_per_req, k_blk=512, rope_base=w.rope_base, want_blocks=True,
+                          to_dev(w.req_row_start), to_dev(w.row_len), to_dev(page_table), w.page_size,
+                          max_len, w.max_rows_per_req, k_blk=512, rope_base=w.rope_base, want_blocks=True,
                           want_pos=True, scores_out=scores)
     pool_g, ring_g = bf16_host(g_pool), bf16_host(g_ring)
     # ring: the last 4 appended tokens (bit copies)
@@ -155,6 +168,45 @@ def test_decode_step_c2_verify_against_the_oracle(qsa):
     # selection, positions and slots bit-exact on the GPU's scores
     sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
     pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
+    assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
+    assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
+
+
+@pytest.mark.parametrize("rows,table", [([5003, 4099, 5000], "unmapped"), ([5003, 4099, 5000], "past_pool"),
+                                        ([5003, 4099, 5000], "other_pages"), ([8190], "unmapped")])
+def test_one_request_with_max_len_past_its_rows(qsa, rows, table):
+    """One request scored and selected with max_len = 131,072, far past its
+    rows (a capacity bound): the one-request scorer's tile list reaches the
+    table's entries past the rows -- unmapped (-1), past the pool, or pages
+    of other data.  No fault may fire, and scores, selection, positions and
+    slots match the oracle."""
+    import torch
+    max_len = 131_072
+    w = decode_workload(71 + len(rows), [rows], page_size=64, k_blk=512, pad_pages=40)
+    pool_h = np.zeros((w.pool_rows, 128), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, w.page_table, w.page_size, w.rope_base, pool_h)
+    used = (max(rows) + w.page_size - 1) // w.page_size
+    pt = np.full((1, max_len // w.page_size), -1, np.int32)
+    pt[0, :used] = w.page_table[0, :used]
+    if table == "past_pool":
+        pt[0, used:] = 1 << 30
+    elif table == "other_pages":
+        pt[0, used:] = np.random.default_rng(5).integers(0, w.pool_rows * 4 // w.page_size, size=pt.shape[1] - used)
+    ld = (max_len // 4 + 3) // 4 * 4
+    scores = torch.full((w.n_rows, ld), float("nan"), device="cuda")
+    out = qsa.indexer_select(bf16_dev(w.q), bf16_dev(pool_h), to_dev(w.req_row_start), to_dev(w.row_len),
+                             to_dev(pt), w.page_size, max_len, w.max_rows_per_req, k_blk=512,
+                             want_blocks=True, want_pos=True, scores_out=scores)
+    s = scores.cpu().numpy()
+    want = oracle.index_scores(w.q, pool_h, w.req_row_start, w.row_len, pt, w.page_size, ld)
+    tol = score_tolerance(w.q, pool_h, w.req_row_start, w.row_len, pt, w.page_size, ld)
+    for t in range(w.n_rows):
+        nb = int(w.row_len[t]) // 4
+        err = np.abs(s[t, :nb].astype(np.float64) - want[t, :nb])
+        assert (err <= tol[t, :nb]).all(), (t, float(err.max()))
+    sel_ref, _ = oracle.topk(s, 512, n_valid=w.row_len // 4)
+    pos_ref, slots_ref = oracle.expand(sel_ref, w.req_row_start, w.row_len, pt, w.page_size)
     assert np.array_equal(out["blocks"].cpu().numpy(), sel_ref)
     assert np.array_equal(out["pos"].cpu().numpy(), pos_ref)
     assert np.array_equal(out["slots"].cpu().numpy(), slots_ref)
