@@ -108,16 +108,27 @@ def _stream(stream=None, device=None):
     global _raw_stream
     torch = _torch()
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
+        return stream.cuda_stream
     if _raw_stream is None:  # the raw query avoids building a Stream object per call
         _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
     if _raw_stream:
         idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
-        return ctypes.c_void_p(_raw_stream(idx))
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+        return _raw_stream(idx)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _dev(t, dtype, name, ndim=None):
+    # one pass of cheap attribute checks; the precise message only on failure
+    try:
+        ok = t.is_cuda and t.dtype is dtype and t.is_contiguous() and (ndim is None or t.dim() == ndim)
+    except AttributeError:
+        ok = False
+    if not ok:
+        _dev_error(t, dtype, name, ndim)
+    return t
+
+
+def _dev_error(t, dtype, name, ndim):
     torch = _torch()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
@@ -125,9 +136,25 @@ def _dev(t, dtype, name, ndim=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if ndim is not None and t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dims")
-    return t
+    raise ValueError(f"{name} must have {ndim} dims")
+
+
+_fast = None
+
+
+def _call(fn, *args):
+    """Call the C entry point `fn`: through the CPython entry points of
+    _fastcall.c when they were built (the per-step calls), else ctypes."""
+    global _fast
+    if _fast is None:
+        lib()
+        try:
+            from . import _fastcall as m
+        except ImportError:
+            m = False
+        _fast = m
+    f = getattr(_fast, fn, None) if _fast else None
+    return (f or getattr(lib(), fn))(*args)
 
 
 def _check(fn, status):
@@ -226,8 +253,8 @@ def decode_step(new_keys, req_tok_start, req_first_pos, ring, q, pool, req_row_s
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     fn = "qsa_decode_step" if head_gates is None else "qsa_decode_step_gated"
     gate_args = () if head_gates is None else (_ptr(head_gates),)
-    _check(fn, getattr(lib(), fn)(
-        _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), _ptr(ring), float(rope_base), _ptr(q),
+    _check(fn, _call(
+        fn, _ptr(new_keys), _ptr(req_tok_start), _ptr(req_first_pos), _ptr(ring), float(rope_base), _ptr(q),
         *gate_args, _ptr(pool), pool.shape[0], n_req, _ptr(req_row_start), n_rows, _ptr(row_len), int(max_len),
         int(max_rows_per_req), _ptr(page_table), page_table.shape[1], int(page_size), int(k_blk), _ptr(blocks),
         _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld, _ptr(workspace),
@@ -297,8 +324,8 @@ def _index_scores_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, page_
         ld = max(1, (max(int(max_len) // BLOCK, int(n_fill)) + 3) // 4 * 4)
         scores = torch.empty((n_rows, ld), dtype=torch.float32, device=q.device)
     _dev(scores, torch.float32, "scores", 2)
-    _check(fn, getattr(lib(), fn)(
-        _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+    _check(fn, _call(
+        fn, _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
         _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
         int(page_size), _ptr(scores), scores.shape[1], int(n_fill), _stream(stream)))
     return scores
@@ -560,8 +587,8 @@ def _indexer_select_call(fn, key_ptrs, pool_rows, q, req_row_start, row_len, pag
             workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         elif workspace is not None:
             ws_bytes = workspace.numel() * workspace.element_size()
-    _check(fn, getattr(lib(), fn)(
-        _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
+    _check(fn, _call(
+        fn, _ptr(q), *key_ptrs, pool_rows, req_row_start.numel() - 1, _ptr(req_row_start), n_rows,
         _ptr(row_len), int(max_len), int(max_rows_per_req), _ptr(page_table), page_table.shape[1],
         int(page_size), int(k_blk), _ptr(blocks), _ptr(pos), _ptr(out_slots), _ptr(scores_out), ld,
         _ptr(workspace), ws_bytes, _stream(stream, q.device)))

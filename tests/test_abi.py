@@ -161,3 +161,33 @@ def test_append_keys_rejects_bad_arguments(L):
     assert f(FAKE, FAKE, FAKE, 2, ctypes.c_void_p(0x1008), FAKE, 4, 64, 10000.0, FAKE, 64, None) == -1
     # no requests: nothing to do
     assert f(None, None, None, 0, None, None, 0, 64, 10000.0, None, 0, None) == 0
+
+
+def test_cpython_entry_points_match_ctypes_on_host_checks(L):
+    """The CPython entry points of the per-step calls (_fastcall.c, built
+    beside the library where the Python headers are present) reach the same
+    C functions as ctypes: the host-side checks give the same statuses, and
+    a wrong argument count or an int32 out of range raises before any call."""
+    from sparse_attention_indexer_index_gb300 import _build
+    if not os.path.exists(_build.fastcall_path()):
+        pytest.skip("the CPython entry points were not built (no Python headers here)")
+    from sparse_attention_indexer_index_gb300 import _fastcall as fc
+    X = 0x1000
+    need = L.qsa_indexer_select_workspace_size(6, 80000, 512)
+    a = (X, X, 1 << 20, 1, X, 6, X, 80000, 6, X, 1250, 64, 512, None, None, X, None, 0, X, need - 1, None)
+    assert fc.qsa_indexer_select(*a) == L.qsa_indexer_select(*a) == -3
+    a_k = a[:12] + (4096,) + a[13:19] + (need,) + a[20:]
+    assert fc.qsa_indexer_select(*a_k) == L.qsa_indexer_select(*a_k) == -2
+    g = a[:1] + (X,) + a[1:]  # gated: the gates after q
+    assert fc.qsa_indexer_select_gated(*g) == L.qsa_indexer_select_gated(*g) == -3
+    z = (None, None, 0, 0, None, 0, None, 0, 0, None, 0, 64, 512, None, None, None, None, 0, None, 0, None)
+    assert fc.qsa_indexer_select(*z) == 0
+    d = (X, X, X, X, 10000.0, X, X, 1 << 20, 1, X, 6, X, 80000, 6, X, 1250, 64, 4096, None, None, X, None, 0, X,
+         need, None)
+    assert fc.qsa_decode_step(*d) == L.qsa_decode_step(*d) == -2
+    dg = d[:6] + (X,) + d[6:]
+    assert fc.qsa_decode_step_gated(*dg) == L.qsa_decode_step_gated(*dg) == -2
+    with pytest.raises(TypeError):
+        fc.qsa_decode_step(*d[:-1])
+    with pytest.raises(OverflowError):
+        fc.qsa_decode_step(*(d[:10] + (1 << 40,) + d[11:]))
