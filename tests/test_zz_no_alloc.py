@@ -109,3 +109,36 @@ def test_noalloc_refuses_calls_beyond_the_scratch_array(lib):
     assert st == -2  # QSA_ERR_UNSUPPORTED
     # the largest call that fits is accepted by the same check (not launched here)
     assert (n_rows - 1) * 4 * (max_len // 4) <= SCRATCH_BYTES
+
+
+def test_noalloc_on_a_decode_batch_and_without_device_allocation(lib):
+    """32 requests of one row each on 64-token pages (the batched decode
+    shape, one-row tiles in the scorer) through the allocation-free call:
+    identical to the workspace path, and a warm call changes the device's
+    free memory by nothing (its outputs allocated beforehand)."""
+    import torch
+    qsa, L = lib
+    rng = np.random.default_rng(64)
+    rows = [[int(x)] for x in rng.integers(4096, 40_000, size=32)]
+    w = decode_workload(64, rows, page_size=64, k_blk=512)
+    d = _device_state(w)
+    got = _noalloc(L, w, d)  # warm: first call on this shape
+    torch.cuda.synchronize()
+    want = _with_workspace(qsa, w, d)
+    torch.cuda.synchronize()
+    for g, e in zip(got, want):
+        assert torch.equal(g, e)
+    width = 4 * w.k_blk + 3
+    slots = torch.full((w.n_rows, width), -7, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    st = L.qsa_indexer_select_noalloc(
+        _ptr(d["q"]), _ptr(d["pool"]), d["pool"].shape[0], w.n_req, _ptr(d["rrs"]), w.n_rows,
+        _ptr(d["rl"]), w.max_len, w.max_rows_per_req, _ptr(d["pt"]), d["pt"].shape[1], w.page_size,
+        w.k_blk, None, None, _ptr(slots), d["stream"])
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert st == 0
+    assert free1 == free0
+    assert torch.equal(slots, want[2])
+    assert qsa.device_status(clear=True) == 0
