@@ -191,3 +191,22 @@ def test_cpython_entry_points_match_ctypes_on_host_checks(L):
         fc.qsa_decode_step(*d[:-1])
     with pytest.raises(OverflowError):
         fc.qsa_decode_step(*(d[:10] + (1 << 40,) + d[11:]))
+
+
+def test_binding_call_path_with_and_without_the_cpython_entry_points(L):
+    """The binding's dispatcher reaches the same C function through the
+    CPython entry points (when built) and through ctypes (when not)."""
+    import sparse_attention_indexer_index_gb300 as qsa
+    X = 0x1000
+    need = L.qsa_indexer_select_workspace_size(6, 80000, 512)
+    d = (X, X, X, X, 10000.0, X, X, 1 << 20, 1, X, 6, X, 80000, 6, X, 1250, 64, 4096, None, None, X, None, 0, X,
+         need, None)
+    saved = qsa._fast
+    try:
+        qsa._fast = None  # load the CPython entry points if they were built
+        assert qsa._call("qsa_decode_step", *d) == -2
+        qsa._fast = False  # ctypes only
+        assert qsa._call("qsa_decode_step", *d) == -2
+        assert qsa._call("qsa_indexer_select_workspace_size", 6, 80000, 512) == need
+    finally:
+        qsa._fast = saved
