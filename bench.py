@@ -951,6 +951,11 @@ def main():
     t_e2e, h2d, d2h = e2e_decode(g, st, min(args.steps, 100), args.warmup)
     e2e_ms = aggregate_time(statistics.mean(t_e2e), ws, device)
 
+    # ---- the timing method's own floor: a graph of one trivial kernel (a
+    # one-element add), timed like the step (L2 flushed, events around it)
+    tiny = torch.zeros(1, device=device)
+    floor_ms = statistics.mean(g.timed(lambda: tiny.add_(1.0), min(args.steps, 50), args.warmup))
+
     out = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -981,6 +986,9 @@ def main():
                 "how": "one pinned host buffer of the step's inputs copied in, one eager decode_step "
                        "call, slots copied back; no graph"},
         "gpu_launches": 3 * args.steps,
+        "timing_floor_us": {"value": 1e3 * floor_ms,
+                            "how": "a CUDA graph of one trivial kernel (a one-element add) timed like the "
+                                   "step: L2 flushed before it, CUDA events around the replay"},
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
     }
