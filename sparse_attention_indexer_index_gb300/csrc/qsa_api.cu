@@ -697,7 +697,7 @@ qsa_status launch_scores_tma(TcArgs t, int64_t n_kt, int64_t row_tiles, int32_t 
 // rows on pages holding a multiple of 8 compressed keys.  About one wave of
 // CTAs (two per SM), at least one tile (16 BF16 or 32 FP8 keys) per warp.
 template <int NT, bool kFp8>
-qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream) {
+qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t stream, int reserve) {
   const size_t smem = sm_smem_bytes(s.n_req, NT);
   // CTAs per SM, queried once (the query costs microseconds of host time on
   // every call otherwise): at the largest shared memory a launch can ask
@@ -716,8 +716,13 @@ qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t s
   const int occ = occ_max;
   const int64_t nb_max = s.max_len / kBlock;
   const int64_t tiles_max = (int64_t)s.n_req * ((nb_max + sm_tile<NT, kFp8>() - 1) / sm_tile<NT, kFp8>());
-  const int64_t ctas =
+  int64_t ctas =
       std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(occ, 1) * sm_count, (tiles_max + kSmWarps - 1) / kSmWarps));
+  // A grid of about one CTA per SM leaves `reserve` SMs to the selection
+  // launched after it, so that its CTAs become resident at once and read
+  // their metadata and page-table entries while the scorer runs.
+  if (reserve > 0 && ctas > sm_count - reserve && ctas <= sm_count + 2 * reserve)
+    ctas = std::max<int64_t>(1, sm_count - reserve);
   if (launch_pdl(score_mma_kernel<NT, kFp8>, dim3((unsigned)ctas), dim3(kSmThreads), smem, stream, s) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -726,7 +731,8 @@ qsa_status launch_scores_mma_nt(const ScoreArgs& s, int sm_count, cudaStream_t s
   return QSA_OK;
 }
 
-qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
+qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream,
+                             int reserve = 0) {
   const int64_t nb_max = s.max_len / kBlock;
   if (s.n_req == 0 || nb_max == 0 || max_rows_per_req <= 0) return QSA_OK;
   const int kpp = s.page_size / kBlock;
@@ -736,10 +742,10 @@ qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_co
   qsa_status st;
   const bool fp8 = s.pool8 != nullptr;
   switch ((max_rows_per_req + 1) / 2) {
-    case 1: st = fp8 ? launch_scores_mma_nt<1, true>(s, sm_count, stream) : launch_scores_mma_nt<1, false>(s, sm_count, stream); break;
-    case 2: st = fp8 ? launch_scores_mma_nt<2, true>(s, sm_count, stream) : launch_scores_mma_nt<2, false>(s, sm_count, stream); break;
-    case 3: st = fp8 ? launch_scores_mma_nt<3, true>(s, sm_count, stream) : launch_scores_mma_nt<3, false>(s, sm_count, stream); break;
-    default: st = fp8 ? launch_scores_mma_nt<4, true>(s, sm_count, stream) : launch_scores_mma_nt<4, false>(s, sm_count, stream); break;
+    case 1: st = fp8 ? launch_scores_mma_nt<1, true>(s, sm_count, stream, reserve) : launch_scores_mma_nt<1, false>(s, sm_count, stream, reserve); break;
+    case 2: st = fp8 ? launch_scores_mma_nt<2, true>(s, sm_count, stream, reserve) : launch_scores_mma_nt<2, false>(s, sm_count, stream, reserve); break;
+    case 3: st = fp8 ? launch_scores_mma_nt<3, true>(s, sm_count, stream, reserve) : launch_scores_mma_nt<3, false>(s, sm_count, stream, reserve); break;
+    default: st = fp8 ? launch_scores_mma_nt<4, true>(s, sm_count, stream, reserve) : launch_scores_mma_nt<4, false>(s, sm_count, stream, reserve); break;
   }
   if (st == QSA_OK && s.n_fill > 0) {
     fill_neginf_kernel<<<(unsigned)s.n_rows, 256, 0, stream>>>(s.row_len, s.max_len, s.scores, s.ld_scores,
@@ -755,8 +761,9 @@ qsa_status launch_scores_mma(const ScoreArgs& s, int max_rows_per_req, int sm_co
 // streaming kernel otherwise.
 qsa_status launch_scores(ScoreArgs s, int sm_count, cudaStream_t stream);
 qsa_status launch_scores_tc(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream);
-qsa_status launch_scorer(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream) {
-  const qsa_status m = launch_scores_mma(s, max_rows_per_req, sm_count, stream);
+qsa_status launch_scorer(const ScoreArgs& s, int max_rows_per_req, int sm_count, cudaStream_t stream,
+                         int reserve = 0) {
+  const qsa_status m = launch_scores_mma(s, max_rows_per_req, sm_count, stream, reserve);
   if (m != QSA_ERR_UNSUPPORTED || s.pool8 != nullptr) return m;  // FP8 keys: the mma.sync scorer only
   return max_rows_per_req >= kTcMinRows ? launch_scores_tc(s, max_rows_per_req, sm_count, stream)
                                         : launch_scores(s, sm_count, stream);
@@ -1268,7 +1275,9 @@ qsa_status indexer_select_impl(const void* q, const void* pool, int64_t pool_row
   ScoreArgs s{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(pool),
               pool_rows, n_req, req_row_start, n_rows, row_len, max_len, page_table, ld_pt,
               page_size, scores, ld, 0, 1, new_pos, pool8, key_scales, head_gates};
-  if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st))
+  // the register-resident selection (one 1024-thread CTA per row) follows
+  const int reserve = (n_rows <= d->sm_count / 2 && nb_max <= kSfMaxRow && k_blk <= kSfMaxK) ? n_rows : 0;
+  if (qsa_status e = launch_scorer(s, max_rows_per_req, d->sm_count, st, reserve))
     return e;
 
   SelectArgs a{};
