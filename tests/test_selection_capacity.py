@@ -1,9 +1,9 @@
 """Capacity of the selection kernels' candidate lists, checked on the CPU.
 
-Two kernels list the entries at or above a lower bound in fixed per-warp
+Three kernels list the entries at or above a lower bound in fixed per-warp
 regions of shared memory; a warp whose region would overflow sends its row
-(select_fast_kernel) or its CTA's slice (select_long_kernel) to a slower
-whole-row path, which is still exact.  These checks replay each kernel's
+(select_fast_kernel, select_rows_kernel) or its CTA's slice
+(select_long_kernel) to a slower whole-row path, which is still exact.  These checks replay each kernel's
 bound, in the kernel's own layout of entries over warps, on seeded rows of
 the benchmark's score distributions, and assert that the per-warp capacity
 read from the kernel sources covers the largest count seen with margin.
@@ -16,6 +16,10 @@ read from the kernel sources covers the largest count seen with margin.
 - select_fast_kernel, top-512 over QSA block rows of 2,048-32,768 entries:
   the bound is the smallest, over full warps, of the ceil(k/F)-th largest of
   the warp's 32 lane maxima, each lane holding entries 4 (t + 1024 j) + c.
+- select_rows_kernel, top-512 over the prefill chunk's rows of up to 32,768
+  entries: the bound is the edge of the top-12-bit bin of the r-th largest
+  of 1024 samples (32 runs of 32), r = ceil(mu + 3.5 sqrt(mu) + 2) with
+  mu = 1024 k / n; each of the 8 warps owns a contiguous segment of the row.
 """
 import math
 import os
@@ -90,6 +94,34 @@ def _fast_warp_counts(row, k):
     v = max(int(per_warp[:full, 32 - kw].min()), 1)
     cand = (vals >= v) & valid
     return cand.reshape(threads // 32, -1).sum(1)
+
+
+def _rows_warp_counts(row, k):
+    """Per-warp candidate counts of select_rows_kernel on one row."""
+    n = row.size
+    warps = _const("select_rows.cuh", "kSrThreads") // 32
+    keys = _keys(row)
+    mu = np.float32(1024.0) * np.float32(k) / np.float32(n)
+    r = int(math.ceil(float(mu + np.float32(3.5) * np.sqrt(mu) + np.float32(2.0))))
+    cand = np.ones(n, bool)
+    if r < 1024:
+        idx = np.concatenate([(((run * n) // 32) & ~3) + np.arange(32) for run in range(32)])
+        idx = idx[idx < n]
+        hist = np.bincount((keys[idx] >> 20).astype(np.int64), minlength=4096)
+        above = np.cumsum(hist[::-1])
+        bin_ = 4095 - int(np.searchsorted(above, r))
+        cand = keys >= (np.uint64(bin_) << 20)
+    seg = (((n + warps - 1) // warps) + 127) & ~127
+    return [int(cand[min(n, w * seg):min(n, w * seg + seg)].sum()) for w in range(warps)]
+
+
+def test_small_cta_lists_cover_the_prefill_rows():
+    cap = _const("select_rows.cuh", "kSrCandCap") // (_const("select_rows.cuh", "kSrThreads") // 32)
+    for dist in ("normal", "relu4"):
+        for n in (8000, 20_000, 32_768):
+            s, _ = topk_scores(np.random.default_rng(n + 1), 60, n, dist)
+            m = max(max(_rows_warp_counts(row, 512)) for row in s)
+            assert m <= 0.8 * cap, (dist, n, m, cap)
 
 
 def test_long_row_lists_cover_the_dsa_rows():
