@@ -626,3 +626,23 @@ def test_append_keys_several_requests_in_one_call():
     for b in (1, 2):
         want = oracle.compress_block(raw_ctx[0][4 * b:4 * b + 4], 4 * b)
         assert np.array_equal(pool_a[oracle.pool_row(pt[0], b, P)], want)
+
+
+def test_openmp_build_computes_the_same_path():
+    """The OpenMP build of the oracle (used only to time the CPU baseline on
+    every host core) gives the single-threaded build's scores, selection,
+    positions and slots to the bit, on several requests of ragged rows."""
+    import subprocess
+    from workloads import decode_workload
+    w = decode_workload(91, [[4099, 4100, 4101], [1030], [9000, 9002]], page_size=64, k_blk=512)
+    pool = np.zeros((w.pool_rows, 128), np.uint16)
+    oracle.compress(w.raw_keys, w.block_req, w.block_id, w.page_table, w.page_size, w.rope_base, pool)
+    args = (w.q, pool, w.req_row_start, w.row_len, w.page_table, w.page_size)
+    one = oracle.indexer_select(*args, k_blk=w.k_blk)
+    try:
+        many = oracle.indexer_select_threads(*args, k_blk=w.k_blk, threads=4)
+    except (OSError, subprocess.CalledProcessError):
+        pytest.skip("no OpenMP toolchain")
+    for key in ("blocks", "pos", "slots"):
+        assert np.array_equal(one[key], many[key]), key
+    assert np.array_equal(one["scores"].view(np.uint32), many["scores"].view(np.uint32))
