@@ -210,3 +210,19 @@ def test_binding_call_path_with_and_without_the_cpython_entry_points(L):
         assert qsa._call("qsa_indexer_select_workspace_size", 6, 80000, 512) == need
     finally:
         qsa._fast = saved
+
+
+def test_cpython_entry_points_are_optional(monkeypatch, tmp_path):
+    """Without the Python headers the CPython entry points are not built (and
+    the binding keeps to ctypes); nothing is raised."""
+    import sysconfig
+    from sparse_attention_indexer_index_gb300 import _build
+    real = sysconfig.get_paths
+
+    def no_headers(*a, **k):
+        paths = dict(real(*a, **k))
+        paths["include"] = str(tmp_path / "no_python_headers")
+        return paths
+
+    monkeypatch.setattr(sysconfig, "get_paths", no_headers)
+    assert _build.build_fastcall(force=True) is None
