@@ -111,3 +111,17 @@ def test_long_rows_take_the_cluster_selection():
     assert bench.topk_kernel_name(6, 20_000, k=512) == "select_fast_kernel"
     assert bench.topk_kernel_name(200, 32_768, k=1024) == "select_fast_kernel"
     assert bench.topk_kernel_name(400, 20_000, k=512) == "select_rows_kernel"
+
+
+def test_nominal_fractions_beside_the_measured_ones():
+    """Every fraction of the measured HBM peak in the line gets its
+    companion against the nominal bandwidth (the same bytes, the same time)."""
+    import bench
+    out = {"step_alg_GBps": 790.0, "step_frac_hbm": 790.0 / 6683.8,
+           "variants": {"a": {"alg_GBps": 3950.0, "frac_hbm": 3950.0 / 6683.8}, "b": {"us_per_call": 1.0},
+                        "c": {"alg_GBps": 10.0}}}
+    bench.add_nominal_fractions(out)
+    assert abs(out["step_frac_hbm_nominal"] - 0.1) < 1e-12
+    assert abs(out["variants"]["a"]["frac_hbm_nominal"] - 0.5) < 1e-12
+    assert "frac_hbm_nominal" not in out["variants"]["b"]
+    assert "frac_hbm_nominal" not in out["variants"]["c"]
